@@ -1,0 +1,438 @@
+"""Benchmark of the KDA forward hot path on GB300.
+
+Default line: chunkwise prefill on 4 sequences x 4096 tokens, H=16,
+d_k=d_v=128, chunk 64, bf16 I/O with fp32 state; one step = one
+kda_chunk_fwd call over the whole batch.  The same run also times the decode
+workload (256 sequences x 32 heads, 128 consecutive steps, 512 MiB state updated
+in place) and reports it under "decode".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill_bf16|long_prefill_bf16|varlen_prefill_bf16|decode_bf16]
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(independent problems, no collective on the data path); the timing is the max
+over ranks and `value` counts the tokens of all ranks.  `--impl reference`
+times the fp64 CPU oracle (the only other implementation of this method) on the
+host cores, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA tokens/sec on 1 GB300 (prefill & decode) and % of roofline"
+D_FLOP_CONST = 180_224          # 6 d^2 + 10 C d flops per token-head at d=128, C=64
+PREFILL_KERNELS = ("kda_chunk_tc_kernel", "kda_chunk_simt_kernel")
+
+
+# ----------------------------------------------------------------- helpers
+def algorithmic_prefill(token_heads: int, pairs: int, d_k: int, d_v: int, io_bytes: int, C=64):
+    """Algorithmic bytes and flops of one prefill launch.
+    bytes: q, k, g (d_k each) and v (d_v) read, beta read, o (d_v) written per
+    token-head, plus the fp32 state read and written once per (sequence, head).
+    flops: 3 state-sized GEMMs (2 d_k d_v each) + 5 chunk products (2 C d each)
+    per token-head, the accounting 2Ld^2 + 2LCd of the chunked-attention cost."""
+    per_tok = io_bytes * (3 * d_k + 2 * d_v) + io_bytes
+    state = 2 * 4 * d_k * d_v
+    flops_tok = 2 * (d_k * d_v) * 3 + 2 * C * d_k * 5
+    return token_heads * per_tok + pairs * state, token_heads * flops_tok
+
+
+def algorithmic_decode(pairs: int, d_k: int, d_v: int, io_bytes: int):
+    per_tok = io_bytes * (3 * d_k + 2 * d_v) + io_bytes
+    return pairs * (per_tok + 2 * 4 * d_k * d_v)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash(kind: str) -> str:
+    name = {"tensor": "kda_chunk_tc.cu", "simt": "kda_chunk_simt.cu", "decode": "kda_decode.cu"}[kind]
+    p = os.path.join(ROOT, "kimi_delta_attention_fwd_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(f"{kind}:{workload}")
+    if not rec or rec.get("source_sha256_16") != kernel_source_hash(kind):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons with NVML (via ctypes on
+    libnvidia-ml), falling back to nvidia-smi, while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks",
+               0x1: "gpu_idle"}
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._nvml = None
+        self._handle = None
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            props = torch.cuda.get_device_properties(device_index)
+            bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                raise OSError("handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._handle = nv, h
+        except Exception:
+            self._nvml = None
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        if self._nvml is None:
+            return
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, ctypes.byref(c)) == 0:
+            self.samples.append(c.value)
+        if self._nvml.nvmlDeviceGetCurrentClocksEventReasons(self._handle, ctypes.byref(r)) == 0:
+            for bit, name in self.REASONS.items():
+                if r.value & bit and name != "gpu_idle":
+                    self.reasons.add(name)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def __enter__(self):
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        self._thread.join()
+
+    def summary(self):
+        if self._nvml is None:
+            return self._smi_fallback()
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": "nvml"}
+
+    @staticmethod
+    def _smi_fallback():
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm", "--format=csv,noheader,nounits"],
+                                 capture_output=True, text=True, timeout=20).stdout.split("\n")[0]
+            cur, mx = (float(x) for x in out.split(","))
+            return {"sm_mhz": cur, "sm_max_mhz": mx, "reasons": [], "samples": 1,
+                    "source": "nvidia-smi after the timed region"}
+        except Exception:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "none"}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_cpu_baseline(x, pairs_limit=None):
+    """Times the oracle, as it stands, on the host cores.  Returns (seconds,
+    tokens processed, token-heads processed, threads, sample description)."""
+    import oracle
+    import numpy as np
+    q, k, v, g, beta, cu, init = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu(),
+                                  x["init_state"])
+    H = q.shape[1]
+    if pairs_limit is not None and pairs_limit < H:
+        q, k, v, g, beta = (t[:, :pairs_limit] for t in (q, k, v, g, beta))
+        init = None if init is None else init[:, :pairs_limit]
+    # widen once outside the timed call (the oracle's input is fp64)
+    q, k, v, g, beta = (t.float().numpy().astype(np.float64) for t in (q, k, v, g, beta))
+    init = None if init is None else init.numpy().astype(np.float64)
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.kda_fwd(q, k, v, g, beta, cu.numpy(), init_state=init, threads=threads)
+    dt = time.perf_counter() - t0
+    tokens = int(cu[-1])
+    heads = q.shape[1]
+    return dt, tokens, tokens * heads, threads, heads
+
+
+# ------------------------------------------------------------- our arm
+def run_prefill(args, ws, rank, dev):
+    import torch
+    from kimi_delta_attention_fwd_gb300 import kda_chunk_fwd, kda_chunk_fwd_workspace_bytes
+    from kimi_delta_attention_fwd_gb300 import workloads as W
+    from kimi_delta_attention_fwd_gb300 import kda as K
+
+    spec = W.named(args.workload)
+    spec = W.PrefillSpec(spec.seqlens, spec.num_heads, spec.d_k, spec.d_v, spec.io_dtype, spec.gate,
+                         spec.init, spec.seed + 1000 * rank)
+    big = spec.total_tokens * spec.num_heads > 4_000_000
+    x = W.prefill_inputs(spec, device=("cuda" if big else "cpu"))
+    d = {kk: (vv.to(dev) if vv is not None else None) for kk, vv in x.items()}
+    T, H, dk, dv, N = spec.total_tokens, spec.num_heads, spec.d_k, spec.d_v, spec.num_seqs
+    io_bytes = 2 if spec.io_dtype == "bf16" else 4
+    out = torch.empty((T, H, dv), dtype=d["q"].dtype, device=dev)
+    fin = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    wsb = kda_chunk_fwd_workspace_bytes(N, T, H, dk, dv, d["q"].dtype, args.algo)
+    work = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    tensor_path = K.kda_chunk_fwd_selected_algo(N, T, H, dk, dv, d["q"].dtype, args.algo) == "tensor"
+
+    def step(o=out, f=fin):
+        kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"],
+                      out=o, final_state=f, workspace=work, algo=args.algo, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    from kimi_delta_attention_fwd_gb300 import kda_workspace_status
+    status = kda_workspace_status(work, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_step = total_ms / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # e2e through the public API: pinned host inputs -> device, kernel, result -> host
+    host_in = {kk: (vv.to("cpu").pin_memory() if vv is not None else None) for kk, vv in x.items()}
+    host_out = torch.empty_like(out, device="cpu").pin_memory()
+    host_fin = torch.empty_like(fin, device="cpu").pin_memory()
+    dev_in = {kk: (torch.empty_like(vv, device=dev) if vv is not None else None) for kk, vv in x.items()}
+    h2d = sum(vv.numel() * vv.element_size() for vv in host_in.values() if vv is not None)
+    d2h = host_out.numel() * host_out.element_size() + host_fin.numel() * host_fin.element_size()
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for kk, vv in host_in.items():
+            if vv is not None:
+                dev_in[kk].copy_(vv, non_blocking=True)
+        kda_chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
+                      dev_in["cu_seqlens"], dev_in["init_state"], out=out, final_state=fin,
+                      workspace=work, algo=args.algo, stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        host_fin.copy_(fin, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    hbm, tflops, peak_src = measured_peaks()
+    alg_bytes, alg_flops = algorithmic_prefill(T * H, N * H, dk, dv, io_bytes)
+    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+    kind = "tensor" if tensor_path else "simt"
+    res = {
+        "metric": METRIC, "value": T * ws / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": N, "total_tokens": T, "num_heads": H,
+                   "d_k": dk, "d_v": dv, "chunk": 64, "io_dtype": spec.io_dtype,
+                   "kernel": kind, "l2": "inputs larger than L2 (%.0f MB read+written per step)" % (alg_bytes / 1e6),
+                   "parallelism": f"replicas x{ws} (independent sequences per GPU)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": recorded_traffic(kind, args.workload),
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "tensor_tflops_algorithmic": alg_flops / (launch_ms * 1e-3) / 1e12,
+                     "tensor_peak_tflops": tflops,
+                     "kernel_ms": launch_ms,
+                     "roofline_ms": max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12)) * 1e3},
+        "e2e": {"value": T * ws / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    return res, x
+
+
+def run_decode(args, ws, rank, dev, name="decode_bf16"):
+    import torch
+    from kimi_delta_attention_fwd_gb300 import kda_decode_step
+    from kimi_delta_attention_fwd_gb300 import workloads as W
+    spec = W.named(name)
+    spec = W.DecodeSpec(spec.num_seqs, spec.num_heads, spec.d_k, spec.d_v, spec.steps, spec.io_dtype,
+                        spec.gate, spec.seed + 1000 * rank)
+    y = W.decode_inputs(spec, device=str(dev))
+    st = y["state"].clone()
+    outs = torch.empty((spec.steps, spec.num_seqs, spec.num_heads, spec.d_v), dtype=y["q"].dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run_all():
+        for t in range(spec.steps):
+            kda_decode_step(y["q"][t], y["k"][t], y["v"][t], y["g"][t], y["beta"][t], st, out=outs[t],
+                            stream=stream)
+
+    for _ in range(max(1, args.warmup)):
+        run_all()
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps, 5))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        a.record(stream)
+        for _ in range(reps):
+            run_all()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (reps * spec.steps)  # per decode step
+    io_bytes = 2 if spec.io_dtype == "bf16" else 4
+    by = algorithmic_decode(spec.num_seqs * spec.num_heads, spec.d_k, spec.d_v, io_bytes)
+    hbm, _, src = measured_peaks()
+    ach = by / (ms * 1e-3) / 1e9
+    return {"workload": name, "value": spec.num_seqs * ws / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_decode_step": ms, "steps_per_rep": spec.steps, "reps": reps,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "traffic": recorded_traffic("decode", name), "peak_source": f"{src} hbm_gbs"},
+            "gpu_launches": reps * spec.steps, "clocks": clk.summary()}
+
+
+def main_ours(args):
+    import torch
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from kimi_delta_attention_fwd_gb300 import build as kbuild
+    if not kbuild.up_to_date():
+        kbuild.build()
+    if args.workload == "decode_bf16":
+        dec = run_decode(args, ws, rank, dev)
+        res = {"metric": METRIC, "value": dec["value"], "unit": "tokens/s", "n_gpus": ws,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_decode_step"],
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+               "data": "synthetic", "config": {"workload": "decode_bf16", "l2": "state 512 MiB > L2"},
+               "roofline": dec["roofline"], "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"]}
+        x = None
+    else:
+        res, x = run_prefill(args, ws, rank, dev)
+        if not args.no_decode and args.workload == "prefill_bf16":
+            res["decode"] = run_decode(args, ws, rank, dev)
+    if rank == 0 and not args.no_cpu_baseline and x is not None:
+        dt, tokens, th, threads, heads = oracle_cpu_baseline(x, pairs_limit=args.cpu_heads)
+        res["cpu_baseline"] = {"value": th / dt / x["q"].shape[1],
+                               "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                               "sample": f"{args.workload}: all {tokens} tokens of {heads} of {x['q'].shape[1]} heads "
+                                         f"({th} token-heads, {dt:.1f} s), scaled to tokens/s over all heads"}
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+# ------------------------------------------------------- reference arm
+def main_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    from kimi_delta_attention_fwd_gb300 import workloads as W
+    spec_name = args.workload if args.workload != "decode_bf16" else "prefill_bf16"
+    spec = W.named(spec_name)
+    x = W.prefill_inputs(spec)
+    H = spec.num_heads
+    heads = args.cpu_heads or H
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, tokens, th, threads, used = oracle_cpu_baseline(x, pairs_limit=heads)
+        if i >= args.warmup:
+            times.append(dt)
+    dt = statistics.mean(times)
+    value = tokens * (used / H) / dt  # tokens/s over all heads, from a sample of heads
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * H / used,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": spec_name, "num_seqs": spec.num_seqs,
+                      "total_tokens": spec.total_tokens, "num_heads": H, "d_k": spec.d_k,
+                      "d_v": spec.d_v},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                            "sample": f"{used} of {H} heads, all {tokens} tokens per step"},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_bf16",
+                    choices=["prefill_bf16", "long_prefill_bf16", "varlen_prefill_bf16", "decode_bf16"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "tensor", "simt"])
+    ap.add_argument("--cpu-heads", type=int, default=None,
+                    help="heads of the workload the CPU oracle runs (default: all)")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,137 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ *
+ * The operation ("Kimi Delta Attention (KDA)", brain.bigb.es, opening equation
+ * and the five-line recurrence in the transposed d_k x d_v layout; "K3 架构图解"
+ * Ch.08 column-vector form).  Per sequence and head, state S in R^{d_k x d_v}:
+ *
+ *   alpha_t = exp(g_t)                 (g_t = log alpha_t <= 0, one per key channel)
+ *   S~_t    = Diag(alpha_t) S_{t-1}    forget
+ *   e_t     = beta_t (v_t - S~_t^T k_t)  predict and correct (beta_t: one per token, head)
+ *   S_t     = S~_t + k_t e_t^T         rank-one write
+ *   o_t     = scale * S_t^T q_t        read after the write
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; nothing is
+ *     allocated, freed or retained by the library.  Calls are asynchronous on
+ *     `stream` (0 = legacy default stream) and enqueue kernels only.
+ *   - Tensors are contiguous, row-major, 16-byte aligned:
+ *       q, k, g : [T_total, H, d_k]        v, out : [T_total, H, d_v]
+ *       beta    : [T_total, H]             states : [N, H, d_k, d_v] fp32
+ *       cu_seqlens : int32 [N + 1] (device), nondecreasing, cu[0] = 0,
+ *                    cu[N] = T_total; sequence n owns tokens [cu[n], cu[n+1]).
+ *   - q, k, v, g, beta and out have the I/O dtype (fp32 or bf16); states are
+ *     always fp32.  q and k are used as given (normalisation belongs to the
+ *     caller).  g must be finite and <= 0.
+ *   - Return value: KDA_OK or a negative KDA_ERR_* code; on error nothing was
+ *     enqueued.  No C++ exception crosses the ABI.
+ */
+#ifndef KDA_GB300_KDA_H_
+#define KDA_GB300_KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  KDA_OK = 0,
+  KDA_ERR_NULL = -1,           /* a required pointer is NULL */
+  KDA_ERR_SHAPE = -2,          /* unsupported or inconsistent sizes */
+  KDA_ERR_ALIGN = -3,          /* a tensor pointer is not 16-byte aligned */
+  KDA_ERR_WORKSPACE = -4,      /* workspace missing or too small */
+  KDA_ERR_LAUNCH = -5,         /* CUDA rejected a launch or an async call */
+  KDA_ERR_DEVICE = -6,         /* current device is not sm_103 or lacks a needed driver entry */
+  KDA_ERR_DEVICE_TIMEOUT = -7, /* (device-reported) a bounded wait in a kernel gave up */
+  KDA_ERR_GATE_RANGE = -8,     /* (device-reported) a chunk's decay exceeded the tensor-core path's range */
+  KDA_ERR_UNSUPPORTED = -9     /* the requested algorithm does not support this dtype or size */
+};
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Which chunk-prefill kernel to run.  AUTO picks TENSOR for bf16 I/O with
+ * d_k = d_v = 128 and SIMT otherwise. */
+typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_TENSOR = 1, KDA_ALGO_SIMT = 2 } kda_algo;
+
+typedef struct {
+  int32_t num_seqs;     /* N >= 0 (sequences; for decode: independent sequences, one token each) */
+  int32_t total_tokens; /* T_total = cu_seqlens[N]; for decode must equal num_seqs */
+  int32_t num_heads;    /* H >= 1 */
+  int32_t d_k;          /* 64 or 128 */
+  int32_t d_v;          /* 64 or 128 */
+  int32_t chunk_size;   /* prefill chunk length: 0 or 64 (both mean 64); ignored by decode */
+  float scale;          /* output scale; <= 0 selects d_k^-1/2 */
+  int32_t io_dtype;     /* kda_dtype of q, k, v, g, beta, out */
+  int32_t algo;         /* kda_algo (prefill only) */
+} kda_shape;
+
+/*
+ * Chunkwise-parallel prefill over packed variable-length sequences
+ * ("Kimi Delta Attention (KDA)", section on the two schedules: chunk-local
+ * cumulative log decays, the interaction matrices A^kk and A^qk, the
+ * triangular solve (I + R_c)^-1, one sequential state scan across chunks, and
+ * the output O_c = s S_c Q_c^boundary + E_c (A^qk_c)^T; the UT/WY form is the
+ * chunked DeltaNet section of "22580: от GPT-2 до Kimi K3").  Gives the same
+ * states and outputs as running the recurrence token by token.
+ *
+ *   q, k, v, g, beta : inputs as above (device).
+ *   init_state  : [N, H, d_k, d_v] fp32, or NULL for zero initial states.
+ *   cu_seqlens  : int32 [N + 1] on the device; read only by the kernels.
+ *   out         : [T_total, H, d_v] (io dtype), written for every token.
+ *   final_state : [N, H, d_k, d_v] fp32 or NULL; may alias init_state exactly
+ *                 (in-place update); no other overlap is allowed.
+ *   workspace   : device scratch of at least kda_chunk_fwd_workspace_bytes()
+ *                 bytes (16-byte aligned).  It holds the device status block
+ *                 read by kda_workspace_status(); calls that share one
+ *                 workspace must be ordered on one stream.
+ * Zero sequences or zero tokens are valid (nothing but the status reset is enqueued).
+ * Sequences must be at most 2^31 - 1 tokens long in total; an empty sequence
+ * copies its initial state to final_state.
+ */
+int kda_chunk_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
+                  const void *g, const void *beta, const float *init_state,
+                  const int32_t *cu_seqlens, void *out, float *final_state, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of workspace kda_chunk_fwd needs for this shape (always > 0), or 0 if
+ * the shape is invalid. */
+size_t kda_chunk_fwd_workspace_bytes(const kda_shape *shape);
+
+/* The prefill kernel a call with this shape runs: KDA_ALGO_TENSOR or
+ * KDA_ALGO_SIMT (AUTO resolved), or a negative KDA_ERR_* code. */
+int kda_chunk_fwd_selected_algo(const kda_shape *shape);
+
+/*
+ * One recurrent step for N independent sequences, one token each (the "fused
+ * recurrent" schedule of "Kimi Delta Attention (KDA)" with a single token):
+ * state is read once, updated in place, and written once.
+ *   q, k, g : [N, H, d_k]; v, out : [N, H, d_v]; beta : [N, H] (io dtype, device)
+ *   state   : [N, H, d_k, d_v] fp32 (device), updated in place.
+ * shape->total_tokens must equal shape->num_seqs; chunk_size and algo are ignored.
+ */
+int kda_decode_step(const kda_shape *shape, const void *q, const void *k, const void *v,
+                    const void *g, const void *beta, float *state, void *out,
+                    cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads the status block that the kernels of the
+ * last kda_chunk_fwd on this workspace wrote: KDA_OK, KDA_ERR_DEVICE_TIMEOUT
+ * or KDA_ERR_GATE_RANGE.  A CUDA error while reading returns KDA_ERR_LAUNCH.
+ */
+int kda_workspace_status(const void *workspace, cudaStream_t stream);
+
+/* Static English description of a status code. */
+const char *kda_status_string(int status);
+
+/* Library ABI version (major * 1000 + minor). */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_KDA_H_ */

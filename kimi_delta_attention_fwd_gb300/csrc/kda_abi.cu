@@ -1,0 +1,174 @@
+// extern "C" entry points of the KDA forward library: argument validation,
+// kernel selection, status handling.  See include/kda.h for the contract.
+#include <cuda_runtime_api.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Common shape checks; `decode` relaxes the chunk/algo fields.
+int check_shape(const kda_shape *s, bool decode) {
+  if (!s) return KDA_ERR_NULL;
+  if (s->num_seqs < 0 || s->total_tokens < 0 || s->num_heads < 1) return KDA_ERR_SHAPE;
+  if (!((s->d_k == 64 || s->d_k == 128) && (s->d_v == 64 || s->d_v == 128))) return KDA_ERR_SHAPE;
+  if (s->io_dtype != KDA_F32 && s->io_dtype != KDA_BF16) return KDA_ERR_SHAPE;
+  if (!(s->scale == s->scale) || isinf(s->scale)) return KDA_ERR_SHAPE;
+  if (decode) {
+    if (s->total_tokens != s->num_seqs) return KDA_ERR_SHAPE;
+  } else {
+    if (s->chunk_size != 0 && s->chunk_size != 64) return KDA_ERR_SHAPE;
+    if (s->algo < KDA_ALGO_AUTO || s->algo > KDA_ALGO_SIMT) return KDA_ERR_SHAPE;
+  }
+  // element counts must stay addressable with 64-bit offsets and 32-bit token ids
+  if ((int64_t)s->num_seqs * s->num_heads > (int64_t)INT32_MAX) return KDA_ERR_SHAPE;
+  return KDA_OK;
+}
+
+float effective_scale(const kda_shape *s) {
+  return s->scale > 0.f ? s->scale : 1.0f / sqrtf((float)s->d_k);
+}
+
+// The library carries sm_103a code only.
+int check_device(int *num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_DEVICE;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return KDA_ERR_DEVICE;
+  if (major != 10 || minor != 3) return KDA_ERR_DEVICE;
+  if (num_sms) *num_sms = sms;
+  return KDA_OK;
+}
+
+bool use_tensor_path(const kda_shape *s) {
+  const bool bf16 = s->io_dtype == KDA_BF16;
+  if (s->algo == KDA_ALGO_SIMT) return false;
+  if (s->algo == KDA_ALGO_TENSOR) return true;
+  return kda::chunk_tc_supported(s->d_k, s->d_v, bf16);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 1000; }
+
+const char *kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_NULL: return "a required pointer is NULL";
+    case KDA_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case KDA_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_LAUNCH: return "CUDA rejected a launch or an asynchronous call";
+    case KDA_ERR_DEVICE: return "current device is not sm_103 or lacks a needed driver entry point";
+    case KDA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    case KDA_ERR_GATE_RANGE: return "a chunk's cumulative decay exceeded the tensor-core path's range";
+    case KDA_ERR_UNSUPPORTED: return "the requested algorithm does not support this dtype or size";
+    default: return "unknown status";
+  }
+}
+
+size_t kda_chunk_fwd_workspace_bytes(const kda_shape *s) {
+  if (check_shape(s, false) != KDA_OK) return 0;
+  size_t bytes = kda::kStatusBytes;
+  if (use_tensor_path(s)) bytes += kda::chunk_tc_scratch_bytes(s->num_seqs, s->num_heads, s->d_k, s->d_v);
+  return bytes;
+}
+
+int kda_chunk_fwd_selected_algo(const kda_shape *s) {
+  const int rc = check_shape(s, false);
+  if (rc != KDA_OK) return rc;
+  if (!use_tensor_path(s)) return KDA_ALGO_SIMT;
+  if (!kda::chunk_tc_supported(s->d_k, s->d_v, s->io_dtype == KDA_BF16)) return KDA_ERR_UNSUPPORTED;
+  return KDA_ALGO_TENSOR;
+}
+
+int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *v, const void *g,
+                  const void *beta, const float *init_state, const int32_t *cu_seqlens, void *out,
+                  float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_shape(s, false);
+  if (rc != KDA_OK) return rc;
+  if (s->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+  if (s->num_seqs > 0 && !cu_seqlens) return KDA_ERR_NULL;
+  if (!workspace) return KDA_ERR_WORKSPACE;
+  if (workspace_bytes < kda_chunk_fwd_workspace_bytes(s)) return KDA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+      !aligned16(init_state) || !aligned16(cu_seqlens) || !aligned16(out) ||
+      !aligned16(final_state) || !aligned16(workspace))
+    return KDA_ERR_ALIGN;
+  const bool tensor = use_tensor_path(s);
+  if (tensor && !kda::chunk_tc_supported(s->d_k, s->d_v, s->io_dtype == KDA_BF16))
+    return KDA_ERR_UNSUPPORTED;
+  int num_sms = 0;
+  rc = check_device(&num_sms);
+  if (rc != KDA_OK) return rc;
+
+  if (cudaMemsetAsync(workspace, 0, kda::kStatusBytes, stream) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (s->num_seqs == 0) return KDA_OK;
+
+  kda::ChunkArgs a;
+  a.num_seqs = s->num_seqs;
+  a.total_tokens = s->total_tokens;
+  a.num_heads = s->num_heads;
+  a.d_k = s->d_k;
+  a.d_v = s->d_v;
+  a.scale = effective_scale(s);
+  a.bf16 = s->io_dtype == KDA_BF16;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.init_state = init_state;
+  a.cu_seqlens = cu_seqlens;
+  a.out = out;
+  a.final_state = final_state;
+  a.status = static_cast<uint32_t *>(workspace);
+  a.scratch = static_cast<unsigned char *>(workspace) + kda::kStatusBytes;
+  a.scratch_bytes = workspace_bytes - kda::kStatusBytes;
+  a.num_sms = num_sms;
+  const cudaError_t err = tensor ? kda::launch_chunk_tc(a, stream) : kda::launch_chunk_simt(a, stream);
+  if (err == cudaErrorInvalidValue) return KDA_ERR_UNSUPPORTED;
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+int kda_decode_step(const kda_shape *s, const void *q, const void *k, const void *v, const void *g,
+                    const void *beta, float *state, void *out, cudaStream_t stream) {
+  int rc = check_shape(s, true);
+  if (rc != KDA_OK) return rc;
+  if (s->num_seqs == 0) return KDA_OK;
+  if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+      !aligned16(state) || !aligned16(out))
+    return KDA_ERR_ALIGN;
+  rc = check_device(nullptr);
+  if (rc != KDA_OK) return rc;
+  kda::DecodeArgs a;
+  a.num_seqs = s->num_seqs;
+  a.num_heads = s->num_heads;
+  a.d_k = s->d_k;
+  a.d_v = s->d_v;
+  a.scale = effective_scale(s);
+  a.bf16 = s->io_dtype == KDA_BF16;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.state = state;
+  a.out = out;
+  const cudaError_t err = kda::launch_decode(a, stream);
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+int kda_workspace_status(const void *workspace, cudaStream_t stream) {
+  if (!workspace) return KDA_ERR_NULL;
+  uint32_t word[2] = {0, 0};
+  if (cudaMemcpyAsync(word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return KDA_ERR_LAUNCH;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_LAUNCH;
+  return word[0] == 0 ? KDA_OK : -(int)word[0];
+}
+
+}  // extern "C"

@@ -1,0 +1,165 @@
+// Single-token KDA decode step (the "fused recurrent" schedule of
+// "Kimi Delta Attention (KDA)", brain.bigb.es, with one token per sequence):
+//
+//   S~ = Diag(exp(g)) S,  e = beta (v - S~^T k),  S <- S~ + k e^T,
+//   o  = scale * S^T q = scale * (S~^T q + e (k . q))
+//
+// One CTA per (sequence, head).  The fp32 state tile [d_k, d_v] is read from
+// HBM exactly once into registers (16-byte streaming loads), decayed, reduced
+// over key channels for both S~^T k and S~^T q in the same pass, updated in
+// registers and written back exactly once.  The work is HBM-bound: 2 * 4 *
+// d_k * d_v bytes of state traffic against ~7 d_k d_v flops.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+template <typename IO>
+__device__ __forceinline__ float to_f32(IO x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename IO>
+__device__ __forceinline__ void store4(IO *p, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float *p, float4 v) {
+  *reinterpret_cast<float4 *>(p) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t *>(&a);
+  u.y = *reinterpret_cast<uint32_t *>(&b);
+  *reinterpret_cast<uint2 *>(p) = u;
+}
+
+constexpr int kDecodeThreads = 256;
+
+template <typename IO, int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+    kda_decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
+                      const IO *__restrict__ v, const IO *__restrict__ g,
+                      const IO *__restrict__ beta, float *__restrict__ state,
+                      IO *__restrict__ out, float scale) {
+  constexpr int TPR = DV / 4;               // threads covering one state row (float4 each)
+  constexpr int RPP = kDecodeThreads / TPR;  // rows covered per pass of the block
+  constexpr int RPT = DK / RPP;              // rows held by each thread
+  static_assert(RPT * RPP == DK, "row split");
+
+  __shared__ float s_q[DK], s_k[DK], s_a[DK], s_v[DV];
+  __shared__ float4 s_red[2][RPP][TPR];
+  __shared__ float4 s_e[TPR];
+  __shared__ float s_kq, s_beta;
+
+  const int pair = blockIdx.x;  // n * H + h
+  const int tid = threadIdx.x;
+  const int c4 = tid % TPR;
+  const int r0 = tid / TPR;
+
+  // Issue the state loads first: they are the only HBM-heavy traffic.
+  float4 *S4 = reinterpret_cast<float4 *>(state + (size_t)pair * DK * DV);
+  float4 s[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&S4[(size_t)(r0 + i * RPP) * TPR + c4]);
+
+  const size_t koff = (size_t)pair * DK, voff = (size_t)pair * DV;
+  for (int i = tid; i < DK; i += kDecodeThreads) {
+    s_q[i] = to_f32(q[koff + i]);
+    s_k[i] = to_f32(k[koff + i]);
+    s_a[i] = __expf(to_f32(g[koff + i]));
+  }
+  for (int i = tid; i < DV; i += kDecodeThreads) s_v[i] = to_f32(v[voff + i]);
+  if (tid == 0) s_beta = to_f32(beta[pair]);
+  __syncthreads();
+
+  if (tid < 32) {  // k . q
+    float acc = 0.f;
+    for (int i = tid; i < DK; i += 32) acc += s_k[i] * s_q[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (tid == 0) s_kq = acc;
+  }
+
+  // Forget, then partial sums of S~^T k and S~^T q over this thread's rows.
+  float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = r0 + i * RPP;
+    const float a = s_a[r], kr = s_k[r], qr = s_q[r];
+    s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+    pk.x += s[i].x * kr; pk.y += s[i].y * kr; pk.z += s[i].z * kr; pk.w += s[i].w * kr;
+    pq.x += s[i].x * qr; pq.y += s[i].y * qr; pq.z += s[i].z * qr; pq.w += s[i].w * qr;
+  }
+  s_red[0][r0][c4] = pk;
+  s_red[1][r0][c4] = pq;
+  __syncthreads();
+
+  if (tid < TPR) {
+    float4 P = s_red[0][0][tid], R = s_red[1][0][tid];
+#pragma unroll
+    for (int j = 1; j < RPP; ++j) {
+      const float4 a = s_red[0][j][tid], b = s_red[1][j][tid];
+      P.x += a.x; P.y += a.y; P.z += a.z; P.w += a.w;
+      R.x += b.x; R.y += b.y; R.z += b.z; R.w += b.w;
+    }
+    const float bt = s_beta, kq = s_kq;
+    const int c = 4 * tid;
+    float4 e, o;
+    e.x = bt * (s_v[c + 0] - P.x);
+    e.y = bt * (s_v[c + 1] - P.y);
+    e.z = bt * (s_v[c + 2] - P.z);
+    e.w = bt * (s_v[c + 3] - P.w);
+    o.x = scale * (R.x + e.x * kq);
+    o.y = scale * (R.y + e.y * kq);
+    o.z = scale * (R.z + e.z * kq);
+    o.w = scale * (R.w + e.w * kq);
+    s_e[tid] = e;
+    store4<IO>(out + voff + c, o);
+  }
+  __syncthreads();
+
+  // Rank-one write and the single store of the new state.
+  const float4 e = s_e[c4];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const float kr = s_k[r0 + i * RPP];
+    s[i].x += kr * e.x; s[i].y += kr * e.y; s[i].z += kr * e.z; s[i].w += kr * e.w;
+    __stcs(&S4[(size_t)(r0 + i * RPP) * TPR + c4], s[i]);
+  }
+}
+
+template <typename IO, int DK, int DV>
+cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
+  const int pairs = a.num_seqs * a.num_heads;
+  if (pairs == 0) return cudaSuccess;
+  kda_decode_kernel<IO, DK, DV><<<pairs, kDecodeThreads, 0, stream>>>(
+      static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
+      static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.state,
+      static_cast<IO *>(a.out), a.scale);
+  return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_decode_io(const DecodeArgs &a, cudaStream_t stream) {
+  if (a.d_k == 128 && a.d_v == 128) return launch_decode_t<IO, 128, 128>(a, stream);
+  if (a.d_k == 128 && a.d_v == 64) return launch_decode_t<IO, 128, 64>(a, stream);
+  if (a.d_k == 64 && a.d_v == 128) return launch_decode_t<IO, 64, 128>(a, stream);
+  if (a.d_k == 64 && a.d_v == 64) return launch_decode_t<IO, 64, 64>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
+  return a.bf16 ? launch_decode_io<__nv_bfloat16>(a, stream) : launch_decode_io<float>(a, stream);
+}
+
+}  // namespace kda

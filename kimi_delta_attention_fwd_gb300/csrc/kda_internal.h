@@ -1,0 +1,47 @@
+// Internal launcher interface shared by the library's translation units.
+// Not part of the public ABI (that is include/kda.h).
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Status block at the start of the workspace, written by the prefill kernels.
+// word 0: first error code recorded (0 = none), word 1: detail (where).
+constexpr size_t kStatusBytes = 256;
+
+struct ChunkArgs {
+  int num_seqs, total_tokens, num_heads, d_k, d_v;
+  float scale;
+  bool bf16;
+  const void *q, *k, *v, *g, *beta;
+  const float *init_state;
+  const int32_t *cu_seqlens;
+  void *out;
+  float *final_state;
+  uint32_t *status;   // device status block (kStatusBytes)
+  void *scratch;      // workspace after the status block
+  size_t scratch_bytes;
+  int num_sms;
+};
+
+struct DecodeArgs {
+  int num_seqs, num_heads, d_k, d_v;
+  float scale;
+  bool bf16;
+  const void *q, *k, *v, *g, *beta;
+  float *state;
+  void *out;
+};
+
+// Each returns cudaSuccess or the launch error; a shape the launcher does not
+// handle returns cudaErrorInvalidValue without launching.
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
+bool chunk_tc_supported(int d_k, int d_v, bool bf16);
+size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int d_k, int d_v);
+
+}  // namespace kda

@@ -1,0 +1,206 @@
+"""Thin Python binding of the C ABI in include/kda.h (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of libkda_gb300.so;
+this module checks tensor metadata, allocates outputs with PyTorch when the
+caller did not pass them, and forwards raw device pointers and the CUDA stream.
+There is no CPU path: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_F32, KDA_BF16 = 0, 1
+_ALGOS = {"auto": 0, "tensor": 1, "simt": 2}
+_DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {kda_status_string(code)} (status {code})")
+
+
+class kda_shape(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("chunk_size", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("io_dtype", ctypes.c_int32), ("algo", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libkda_gb300.so (built by __graft_entry__.build() or build.py)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"KDA CUDA library not built ({path} missing); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        lib = ctypes.CDLL(path)
+        vp, sp = ctypes.c_void_p, ctypes.POINTER(kda_shape)
+        lib.kda_chunk_fwd.restype = ctypes.c_int
+        lib.kda_chunk_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.kda_chunk_fwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_chunk_fwd_workspace_bytes.argtypes = [sp]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.kda_workspace_status.restype = ctypes.c_int
+        lib.kda_workspace_status.argtypes = [vp, vp]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_version.restype = ctypes.c_int
+        lib.kda_chunk_fwd_selected_algo.restype = ctypes.c_int
+        lib.kda_chunk_fwd_selected_algo.argtypes = [sp]
+        _lib = lib
+        return lib
+
+
+def kda_status_string(code: int) -> str:
+    return load_library().kda_status_string(int(code)).decode()
+
+
+def kda_version() -> int:
+    return int(load_library().kda_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _make_shape(num_seqs, total_tokens, H, dk, dv, scale, io, algo="auto"):
+    return kda_shape(int(num_seqs), int(total_tokens), int(H), int(dk), int(dv), 64,
+                     float(scale) if scale is not None else 0.0, io, _ALGOS[algo])
+
+
+def _check_io(name, t, shape, dtype, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def kda_chunk_fwd_workspace_bytes(num_seqs, total_tokens, num_heads, d_k, d_v, io_dtype=torch.bfloat16,
+                                  algo="auto") -> int:
+    shape = _make_shape(num_seqs, total_tokens, num_heads, d_k, d_v, None, _DTYPES[io_dtype], algo)
+    n = int(load_library().kda_chunk_fwd_workspace_bytes(ctypes.byref(shape)))
+    if n == 0:
+        raise KdaError(-2, "kda_chunk_fwd_workspace_bytes")
+    return n
+
+
+def kda_chunk_fwd_selected_algo(num_seqs, total_tokens, num_heads, d_k, d_v, io_dtype=torch.bfloat16,
+                                algo="auto") -> str:
+    """Which prefill kernel a call with these sizes runs: "tensor" or "simt"."""
+    shape = _make_shape(num_seqs, total_tokens, num_heads, d_k, d_v, None, _DTYPES[io_dtype], algo)
+    r = int(load_library().kda_chunk_fwd_selected_algo(ctypes.byref(shape)))
+    if r < 0:
+        raise KdaError(r, "kda_chunk_fwd_selected_algo")
+    return {1: "tensor", 2: "simt"}[r]
+
+
+def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, final_state=None,
+                  output_final_state=True, workspace=None, scale=None, algo="auto", stream=None,
+                  check=False):
+    """Chunkwise prefill over packed sequences (see include/kda.h).
+
+    q, k, g: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (one dtype: bf16 or fp32, CUDA);
+    cu_seqlens: int32 [N+1] (CUDA); init_state: fp32 [N, H, d_k, d_v] or None.
+    final_state may be the init_state tensor itself (in-place update).
+    Returns (out, final_state or None).  With check=True the call synchronises and
+    raises if a kernel recorded a device-side error in the workspace.
+    """
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_chunk_fwd runs on CUDA tensors only")
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, (T, H, dk)),
+                         ("v", v, (T, H, dv)), ("beta", beta, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    if init_state is not None:
+        _check_io("init_state", init_state, (N, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=dt, device=dev)
+    _check_io("out", out, (T, H, dv), dt, dev)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
+    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], algo)
+    lib = load_library()
+    need = int(lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib.kda_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                           _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd")
+    if check:
+        st = kda_workspace_status(workspace, stream)
+        if st != KDA_OK:
+            raise KdaError(st, "kda_chunk_fwd (device status)")
+    return out, final_state
+
+
+def kda_workspace_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the device status of the last
+    kda_chunk_fwd that used this workspace."""
+    return int(load_library().kda_workspace_status(_ptr(workspace), _stream(stream)))
+
+
+def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=None):
+    """One single-token step for N sequences: q, k, g [N, H, d_k]; v [N, H, d_v];
+    beta [N, H]; state fp32 [N, H, d_k, d_v] updated in place.  Returns out [N, H, d_v]."""
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    dev, dt = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("kda_decode_step runs on CUDA tensors only")
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)),
+                         ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("state", state, (N, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=dt, device=dev)
+    _check_io("out", out, (N, H, dv), dt, dev)
+    shape = _make_shape(N, N, H, dk, dv, scale, _DTYPES[dt])
+    rc = load_library().kda_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step")
+    return out

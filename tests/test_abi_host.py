@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads without a
+GPU, exports every function include/kda.h declares, and rejects bad arguments
+before touching the device.  No call here reaches a kernel: every call either
+fails validation or has nothing to do."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from kimi_delta_attention_fwd_gb300 import build as kbuild
+from kimi_delta_attention_fwd_gb300 import kda as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return K.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_bytes",
+                 "kda_workspace_status", "kda_status_string", "kda_version"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", kbuild.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kda_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_library_is_sm103a_only():
+    src = open(os.path.join(kbuild.PKG, "build.py")).read()
+    assert "arch=compute_103a,code=sm_103a" in src
+
+
+def _shape(**kw):
+    d = dict(num_seqs=2, total_tokens=128, num_heads=4, d_k=128, d_v=128, chunk_size=64, scale=0.0,
+             io_dtype=1, algo=0)
+    d.update(kw)
+    return K.kda_shape(**d)
+
+
+FAKE = 0x10000  # aligned fake device address: never dereferenced (validation fails first)
+
+
+def _chunk(lib, shape, ptr=FAKE, ws=FAKE, ws_bytes=None, init=None):
+    if ws_bytes is None:
+        ws_bytes = lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(shape))
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_chunk_fwd(ctypes.byref(shape), p, p, p, p, p, init, p, p, p,
+                             ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+
+def test_workspace_size(lib):
+    n = lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape()))
+    assert n >= 256 and n % 16 == 0
+    assert lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(d_k=96))) == 0
+    assert lib.kda_chunk_fwd_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("bad", [dict(d_k=96), dict(d_v=32), dict(num_heads=0), dict(num_seqs=-1),
+                                 dict(chunk_size=128), dict(io_dtype=5), dict(algo=9),
+                                 dict(total_tokens=-3)])
+def test_rejects_bad_shapes(lib, bad):
+    assert _chunk(lib, _shape(**bad)) == -2
+
+
+def test_rejects_null_and_small_workspace_and_misalignment(lib):
+    s = _shape()
+    assert lib.kda_chunk_fwd(None, None, None, None, None, None, None, None, None, None, None, 0,
+                             None) == -1
+    assert _chunk(lib, s, ptr=0) == -1                     # q == NULL with tokens > 0
+    assert _chunk(lib, s, ws=0) == -4                      # no workspace
+    assert _chunk(lib, s, ws_bytes=8) == -4                # too small
+    assert _chunk(lib, s, ptr=FAKE + 4) == -3              # misaligned tensors
+    assert _chunk(lib, s, ws=FAKE + 8) == -3               # misaligned workspace
+
+
+def test_decode_validation(lib):
+    s = _shape(total_tokens=2)
+    p = ctypes.c_void_p(FAKE)
+    assert lib.kda_decode_step(ctypes.byref(_shape(total_tokens=3)), p, p, p, p, p, p, p, None) == -2
+    assert lib.kda_decode_step(ctypes.byref(s), None, p, p, p, p, p, p, None) == -1
+    q = ctypes.c_void_p(FAKE + 2)
+    assert lib.kda_decode_step(ctypes.byref(s), q, p, p, p, p, p, p, None) == -3
+    # no sequences: nothing to do, nothing touched
+    assert lib.kda_decode_step(ctypes.byref(_shape(num_seqs=0, total_tokens=0)), None, None, None,
+                               None, None, None, None, None) == 0
+
+
+def test_status_strings(lib):
+    seen = set()
+    for code in range(0, -10, -1):
+        s = lib.kda_status_string(code).decode()
+        assert s and s != "unknown status"
+        seen.add(s)
+    assert len(seen) == 10
+    assert lib.kda_status_string(-99).decode() == "unknown status"
+    assert lib.kda_workspace_status(None, None) == -1
+    assert lib.kda_version() >= 1000
