@@ -15,11 +15,14 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; nothing is
  *     allocated, freed or retained by the library.  Calls are asynchronous on
  *     `stream` (0 = legacy default stream) and enqueue kernels only.
- *   - Tensors are contiguous, row-major, 16-byte aligned:
+ *   - Tensors are contiguous and row-major:
  *       q, k, g : [T_total, H, d_k]        v, out : [T_total, H, d_v]
  *       beta    : [T_total, H]             states : [N, H, d_k, d_v] fp32
  *       cu_seqlens : int32 [N + 1] (device), nondecreasing, cu[0] = 0,
  *                    cu[N] = T_total; sequence n owns tokens [cu[n], cu[n+1]).
+ *   - Alignment: states, workspace and (prefill) q, k, v, g, out start on a
+ *     16-byte boundary; beta and (decode) q, k, v, g on their element size;
+ *     cu_seqlens on 4 bytes; the decode output on 4 elements.
  *   - q, k, v, g, beta and out have the I/O dtype (fp32 or bf16); states are
  *     always fp32.  q and k are used as given (normalisation belongs to the
  *     caller).  g must be finite and <= 0.
@@ -42,7 +45,7 @@ enum {
   KDA_OK = 0,
   KDA_ERR_NULL = -1,           /* a required pointer is NULL */
   KDA_ERR_SHAPE = -2,          /* unsupported or inconsistent sizes */
-  KDA_ERR_ALIGN = -3,          /* a tensor pointer is not 16-byte aligned */
+  KDA_ERR_ALIGN = -3,          /* a pointer breaks the alignment stated below */
   KDA_ERR_WORKSPACE = -4,      /* workspace missing or too small */
   KDA_ERR_LAUNCH = -5,         /* CUDA rejected a launch or an async call */
   KDA_ERR_DEVICE = -6,         /* current device is not sm_103 or lacks a needed driver entry */

@@ -10,7 +10,10 @@
 
 namespace {
 
-bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void *p, uintptr_t bytes) {
+  return p == nullptr || (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
+}
+bool aligned16(const void *p) { return aligned(p, 16); }
 
 // Common shape checks; `decode` relaxes the chunk/algo fields.
 int check_shape(const kda_shape *s, bool decode) {
@@ -66,7 +69,7 @@ const char *kda_status_string(int status) {
     case KDA_OK: return "ok";
     case KDA_ERR_NULL: return "a required pointer is NULL";
     case KDA_ERR_SHAPE: return "unsupported or inconsistent sizes";
-    case KDA_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case KDA_ERR_ALIGN: return "a pointer is not aligned as the ABI requires";
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
     case KDA_ERR_LAUNCH: return "CUDA rejected a launch or an asynchronous call";
     case KDA_ERR_DEVICE: return "current device is not sm_103 or lacks a needed driver entry point";
@@ -101,8 +104,9 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
   if (s->num_seqs > 0 && !cu_seqlens) return KDA_ERR_NULL;
   if (!workspace) return KDA_ERR_WORKSPACE;
   if (workspace_bytes < kda_chunk_fwd_workspace_bytes(s)) return KDA_ERR_WORKSPACE;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
-      !aligned16(init_state) || !aligned16(cu_seqlens) || !aligned16(out) ||
+  const uintptr_t esz = s->io_dtype == KDA_BF16 ? 2 : 4;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned(beta, esz) ||
+      !aligned16(init_state) || !aligned(cu_seqlens, 4) || !aligned16(out) ||
       !aligned16(final_state) || !aligned16(workspace))
     return KDA_ERR_ALIGN;
   const bool tensor = use_tensor_path(s);
@@ -143,8 +147,9 @@ int kda_decode_step(const kda_shape *s, const void *q, const void *k, const void
   if (rc != KDA_OK) return rc;
   if (s->num_seqs == 0) return KDA_OK;
   if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
-      !aligned16(state) || !aligned16(out))
+  const uintptr_t esz = s->io_dtype == KDA_BF16 ? 2 : 4;
+  if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(g, esz) ||
+      !aligned(beta, esz) || !aligned16(state) || !aligned(out, 4 * esz))
     return KDA_ERR_ALIGN;
   rc = check_device(nullptr);
   if (rc != KDA_OK) return rc;

@@ -97,8 +97,11 @@ def test_decode_validation(lib):
     p = ctypes.c_void_p(FAKE)
     assert lib.kda_decode_step(ctypes.byref(_shape(total_tokens=3)), p, p, p, p, p, p, p, None) == -2
     assert lib.kda_decode_step(ctypes.byref(s), None, p, p, p, p, p, p, None) == -1
-    q = ctypes.c_void_p(FAKE + 2)
-    assert lib.kda_decode_step(ctypes.byref(s), q, p, p, p, p, p, p, None) == -3
+    odd = ctypes.c_void_p(FAKE + 1)
+    assert lib.kda_decode_step(ctypes.byref(s), odd, p, p, p, p, p, p, None) == -3  # q not 2-aligned
+    two = ctypes.c_void_p(FAKE + 2)
+    assert lib.kda_decode_step(ctypes.byref(s), p, p, p, p, p, two, p, None) == -3  # state not 16-aligned
+    assert lib.kda_decode_step(ctypes.byref(s), p, p, p, p, p, p, two, None) == -3  # out not 8-aligned
     # no sequences: nothing to do, nothing touched
     assert lib.kda_decode_step(ctypes.byref(_shape(num_seqs=0, total_tokens=0)), None, None, None,
                                None, None, None, None, None) == 0
