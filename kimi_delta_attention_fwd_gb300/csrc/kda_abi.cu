@@ -3,6 +3,7 @@
 #include <cuda_runtime_api.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "kda.h"
@@ -136,6 +137,10 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
   a.scratch = static_cast<unsigned char *>(workspace) + kda::kStatusBytes;
   a.scratch_bytes = workspace_bytes - kda::kStatusBytes;
   a.num_sms = num_sms;
+  // Test hook: KDA_TEST_FORCE_WAIT_TIMEOUT=1 makes the tensor-core kernel wait once on a
+  // barrier that nothing arrives on, so its bounded-wait error path can be exercised.
+  const char *force = getenv("KDA_TEST_FORCE_WAIT_TIMEOUT");
+  a.test_flags = (force && force[0] == '1') ? 1 : 0;
   const cudaError_t err = tensor ? kda::launch_chunk_tc(a, stream) : kda::launch_chunk_simt(a, stream);
   if (err == cudaErrorInvalidValue) return KDA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;

@@ -25,6 +25,7 @@ struct ChunkArgs {
   void *scratch;      // workspace after the status block
   size_t scratch_bytes;
   int num_sms;
+  int test_flags;     // bit 0: make the tensor-core kernel time out one wait (test hook)
 };
 
 struct DecodeArgs {
