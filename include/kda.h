@@ -51,7 +51,8 @@ enum {
   KDA_ERR_DEVICE = -6,         /* current device is not sm_103 or lacks a needed driver entry */
   KDA_ERR_DEVICE_TIMEOUT = -7, /* (device-reported) a bounded wait in a kernel gave up */
   KDA_ERR_GATE_RANGE = -8,     /* (device-reported) a chunk's decay exceeded the tensor-core path's range */
-  KDA_ERR_UNSUPPORTED = -9     /* the requested algorithm does not support this dtype or size */
+  KDA_ERR_UNSUPPORTED = -9,    /* the requested algorithm does not support this dtype or size */
+  KDA_ERR_NOALLOC_LIMIT = -10  /* the shape needs more scratch than kda_chunk_fwd_noalloc's built-in buffer */
 };
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -119,6 +120,30 @@ int kda_chunk_fwd_selected_algo(const kda_shape *shape);
 int kda_decode_step(const kda_shape *shape, const void *q, const void *k, const void *v,
                     const void *g, const void *beta, float *state, void *out,
                     cudaStream_t stream);
+
+/*
+ * kda_chunk_fwd for callers that cannot allocate device memory.  The method
+ * itself has no counterpart to this: it exists for callers that own only their
+ * input and output buffers (a host framework whose device memory is all
+ * reserved by its own allocator, a plug-in handed tensors but no allocator, or
+ * a latency-critical path where cudaMalloc, which can synchronise the device,
+ * is not acceptable).
+ *
+ * Same arguments and results as kda_chunk_fwd, without the workspace: the
+ * scratch comes from a 256 KiB buffer compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  Shapes whose
+ * kda_chunk_fwd_workspace_bytes() exceeds 256 KiB are rejected with
+ * KDA_ERR_NOALLOC_LIMIT.  Nothing is allocated or freed.  The first call on a
+ * device (made while that device is current) looks the buffer's address up,
+ * so make that first call before any stream capture.  All calls on one device
+ * share the buffer and it keeps the last call's contents (each call clears the
+ * status block it needs); calls whose kernels overlap on the GPU race on it, so
+ * order them on one stream.
+ */
+int kda_chunk_fwd_noalloc(const kda_shape *shape, const void *q, const void *k, const void *v,
+                          const void *g, const void *beta, const float *init_state,
+                          const int32_t *cu_seqlens, void *out, float *final_state,
+                          cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads the status block that the kernels of the

@@ -77,6 +77,7 @@ const char *kda_status_string(int status) {
     case KDA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up";
     case KDA_ERR_GATE_RANGE: return "a chunk's cumulative decay exceeded the tensor-core path's range";
     case KDA_ERR_UNSUPPORTED: return "the requested algorithm does not support this dtype or size";
+    case KDA_ERR_NOALLOC_LIMIT: return "the shape needs more scratch than the built-in no-allocation buffer";
     default: return "unknown status";
   }
 }

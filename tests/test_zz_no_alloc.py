@@ -1,0 +1,66 @@
+"""kda_chunk_fwd_noalloc: the prefill entry point for callers that cannot
+allocate device memory (they own only their inputs and outputs, e.g. a
+framework whose device memory is all reserved by its own allocator).  It takes
+its scratch from a buffer built into the library instead of a caller workspace.
+
+Called through the C ABI and compared with kda_chunk_fwd on the same inputs,
+twice in a row (the built-in buffer keeps the previous call's contents, so the
+second call checks that each call starts from a clean status block).  This file
+sorts last so that a run stopping at the first failure has run everything else.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from kimi_delta_attention_fwd_gb300 import build as kbuild
+from kimi_delta_attention_fwd_gb300 import kda as K
+from kimi_delta_attention_fwd_gb300 import kda_chunk_fwd
+from kimi_delta_attention_fwd_gb300 import workloads as W
+
+from parity import TOL_BF16, rel_l2_per_head, rel_l2_states, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(lib, d, out, fin):
+    T, H, dk = d["q"].shape
+    dv = d["v"].shape[2]
+    N = d["cu_seqlens"].shape[0] - 1
+    shape = K.kda_shape(N, T, H, dk, dv, 64, 0.0, K.KDA_BF16, 0)
+    p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    rc = lib.kda_chunk_fwd_noalloc(ctypes.byref(shape), p(d["q"]), p(d["k"]), p(d["v"]), p(d["g"]),
+                                   p(d["beta"]), p(d["init_state"]), p(d["cu_seqlens"]), p(out),
+                                   p(fin), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return rc
+
+
+def test_noalloc_matches_kda_chunk_fwd_on_two_calls():
+    kbuild.build()
+    lib = K.load_library()
+    lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(K.kda_shape)] + [ctypes.c_void_p] * 10
+    for seed, lens in ((51, [300, 1, 129]), (52, [64, 1000])):
+        x = W.prefill_inputs(W.custom_prefill(lens, num_heads=3, d=128, seed=seed))
+        d = to_dev(x)
+        ref_o, ref_f = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                     d["init_state"], check=True)
+        out = torch.full_like(ref_o, float("nan"))
+        fin = torch.full_like(ref_f, float("nan"))
+        assert _noalloc(lib, d, out, fin) == 0
+        torch.cuda.synchronize()
+        cu = x["cu_seqlens"].numpy()
+        assert rel_l2_per_head(out.float().cpu().numpy(), ref_o.float().cpu().numpy(), cu) <= TOL_BF16
+        assert rel_l2_states(fin.cpu().numpy(), ref_f.cpu().numpy()) <= TOL_BF16
+        assert np.isfinite(out.float().cpu().numpy()).all()
+
+
+def test_noalloc_rejects_bad_shapes_without_launching():
+    kbuild.build()
+    lib = K.load_library()
+    lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(K.kda_shape)] + [ctypes.c_void_p] * 10
+    bad = K.kda_shape(1, 64, 1, 96, 128, 64, 0.0, K.KDA_BF16, 0)
+    assert lib.kda_chunk_fwd_noalloc(ctypes.byref(bad), *([None] * 10)) == -2
+    assert lib.kda_chunk_fwd_noalloc(None, *([None] * 10)) == -1
