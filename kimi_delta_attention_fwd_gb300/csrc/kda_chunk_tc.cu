@@ -3,29 +3,28 @@
 // The chunk algebra is the chunkwise schedule of "Kimi Delta Attention (KDA)"
 // (brain.bigb.es, section on the two schedules) in the WY / UT form of the
 // chunked DeltaNet section of "22580: от GPT-2 до Kimi K3", for the d_k x d_v
-// state layout.  For a chunk of C = 64 rows with incoming state S and
-// G = chunk-local inclusive cumsum of g (per key channel), Gl = G of the last row:
+// state layout.  For a chunk of C = 64 rows with incoming state S, G = the
+// chunk-local inclusive cumsum of g (per key channel) and gamma = exp(G_last):
 //
-//   Kb   = K * exp(G - Gl)     Qb = Q * exp(G - Gl)     Kend = K * exp(Gl - G)
-//   [Kb; Qb] Kend^T            -> rows: A^kk / beta_i (j < i), A^qk (j <= i)
-//   T    = (I + A^kk)^-1,  Tb = T diag(beta)           (fp32 triangular solve)
-//   Pb   = A^qk Tb
-//   [Tb; Pb] [Kb | V]          -> Wbar = Tb Kb, U = Tb V; Pb Kb, O_intra = Pb V
-//   W    = Wbar diag(e^Gl)     Q' = (Qb - Pb Kb) diag(e^Gl)
-//   [E; O/s] = [U; O_intra] + [-W; Q'] S                (state-dependent)
-//   S   <- diag(e^Gl) S + Kend^T E                       (state-dependent)
+//   Kh  = K * exp(G)     Qh = Q * exp(G)     Kc = K * exp(-G)
+//   [Kh; Qh] Kc^T              -> rows: A^kk / beta_i (j < i), A^qk (j <= i)
+//   T   = (I + A^kk)^-1,  Tb = T diag(beta)            (fp32 triangular solve)
+//   Pb  = A^qk Tb
+//   [Tb; Pb] [Kh | V]          -> W = Tb Kh, U = Tb V; A^qk W, O_intra = Pb V
+//   [E; O/s] = [U; O_intra] + [-W; Qh - A^qk W] S      (state-dependent)
+//   S  <- gamma * S + gamma * (Kc^T E)                  (state-dependent)
 //
-// Anchoring the decay at the chunk end keeps every factor finite as long as a
-// chunk's total log decay per channel stays above -80 (checked; beyond it the
-// call reports KDA_ERR_GATE_RANGE).  The products use bf16 operands with fp32
-// accumulation in tensor memory; the state, the cumsum and the solve are fp32.
+// exp(G) <= 1 and exp(-G) <= exp(-G_last); every factor stays finite as long
+// as a chunk's total log decay per channel is above -80 (checked; beyond it
+// the call reports KDA_ERR_GATE_RANGE).  The products use bf16 operands with
+// fp32 accumulation in tensor memory; the state, the cumsum and the solve are fp32.
 //
 // One CTA owns (sequence, head, 64-column d_v tile) and walks its chunks in
 // order.  Warp roles:
-//   warps 0-3  K-side: everything that does not depend on S, one chunk ahead
-//   warps 4-7  S-side: holds S (fp32, one key channel per thread) in registers
-//              and runs the two state-dependent products per chunk
-//   warp  8    TMA producer (q, k, g, v boxes into a 2-stage ring) and TMEM owner
+//   warps 0-7   K-side: everything that does not depend on S, one chunk ahead
+//   warps 8-11  S-side: holds S (fp32, one key channel per thread) in registers
+//               and runs the two state-dependent products per chunk
+//   warp  12    TMA producer (q, k, g, v boxes into a 2-stage ring) and TMEM owner
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // KDA_ERR_DEVICE_TIMEOUT in the status word and runs to completion without
 // waiting again (outputs are then undefined, nothing blocks or faults).
@@ -48,32 +47,33 @@ constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr int BV = 64;                      // d_v columns per CTA
-constexpr int kThreads = 288;
+constexpr int kThreads = 416;  // 8 K-side warps, 4 S-side warps, 1 producer warp
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinChunkLogDecay = -80.f;
 constexpr uint32_t kStatusTimeout = 7;      // -KDA_ERR_DEVICE_TIMEOUT
 constexpr uint32_t kStatusGateRange = 8;    // -KDA_ERR_GATE_RANGE
+constexpr int kLd = 68;                     // row stride (floats) of the fp32 64 x 64 matrices
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 struct L {
   // stage: [k ch0-63 | q ch0-63] [k ch64-127 | q ch64-127] [g ch0-63] [g ch64-127] [v tile]
   static constexpr uint32_t kKQ1 = 16384, kQoff = 8192, kG = 32768, kV = 49152;
   static constexpr uint32_t kStageBytes = 49152 + C * BV * 2;
-  static constexpr uint32_t kKend = 2 * kStageBytes;          // 2 x [ch0-63 | ch64-127]
-  static constexpr uint32_t kTP = kKend + 2 * 16384;          // [Tb rows 0-63 | A^qk / Pb rows 64-127]
+  static constexpr uint32_t kKc = 2 * kStageBytes;          // 2 x Kc [ch0-63 | ch64-127]
+  static constexpr uint32_t kTP = kKc + 2 * 16384;          // [Tb rows 0-63 | A^qk / Pb rows 64-127]
   static constexpr uint32_t kSb = kTP + 16384;                // S in bf16, [DK rows][BV]
   static constexpr uint32_t kEb = kSb + DK * BV * 2;          // E in bf16, [C rows][BV]
-  static constexpr uint32_t kAf = kEb + C * BV * 2;           // fp32 A^kk [64][65]
-  static constexpr uint32_t kTf = kAf + 64 * 65 * 4;          // fp32 T [64][65]
-  static constexpr uint32_t kBeta = kTf + 64 * 65 * 4;        // fp32 beta [64]
+  static constexpr uint32_t kAf = kEb + C * BV * 2;           // fp32 A^kk [64][kLd]
+  static constexpr uint32_t kTf = kAf + 64 * 68 * 4;          // fp32 T [64][kLd]
+  static constexpr uint32_t kBeta = kTf + 64 * 68 * 4;        // fp32 beta [64]
   static constexpr uint32_t kGamma = kBeta + 256;             // fp32 e^Gl [2][128]
   static constexpr uint32_t kBars = kGamma + 1024;            // mbarriers
   static constexpr uint32_t kMisc = kBars + 128;              // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
-static_assert(L::kKend % 1024 == 0 && L::kTP % 1024 == 0 && L::kSb % 1024 == 0 &&
+static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kSb % 1024 == 0 &&
                   L::kEb % 1024 == 0 && L::kAf % 1024 == 0,
               "operand tiles must be 1024-byte aligned");
 static_assert(L::kAlloc <= 232448, "shared memory budget");
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(ctx.bar(i), 1);
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if ((tid & 31) == 0) {
       tma_prefetch_desc(&tm_q);
@@ -206,10 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < 2; ++s)
         if (issued[s] >= 0) mbar_wait(ctx.bar(kFull0 + s), (issued[s] >> 1) & 1, kWaitCycles);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ K-side
-    const int t = tid;  // 0..127
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    const int t = tid;                  // 0..255
+    const int wq = warp & 3;            // TMEM lane quarter of this warp
+    const int wh = warp >> 2;           // which half of the columns this warp reads
+    const int row = 32 * wq + (t & 31); // TMEM lane = row of an M = 128 result
+    const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
     if ((p.flags & 1) && t == 0) {
       // test hook: a wait that can only time out
       if (!mbar_wait(ctx.bar(kNever), 0, 2000000LL)) {
@@ -218,26 +221,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     uint32_t kph = 0;
-    const int cg = t & 15, half = cg >> 3, ck = cg & 7, rg = t >> 4;
+    // gate layout: a warp holds all 16 row groups (4 rows each) of two 8-channel groups,
+    // so the cumulative sum across row groups is a 16-lane shuffle scan
+    const int rg = t & 15, cg = 2 * warp + ((t >> 4) & 1), half = cg >> 3, ck = cg & 7;
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1;
       const int t0 = bos + c * C;
       const int len = min(C, eos - t0);
       const uint32_t st = sbase + s * L::kStageBytes;
-      const uint32_t kend = sbase + L::kKend + s * 16384;
-      if (c >= 2) ctx.wait(kDone0 + s, ((c >> 1) - 1) & 1);  // Kend[s], ACC[s], gamma[s] free
-      ctx.wait(kFull0 + s, (c >> 1) & 1);
-      if (t < C) betas[t] = t < len ? __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]) : 0.f;
+      const uint32_t kc = sbase + L::kKc + s * 16384;
+      float bnext = 0.f;  // beta of this chunk, loaded early to hide the global latency
+      if (t < C && t < len) bnext = __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]);
+      // one thread polls the mbarriers, the others park on the named barrier
+      if (t == 0) {
+        if (c >= 2) ctx.wait(kDone0 + s, ((c >> 1) - 1) & 1);  // Kc[s], ACC[s], gamma[s] free
+        ctx.wait(kFull0 + s, (c >> 1) & 1);
+      }
+      bar_sync(1, 256);
 
-      // a1: chunk-local cumulative log decay, 8 rows x 8 channels per thread
+      // a1: chunk-local cumulative log decay, 4 rows x 8 channels per thread
       const uint32_t kq = st + half * L::kKQ1;
       const uint32_t ga = st + L::kG + half * 8192;
-      float gl[8][8], run[8];
+      float gl[4][8], run[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) run[j] = 0.f;
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int r = rg * 8 + rr;
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = rg * 4 + rr;
         float gv[8];
         unpack8(ld_shared_v4(ga + sw128(r, ck)), gv);
         const bool valid = r < len;
@@ -247,40 +257,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           gl[rr][j] = run[j];
         }
       }
-      float *part = Af;  // [8][128] partial sums (Af is free here)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) part[rg * 128 + cg * 8 + j] = run[j];
-      bar_sync(1, 128);
       float pre[8], tot[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) pre[j] = tot[j] = 0.f;
+      for (int j = 0; j < 8; ++j) {
+        float v = run[j];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float v = part[q * 128 + cg * 8 + j];
-          if (q < rg) pre[j] += v;
-          tot[j] += v;
+        for (int d = 1; d < 16; d <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, v, d, 16);
+          if (rg >= d) v += u;
         }
+        pre[j] = v - run[j];                            // exclusive prefix over row groups
+        tot[j] = __shfl_sync(0xffffffffu, v, 15, 16);   // whole chunk
       }
       if (rg == 0) {
         bool bad = false;
+        float gm[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          gamma[s * 128 + cg * 8 + j] = fast_exp2(tot[j] * kLog2e);
+          gm[j] = fast_exp2(tot[j] * kLog2e);
           bad |= !(tot[j] >= kMinChunkLogDecay);
         }
+        *reinterpret_cast<float4 *>(gamma + s * 128 + cg * 8) = make_float4(gm[0], gm[1], gm[2], gm[3]);
+        *reinterpret_cast<float4 *>(gamma + s * 128 + cg * 8 + 4) = make_float4(gm[4], gm[5], gm[6], gm[7]);
         if (bad) atomicCAS(p.status, 0u, kStatusGateRange);
       }
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int r = rg * 8 + rr;
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = rg * 4 + rr;
         float kv[8], qv[8], f[8], fe[8];
         unpack8(ld_shared_v4(kq + sw128(r, ck)), kv);
         unpack8(ld_shared_v4(kq + L::kQoff + sw128(r, ck)), qv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float d = (pre[j] + gl[rr][j] - tot[j]) * kLog2e;  // (G - Gl) log2 e <= 0
+          const float d = (pre[j] + gl[rr][j]) * kLog2e;  // G log2 e, in [Gl log2 e, 0]
           f[j] = fast_exp2(d);
           fe[j] = fast_exp2(-d);
         }
@@ -293,121 +302,156 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         st8(kq + sw128(r, ck), kb);
         st8(kq + L::kQoff + sw128(r, ck), qb);
-        st8(kend + half * 8192 + sw128(r, ck), ke);
+        st8(kc + half * 8192 + sw128(r, ck), ke);
       }
+      if (t < C) betas[t] = bnext;
       fence_async_smem();
-      bar_sync(1, 128);
+      bar_sync(1, 256);
 
-      // a2: [Kb; Qb] Kend^T -> D1 (rows 0-63: K^kk, rows 64-127: A^qk)
+      // a2: [Kh; Qh] Kc^T -> D1 (rows 0-63: A^kk / beta, rows 64-127: A^qk)
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, 64, false, false);
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8) {
           const uint64_t ad = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kend + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kc + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
           mma_bf16(tmem + kD1, ad, bd, id, k8 > 0);
         }
         mma_commit(ctx.bar(kMmaK));
       }
-      ctx.wait(kMmaK, kph++ & 1);
+      if (t == 0) ctx.wait(kMmaK, kph & 1);
+      ++kph;
+      bar_sync(1, 256);
       tc_fence_after();
-      {
+      {  // each warp reads 32 of the 64 columns of its 32 rows
         float a[32];
-        if (t < 64) {
-          const float bi = betas[t];
+        tmem_ld32(tmem + lane_base + kD1 + 32 * wh, a);
+        if (row < 64) {  // A^kk row (beta_row, strictly lower) -> fp32 Af
+          const float bi = betas[row];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            tmem_ld32(tmem + lane_base + kD1 + 32 * hh, a);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int j = 32 * hh + jj;
-              Af[t * 65 + j] = j < t ? bi * a[jj] : 0.f;
-            }
+          for (int q = 0; q < 8; ++q) {
+            const int j = 32 * wh + 4 * q;
+            float4 v;
+            v.x = j + 0 < row ? bi * a[4 * q + 0] : 0.f;
+            v.y = j + 1 < row ? bi * a[4 * q + 1] : 0.f;
+            v.z = j + 2 < row ? bi * a[4 * q + 2] : 0.f;
+            v.w = j + 3 < row ? bi * a[4 * q + 3] : 0.f;
+            *reinterpret_cast<float4 *>(Af + row * kLd + j) = v;
           }
-        } else {
-          const int i = t - 64;
+        } else {  // A^qk row (lower, diagonal included) -> bf16 TP rows 64-127
+          const int i = row - 64;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            tmem_ld32(tmem + lane_base + kD1 + 32 * hh, a);
+          for (int q = 0; q < 4; ++q) {
+            float v[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float v[8];
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                const int j = 32 * hh + 8 * q + jj;
-                v[jj] = j <= i ? a[8 * q + jj] : 0.f;
-              }
-              st8(sbase + L::kTP + sw128(64 + i, 4 * hh + q), v);
+            for (int jj = 0; jj < 8; ++jj) {
+              const int j = 32 * wh + 8 * q + jj;
+              v[jj] = j <= i ? a[8 * q + jj] : 0.f;
             }
+            st8(sbase + L::kTP + sw128(row, 4 * wh + q), v);
           }
+        }
+        if (t >= 128) {  // the two zero blocks above the diagonal that the 32-wide products read
+          const int i = t - 128, zr = i >> 2, zc = (i & 3) * 4;
+          if (i < 64)
+            *reinterpret_cast<float4 *>(Tf + zr * kLd + 16 + zc) = make_float4(0.f, 0.f, 0.f, 0.f);
+          else
+            *reinterpret_cast<float4 *>(Tf + (32 + zr - 16) * kLd + 48 + zc) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       tc_fence_before();
-      bar_sync(1, 128);
+      bar_sync(1, 256);
 
-      // a3: T = (I + A^kk)^-1, 16 x 16 diagonal blocks by forward substitution,
-      // then the off-diagonal blocks by block diagonals:
-      //   T_IJ = -T_II sum_{J <= K < I} A_IK T_KJ
+      // a3: T = (I + A^kk)^-1 by recursive doubling of the block inverse
+      //   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
+      // 16 x 16 diagonal blocks first (right-looking substitution, one column
+      // per thread), then the 16-wide and the 32-wide off-diagonal blocks.
       if (t < 64) {
         const int I = t >> 4, cc = t & 15;
-        const float *Ab = Af + (16 * I) * 65 + 16 * I;
-        float x[16];
+        const float *Ab = Af + (16 * I) * kLd + 16 * I;
+        float x[16], acc[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = r == cc ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-        for (int r = 1; r < 16; ++r) {
-          float acc = 0.f;
+        for (int m = 0; m < 16; ++m) {
+          x[m] = m == cc ? 1.f : (m > cc ? -acc[m] : 0.f);
 #pragma unroll
-          for (int m = 0; m < r; ++m) acc = fmaf(Ab[r * 65 + m], x[m], acc);
-          if (r > cc) x[r] = -acc;
+          for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(Ab[r * kLd + m], x[m], acc[r]);
         }
-        float *Tb = Tf + (16 * I) * 65 + 16 * I + cc;
+        float *Tb = Tf + (16 * I) * kLd + 16 * I + cc;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[r * 65] = x[r];
+        for (int r = 0; r < 16; ++r) Tb[r * kLd] = x[r];
       }
-      bar_sync(1, 128);
-      float *Ys = reinterpret_cast<float *>(smem + (ga - sbase) - half * 8192);  // stage g area
-      for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;
-        for (int e = t; e < nb * 256; e += 128) {
-          const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-          const int I = d + b, J = b;
-          const float *arow = Af + (16 * I + r) * 65;
-          float acc = 0.f;
-          for (int K = J; K < I; ++K) {
+      bar_sync(1, 256);
+      float *Ys = reinterpret_cast<float *>(smem + L::kTP);  // TP rows 0-63 are free until Tb
+      {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y; 2 columns each
+        const int b = t >> 7, r = (t >> 3) & 15, c2 = (t & 7) * 2;
+        const int r0 = 32 * b + 16, c0 = 32 * b;
+        float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-              acc = fmaf(arow[16 * K + m], Tf[(16 * K + m) * 65 + 16 * J + cc], acc);
-          }
-          Ys[(b * 16 + r) * 17 + cc] = acc;
+        for (int k = 0; k < 16; ++k) {
+          const float av = Af[(r0 + r) * kLd + c0 + k];
+          const float2 tv = *reinterpret_cast<const float2 *>(Tf + (c0 + k) * kLd + c0 + c2);
+          y0 = fmaf(av, tv.x, y0);
+          y1 = fmaf(av, tv.y, y1);
         }
-        bar_sync(1, 128);
-        for (int e = t; e < nb * 256; e += 128) {
-          const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-          const int I = d + b, J = b;
-          const float *trow = Tf + (16 * I + r) * 65 + 16 * I;
-          float acc = 0.f;
-          for (int m = 0; m <= r; ++m) acc = fmaf(trow[m], Ys[(b * 16 + m) * 17 + cc], acc);
-          Tf[(16 * I + r) * 65 + 16 * J + cc] = -acc;
+        *reinterpret_cast<float2 *>(Ys + (b * 16 + r) * 20 + c2) = make_float2(y0, y1);
+        bar_sync(1, 256);
+        float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float tv = Tf[(r0 + r) * kLd + r0 + k];
+          const float2 yv = *reinterpret_cast<const float2 *>(Ys + (b * 16 + k) * 20 + c2);
+          z0 = fmaf(tv, yv.x, z0);
+          z1 = fmaf(tv, yv.y, z1);
         }
-        bar_sync(1, 128);
+        *reinterpret_cast<float2 *>(Tf + (r0 + r) * kLd + c0 + c2) = make_float2(-z0, -z1);
       }
-      {  // Tb = T diag(beta) -> TP rows 0-63
-        const int i = t & 63, hh = t >> 6;
+      bar_sync(1, 256);
+      {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
+        const int rr = t >> 3, c4 = (t & 7) * 4;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int k = 0; k < 32; ++k) {
+          const float av = Af[(32 + rr) * kLd + k];
+          const float4 tv = *reinterpret_cast<const float4 *>(Tf + k * kLd + c4);
+          y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
+          y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
+        }
+        *reinterpret_cast<float4 *>(Ys + rr * 36 + c4) = y;
+        bar_sync(1, 256);
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float tv = Tf[(32 + rr) * kLd + 32 + k];
+          const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + c4);
+          z.x = fmaf(tv, yv.x, z.x); z.y = fmaf(tv, yv.y, z.y);
+          z.z = fmaf(tv, yv.z, z.z); z.w = fmaf(tv, yv.w, z.w);
+        }
+        *reinterpret_cast<float4 *>(Tf + (32 + rr) * kLd + c4) = make_float4(-z.x, -z.y, -z.z, -z.w);
+      }
+      bar_sync(1, 256);
+      {  // Tb = T diag(beta) -> TP rows 0-63, 16 columns per thread
+        const int i = t & 63, qq = t >> 6;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int j0 = 16 * qq + 8 * q;
+          const float4 t0v = *reinterpret_cast<const float4 *>(Tf + i * kLd + j0);
+          const float4 t1v = *reinterpret_cast<const float4 *>(Tf + i * kLd + j0 + 4);
+          const float4 b0 = *reinterpret_cast<const float4 *>(betas + j0);
+          const float4 b1 = *reinterpret_cast<const float4 *>(betas + j0 + 4);
+          const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+          const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
           float v[8];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = 32 * hh + 8 * q + jj;
-            v[jj] = j <= i ? Tf[i * 65 + j] * betas[j] : 0.f;
-          }
-          st8(sbase + L::kTP + sw128(i, 4 * hh + q), v);
+          for (int jj = 0; jj < 8; ++jj) v[jj] = j0 + jj <= i ? tv[jj] * bv[jj] : 0.f;
+          st8(sbase + L::kTP + sw128(i, 2 * qq + q), v);
         }
       }
       fence_async_smem();
-      bar_sync(1, 128);
+      bar_sync(1, 256);
 
       // Pb = A^qk Tb  (M = 128 with Tb stacked on top; rows 64-127 are used)
       if (t == 0) {
@@ -421,28 +465,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(ctx.bar(kMmaK));
       }
-      ctx.wait(kMmaK, kph++ & 1);
+      if (t == 0) ctx.wait(kMmaK, kph & 1);
+      ++kph;
+      bar_sync(1, 256);
       tc_fence_after();
-      if (t >= 64) {
-        const int i = t - 64;
+      if (row >= 64) {
         float a[32];
+        tmem_ld32(tmem + lane_base + kDP + 32 * wh, a);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          tmem_ld32(tmem + lane_base + kDP + 32 * hh, a);
+        for (int q = 0; q < 4; ++q) {
+          float v[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float v[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) v[jj] = a[8 * q + jj];
-            st8(sbase + L::kTP + sw128(64 + i, 4 * hh + q), v);
-          }
+          for (int jj = 0; jj < 8; ++jj) v[jj] = a[8 * q + jj];
+          st8(sbase + L::kTP + sw128(row, 4 * wh + q), v);
         }
       }
       fence_async_smem();
       tc_fence_before();
-      bar_sync(1, 128);
+      bar_sync(1, 256);
 
-      // [Tb; Pb] [Kb | V] -> D2 (Wbar | Pb Kb) and ACC[s] (U | O_intra)
+      // [Tb; Pb] [Kh | V] -> D2 (W | A^qk W) and ACC[s] (U | O_intra)
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
@@ -457,29 +499,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(ctx.bar(kMmaK));
       }
-      ctx.wait(kMmaK, kph++ & 1);
+      if (t == 0) ctx.wait(kMmaK, kph & 1);
+      ++kph;
+      bar_sync(1, 256);
       tc_fence_after();
-      {  // -W -> over Kb, Q' -> over Qb (the A operand of the state product)
-        const int i = t & 63;
-        const uint32_t qoff = t < 64 ? 0u : L::kQoff;
-        float a[32];
+      {  // -W over Kh, Qh - A^qk W over Qh (the A operand of the state product); 64 channels each
+        const int i = row & 63;
+        const uint32_t qoff = row < 64 ? 0u : L::kQoff;
+        const uint32_t base = st + wh * L::kKQ1 + qoff;  // channels 64 wh .. 64 wh + 63
 #pragma unroll
-        for (int cc4 = 0; cc4 < 4; ++cc4) {
-          tmem_ld32(tmem + lane_base + kD2 + 32 * cc4, a);
+        for (int hh = 0; hh < 2; ++hh) {
+          float a[32];
+          tmem_ld32(tmem + lane_base + kD2 + 64 * wh + 32 * hh, a);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int ch0 = 32 * cc4 + 8 * q;
-            const uint32_t addr = st + (ch0 >> 6) * L::kKQ1 + qoff + sw128(i, (ch0 & 63) >> 3);
+            const int chl = 32 * hh + 8 * q;  // channel within the 64-channel half
+            const uint32_t addr = base + sw128(i, chl >> 3);
             float v[8];
-            if (t < 64) {
+            if (row < 64) {
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) v[jj] = -a[8 * q + jj] * gamma[s * 128 + ch0 + jj];
+              for (int jj = 0; jj < 8; ++jj) v[jj] = -a[8 * q + jj];
             } else {
               float qb[8];
               unpack8(ld_shared_v4(addr), qb);
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj)
-                v[jj] = (qb[jj] - a[8 * q + jj]) * gamma[s * 128 + ch0 + jj];
+              for (int jj = 0; jj < 8; ++jj) v[jj] = qb[jj] - a[8 * q + jj];
             }
             st8(addr, v);
           }
@@ -487,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       tc_fence_before();
-      bar_sync(1, 128);
+      bar_sync(1, 256);
       if (t == 0) mbar_arrive(ctx.bar(kReady0 + s));
     }
     if (t == 0) {  // all K-side MMAs retired before TMEM is released
@@ -496,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ S-side
-    const int t = tid - 128;  // key channel of the state row this thread holds
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp - 4)) << 16;
+    const int t = tid - 256;  // key channel of the state row this thread holds
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp - 8)) << 16;
     const size_t soff = (size_t)pair * DK * DV + (size_t)t * DV + tile * BV;
     float S[BV];
     if (p.init_state) {
@@ -525,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       bar_sync(2, 128);
-      ctx.wait(kReady0 + s, (c >> 1) & 1);
+      if (t == 0) ctx.wait(kReady0 + s, (c >> 1) & 1);
+      bar_sync(2, 128);
       tc_fence_after();
       // a4/a5: [U; O_intra] += [-W; Q'] S
       if (t == 0) {
@@ -539,7 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(ctx.bar(kMmaS));
         mma_commit(ctx.bar(kEmpty0 + s));  // the stage may be refilled once this retires
       }
-      ctx.wait(kMmaS, sph++ & 1);
+      if (t == 0) ctx.wait(kMmaS, sph & 1);
+      ++sph;
+      bar_sync(2, 128);
       tc_fence_after();
       {
         float a[32];
@@ -576,20 +623,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       tc_fence_before();
       bar_sync(2, 128);
-      // a4: Kend^T E -> D4
+      // a4: Kc^T E -> D4
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, BV, true, true);
-        const uint32_t kend = sbase + L::kKend + s * 16384;
+        const uint32_t kc = sbase + L::kKc + s * 16384;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(kend + k4 * 2048, 8192, 1024);
+          const uint64_t ad = sdesc_sw128(kc + k4 * 2048, 8192, 1024);
           const uint64_t bd = sdesc_sw128(sbase + L::kEb + k4 * 2048, 8192, 1024);
           mma_bf16(tmem + kD4, ad, bd, id, k4 > 0);
         }
         mma_commit(ctx.bar(kMmaS));
       }
-      ctx.wait(kMmaS, sph++ & 1);
+      if (t == 0) ctx.wait(kMmaS, sph & 1);
+      ++sph;
+      bar_sync(2, 128);
       tc_fence_after();
       {
         const float gm = gamma[s * 128 + t];
@@ -598,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < BV / 32; ++hh) {
           tmem_ld32(tmem + lane_base + kD4 + 32 * hh, a);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) S[32 * hh + jj] = fmaf(gm, S[32 * hh + jj], a[jj]);
+          for (int jj = 0; jj < 32; ++jj) S[32 * hh + jj] = fmaf(gm, S[32 * hh + jj], gm * a[jj]);
         }
       }
       tc_fence_before();
@@ -619,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
