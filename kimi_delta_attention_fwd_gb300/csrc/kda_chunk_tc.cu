@@ -53,39 +53,45 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinChunkLogDecay = -80.f;
 constexpr uint32_t kStatusTimeout = 7;      // -KDA_ERR_DEVICE_TIMEOUT
 constexpr uint32_t kStatusGateRange = 8;    // -KDA_ERR_GATE_RANGE
-constexpr int kLd = 68;                     // row stride (floats) of the fp32 64 x 64 matrices
+
+// fp32 64 x 64 matrix in 16 KB: 16-byte chunks of each row XOR-swizzled by the
+// row, so that row-wise, column-wise and float4 accesses are all conflict-free.
+__device__ __forceinline__ int af_idx(int i, int j) {
+  return i * 64 + ((((j >> 2) ^ i) & 15) << 2) + (j & 3);
+}
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 struct L {
-  // stage: [k ch0-63 | q ch0-63] [k ch64-127 | q ch64-127] [g ch0-63] [g ch64-127] [v tile]
+  // stage: [k ch0-63 | q ch0-63] [k ch64-127 | q ch64-127] [g ch0-63] [g ch64-127] [v tile];
+  // the g area later holds the fp32 A^kk / T (64 x 64, af_idx layout)
   static constexpr uint32_t kKQ1 = 16384, kQoff = 8192, kG = 32768, kV = 49152;
   static constexpr uint32_t kStageBytes = 49152 + C * BV * 2;
   static constexpr uint32_t kKc = 2 * kStageBytes;          // 2 x Kc [ch0-63 | ch64-127]
-  static constexpr uint32_t kTP = kKc + 2 * 16384;          // [Tb rows 0-63 | A^qk / Pb rows 64-127]
-  static constexpr uint32_t kSb = kTP + 16384;                // S in bf16, [DK rows][BV]
+  static constexpr uint32_t kTP = kKc + 2 * 16384;            // 2 x [Tb rows 0-63 | A^qk / Pb rows 64-127]
+  static constexpr uint32_t kSb = kTP + 2 * 16384;            // S in bf16, [DK rows][BV]
   static constexpr uint32_t kEb = kSb + DK * BV * 2;          // E in bf16, [C rows][BV]
-  static constexpr uint32_t kAf = kEb + C * BV * 2;           // fp32 A^kk [64][kLd]
-  static constexpr uint32_t kTf = kAf + 64 * 68 * 4;          // fp32 T [64][kLd]
-  static constexpr uint32_t kBeta = kTf + 64 * 68 * 4;        // fp32 beta [64]
-  static constexpr uint32_t kGamma = kBeta + 256;             // fp32 e^Gl [2][128]
+  static constexpr uint32_t kLtri = kEb + C * BV * 2;         // bf16 [Ltri; Ltri], 128 x 64
+  static constexpr uint32_t kBeta = kLtri + 16384;            // fp32 beta [2][64]
+  static constexpr uint32_t kGamma = kBeta + 512;             // fp32 e^Gl [2][128]
   static constexpr uint32_t kBars = kGamma + 1024;            // mbarriers
   static constexpr uint32_t kMisc = kBars + 128;              // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
 static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kSb % 1024 == 0 &&
-                  L::kEb % 1024 == 0 && L::kAf % 1024 == 0,
+                  L::kEb % 1024 == 0 && L::kLtri % 1024 == 0,
               "operand tiles must be 1024-byte aligned");
 static_assert(L::kAlloc <= 232448, "shared memory budget");
 
 // mbarrier slots
 enum : uint32_t {
-  kFull0 = 0, kEmpty0 = 2, kReady0 = 4, kDone0 = 6, kMmaK = 8, kMmaS = 9, kFinK = 10, kFinS = 11,
-  kNever = 12, kNumBars = 13
+  kFull0 = 0, kEmpty0 = 2, kReady0 = 4, kDone0 = 6, kMmaK0 = 8, kMmaS = 10, kFinK0 = 11, kFinS = 13,
+  kNever = 14, kNumBars = 15
 };
 
 // TMEM columns
-constexpr uint32_t kD1 = 0, kDP = 64, kD2 = 128, kAcc0 = 256, kD4 = 256 + 2 * BV;
+// K-side group kw: [128 kw, 128 kw + 128) holds G, then D1 (+0) and DP (+64), then D2.
+constexpr uint32_t kAcc0 = 256, kD4 = 256 + 2 * BV;
 
 struct TcParams {
   const __nv_bfloat16 *beta;
@@ -144,9 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  float *Af = reinterpret_cast<float *>(smem + L::kAf);
-  float *Tf = reinterpret_cast<float *>(smem + L::kTf);
-  float *betas = reinterpret_cast<float *>(smem + L::kBeta);
+  float *betas_all = reinterpret_cast<float *>(smem + L::kBeta);
   float *gamma = reinterpret_cast<float *>(smem + L::kGamma);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
@@ -172,6 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  // constant A operand of the cumsum product: [Ltri; Ltri], Ltri[r][u] = (u <= r), bf16
+  for (int idx = tid; idx < 128 * 8; idx += kThreads) {
+    const int r = idx >> 3, ch = idx & 7, r64 = r & 63;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int lo = 8 * ch + 2 * i;
+      w[i] = (lo <= r64 ? 0x3F80u : 0u) | ((lo + 1 <= r64 ? 0x3F80u : 0u) << 16);
+    }
+    st_shared_v4(sbase + L::kLtri + sw128(r, ch), w[0], w[1], w[2], w[3]);
+  }
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -208,12 +224,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ K-side
-    const int t = tid;                  // 0..255
+    // Two groups of 4 warps; group kw takes the chunks c = kw, kw + 2, ... and
+    // owns stage kw, Kc[kw], TP[kw], beta[kw] and TMEM columns [128 kw, 128 kw + 128),
+    // so the dependent chain of one chunk overlaps the other group's chunk.
+    const int kw = warp >> 2;
+    const int t = tid & 127;            // thread within the group
     const int wq = warp & 3;            // TMEM lane quarter of this warp
-    const int wh = warp >> 2;           // which half of the columns this warp reads
     const int row = 32 * wq + (t & 31); // TMEM lane = row of an M = 128 result
     const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
-    if ((p.flags & 1) && t == 0) {
+    const uint32_t bar_id = kw ? 3u : 1u;
+    const uint32_t tm = tmem + 128u * kw;  // G / D1 (+0) / DP (+64) / D2 (+0), time-shared
+    const uint32_t st = sbase + kw * L::kStageBytes;
+    const uint32_t kcb = sbase + L::kKc + kw * 16384;
+    const uint32_t tp = sbase + L::kTP + kw * 16384;
+    float *betas = betas_all + kw * 64;
+    float *Af = reinterpret_cast<float *>(smem + kw * L::kStageBytes + L::kG);  // after the cumsum
+    float *Ys = reinterpret_cast<float *>(smem + L::kTP + kw * 16384);          // TP rows 0-63
+    const uint32_t mma_bar = ctx.bar(kMmaK0 + kw);
+    if ((p.flags & 1) && tid == 0) {
       // test hook: a wait that can only time out
       if (!mbar_wait(ctx.bar(kNever), 0, 2000000LL)) {
         *abort_flag = 1;
@@ -221,15 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     uint32_t kph = 0;
-    // gate layout: a warp holds all 16 row groups (4 rows each) of two 8-channel groups,
-    // so the cumulative sum across row groups is a 16-lane shuffle scan
-    const int rg = t & 15, cg = 2 * warp + ((t >> 4) & 1), half = cg >> 3, ck = cg & 7;
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
+    for (int c = kw; c < nchunks; c += 2) {
+      const int s = kw;  // == c & 1
       const int t0 = bos + c * C;
       const int len = min(C, eos - t0);
-      const uint32_t st = sbase + s * L::kStageBytes;
-      const uint32_t kc = sbase + L::kKc + s * 16384;
       float bnext = 0.f;  // beta of this chunk, loaded early to hide the global latency
       if (t < C && t < len) bnext = __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]);
       // one thread polls the mbarriers, the others park on the named barrier
@@ -237,76 +260,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c >= 2) ctx.wait(kDone0 + s, ((c >> 1) - 1) & 1);  // Kc[s], ACC[s], gamma[s] free
         ctx.wait(kFull0 + s, (c >> 1) & 1);
       }
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
 
-      // a1: chunk-local cumulative log decay, 4 rows x 8 channels per thread
+      // a1: G = [Ltri; Ltri] g on the tensor cores, straight from the TMA'd g tile:
+      // the chunk-local inclusive cumsum per channel (rows 64-127 repeat rows 0-63).
+      // Each thread then owns row r and 64 channels of the elementwise decay work.
+      const int r = row & 63, half = row >> 6;
       const uint32_t kq = st + half * L::kKQ1;
-      const uint32_t ga = st + L::kG + half * 8192;
-      float gl[4][8], run[8];
+      if (t == 0) {
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 128, false, true);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) run[j] = 0.f;
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = rg * 4 + rr;
-        float gv[8];
-        unpack8(ld_shared_v4(ga + sw128(r, ck)), gv);
-        const bool valid = r < len;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          run[j] += valid ? gv[j] : 0.f;
-          gl[rr][j] = run[j];
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint64_t ad = sdesc_sw128(sbase + L::kLtri + k4 * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(st + L::kG + k4 * 2048, 8192, 1024);
+          mma_bf16(tm, ad, bd, id, k4 > 0);
         }
+        mma_commit(mma_bar);
+        ctx.wait(kMmaK0 + kw, kph & 1);
       }
-      float pre[8], tot[8];
+      ++kph;
+      bar_sync(bar_id, 128);
+      tc_fence_after();
+      const bool valid = r < len;  // rows past the sequence end write and decay nothing
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float G[32];
+        tmem_ld32(tm + lane_base + 64 * half + 32 * hh, G);
+        if (r == len - 1) {  // the chunk's last valid row: gamma = exp(G_last), range check
+          bool bad = false;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float v = run[j];
+          for (int j = 0; j < 32; j += 4) {
+            *reinterpret_cast<float4 *>(gamma + s * 128 + 64 * half + 32 * hh + j) =
+                make_float4(fast_exp2(G[j] * kLog2e), fast_exp2(G[j + 1] * kLog2e),
+                            fast_exp2(G[j + 2] * kLog2e), fast_exp2(G[j + 3] * kLog2e));
 #pragma unroll
-        for (int d = 1; d < 16; d <<= 1) {
-          const float u = __shfl_up_sync(0xffffffffu, v, d, 16);
-          if (rg >= d) v += u;
+            for (int jj = 0; jj < 4; ++jj) bad |= !(G[j + jj] >= kMinChunkLogDecay);
+          }
+          if (bad) atomicCAS(p.status, 0u, kStatusGateRange);
         }
-        pre[j] = v - run[j];                            // exclusive prefix over row groups
-        tot[j] = __shfl_sync(0xffffffffu, v, 15, 16);   // whole chunk
-      }
-      if (rg == 0) {
-        bool bad = false;
-        float gm[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          gm[j] = fast_exp2(tot[j] * kLog2e);
-          bad |= !(tot[j] >= kMinChunkLogDecay);
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t addr = kq + sw128(r, 4 * hh + q);
+          float kv[8], qv[8], kh[8], qh[8], kc[8];
+          unpack8(ld_shared_v4(addr), kv);
+          unpack8(ld_shared_v4(addr + L::kQoff), qv);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float d = G[8 * q + j] * kLog2e;  // G log2 e, in [Gl log2 e, 0]
+            const float f = fast_exp2(d), fe = fast_exp2(-d);
+            kh[j] = valid ? kv[j] * f : 0.f;
+            qh[j] = valid ? qv[j] * f : 0.f;
+            kc[j] = valid ? kv[j] * fe : 0.f;
+          }
+          st8(addr, kh);
+          st8(addr + L::kQoff, qh);
+          st8(kcb + half * 8192 + sw128(r, 4 * hh + q), kc);
         }
-        *reinterpret_cast<float4 *>(gamma + s * 128 + cg * 8) = make_float4(gm[0], gm[1], gm[2], gm[3]);
-        *reinterpret_cast<float4 *>(gamma + s * 128 + cg * 8 + 4) = make_float4(gm[4], gm[5], gm[6], gm[7]);
-        if (bad) atomicCAS(p.status, 0u, kStatusGateRange);
-      }
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = rg * 4 + rr;
-        float kv[8], qv[8], f[8], fe[8];
-        unpack8(ld_shared_v4(kq + sw128(r, ck)), kv);
-        unpack8(ld_shared_v4(kq + L::kQoff + sw128(r, ck)), qv);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float d = (pre[j] + gl[rr][j]) * kLog2e;  // G log2 e, in [Gl log2 e, 0]
-          f[j] = fast_exp2(d);
-          fe[j] = fast_exp2(-d);
-        }
-        float kb[8], qb[8], ke[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          kb[j] = kv[j] * f[j];
-          qb[j] = qv[j] * f[j];
-          ke[j] = kv[j] * fe[j];
-        }
-        st8(kq + sw128(r, ck), kb);
-        st8(kq + L::kQoff + sw128(r, ck), qb);
-        st8(kc + half * 8192 + sw128(r, ck), ke);
       }
       if (t < C) betas[t] = bnext;
       fence_async_smem();
-      bar_sync(1, 256);
+      tc_fence_before();
+      bar_sync(bar_id, 128);
 
       // a2: [Kh; Qh] Kc^T -> D1 (rows 0-63: A^kk / beta, rows 64-127: A^qk)
       if (t == 0) {
@@ -315,29 +330,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8) {
           const uint64_t ad = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kc + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
-          mma_bf16(tmem + kD1, ad, bd, id, k8 > 0);
+          const uint64_t bd = sdesc_sw128(kcb + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
+          mma_bf16(tm, ad, bd, id, k8 > 0);
         }
-        mma_commit(ctx.bar(kMmaK));
+        mma_commit(mma_bar);
+        ctx.wait(kMmaK0 + kw, kph & 1);
       }
-      if (t == 0) ctx.wait(kMmaK, kph & 1);
       ++kph;
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
       tc_fence_after();
-      {  // each warp reads 32 of the 64 columns of its 32 rows
+      // A^kk (fp32, strictly lower, beta applied) goes to the stage's g area, which
+      // the cumsum product has finished reading; T is then computed in place there.
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
         float a[32];
-        tmem_ld32(tmem + lane_base + kD1 + 32 * wh, a);
-        if (row < 64) {  // A^kk row (beta_row, strictly lower) -> fp32 Af
+        tmem_ld32(tm + lane_base + 32 * hh, a);
+        if (row < 64) {  // A^kk row (beta_row, strictly lower)
           const float bi = betas[row];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const int j = 32 * wh + 4 * q;
+            const int j = 32 * hh + 4 * q;
             float4 v;
             v.x = j + 0 < row ? bi * a[4 * q + 0] : 0.f;
             v.y = j + 1 < row ? bi * a[4 * q + 1] : 0.f;
             v.z = j + 2 < row ? bi * a[4 * q + 2] : 0.f;
             v.w = j + 3 < row ? bi * a[4 * q + 3] : 0.f;
-            *reinterpret_cast<float4 *>(Af + row * kLd + j) = v;
+            *reinterpret_cast<float4 *>(Af + af_idx(row, j)) = v;
           }
         } else {  // A^qk row (lower, diagonal included) -> bf16 TP rows 64-127
           const int i = row - 64;
@@ -346,100 +364,106 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
-              const int j = 32 * wh + 8 * q + jj;
+              const int j = 32 * hh + 8 * q + jj;
               v[jj] = j <= i ? a[8 * q + jj] : 0.f;
             }
-            st8(sbase + L::kTP + sw128(row, 4 * wh + q), v);
+            st8(tp + sw128(row, 4 * hh + q), v);
           }
-        }
-        if (t >= 128) {  // the two zero blocks above the diagonal that the 32-wide products read
-          const int i = t - 128, zr = i >> 2, zc = (i & 3) * 4;
-          if (i < 64)
-            *reinterpret_cast<float4 *>(Tf + zr * kLd + 16 + zc) = make_float4(0.f, 0.f, 0.f, 0.f);
-          else
-            *reinterpret_cast<float4 *>(Tf + (32 + zr - 16) * kLd + 48 + zc) =
-                make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       tc_fence_before();
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
 
-      // a3: T = (I + A^kk)^-1 by recursive doubling of the block inverse
+      // a3: T = (I + A^kk)^-1 in place, by recursive doubling of the block inverse
       //   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
       // 16 x 16 diagonal blocks first (right-looking substitution, one column
-      // per thread), then the 16-wide and the 32-wide off-diagonal blocks.
-      if (t < 64) {
+      // per thread), then the 16-wide and the 32-wide off-diagonal blocks.  The
+      // zero upper triangle of A^kk is the zero upper triangle of T.
+      {
+        float x[16];
         const int I = t >> 4, cc = t & 15;
-        const float *Ab = Af + (16 * I) * kLd + 16 * I;
-        float x[16], acc[16];
+        if (t < 64) {
+          float acc[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+          for (int r2 = 0; r2 < 16; ++r2) acc[r2] = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          x[m] = m == cc ? 1.f : (m > cc ? -acc[m] : 0.f);
+          for (int m = 0; m < 16; ++m) {
+            x[m] = m == cc ? 1.f : (m > cc ? -acc[m] : 0.f);
 #pragma unroll
-          for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(Ab[r * kLd + m], x[m], acc[r]);
+            for (int r2 = m + 1; r2 < 16; ++r2)
+              acc[r2] = fmaf(Af[af_idx(16 * I + r2, 16 * I + m)], x[m], acc[r2]);
+          }
         }
-        float *Tb = Tf + (16 * I) * kLd + 16 * I + cc;
+        bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
+        if (t < 64) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[r * kLd] = x[r];
+          for (int r2 = 0; r2 < 16; ++r2) Af[af_idx(16 * I + r2, 16 * I + cc)] = x[r2];
+        }
       }
-      bar_sync(1, 256);
-      float *Ys = reinterpret_cast<float *>(smem + L::kTP);  // TP rows 0-63 are free until Tb
-      {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y; 2 columns each
-        const int b = t >> 7, r = (t >> 3) & 15, c2 = (t & 7) * 2;
+      bar_sync(bar_id, 128);
+      {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y; 4 columns each
+        const int b = t >> 6, r2 = (t >> 2) & 15, c4 = (t & 3) * 4;
         const int r0 = 32 * b + 16, c0 = 32 * b;
-        float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float av = Af[(r0 + r) * kLd + c0 + k];
-          const float2 tv = *reinterpret_cast<const float2 *>(Tf + (c0 + k) * kLd + c0 + c2);
-          y0 = fmaf(av, tv.x, y0);
-          y1 = fmaf(av, tv.y, y1);
-        }
-        *reinterpret_cast<float2 *>(Ys + (b * 16 + r) * 20 + c2) = make_float2(y0, y1);
-        bar_sync(1, 256);
-        float z0 = 0.f, z1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float tv = Tf[(r0 + r) * kLd + r0 + k];
-          const float2 yv = *reinterpret_cast<const float2 *>(Ys + (b * 16 + k) * 20 + c2);
-          z0 = fmaf(tv, yv.x, z0);
-          z1 = fmaf(tv, yv.y, z1);
-        }
-        *reinterpret_cast<float2 *>(Tf + (r0 + r) * kLd + c0 + c2) = make_float2(-z0, -z1);
-      }
-      bar_sync(1, 256);
-      {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
-        const int rr = t >> 3, c4 = (t & 7) * 4;
         float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float av = Af[(32 + rr) * kLd + k];
-          const float4 tv = *reinterpret_cast<const float4 *>(Tf + k * kLd + c4);
+        for (int k = 0; k < 16; ++k) {
+          const float av = Af[af_idx(r0 + r2, c0 + k)];
+          const float4 tv = *reinterpret_cast<const float4 *>(Af + af_idx(c0 + k, c0 + c4));
           y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
           y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
         }
-        *reinterpret_cast<float4 *>(Ys + rr * 36 + c4) = y;
-        bar_sync(1, 256);
+        *reinterpret_cast<float4 *>(Ys + (b * 16 + r2) * 20 + c4) = y;
+        bar_sync(bar_id, 128);
         float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float tv = Tf[(32 + rr) * kLd + 32 + k];
-          const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + c4);
+        for (int k = 0; k < 16; ++k) {
+          const float tv = Af[af_idx(r0 + r2, r0 + k)];
+          const float4 yv = *reinterpret_cast<const float4 *>(Ys + (b * 16 + k) * 20 + c4);
           z.x = fmaf(tv, yv.x, z.x); z.y = fmaf(tv, yv.y, z.y);
           z.z = fmaf(tv, yv.z, z.z); z.w = fmaf(tv, yv.w, z.w);
         }
-        *reinterpret_cast<float4 *>(Tf + (32 + rr) * kLd + c4) = make_float4(-z.x, -z.y, -z.z, -z.w);
+        *reinterpret_cast<float4 *>(Af + af_idx(r0 + r2, c0 + c4)) =
+            make_float4(-z.x, -z.y, -z.z, -z.w);
       }
-      bar_sync(1, 256);
-      {  // Tb = T diag(beta) -> TP rows 0-63, 16 columns per thread
-        const int i = t & 63, qq = t >> 6;
+      bar_sync(bar_id, 128);
+      {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
+        const int rp = t >> 3, c4 = (t & 7) * 4;  // rows 2 rp, 2 rp + 1; columns c4 .. c4 + 3
+        float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int j0 = 16 * qq + 8 * q;
-          const float4 t0v = *reinterpret_cast<const float4 *>(Tf + i * kLd + j0);
-          const float4 t1v = *reinterpret_cast<const float4 *>(Tf + i * kLd + j0 + 4);
+        for (int k = 0; k < 32; ++k) {
+          const float a0 = Af[af_idx(32 + 2 * rp, k)], a1 = Af[af_idx(33 + 2 * rp, k)];
+          const float4 tv = *reinterpret_cast<const float4 *>(Af + af_idx(k, c4));
+          y0.x = fmaf(a0, tv.x, y0.x); y0.y = fmaf(a0, tv.y, y0.y);
+          y0.z = fmaf(a0, tv.z, y0.z); y0.w = fmaf(a0, tv.w, y0.w);
+          y1.x = fmaf(a1, tv.x, y1.x); y1.y = fmaf(a1, tv.y, y1.y);
+          y1.z = fmaf(a1, tv.z, y1.z); y1.w = fmaf(a1, tv.w, y1.w);
+        }
+        *reinterpret_cast<float4 *>(Ys + (2 * rp) * 36 + c4) = y0;
+        *reinterpret_cast<float4 *>(Ys + (2 * rp + 1) * 36 + c4) = y1;
+        bar_sync(bar_id, 128);
+        float4 z0 = make_float4(0.f, 0.f, 0.f, 0.f), z1 = z0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float t0v = Af[af_idx(32 + 2 * rp, 32 + k)], t1v = Af[af_idx(33 + 2 * rp, 32 + k)];
+          const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + c4);
+          z0.x = fmaf(t0v, yv.x, z0.x); z0.y = fmaf(t0v, yv.y, z0.y);
+          z0.z = fmaf(t0v, yv.z, z0.z); z0.w = fmaf(t0v, yv.w, z0.w);
+          z1.x = fmaf(t1v, yv.x, z1.x); z1.y = fmaf(t1v, yv.y, z1.y);
+          z1.z = fmaf(t1v, yv.z, z1.z); z1.w = fmaf(t1v, yv.w, z1.w);
+        }
+        *reinterpret_cast<float4 *>(Af + af_idx(32 + 2 * rp, c4)) =
+            make_float4(-z0.x, -z0.y, -z0.z, -z0.w);
+        *reinterpret_cast<float4 *>(Af + af_idx(33 + 2 * rp, c4)) =
+            make_float4(-z1.x, -z1.y, -z1.z, -z1.w);
+      }
+      bar_sync(bar_id, 128);
+      {  // Tb = T diag(beta) -> TP rows 0-63, 32 columns per thread
+        const int i = t & 63, hh = t >> 6;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j0 = 32 * hh + 8 * q;
+          const float4 t0v = *reinterpret_cast<const float4 *>(Af + af_idx(i, j0));
+          const float4 t1v = *reinterpret_cast<const float4 *>(Af + af_idx(i, j0 + 4));
           const float4 b0 = *reinterpret_cast<const float4 *>(betas + j0);
           const float4 b1 = *reinterpret_cast<const float4 *>(betas + j0 + 4);
           const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
@@ -447,11 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) v[jj] = j0 + jj <= i ? tv[jj] * bv[jj] : 0.f;
-          st8(sbase + L::kTP + sw128(i, 2 * qq + q), v);
+          st8(tp + sw128(i, 4 * hh + q), v);
         }
       }
       fence_async_smem();
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
 
       // Pb = A^qk Tb  (M = 128 with Tb stacked on top; rows 64-127 are used)
       if (t == 0) {
@@ -459,30 +483,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t id = idesc_bf16(128, 64, false, true);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(sbase + L::kTP + k4 * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sbase + L::kTP + k4 * 2048, 8192, 1024);
-          mma_bf16(tmem + kDP, ad, bd, id, k4 > 0);
+          const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(tp + k4 * 2048, 8192, 1024);
+          mma_bf16(tm + 64, ad, bd, id, k4 > 0);
         }
-        mma_commit(ctx.bar(kMmaK));
+        mma_commit(mma_bar);
+        ctx.wait(kMmaK0 + kw, kph & 1);
       }
-      if (t == 0) ctx.wait(kMmaK, kph & 1);
       ++kph;
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
       tc_fence_after();
       if (row >= 64) {
-        float a[32];
-        tmem_ld32(tmem + lane_base + kDP + 32 * wh, a);
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float a[32];
+          tmem_ld32(tm + lane_base + 64 + 32 * hh, a);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[8];
+          for (int q = 0; q < 4; ++q) {
+            float v[8];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) v[jj] = a[8 * q + jj];
-          st8(sbase + L::kTP + sw128(row, 4 * wh + q), v);
+            for (int jj = 0; jj < 8; ++jj) v[jj] = a[8 * q + jj];
+            st8(tp + sw128(row, 4 * hh + q), v);
+          }
         }
       }
       fence_async_smem();
       tc_fence_before();
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
 
       // [Tb; Pb] [Kh | V] -> D2 (W | A^qk W) and ACC[s] (U | O_intra)
       if (t == 0) {
@@ -491,30 +518,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t id_v = idesc_bf16(128, BV, false, true);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(sbase + L::kTP + k4 * 32, 16, 1024);
+          const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
           const uint64_t bk = sdesc_sw128(st + k4 * 2048, L::kKQ1, 1024);
           const uint64_t bv = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
-          mma_bf16(tmem + kD2, ad, bk, id_k, k4 > 0);
+          mma_bf16(tm, ad, bk, id_k, k4 > 0);
           mma_bf16(tmem + kAcc0 + s * BV, ad, bv, id_v, k4 > 0);
         }
-        mma_commit(ctx.bar(kMmaK));
+        mma_commit(mma_bar);
+        ctx.wait(kMmaK0 + kw, kph & 1);
       }
-      if (t == 0) ctx.wait(kMmaK, kph & 1);
       ++kph;
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
       tc_fence_after();
-      {  // -W over Kh, Qh - A^qk W over Qh (the A operand of the state product); 64 channels each
+      {  // -W over Kh, Qh - A^qk W over Qh (the A operand of the state product)
         const int i = row & 63;
         const uint32_t qoff = row < 64 ? 0u : L::kQoff;
-        const uint32_t base = st + wh * L::kKQ1 + qoff;  // channels 64 wh .. 64 wh + 63
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll 1
+        for (int cc4 = 0; cc4 < 4; ++cc4) {
           float a[32];
-          tmem_ld32(tmem + lane_base + kD2 + 64 * wh + 32 * hh, a);
+          tmem_ld32(tm + lane_base + 32 * cc4, a);
+          const uint32_t base = st + (cc4 >> 1) * L::kKQ1 + qoff;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int chl = 32 * hh + 8 * q;  // channel within the 64-channel half
-            const uint32_t addr = base + sw128(i, chl >> 3);
+            const uint32_t addr = base + sw128(i, 4 * (cc4 & 1) + q);
             float v[8];
             if (row < 64) {
 #pragma unroll
@@ -531,12 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       tc_fence_before();
-      bar_sync(1, 256);
+      bar_sync(bar_id, 128);
       if (t == 0) mbar_arrive(ctx.bar(kReady0 + s));
     }
-    if (t == 0) {  // all K-side MMAs retired before TMEM is released
-      mma_commit(ctx.bar(kFinK));
-      mbar_wait(ctx.bar(kFinK), 0, kWaitCycles);
+    if (t == 0) {  // all of this group's MMAs retired before TMEM is released
+      mma_commit(ctx.bar(kFinK0 + kw));
+      mbar_wait(ctx.bar(kFinK0 + kw), 0, kWaitCycles);
     }
   } else {
     // ------------------------------------------------------------ S-side
