@@ -163,6 +163,26 @@ def dist_info():
     return ws, rank, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own independent problem (weak scaling, no data exchange)."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """The job's time is the slowest rank's (all_reduce MAX; a no-op on one rank)."""
+    if ws <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: int, ws: int, ms_per_step: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return units_per_rank * ws / (ms_per_step * 1e-3)
+
+
 def oracle_cpu_baseline(x, pairs_limit=None):
     """Times the oracle, as it stands, on the host cores.  Returns (seconds,
     tokens processed, token-heads processed, threads, sample description)."""
@@ -195,7 +215,7 @@ def run_prefill(args, ws, rank, dev):
 
     spec = W.named(args.workload)
     spec = W.PrefillSpec(spec.seqlens, spec.num_heads, spec.d_k, spec.d_v, spec.io_dtype, spec.gate,
-                         spec.init, spec.seed + 1000 * rank)
+                         spec.init, rank_seed(spec.seed, rank))
     big = spec.total_tokens * spec.num_heads > 4_000_000
     x = W.prefill_inputs(spec, device=("cuda" if big else "cpu"))
     d = {kk: (vv.to(dev) if vv is not None else None) for kk, vv in x.items()}
@@ -239,11 +259,7 @@ def run_prefill(args, ws, rank, dev):
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    ms_step = total_ms / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, ws, dev)
 
     # e2e through the public API: pinned host inputs -> device, kernel, result -> host
     host_in = {kk: (vv.to("cpu").pin_memory() if vv is not None else None) for kk, vv in x.items()}
@@ -272,18 +288,14 @@ def run_prefill(args, ws, rank, dev):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, ws, dev)
 
     hbm, tflops, peak_src = measured_peaks()
     alg_bytes, alg_flops = algorithmic_prefill(T * H, N * H, dk, dv, io_bytes)
     achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
     kind = "tensor" if tensor_path else "simt"
     res = {
-        "metric": METRIC, "value": T * ws / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
+        "metric": METRIC, "value": aggregate_throughput(T, ws, ms_step), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
@@ -298,7 +310,7 @@ def run_prefill(args, ws, rank, dev):
                      "tensor_peak_tflops": tflops,
                      "kernel_ms": launch_ms,
                      "roofline_ms": max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12)) * 1e3},
-        "e2e": {"value": T * ws / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": aggregate_throughput(T, ws, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
@@ -312,7 +324,7 @@ def run_decode(args, ws, rank, dev, name="decode_bf16"):
     from kimi_delta_attention_fwd_gb300 import workloads as W
     spec = W.named(name)
     spec = W.DecodeSpec(spec.num_seqs, spec.num_heads, spec.d_k, spec.d_v, spec.steps, spec.io_dtype,
-                        spec.gate, spec.seed + 1000 * rank)
+                        spec.gate, rank_seed(spec.seed, rank))
     y = W.decode_inputs(spec, device=str(dev))
     st = y["state"].clone()
     outs = torch.empty((spec.steps, spec.num_seqs, spec.num_heads, spec.d_v), dtype=y["q"].dtype, device=dev)
@@ -334,12 +346,12 @@ def run_decode(args, ws, rank, dev, name="decode_bf16"):
             run_all()
         b.record(stream)
         torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / (reps * spec.steps)  # per decode step
+    ms = max_over_ranks(a.elapsed_time(b) / (reps * spec.steps), ws, dev)  # per decode step
     io_bytes = 2 if spec.io_dtype == "bf16" else 4
     by = algorithmic_decode(spec.num_seqs * spec.num_heads, spec.d_k, spec.d_v, io_bytes)
     hbm, _, src = measured_peaks()
     ach = by / (ms * 1e-3) / 1e9
-    return {"workload": name, "value": spec.num_seqs * ws / (ms * 1e-3), "unit": "tokens/s",
+    return {"workload": name, "value": aggregate_throughput(spec.num_seqs, ws, ms), "unit": "tokens/s",
             "ms_per_decode_step": ms, "steps_per_rep": spec.steps, "reps": reps,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                          "traffic": recorded_traffic("decode", name), "peak_source": f"{src} hbm_gbs"},
