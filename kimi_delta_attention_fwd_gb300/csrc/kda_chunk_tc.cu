@@ -54,16 +54,19 @@ constexpr float kMinChunkLogDecay = -80.f;
 constexpr uint32_t kStatusTimeout = 7;      // -KDA_ERR_DEVICE_TIMEOUT
 constexpr uint32_t kStatusGateRange = 8;    // -KDA_ERR_GATE_RANGE
 
-// fp32 64 x 64 matrix in 16 KB: 16-byte chunks of each row XOR-swizzled by the
-// row, so that row-wise, column-wise and float4 accesses are all conflict-free.
-__device__ __forceinline__ int af_idx(int i, int j) {
-  return i * 64 + ((((j >> 2) ^ i) & 15) << 2) + (j & 3);
-}
+// Compact fp32 layout of the 64 x 64 unit-lower-triangular solve (12 KB):
+// the four 16 x 16 diagonal blocks, the sub-diagonal blocks (1,0) and (3,2), and
+// the lower-left 32 x 32 block; row strides keep 16-byte alignment and spread
+// the rows of a column over the shared-memory banks.
+constexpr int kSdLd = 20, kSlLd = 36;
+__device__ __forceinline__ int sd_idx(int blk, int r, int c) { return (blk * 16 + r) * kSdLd + c; }
+__device__ __forceinline__ int so_idx(int blk, int r, int c) { return (blk * 16 + r) * kSdLd + c; }
+__device__ __forceinline__ int sl_idx(int r, int c) { return r * kSlLd + c; }
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 struct L {
   // stage: [k ch0-63 | q ch0-63] [k ch64-127 | q ch64-127] [g ch0-63] [g ch64-127] [v tile];
-  // the g area later holds the fp32 A^kk / T (64 x 64, af_idx layout)
+  // the g area later holds the fp32 A^kk / T in the compact solve layout
   static constexpr uint32_t kKQ1 = 16384, kQoff = 8192, kG = 32768, kV = 49152;
   static constexpr uint32_t kStageBytes = 49152 + C * BV * 2;
   static constexpr uint32_t kKc = 2 * kStageBytes;          // 2 x Kc [ch0-63 | ch64-127]
@@ -238,7 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t kcb = sbase + L::kKc + kw * 16384;
     const uint32_t tp = sbase + L::kTP + kw * 16384;
     float *betas = betas_all + kw * 64;
-    float *Af = reinterpret_cast<float *>(smem + kw * L::kStageBytes + L::kG);  // after the cumsum
+    // compact fp32 solve layout in the stage's g area (after the cumsum product has read g)
+    float *Sd = reinterpret_cast<float *>(smem + kw * L::kStageBytes + L::kG);  // [4][16][20]
+    float *So = Sd + 4 * 16 * kSdLd;                                            // [2][16][20]
+    float *Sl = So + 2 * 16 * kSdLd;                                            // [32][36]
     float *Ys = reinterpret_cast<float *>(smem + L::kTP + kw * 16384);          // TP rows 0-63
     const uint32_t mma_bar = ctx.bar(kMmaK0 + kw);
     if ((p.flags & 1) && tid == 0) {
@@ -340,22 +346,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_sync(bar_id, 128);
       tc_fence_after();
       // A^kk (fp32, strictly lower, beta applied) goes to the stage's g area, which
-      // the cumsum product has finished reading; T is then computed in place there.
+      // the cumsum product has finished reading, in the compact solve layout
+      // (diagonal 16-blocks, the two 16-wide sub-diagonal blocks, the lower-left
+      // 32 x 32 block; the zero blocks above the diagonal are not stored).  T is
+      // then computed in place there.
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float a[32];
         tmem_ld32(tm + lane_base + 32 * hh, a);
         if (row < 64) {  // A^kk row (beta_row, strictly lower)
           const float bi = betas[row];
+          const int I = row >> 4, rl = row & 15;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const int j = 32 * hh + 4 * q;
+            const int j = 32 * hh + 4 * q;  // global column of this float4
             float4 v;
             v.x = j + 0 < row ? bi * a[4 * q + 0] : 0.f;
             v.y = j + 1 < row ? bi * a[4 * q + 1] : 0.f;
             v.z = j + 2 < row ? bi * a[4 * q + 2] : 0.f;
             v.w = j + 3 < row ? bi * a[4 * q + 3] : 0.f;
-            *reinterpret_cast<float4 *>(Af + af_idx(row, j)) = v;
+            const int J = j >> 4;  // block column (compile-time)
+            if (J == I) *reinterpret_cast<float4 *>(Sd + sd_idx(I, rl, j & 15)) = v;
+            if ((I == 1 && J == 0) || (I == 3 && J == 2))
+              *reinterpret_cast<float4 *>(So + so_idx(I >> 1, rl, j & 15)) = v;
+            if (row >= 32 && j < 32) *reinterpret_cast<float4 *>(Sl + sl_idx(row - 32, j)) = v;
           }
         } else {  // A^qk row (lower, diagonal included) -> bf16 TP rows 64-127
           const int i = row - 64;
@@ -377,12 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a3: T = (I + A^kk)^-1 in place, by recursive doubling of the block inverse
       //   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
       // 16 x 16 diagonal blocks first (right-looking substitution, one column
-      // per thread), then the 16-wide and the 32-wide off-diagonal blocks.  The
-      // zero upper triangle of A^kk is the zero upper triangle of T.
+      // per thread), then the 16-wide and the 32-wide off-diagonal blocks.
       {
         float x[16];
         const int I = t >> 4, cc = t & 15;
         if (t < 64) {
+          const float *Ab = Sd + sd_idx(I, 0, 0);
           float acc[16];
 #pragma unroll
           for (int r2 = 0; r2 < 16; ++r2) acc[r2] = 0.f;
@@ -390,83 +404,128 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int m = 0; m < 16; ++m) {
             x[m] = m == cc ? 1.f : (m > cc ? -acc[m] : 0.f);
 #pragma unroll
-            for (int r2 = m + 1; r2 < 16; ++r2)
-              acc[r2] = fmaf(Af[af_idx(16 * I + r2, 16 * I + m)], x[m], acc[r2]);
+            for (int r2 = m + 1; r2 < 16; ++r2) acc[r2] = fmaf(Ab[r2 * kSdLd + m], x[m], acc[r2]);
           }
         }
         bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
         if (t < 64) {
+          float *Tb = Sd + sd_idx(I, 0, cc);
 #pragma unroll
-          for (int r2 = 0; r2 < 16; ++r2) Af[af_idx(16 * I + r2, 16 * I + cc)] = x[r2];
+          for (int r2 = 0; r2 < 16; ++r2) Tb[r2 * kSdLd] = x[r2];
         }
       }
       bar_sync(bar_id, 128);
       {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y; 4 columns each
         const int b = t >> 6, r2 = (t >> 2) & 15, c4 = (t & 3) * 4;
-        const int r0 = 32 * b + 16, c0 = 32 * b;
+        const float *Lo = So + so_idx(b, r2, 0);           // row r2 of L_{b+1,b}
+        const float *Tbb = Sd + sd_idx(2 * b, 0, c4);      // T_bb, columns c4..
         float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float av = Af[af_idx(r0 + r2, c0 + k)];
-          const float4 tv = *reinterpret_cast<const float4 *>(Af + af_idx(c0 + k, c0 + c4));
+          const float av = Lo[k];
+          const float4 tv = *reinterpret_cast<const float4 *>(Tbb + k * kSdLd);
           y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
           y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
         }
         *reinterpret_cast<float4 *>(Ys + (b * 16 + r2) * 20 + c4) = y;
         bar_sync(bar_id, 128);
+        const float *Td = Sd + sd_idx(2 * b + 1, r2, 0);   // row r2 of T_{b+1,b+1}
         float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float tv = Af[af_idx(r0 + r2, r0 + k)];
+          const float tv = Td[k];
           const float4 yv = *reinterpret_cast<const float4 *>(Ys + (b * 16 + k) * 20 + c4);
           z.x = fmaf(tv, yv.x, z.x); z.y = fmaf(tv, yv.y, z.y);
           z.z = fmaf(tv, yv.z, z.z); z.w = fmaf(tv, yv.w, z.w);
         }
-        *reinterpret_cast<float4 *>(Af + af_idx(r0 + r2, c0 + c4)) =
-            make_float4(-z.x, -z.y, -z.z, -z.w);
+        *reinterpret_cast<float4 *>(So + so_idx(b, r2, c4)) = make_float4(-z.x, -z.y, -z.z, -z.w);
       }
       bar_sync(bar_id, 128);
       {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
-        const int rp = t >> 3, c4 = (t & 7) * 4;  // rows 2 rp, 2 rp + 1; columns c4 .. c4 + 3
+        // warp w: column half ch = w & 1, row half rh = w >> 1 (warp-uniform block shapes)
+        const int ch = wq & 1, rh = wq >> 1, cg4 = (t & 3) * 4, rp = (t & 31) >> 2;
+        const int r0 = 16 * rh + 2 * rp;   // rows r0, r0 + 1 of the 32 x 32 block
+        const int col = 16 * ch + cg4;     // columns col .. col + 3
+        const float *a0 = Sl + sl_idx(r0, 0), *a1 = Sl + sl_idx(r0 + 1, 0);
         float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+        if (ch == 0) {  // T[0:32, 0:16] = [T_00; T_10]
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float a0 = Af[af_idx(32 + 2 * rp, k)], a1 = Af[af_idx(33 + 2 * rp, k)];
-          const float4 tv = *reinterpret_cast<const float4 *>(Af + af_idx(k, c4));
-          y0.x = fmaf(a0, tv.x, y0.x); y0.y = fmaf(a0, tv.y, y0.y);
-          y0.z = fmaf(a0, tv.z, y0.z); y0.w = fmaf(a0, tv.w, y0.w);
-          y1.x = fmaf(a1, tv.x, y1.x); y1.y = fmaf(a1, tv.y, y1.y);
-          y1.z = fmaf(a1, tv.z, y1.z); y1.w = fmaf(a1, tv.w, y1.w);
+          for (int k = 0; k < 32; ++k) {
+            const float4 tv = *reinterpret_cast<const float4 *>(
+                k < 16 ? Sd + sd_idx(0, k, cg4) : So + so_idx(0, k - 16, cg4));
+            const float av0 = a0[k], av1 = a1[k];
+            y0.x = fmaf(av0, tv.x, y0.x); y0.y = fmaf(av0, tv.y, y0.y);
+            y0.z = fmaf(av0, tv.z, y0.z); y0.w = fmaf(av0, tv.w, y0.w);
+            y1.x = fmaf(av1, tv.x, y1.x); y1.y = fmaf(av1, tv.y, y1.y);
+            y1.z = fmaf(av1, tv.z, y1.z); y1.w = fmaf(av1, tv.w, y1.w);
+          }
+        } else {        // T[0:32, 16:32] = [0; T_11]
+#pragma unroll
+          for (int k = 16; k < 32; ++k) {
+            const float4 tv = *reinterpret_cast<const float4 *>(Sd + sd_idx(1, k - 16, cg4));
+            const float av0 = a0[k], av1 = a1[k];
+            y0.x = fmaf(av0, tv.x, y0.x); y0.y = fmaf(av0, tv.y, y0.y);
+            y0.z = fmaf(av0, tv.z, y0.z); y0.w = fmaf(av0, tv.w, y0.w);
+            y1.x = fmaf(av1, tv.x, y1.x); y1.y = fmaf(av1, tv.y, y1.y);
+            y1.z = fmaf(av1, tv.z, y1.z); y1.w = fmaf(av1, tv.w, y1.w);
+          }
         }
-        *reinterpret_cast<float4 *>(Ys + (2 * rp) * 36 + c4) = y0;
-        *reinterpret_cast<float4 *>(Ys + (2 * rp + 1) * 36 + c4) = y1;
+        *reinterpret_cast<float4 *>(Ys + r0 * 36 + col) = y0;
+        *reinterpret_cast<float4 *>(Ys + (r0 + 1) * 36 + col) = y1;
         bar_sync(bar_id, 128);
         float4 z0 = make_float4(0.f, 0.f, 0.f, 0.f), z1 = z0;
+        if (rh == 0) {  // T[32:48, 32:64] = [T_22, 0]
+          const float *t0 = Sd + sd_idx(2, r0, 0), *t1 = Sd + sd_idx(2, r0 + 1, 0);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float t0v = Af[af_idx(32 + 2 * rp, 32 + k)], t1v = Af[af_idx(33 + 2 * rp, 32 + k)];
-          const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + c4);
-          z0.x = fmaf(t0v, yv.x, z0.x); z0.y = fmaf(t0v, yv.y, z0.y);
-          z0.z = fmaf(t0v, yv.z, z0.z); z0.w = fmaf(t0v, yv.w, z0.w);
-          z1.x = fmaf(t1v, yv.x, z1.x); z1.y = fmaf(t1v, yv.y, z1.y);
-          z1.z = fmaf(t1v, yv.z, z1.z); z1.w = fmaf(t1v, yv.w, z1.w);
+          for (int k = 0; k < 16; ++k) {
+            const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + col);
+            const float tv0 = t0[k], tv1 = t1[k];
+            z0.x = fmaf(tv0, yv.x, z0.x); z0.y = fmaf(tv0, yv.y, z0.y);
+            z0.z = fmaf(tv0, yv.z, z0.z); z0.w = fmaf(tv0, yv.w, z0.w);
+            z1.x = fmaf(tv1, yv.x, z1.x); z1.y = fmaf(tv1, yv.y, z1.y);
+            z1.z = fmaf(tv1, yv.z, z1.z); z1.w = fmaf(tv1, yv.w, z1.w);
+          }
+        } else {        // T[48:64, 32:64] = [T_32, T_33]
+          const int rl = r0 - 16;
+          const float *o0 = So + so_idx(1, rl, 0), *o1 = So + so_idx(1, rl + 1, 0);
+          const float *d0 = Sd + sd_idx(3, rl, 0), *d1 = Sd + sd_idx(3, rl + 1, 0);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + col);
+            const float tv0 = k < 16 ? o0[k] : d0[k - 16], tv1 = k < 16 ? o1[k] : d1[k - 16];
+            z0.x = fmaf(tv0, yv.x, z0.x); z0.y = fmaf(tv0, yv.y, z0.y);
+            z0.z = fmaf(tv0, yv.z, z0.z); z0.w = fmaf(tv0, yv.w, z0.w);
+            z1.x = fmaf(tv1, yv.x, z1.x); z1.y = fmaf(tv1, yv.y, z1.y);
+            z1.z = fmaf(tv1, yv.z, z1.z); z1.w = fmaf(tv1, yv.w, z1.w);
+          }
         }
-        *reinterpret_cast<float4 *>(Af + af_idx(32 + 2 * rp, c4)) =
-            make_float4(-z0.x, -z0.y, -z0.z, -z0.w);
-        *reinterpret_cast<float4 *>(Af + af_idx(33 + 2 * rp, c4)) =
+        bar_sync(bar_id, 128);  // every read of the lower-left L block is done
+        *reinterpret_cast<float4 *>(Sl + sl_idx(r0, col)) = make_float4(-z0.x, -z0.y, -z0.z, -z0.w);
+        *reinterpret_cast<float4 *>(Sl + sl_idx(r0 + 1, col)) =
             make_float4(-z1.x, -z1.y, -z1.z, -z1.w);
       }
       bar_sync(bar_id, 128);
       {  // Tb = T diag(beta) -> TP rows 0-63, 32 columns per thread
-        const int i = t & 63, hh = t >> 6;
+        const int i = t & 63, hh = t >> 6, I = i >> 4, il = i & 15;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int j0 = 32 * hh + 8 * q;
-          const float4 t0v = *reinterpret_cast<const float4 *>(Af + af_idx(i, j0));
-          const float4 t1v = *reinterpret_cast<const float4 *>(Af + af_idx(i, j0 + 4));
+          const int j0 = 32 * hh + 8 * q, J = j0 >> 4, jl = j0 & 15;
+          const float *src = nullptr;  // 8 consecutive T entries of row i, or zeros
+          if (J == I) src = Sd + sd_idx(I, il, jl);
+          else if ((I == 1 && J == 0) || (I == 3 && J == 2)) src = So + so_idx(I >> 1, il, jl);
+          else if (I >= 2 && J <= 1) src = Sl + sl_idx(i - 32, j0);
+          float tv[8];
+          if (src) {
+            const float4 t0v = *reinterpret_cast<const float4 *>(src);
+            const float4 t1v = *reinterpret_cast<const float4 *>(src + 4);
+            tv[0] = t0v.x; tv[1] = t0v.y; tv[2] = t0v.z; tv[3] = t0v.w;
+            tv[4] = t1v.x; tv[5] = t1v.y; tv[6] = t1v.z; tv[7] = t1v.w;
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) tv[jj] = 0.f;
+          }
           const float4 b0 = *reinterpret_cast<const float4 *>(betas + j0);
           const float4 b1 = *reinterpret_cast<const float4 *>(betas + j0 + 4);
-          const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
           const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
           float v[8];
 #pragma unroll
