@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_sync(bar_id, 128);
       tc_fence_after();
       const bool valid = r < len;  // rows past the sequence end write and decay nothing
+      const float vm = valid ? 1.f : 0.f;
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float G[32];
@@ -314,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float d = G[8 * q + j] * kLog2e;  // G log2 e, in [Gl log2 e, 0]
-            const float f = fast_exp2(d), fe = fast_exp2(-d);
-            kh[j] = valid ? kv[j] * f : 0.f;
-            qh[j] = valid ? qv[j] * f : 0.f;
-            kc[j] = valid ? kv[j] * fe : 0.f;
+            const float f = fast_exp2(d) * vm, fe = fast_exp2(-d) * vm;
+            kh[j] = kv[j] * f;
+            qh[j] = qv[j] * f;
+            kc[j] = kv[j] * fe;
           }
           st8(addr, kh);
           st8(addr + L::kQoff, qh);
@@ -592,14 +593,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       {  // -W over Kh, Qh - A^qk W over Qh (the A operand of the state product)
         const int i = row & 63;
         const uint32_t qoff = row < 64 ? 0u : L::kQoff;
+        const uint32_t rx = static_cast<uint32_t>(i & 7);
 #pragma unroll 1
-        for (int cc4 = 0; cc4 < 4; ++cc4) {
-          float a[32];
-          tmem_ld32(tm + lane_base + 32 * cc4, a);
-          const uint32_t base = st + (cc4 >> 1) * L::kKQ1 + qoff;
+        for (int hh = 0; hh < 2; ++hh) {  // channels 64 hh .. 64 hh + 63
+          float a[64];
+          tmem_ld64(tm + lane_base + 64 * hh, a);
+          const uint32_t base = st + hh * L::kKQ1 + qoff + i * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t addr = base + sw128(i, 4 * (cc4 & 1) + q);
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t addr = base + ((static_cast<uint32_t>(q) ^ rx) << 4);
             float v[8];
             if (row < 64) {
 #pragma unroll
