@@ -416,94 +416,96 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       bar_sync(bar_id, 128);
-      {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y; 4 columns each
-        const int b = t >> 6, r2 = (t >> 2) & 15, c4 = (t & 3) * 4;
-        const float *Lo = So + so_idx(b, r2, 0);           // row r2 of L_{b+1,b}
-        const float *Tbb = Sd + sd_idx(2 * b, 0, c4);      // T_bb, columns c4..
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
+      // (16 x 8 tiles; TF32 operands rounded to nearest, fp32 accumulation).
+      const int lg = (t & 31) >> 2, lc = t & 3;  // fragment coordinates of this lane
+      {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y
+        const int b = wq >> 1, n0 = 8 * (wq & 1);  // warp: block b, 8 output columns
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float av = Lo[k];
-          const float4 tv = *reinterpret_cast<const float4 *>(Tbb + k * kSdLd);
-          y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
-          y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
+        for (int k0 = 0; k0 < 16; k0 += 8) {
+          const uint32_t a[4] = {to_tf32(So[so_idx(b, lg, k0 + lc)]),
+                                 to_tf32(So[so_idx(b, lg + 8, k0 + lc)]),
+                                 to_tf32(So[so_idx(b, lg, k0 + lc + 4)]),
+                                 to_tf32(So[so_idx(b, lg + 8, k0 + lc + 4)])};
+          const uint32_t bb[2] = {to_tf32(Sd[sd_idx(2 * b, k0 + lc, n0 + lg)]),
+                                  to_tf32(Sd[sd_idx(2 * b, k0 + lc + 4, n0 + lg)])};
+          mma_tf32_16x8x8(y, a, bb);
         }
-        *reinterpret_cast<float4 *>(Ys + (b * 16 + r2) * 20 + c4) = y;
+        float *yb = Ys + b * 16 * 20;
+        *reinterpret_cast<float2 *>(yb + lg * 20 + n0 + 2 * lc) = make_float2(y[0], y[1]);
+        *reinterpret_cast<float2 *>(yb + (lg + 8) * 20 + n0 + 2 * lc) = make_float2(y[2], y[3]);
         bar_sync(bar_id, 128);
-        const float *Td = Sd + sd_idx(2 * b + 1, r2, 0);   // row r2 of T_{b+1,b+1}
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float tv = Td[k];
-          const float4 yv = *reinterpret_cast<const float4 *>(Ys + (b * 16 + k) * 20 + c4);
-          z.x = fmaf(tv, yv.x, z.x); z.y = fmaf(tv, yv.y, z.y);
-          z.z = fmaf(tv, yv.z, z.z); z.w = fmaf(tv, yv.w, z.w);
+        for (int k0 = 0; k0 < 16; k0 += 8) {
+          const uint32_t a[4] = {to_tf32(Sd[sd_idx(2 * b + 1, lg, k0 + lc)]),
+                                 to_tf32(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc)]),
+                                 to_tf32(Sd[sd_idx(2 * b + 1, lg, k0 + lc + 4)]),
+                                 to_tf32(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc + 4)])};
+          const uint32_t bb[2] = {to_tf32(yb[(k0 + lc) * 20 + n0 + lg]),
+                                  to_tf32(yb[(k0 + lc + 4) * 20 + n0 + lg])};
+          mma_tf32_16x8x8(z, a, bb);
         }
-        *reinterpret_cast<float4 *>(So + so_idx(b, r2, c4)) = make_float4(-z.x, -z.y, -z.z, -z.w);
+        *reinterpret_cast<float2 *>(So + so_idx(b, lg, n0 + 2 * lc)) = make_float2(-z[0], -z[1]);
+        *reinterpret_cast<float2 *>(So + so_idx(b, lg + 8, n0 + 2 * lc)) = make_float2(-z[2], -z[3]);
       }
       bar_sync(bar_id, 128);
       {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
-        // warp w: column half ch = w & 1, row half rh = w >> 1 (warp-uniform block shapes)
-        const int ch = wq & 1, rh = wq >> 1, cg4 = (t & 3) * 4, rp = (t & 31) >> 2;
-        const int r0 = 16 * rh + 2 * rp;   // rows r0, r0 + 1 of the 32 x 32 block
-        const int col = 16 * ch + cg4;     // columns col .. col + 3
-        const float *a0 = Sl + sl_idx(r0, 0), *a1 = Sl + sl_idx(r0 + 1, 0);
-        float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-        if (ch == 0) {  // T[0:32, 0:16] = [T_00; T_10]
+        // warp: rows 16 rh .. 16 rh + 15, columns 16 ch .. 16 ch + 15 (two 8-wide tiles)
+        const int ch = wq & 1, rh = wq >> 1;
+        float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
+        // T[0:32, 0:16] = [T_00; T_10];  T[0:32, 16:32] = [0; T_11]
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float4 tv = *reinterpret_cast<const float4 *>(
-                k < 16 ? Sd + sd_idx(0, k, cg4) : So + so_idx(0, k - 16, cg4));
-            const float av0 = a0[k], av1 = a1[k];
-            y0.x = fmaf(av0, tv.x, y0.x); y0.y = fmaf(av0, tv.y, y0.y);
-            y0.z = fmaf(av0, tv.z, y0.z); y0.w = fmaf(av0, tv.w, y0.w);
-            y1.x = fmaf(av1, tv.x, y1.x); y1.y = fmaf(av1, tv.y, y1.y);
-            y1.z = fmaf(av1, tv.z, y1.z); y1.w = fmaf(av1, tv.w, y1.w);
-          }
-        } else {        // T[0:32, 16:32] = [0; T_11]
-#pragma unroll
-          for (int k = 16; k < 32; ++k) {
-            const float4 tv = *reinterpret_cast<const float4 *>(Sd + sd_idx(1, k - 16, cg4));
-            const float av0 = a0[k], av1 = a1[k];
-            y0.x = fmaf(av0, tv.x, y0.x); y0.y = fmaf(av0, tv.y, y0.y);
-            y0.z = fmaf(av0, tv.z, y0.z); y0.w = fmaf(av0, tv.w, y0.w);
-            y1.x = fmaf(av1, tv.x, y1.x); y1.y = fmaf(av1, tv.y, y1.y);
-            y1.z = fmaf(av1, tv.z, y1.z); y1.w = fmaf(av1, tv.w, y1.w);
-          }
+        for (int k0 = 0; k0 < 32; k0 += 8) {
+          if (ch == 1 && k0 < 16) continue;
+          const int ra = 16 * rh + lg;
+          const uint32_t a[4] = {to_tf32(Sl[sl_idx(ra, k0 + lc)]), to_tf32(Sl[sl_idx(ra + 8, k0 + lc)]),
+                                 to_tf32(Sl[sl_idx(ra, k0 + lc + 4)]),
+                                 to_tf32(Sl[sl_idx(ra + 8, k0 + lc + 4)])};
+          auto tlo = [&](int k, int c) -> float {  // T[k][16 ch + c], k in 0..31, c in 0..15
+            if (ch == 0) return k < 16 ? Sd[sd_idx(0, k, c)] : So[so_idx(0, k - 16, c)];
+            return Sd[sd_idx(1, k - 16, c)];
+          };
+          const uint32_t b0[2] = {to_tf32(tlo(k0 + lc, lg)), to_tf32(tlo(k0 + lc + 4, lg))};
+          const uint32_t b1[2] = {to_tf32(tlo(k0 + lc, 8 + lg)), to_tf32(tlo(k0 + lc + 4, 8 + lg))};
+          mma_tf32_16x8x8(y0, a, b0);
+          mma_tf32_16x8x8(y1, a, b1);
         }
-        *reinterpret_cast<float4 *>(Ys + r0 * 36 + col) = y0;
-        *reinterpret_cast<float4 *>(Ys + (r0 + 1) * 36 + col) = y1;
+        {
+          float *yr0 = Ys + (16 * rh + lg) * 36 + 16 * ch + 2 * lc;
+          float *yr1 = Ys + (16 * rh + lg + 8) * 36 + 16 * ch + 2 * lc;
+          *reinterpret_cast<float2 *>(yr0) = make_float2(y0[0], y0[1]);
+          *reinterpret_cast<float2 *>(yr1) = make_float2(y0[2], y0[3]);
+          *reinterpret_cast<float2 *>(yr0 + 8) = make_float2(y1[0], y1[1]);
+          *reinterpret_cast<float2 *>(yr1 + 8) = make_float2(y1[2], y1[3]);
+        }
         bar_sync(bar_id, 128);
-        float4 z0 = make_float4(0.f, 0.f, 0.f, 0.f), z1 = z0;
-        if (rh == 0) {  // T[32:48, 32:64] = [T_22, 0]
-          const float *t0 = Sd + sd_idx(2, r0, 0), *t1 = Sd + sd_idx(2, r0 + 1, 0);
+        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+        // T[32:48, 32:64] = [T_22, 0];  T[48:64, 32:64] = [T_32, T_33]
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + col);
-            const float tv0 = t0[k], tv1 = t1[k];
-            z0.x = fmaf(tv0, yv.x, z0.x); z0.y = fmaf(tv0, yv.y, z0.y);
-            z0.z = fmaf(tv0, yv.z, z0.z); z0.w = fmaf(tv0, yv.w, z0.w);
-            z1.x = fmaf(tv1, yv.x, z1.x); z1.y = fmaf(tv1, yv.y, z1.y);
-            z1.z = fmaf(tv1, yv.z, z1.z); z1.w = fmaf(tv1, yv.w, z1.w);
-          }
-        } else {        // T[48:64, 32:64] = [T_32, T_33]
-          const int rl = r0 - 16;
-          const float *o0 = So + so_idx(1, rl, 0), *o1 = So + so_idx(1, rl + 1, 0);
-          const float *d0 = Sd + sd_idx(3, rl, 0), *d1 = Sd + sd_idx(3, rl + 1, 0);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float4 yv = *reinterpret_cast<const float4 *>(Ys + k * 36 + col);
-            const float tv0 = k < 16 ? o0[k] : d0[k - 16], tv1 = k < 16 ? o1[k] : d1[k - 16];
-            z0.x = fmaf(tv0, yv.x, z0.x); z0.y = fmaf(tv0, yv.y, z0.y);
-            z0.z = fmaf(tv0, yv.z, z0.z); z0.w = fmaf(tv0, yv.w, z0.w);
-            z1.x = fmaf(tv1, yv.x, z1.x); z1.y = fmaf(tv1, yv.y, z1.y);
-            z1.z = fmaf(tv1, yv.z, z1.z); z1.w = fmaf(tv1, yv.w, z1.w);
-          }
+        for (int k0 = 0; k0 < 32; k0 += 8) {
+          if (rh == 0 && k0 >= 16) continue;
+          auto thi = [&](int r, int k) -> float {  // T[32 + 16 rh + r][32 + k]
+            if (rh == 0) return Sd[sd_idx(2, r, k)];
+            return k < 16 ? So[so_idx(1, r, k)] : Sd[sd_idx(3, r, k - 16)];
+          };
+          const uint32_t a[4] = {to_tf32(thi(lg, k0 + lc)), to_tf32(thi(lg + 8, k0 + lc)),
+                                 to_tf32(thi(lg, k0 + lc + 4)), to_tf32(thi(lg + 8, k0 + lc + 4))};
+          const float *yk0 = Ys + (k0 + lc) * 36 + 16 * ch + lg;
+          const float *yk1 = Ys + (k0 + lc + 4) * 36 + 16 * ch + lg;
+          const uint32_t b0[2] = {to_tf32(yk0[0]), to_tf32(yk1[0])};
+          const uint32_t b1[2] = {to_tf32(yk0[8]), to_tf32(yk1[8])};
+          mma_tf32_16x8x8(z0, a, b0);
+          mma_tf32_16x8x8(z1, a, b1);
         }
-        bar_sync(bar_id, 128);  // every read of the lower-left L block is done
-        *reinterpret_cast<float4 *>(Sl + sl_idx(r0, col)) = make_float4(-z0.x, -z0.y, -z0.z, -z0.w);
-        *reinterpret_cast<float4 *>(Sl + sl_idx(r0 + 1, col)) =
-            make_float4(-z1.x, -z1.y, -z1.z, -z1.w);
+        // only Ys, Sd and So are read in this stage, so the lower-left block can be overwritten
+        float *s0 = Sl + sl_idx(16 * rh + lg, 16 * ch + 2 * lc);
+        float *s1 = Sl + sl_idx(16 * rh + lg + 8, 16 * ch + 2 * lc);
+        *reinterpret_cast<float2 *>(s0) = make_float2(-z0[0], -z0[1]);
+        *reinterpret_cast<float2 *>(s1) = make_float2(-z0[2], -z0[3]);
+        *reinterpret_cast<float2 *>(s0 + 8) = make_float2(-z1[0], -z1[1]);
+        *reinterpret_cast<float2 *>(s1 + 8) = make_float2(-z1[2], -z1[3]);
       }
       bar_sync(bar_id, 128);
       {  // Tb = T diag(beta) -> TP rows 0-63, 32 columns per thread

@@ -143,6 +143,25 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ------------------------------------------------ warp-level TF32 MMA (small blocks)
+// Round-to-nearest conversion of an fp32 value to the TF32 operand format.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// D (16 x 8, fp32) += A (16 x 8, row) * B (8 x 8, col) with TF32 inputs.  With
+// g = lane / 4 and c = lane % 4: a = {A[g][c], A[g+8][c], A[g][c+4], A[g+8][c+4]},
+// b = {B[c][g], B[c+4][g]}, d = {D[g][2c], D[g][2c+1], D[g+8][2c], D[g+8][2c+1]}.
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
+                                                const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // ------------------------------------------------------ MMA and descriptors
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
 //   K-major  : rows of 128 B hold 64 bf16 along K; 8-row groups `sbo` bytes apart.
