@@ -77,7 +77,7 @@ struct L {
   static constexpr uint32_t kBeta = kLtri + 16384;            // fp32 beta [2][64]
   static constexpr uint32_t kGamma = kBeta + 512;             // fp32 e^Gl [2][128]
   static constexpr uint32_t kBars = kGamma + 1024;            // mbarriers
-  static constexpr uint32_t kMisc = kBars + 128;              // tmem slot, abort flag
+  static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
@@ -87,9 +87,12 @@ static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kSb % 1024 == 0 &&
 static_assert(L::kAlloc <= 232448, "shared memory budget");
 
 // mbarrier slots
+// full / empty: stage loaded / stage free (K-side done with it); ready: a chunk's
+// state-independent operands are complete; tmfree / accfree / kcfree: the S-side
+// has finished with the group's TMEM operand, ACC[s], Kc[s].
 enum : uint32_t {
-  kFull0 = 0, kEmpty0 = 2, kReady0 = 4, kDone0 = 6, kMmaK0 = 8, kMmaS = 10, kFinK0 = 11, kFinS = 13,
-  kNever = 14, kNumBars = 15
+  kFull0 = 0, kEmpty0 = 2, kReady0 = 4, kTmFree0 = 6, kAccFree0 = 8, kKcFree0 = 10, kMmaK0 = 12,
+  kMmaS = 14, kFinK0 = 15, kFinS = 17, kNever = 18, kNumBars = 19
 };
 
 // TMEM columns
@@ -262,8 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float bnext = 0.f;  // beta of this chunk, loaded early to hide the global latency
       if (t < C && t < len) bnext = __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]);
       // one thread polls the mbarriers, the others park on the named barrier
+      const uint32_t prev = ((c >> 1) - 1) & 1;  // parity of chunk c - 2's release signals
       if (t == 0) {
-        if (c >= 2) ctx.wait(kDone0 + s, ((c >> 1) - 1) & 1);  // Kc[s], ACC[s], gamma[s] free
+        if (c >= 2) ctx.wait(kTmFree0 + s, prev);  // the S-side read this group's TMEM operand
         ctx.wait(kFull0 + s, (c >> 1) & 1);
       }
       bar_sync(bar_id, 128);
@@ -284,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
+        if (c >= 2) ctx.wait(kKcFree0 + s, prev);  // Kc[s] and gamma[s] are free again
       }
       ++kph;
       bar_sync(bar_id, 128);
@@ -575,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // [Tb; Pb] [Kh | V] -> D2 (W | A^qk W) and ACC[s] (U | O_intra)
       if (t == 0) {
+        if (c >= 2) ctx.wait(kAccFree0 + s, prev);  // ACC[s] is free again
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id_v = idesc_bf16(128, BV, false, true);
@@ -592,35 +598,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++kph;
       bar_sync(bar_id, 128);
       tc_fence_after();
-      {  // -W over Kh, Qh - A^qk W over Qh (the A operand of the state product)
+      {  // [-W; Qh - A^qk W] (the A operand of the state product) -> this group's TMEM,
+         // packed bf16 pairs in columns 0-63, over the fp32 W this thread has read
         const int i = row & 63;
-        const uint32_t qoff = row < 64 ? 0u : L::kQoff;
         const uint32_t rx = static_cast<uint32_t>(i & 7);
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {  // channels 64 hh .. 64 hh + 63
           float a[64];
           tmem_ld64(tm + lane_base + 64 * hh, a);
-          const uint32_t base = st + hh * L::kKQ1 + qoff + i * 128;
+          uint32_t pk[32];
+          if (row < 64) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t addr = base + ((static_cast<uint32_t>(q) ^ rx) << 4);
-            float v[8];
-            if (row < 64) {
+            for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16x2(-a[2 * jj], -a[2 * jj + 1]);
+          } else {
+            const uint32_t base = st + hh * L::kKQ1 + L::kQoff + i * 128;
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) v[jj] = -a[8 * q + jj];
-            } else {
+            for (int q = 0; q < 8; ++q) {
               float qb[8];
-              unpack8(ld_shared_v4(addr), qb);
+              unpack8(ld_shared_v4(base + ((static_cast<uint32_t>(q) ^ rx) << 4)), qb);
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) v[jj] = qb[jj] - a[8 * q + jj];
+              for (int jj = 0; jj < 4; ++jj)
+                pk[4 * q + jj] = pack_bf16x2(qb[2 * jj] - a[8 * q + 2 * jj],
+                                             qb[2 * jj + 1] - a[8 * q + 2 * jj + 1]);
             }
-            st8(addr, v);
           }
+          tmem_st32(tm + lane_base + 32 * hh, pk);
         }
       }
-      fence_async_smem();
       tc_fence_before();
       bar_sync(bar_id, 128);
+      if (t == 0) mbar_arrive(ctx.bar(kEmpty0 + s));  // the stage may be refilled
       if (t == 0) mbar_arrive(ctx.bar(kReady0 + s));
     }
     if (t == 0) {  // all of this group's MMAs retired before TMEM is released
@@ -661,19 +668,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == 0) ctx.wait(kReady0 + s, (c >> 1) & 1);
       bar_sync(2, 128);
       tc_fence_after();
-      // a4/a5: [U; O_intra] += [-W; Q'] S
+      const float gm = gamma[s * 128 + t];  // read early: gamma[s] is rewritten after kcfree
+      // a4/a5: [U; O_intra] += [-W; Q'] S, the A operand from the K-side group's TMEM
       if (t == 0) {
         constexpr uint32_t id = idesc_bf16(128, BV, false, true);
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8) {
-          const uint64_t ad = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(sbase + L::kSb + k8 * 2048, 8192, 1024);
-          mma_bf16(tmem + kAcc0 + s * BV, ad, bd, id, 1);
+          mma_bf16_tmem_a(tmem + kAcc0 + s * BV, tmem + 128u * s + 8 * k8, bd, id, 1);
         }
         mma_commit(ctx.bar(kMmaS));
-        mma_commit(ctx.bar(kEmpty0 + s));  // the stage may be refilled once this retires
+        ctx.wait(kMmaS, sph & 1);
+        mbar_arrive(ctx.bar(kTmFree0 + s));  // the group's TMEM operand has been read
       }
-      if (t == 0) ctx.wait(kMmaS, sph & 1);
       ++sph;
       bar_sync(2, 128);
       tc_fence_after();
@@ -714,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_sync(2, 128);
       // a4: Kc^T E -> D4
       if (t == 0) {
+        mbar_arrive(ctx.bar(kAccFree0 + s));  // E and O have been read out of ACC[s]
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, BV, true, true);
         const uint32_t kc = sbase + L::kKc + s * 16384;
@@ -724,13 +732,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tmem + kD4, ad, bd, id, k4 > 0);
         }
         mma_commit(ctx.bar(kMmaS));
+        ctx.wait(kMmaS, sph & 1);
+        mbar_arrive(ctx.bar(kKcFree0 + s));  // Kc[s] has been read
       }
-      if (t == 0) ctx.wait(kMmaS, sph & 1);
       ++sph;
       bar_sync(2, 128);
       tc_fence_after();
       {
-        const float gm = gamma[s * 128 + t];
         float a[32];
 #pragma unroll
         for (int hh = 0; hh < BV / 32; ++hh) {
@@ -739,9 +747,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 32; ++jj) S[32 * hh + jj] = fmaf(gm, S[32 * hh + jj], gm * a[jj]);
         }
       }
-      tc_fence_before();
-      bar_sync(2, 128);
-      if (t == 0) mbar_arrive(ctx.bar(kDone0 + s));
     }
     if (p.final_state) {
 #pragma unroll
