@@ -9,10 +9,16 @@
 //   Kh  = K * exp(G)     Qh = Q * exp(G)     Kc = K * exp(-G)
 //   [Kh; Qh] Kc^T              -> rows: A^kk / beta_i (j < i), A^qk (j <= i)
 //   T   = (I + A^kk)^-1,  Tb = T diag(beta)            (fp32 triangular solve)
-//   Pb  = A^qk Tb
-//   [Tb; Pb] [Kh | V]          -> W = Tb Kh, U = Tb V; A^qk W, O_intra = Pb V
-//   [E; O/s] = [U; O_intra] + [-W; Qh - A^qk W] S      (state-dependent)
-//   S  <- gamma * S + gamma * (Kc^T E)                  (state-dependent)
+//   [Tb; A^qk] [Kh | V]        -> rows 0-63: W = Tb Kh, U = Tb V;  rows 64-127: A^qk V
+//   [E; X] = [U; A^qk V] + [-W; Qh] S                  (state-dependent; E = U - W S)
+//   O / s  = X + A^qk (E - V) = Qh S + A^qk E          (state-dependent)
+//   S  <- gamma * S + gamma * (Kc^T (E - V) + Kc^T V)   (state-dependent)
+//
+// The output is the inter-chunk term Qh S plus the masked intra-chunk product
+// A^qk applied to the new values E.  E - V is the operand the state side rounds
+// to bf16 for both of its last two products: the A^qk V and Kc^T V terms it is
+// combined with were formed from V itself, so they add back exactly what was
+// subtracted.
 //
 // exp(G) <= 1 and exp(-G) <= exp(-G_last); every factor stays finite as long
 // as a chunk's total log decay per channel is above -80 (checked; beyond it
@@ -21,10 +27,12 @@
 //
 // One CTA owns (sequence, head, 64-column d_v tile) and walks its chunks in
 // order.  Warp roles:
-//   warps 0-7   K-side: everything that does not depend on S, one chunk ahead
-//   warps 8-11  S-side: holds S (fp32, one key channel per thread) in registers
-//               and runs the two state-dependent products per chunk
-//   warp  12    TMA producer (q, k, g, v boxes into a 2-stage ring) and TMEM owner
+//   warps 0-7    K-side: two groups of 4 warps on alternating chunks, everything
+//                that does not depend on S
+//   warps 8-11   S-side: holds S (fp32, one key channel per thread) in registers
+//                and runs the state-dependent products per chunk
+//   warps 12-13  TMA producers, one per stage: the q, g, k and v parts of a stage
+//                are refilled as soon as each is released; warp 12 owns the TMEM
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // KDA_ERR_DEVICE_TIMEOUT in the status word and runs to completion without
 // waiting again (outputs are then undefined, nothing blocks or faults).
@@ -47,7 +55,7 @@ constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr int BV = 64;                      // d_v columns per CTA
-constexpr int kThreads = 416;  // 8 K-side warps, 4 S-side warps, 1 producer warp
+constexpr int kThreads = 448;  // 8 K-side warps, 4 S-side warps, 2 producer warps
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinChunkLogDecay = -80.f;
@@ -69,35 +77,40 @@ struct L {
   // the g area later holds the fp32 A^kk / T in the compact solve layout
   static constexpr uint32_t kKQ1 = 16384, kQoff = 8192, kG = 32768, kV = 49152;
   static constexpr uint32_t kStageBytes = 49152 + C * BV * 2;
-  static constexpr uint32_t kKc = 2 * kStageBytes;          // 2 x Kc [ch0-63 | ch64-127]
-  static constexpr uint32_t kTP = kKc + 2 * 16384;            // 2 x [Tb rows 0-63 | A^qk / Pb rows 64-127]
-  static constexpr uint32_t kSb = kTP + 2 * 16384;            // S in bf16, [DK rows][BV]
-  static constexpr uint32_t kEb = kSb + DK * BV * 2;          // E in bf16, [C rows][BV]
-  static constexpr uint32_t kLtri = kEb + C * BV * 2;         // bf16 [Ltri; Ltri], 128 x 64
-  static constexpr uint32_t kBeta = kLtri + 16384;            // fp32 beta [2][64]
-  static constexpr uint32_t kGamma = kBeta + 512;             // fp32 e^Gl [2][128]
-  static constexpr uint32_t kBars = kGamma + 1024;            // mbarriers
-  static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, abort flag
+  static constexpr uint32_t kKc = 2 * kStageBytes;      // 3 x Kc [ch0-63 | ch64-127], slot = chunk % 3
+  static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [Tb rows 0-63 | A^qk rows 64-127]
+  static constexpr uint32_t kSb = kTP + 2 * 16384;        // S in bf16 [DK rows][BV]; rows 0-63 then E - V
+  static constexpr uint32_t kLtri = kSb + DK * BV * 2;    // bf16 [Ltri; Ltri], 128 x 64
+  static constexpr uint32_t kBeta = kLtri + 16384;        // fp32 beta [2][64]
+  static constexpr uint32_t kGamma = kBeta + 512;         // fp32 e^Gl [2][128]
+  static constexpr uint32_t kBars = kGamma + 1024;        // mbarriers
+  static constexpr uint32_t kMisc = kBars + 256;          // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
 static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kSb % 1024 == 0 &&
-                  L::kEb % 1024 == 0 && L::kLtri % 1024 == 0,
+                  L::kLtri % 1024 == 0,
               "operand tiles must be 1024-byte aligned");
 static_assert(L::kAlloc <= 232448, "shared memory budget");
 
-// mbarrier slots
-// full / empty: stage loaded / stage free (K-side done with it); ready: a chunk's
-// state-independent operands are complete; tmfree / accfree / kcfree: the S-side
-// has finished with the group's TMEM operand, ACC[s], Kc[s].
+// mbarrier slots (count 1 each; [s] = stage / K-side group, [b] = Kc slot)
 enum : uint32_t {
-  kFull0 = 0, kEmpty0 = 2, kReady0 = 4, kTmFree0 = 6, kAccFree0 = 8, kKcFree0 = 10, kMmaK0 = 12,
-  kMmaS = 14, kFinK0 = 15, kFinS = 17, kNever = 18, kNumBars = 19
+  kFullQ0 = 0, kFullG0 = 2, kFullK0 = 4, kFullV0 = 6,        // part of stage s loaded
+  kEmptyQ0 = 8, kEmptyG0 = 10, kEmptyK0 = 12, kEmptyV0 = 14,  // part of stage s released
+  kReady0 = 16,   // K-side -> S-side: the chunk's state-independent operands are complete
+  kSDone0 = 18,   // S-side -> K-side: Aop[s], ACC[s] and TP[s] have been read
+  kGmRead0 = 20,  // S-side -> K-side: gamma[s] has been read
+  kKcFree0 = 22,  // S-side -> K-side: Kc[b] has been read (3 slots)
+  kMmaK0 = 25, kMmaS = 27, kFinK0 = 28, kFinS = 30, kNever = 31, kNumBars = 32
 };
+static_assert(kNumBars * 8 <= 256, "mbarrier area");
 
 // TMEM columns
-// K-side group kw: [128 kw, 128 kw + 128) holds G, then D1 (+0) and DP (+64), then D2.
-constexpr uint32_t kAcc0 = 256, kD4 = 256 + 2 * BV;
+//   [128 kw, +128)   K-side group kw: G, then D1 (+0), then D2
+//   [256 + 64 s, +64) Aop[s]: the A operand [-W; Qh] of the state product (bf16
+//                    pairs), then D4 = Kc^T E (fp32)
+//   [384 + 64 s, +64) ACC[s]: [U; A^qk V], then [E; X], then [.; O / s]
+constexpr uint32_t kAop0 = 256, kAcc0 = 384;
 
 struct TcParams {
   const __nv_bfloat16 *beta;
@@ -199,49 +212,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 12) {
-    // ------------------------------------------------------------ producer
+  if (warp >= 12) {
+    // ------------------------------------------------------------ producers
+    // warp 12 fills stage 0 (even chunks), warp 13 stage 1 (odd chunks).  The parts
+    // of a stage are released at different points of the chunk (q after the
+    // state-product operand has been copied out, g after the solve, k after the
+    // W / U product, v after the state side's last product) and each is refilled
+    // for chunk c + 2 as soon as it is free.
     if ((tid & 31) == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_g);
-      tma_prefetch_desc(&tm_v);
-      int issued[2] = {-1, -1};
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        if (c >= 2) ctx.wait(kEmpty0 + s, ((c >> 1) - 1) & 1);
-        if (*abort_flag) break;
-        const uint32_t st = sbase + s * L::kStageBytes;
-        const uint32_t fb = ctx.bar(kFull0 + s);
-        const int t0 = bos + c * C;
-        mbar_arrive_expect_tx(fb, L::kStageBytes);
-        tma_load_3d(st, &tm_k, fb, 0, h, t0);
-        tma_load_3d(st + L::kQoff, &tm_q, fb, 0, h, t0);
-        tma_load_3d(st + L::kKQ1, &tm_k, fb, 64, h, t0);
-        tma_load_3d(st + L::kKQ1 + L::kQoff, &tm_q, fb, 64, h, t0);
-        tma_load_3d(st + L::kG, &tm_g, fb, 0, h, t0);
-        tma_load_3d(st + L::kG + 8192, &tm_g, fb, 64, h, t0);
-        tma_load_3d(st + L::kV, &tm_v, fb, tile * BV, h, t0);
-        issued[s] = c;
+      const int s = warp - 12;
+      if (s == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_g);
+        tma_prefetch_desc(&tm_v);
       }
-      // never leave a copy in flight: wait (bounded) for the last load of each stage
-      for (int s = 0; s < 2; ++s)
-        if (issued[s] >= 0) mbar_wait(ctx.bar(kFull0 + s), (issued[s] >> 1) & 1, kWaitCycles);
+      const uint32_t st = sbase + s * L::kStageBytes;
+      int last[4] = {-1, -1, -1, -1};  // last chunk loaded, per part
+      for (int c = s; c < nchunks && !*abort_flag; c += 2) {
+        const uint32_t prev = ((c >> 1) - 1) & 1;
+        const int t0 = bos + c * C;
+#pragma unroll 1
+        for (int part = 0; part < 4; ++part) {  // q, g, k, v: the order they are released in
+          if (c >= 2) ctx.wait(kEmptyQ0 + 2 * part + s, prev);
+          if (*abort_flag) break;
+          const uint32_t fb = ctx.bar(kFullQ0 + 2 * part + s);
+          if (part == 0) {
+            mbar_arrive_expect_tx(fb, 16384);
+            tma_load_3d(st + L::kQoff, &tm_q, fb, 0, h, t0);
+            tma_load_3d(st + L::kKQ1 + L::kQoff, &tm_q, fb, 64, h, t0);
+          } else if (part == 1) {
+            mbar_arrive_expect_tx(fb, 16384);
+            tma_load_3d(st + L::kG, &tm_g, fb, 0, h, t0);
+            tma_load_3d(st + L::kG + 8192, &tm_g, fb, 64, h, t0);
+          } else if (part == 2) {
+            mbar_arrive_expect_tx(fb, 16384);
+            tma_load_3d(st, &tm_k, fb, 0, h, t0);
+            tma_load_3d(st + L::kKQ1, &tm_k, fb, 64, h, t0);
+          } else {
+            mbar_arrive_expect_tx(fb, C * BV * 2);
+            tma_load_3d(st + L::kV, &tm_v, fb, tile * BV, h, t0);
+          }
+          last[part] = c;
+        }
+      }
+      // never leave a copy in flight: wait (bounded) for the last load of every part
+      for (int part = 0; part < 4; ++part)
+        if (last[part] >= 0)
+          mbar_wait(ctx.bar(kFullQ0 + 2 * part + s), (last[part] >> 1) & 1, kWaitCycles);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ K-side
     // Two groups of 4 warps; group kw takes the chunks c = kw, kw + 2, ... and
-    // owns stage kw, Kc[kw], TP[kw], beta[kw] and TMEM columns [128 kw, 128 kw + 128),
-    // so the dependent chain of one chunk overlaps the other group's chunk.
+    // owns stage kw, TP[kw], beta[kw], Aop[kw], ACC[kw] and TMEM columns
+    // [128 kw, 128 kw + 128), so the dependent chain of one chunk overlaps the
+    // other group's chunk.  Kc rotates over three slots (chunk % 3).
     const int kw = warp >> 2;
     const int t = tid & 127;            // thread within the group
     const int wq = warp & 3;            // TMEM lane quarter of this warp
-    const int row = 32 * wq + (t & 31); // TMEM lane = row of an M = 128 result
+    const int row = 32 * wq + (t & 31); // TMEM lane = row of an M = 128 result (== t)
     const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t bar_id = kw ? 3u : 1u;
-    const uint32_t tm = tmem + 128u * kw;  // G / D1 (+0) / DP (+64) / D2 (+0), time-shared
+    const uint32_t tm = tmem + 128u * kw;          // G, then D1 (+0), then D2
+    const uint32_t aop = tmem + kAop0 + 64u * kw;  // [-W; Qh] for the state product
     const uint32_t st = sbase + kw * L::kStageBytes;
-    const uint32_t kcb = sbase + L::kKc + kw * 16384;
     const uint32_t tp = sbase + L::kTP + kw * 16384;
     float *betas = betas_all + kw * 64;
     // compact fp32 solve layout in the stage's g area (after the cumsum product has read g)
@@ -250,6 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Sl = So + 2 * 16 * kSdLd;                                            // [32][36]
     float *Ys = reinterpret_cast<float *>(smem + L::kTP + kw * 16384);          // TP rows 0-63
     const uint32_t mma_bar = ctx.bar(kMmaK0 + kw);
+    // a1: G = [Ltri; Ltri] g on the tensor cores, straight from the TMA'd g tile:
+    // the chunk-local inclusive cumsum per channel (rows 64-127 repeat rows 0-63)
+    auto issue_cumsum = [&]() {
+      tc_fence_after();
+      constexpr uint32_t id = idesc_bf16(128, 128, false, true);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const uint64_t ad = sdesc_sw128(sbase + L::kLtri + k4 * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(st + L::kG + k4 * 2048, 8192, 1024);
+        mma_bf16(tm, ad, bd, id, k4 > 0);
+      }
+      mma_commit(mma_bar);
+    };
     if ((p.flags & 1) && tid == 0) {
       // test hook: a wait that can only time out
       if (!mbar_wait(ctx.bar(kNever), 0, 2000000LL)) {
@@ -262,37 +309,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = kw;  // == c & 1
       const int t0 = bos + c * C;
       const int len = min(C, eos - t0);
+      const int kb = c % 3;  // Kc slot
+      const uint32_t kcb = sbase + L::kKc + kb * 16384;
       float bnext = 0.f;  // beta of this chunk, loaded early to hide the global latency
       if (t < C && t < len) bnext = __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]);
       // one thread polls the mbarriers, the others park on the named barrier
       const uint32_t prev = ((c >> 1) - 1) & 1;  // parity of chunk c - 2's release signals
+      const uint32_t cur = (c >> 1) & 1;          // parity of this chunk's loads
       if (t == 0) {
-        if (c >= 2) ctx.wait(kTmFree0 + s, prev);  // the S-side read this group's TMEM operand
-        ctx.wait(kFull0 + s, (c >> 1) & 1);
-      }
-      bar_sync(bar_id, 128);
-
-      // a1: G = [Ltri; Ltri] g on the tensor cores, straight from the TMA'd g tile:
-      // the chunk-local inclusive cumsum per channel (rows 64-127 repeat rows 0-63).
-      // Each thread then owns row r and 64 channels of the elementwise decay work.
-      const int r = row & 63, half = row >> 6;
-      const uint32_t kq = st + half * L::kKQ1;
-      if (t == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc_bf16(128, 128, false, true);
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(sbase + L::kLtri + k4 * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(st + L::kG + k4 * 2048, 8192, 1024);
-          mma_bf16(tm, ad, bd, id, k4 > 0);
+        if (c < 2) {  // later chunks had their cumsum product issued at the end of chunk c - 2
+          ctx.wait(kFullG0 + s, cur);
+          issue_cumsum();
         }
-        mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
-        if (c >= 2) ctx.wait(kKcFree0 + s, prev);  // Kc[s] and gamma[s] are free again
+        ctx.wait(kFullK0 + s, cur);
+        ctx.wait(kFullQ0 + s, cur);
+        if (c >= 3) ctx.wait(kKcFree0 + kb, ((c / 3) - 1) & 1);  // chunk c - 3 is done with Kc[kb]
+        if (c >= 2) ctx.wait(kGmRead0 + s, prev);                  // chunk c - 2 is done with gamma[s]
       }
       ++kph;
       bar_sync(bar_id, 128);
       tc_fence_after();
+
+      // Each thread owns row r and 64 channels of the elementwise decay work.
+      const int r = row & 63, half = row >> 6;
+      const uint32_t kq = st + half * L::kKQ1;
       const bool valid = r < len;  // rows past the sequence end write and decay nothing
       const float vm = valid ? 1.f : 0.f;
 #pragma unroll 1
@@ -347,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
+        if (c >= 2) ctx.wait(kSDone0 + s, prev);  // chunk c - 2 is done with TP[s], Aop[s], ACC[s]
       }
       ++kph;
       bar_sync(bar_id, 128);
@@ -412,7 +454,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int r2 = m + 1; r2 < 16; ++r2) acc[r2] = fmaf(Ab[r2 * kSdLd + m], x[m], acc[r2]);
           }
+        } else {
+          // meanwhile rows 64-127 copy Qh (bf16 pairs, all 128 channels of token
+          // row - 64) into Aop[s]: the lower half of the state product's A operand
+          const int i = row - 64;
+          const uint32_t rx = static_cast<uint32_t>(i & 7);
+#pragma unroll 1
+          for (int hq = 0; hq < 2; ++hq) {
+            const uint32_t base = st + hq * L::kKQ1 + L::kQoff + i * 128;
+            uint32_t pk[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 w = ld_shared_v4(base + ((static_cast<uint32_t>(q) ^ rx) << 4));
+              pk[4 * q] = w.x; pk[4 * q + 1] = w.y; pk[4 * q + 2] = w.z; pk[4 * q + 3] = w.w;
+            }
+            tmem_st32(aop + lane_base + 32 * hq, pk);
+          }
         }
+        tc_fence_before();
         bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
         if (t < 64) {
           float *Tb = Sd + sd_idx(I, 0, cc);
@@ -421,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       bar_sync(bar_id, 128);
+      if (t == 0) mbar_arrive(ctx.bar(kEmptyQ0 + s));  // the q area has been read by a2 and the copy
       // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
       // (16 x 8 tiles; TF32 operands rounded to nearest, fp32 accumulation).
       const int lg = (t & 31) >> 2, lc = t & 3;  // fragment coordinates of this lane
@@ -541,46 +601,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           st8(tp + sw128(i, 4 * hh + q), v);
         }
       }
+
       fence_async_smem();
       bar_sync(bar_id, 128);
+      if (t == 0) mbar_arrive(ctx.bar(kEmptyG0 + s));  // the g area (solve scratch) may be refilled
 
-      // Pb = A^qk Tb  (M = 128 with Tb stacked on top; rows 64-127 are used)
+      // [Tb; A^qk] [Kh | V] -> D2 (rows 0-63: W) and ACC[s] (U | A^qk V)
       if (t == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc_bf16(128, 64, false, true);
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(tp + k4 * 2048, 8192, 1024);
-          mma_bf16(tm + 64, ad, bd, id, k4 > 0);
-        }
-        mma_commit(mma_bar);
-        ctx.wait(kMmaK0 + kw, kph & 1);
-      }
-      ++kph;
-      bar_sync(bar_id, 128);
-      tc_fence_after();
-      if (row >= 64) {
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float a[32];
-          tmem_ld32(tm + lane_base + 64 + 32 * hh, a);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float v[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) v[jj] = a[8 * q + jj];
-            st8(tp + sw128(row, 4 * hh + q), v);
-          }
-        }
-      }
-      fence_async_smem();
-      tc_fence_before();
-      bar_sync(bar_id, 128);
-
-      // [Tb; Pb] [Kh | V] -> D2 (W | A^qk W) and ACC[s] (U | O_intra)
-      if (t == 0) {
-        if (c >= 2) ctx.wait(kAccFree0 + s, prev);  // ACC[s] is free again
+        ctx.wait(kFullV0 + s, cur);
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id_v = idesc_bf16(128, BV, false, true);
@@ -594,41 +622,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
+        mbar_arrive(ctx.bar(kEmptyK0 + s));  // Kh (the k area) is no longer read
       }
       ++kph;
       bar_sync(bar_id, 128);
       tc_fence_after();
-      {  // [-W; Qh - A^qk W] (the A operand of the state product) -> this group's TMEM,
-         // packed bf16 pairs in columns 0-63, over the fp32 W this thread has read
-        const int i = row & 63;
-        const uint32_t rx = static_cast<uint32_t>(i & 7);
+      if (row < 64) {  // -W (bf16 pairs) -> Aop[s] rows 0-63, from the fp32 W rows of D2
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {  // channels 64 hh .. 64 hh + 63
           float a[64];
           tmem_ld64(tm + lane_base + 64 * hh, a);
           uint32_t pk[32];
-          if (row < 64) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16x2(-a[2 * jj], -a[2 * jj + 1]);
-          } else {
-            const uint32_t base = st + hh * L::kKQ1 + L::kQoff + i * 128;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float qb[8];
-              unpack8(ld_shared_v4(base + ((static_cast<uint32_t>(q) ^ rx) << 4)), qb);
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj)
-                pk[4 * q + jj] = pack_bf16x2(qb[2 * jj] - a[8 * q + 2 * jj],
-                                             qb[2 * jj + 1] - a[8 * q + 2 * jj + 1]);
-            }
-          }
-          tmem_st32(tm + lane_base + 32 * hh, pk);
+          for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16x2(-a[2 * jj], -a[2 * jj + 1]);
+          tmem_st32(aop + lane_base + 32 * hh, pk);
         }
       }
       tc_fence_before();
       bar_sync(bar_id, 128);
-      if (t == 0) mbar_arrive(ctx.bar(kEmpty0 + s));  // the stage may be refilled
-      if (t == 0) mbar_arrive(ctx.bar(kReady0 + s));
+      if (t == 0) {
+        mbar_arrive(ctx.bar(kReady0 + s));
+        if (c + 2 < nchunks) {  // a1 of chunk c + 2: the group's TMEM columns are free again
+          ctx.wait(kFullG0 + s, cur ^ 1);
+          issue_cumsum();
+        }
+      }
     }
     if (t == 0) {  // all of this group's MMAs retired before TMEM is released
       mma_commit(ctx.bar(kFinK0 + kw));
@@ -655,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = c & 1;
       const int t0 = bos + c * C;
       const int len = min(C, eos - t0);
+      const int kb = c % 3;
       const uint32_t st = sbase + s * L::kStageBytes;
 #pragma unroll
       for (int q = 0; q < BV / 8; ++q) {
@@ -664,89 +683,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         st8(sbase + L::kSb + sw128(t, q), v);
       }
       fence_async_smem();
+      tc_fence_before();
       bar_sync(2, 128);
-      if (t == 0) ctx.wait(kReady0 + s, (c >> 1) & 1);
+      if (t == 0) {
+        // the previous chunk's outputs and state update have been read out of TMEM
+        if (c >= 1) mbar_arrive(ctx.bar(kSDone0 + (s ^ 1)));
+        ctx.wait(kReady0 + s, (c >> 1) & 1);
+      }
       bar_sync(2, 128);
       tc_fence_after();
-      const float gm = gamma[s * 128 + t];  // read early: gamma[s] is rewritten after kcfree
-      // a4/a5: [U; O_intra] += [-W; Q'] S, the A operand from the K-side group's TMEM
+      const float gm = gamma[s * 128 + t];
+      // a4/a5: [E; X] = [U; A^qk V] + [-W; Qh] S, the A operand from Aop[s] in TMEM
       if (t == 0) {
         constexpr uint32_t id = idesc_bf16(128, BV, false, true);
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8) {
           const uint64_t bd = sdesc_sw128(sbase + L::kSb + k8 * 2048, 8192, 1024);
-          mma_bf16_tmem_a(tmem + kAcc0 + s * BV, tmem + 128u * s + 8 * k8, bd, id, 1);
+          mma_bf16_tmem_a(tmem + kAcc0 + s * BV, tmem + kAop0 + 64u * s + 8 * k8, bd, id, 1);
         }
         mma_commit(ctx.bar(kMmaS));
         ctx.wait(kMmaS, sph & 1);
-        mbar_arrive(ctx.bar(kTmFree0 + s));  // the group's TMEM operand has been read
       }
       ++sph;
       bar_sync(2, 128);
+      if (t == 0) mbar_arrive(ctx.bar(kGmRead0 + s));  // every thread has read gamma[s]
       tc_fence_after();
-      {
-        float a[32];
-        if (t < 64) {  // E rows -> bf16 operand
+      if (t < 64) {  // E - V (rows 0-63) -> bf16 over the first half of Sb
 #pragma unroll
-          for (int hh = 0; hh < BV / 32; ++hh) {
-            tmem_ld32(tmem + lane_base + kAcc0 + s * BV + 32 * hh, a);
+        for (int hh = 0; hh < BV / 32; ++hh) {
+          float a[32];
+          tmem_ld32(tmem + lane_base + kAcc0 + s * BV + 32 * hh, a);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float v[8];
+          for (int q = 0; q < 4; ++q) {
+            float vv[8], e[8];
+            unpack8(ld_shared_v4(st + L::kV + sw128(t, 4 * hh + q)), vv);
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) v[jj] = a[8 * q + jj];
-              st8(sbase + L::kEb + sw128(t, 4 * hh + q), v);
-            }
-          }
-        } else {  // output rows
-          const int i = t - 64;
-          __nv_bfloat16 *orow = p.out + ((size_t)(t0 + i) * H + h) * DV + tile * BV;
-#pragma unroll
-          for (int hh = 0; hh < BV / 32; ++hh) {
-            tmem_ld32(tmem + lane_base + kAcc0 + s * BV + 32 * hh, a);
-            if (i < len) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                float v[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) v[jj] = p.scale * a[8 * q + jj];
-                *reinterpret_cast<uint4 *>(orow + 32 * hh + 8 * q) = pack8(v);
-              }
-            }
+            for (int jj = 0; jj < 8; ++jj) e[jj] = a[8 * q + jj] - vv[jj];
+            st8(sbase + L::kSb + sw128(t, 4 * hh + q), e);
           }
         }
       }
       fence_async_smem();
       tc_fence_before();
       bar_sync(2, 128);
-      // a4: Kc^T E -> D4
+      // a4: D4 = Kc^T (E - V) + Kc^T V over Aop[s] (read by the product above);
+      // a5: ACC[s] += [Tb; A^qk] (E - V), which turns rows 64-127 into O / s
       if (t == 0) {
-        mbar_arrive(ctx.bar(kAccFree0 + s));  // E and O have been read out of ACC[s]
         tc_fence_after();
-        constexpr uint32_t id = idesc_bf16(128, BV, true, true);
-        const uint32_t kc = sbase + L::kKc + s * 16384;
+        constexpr uint32_t id4 = idesc_bf16(128, BV, true, true);
+        constexpr uint32_t ido = idesc_bf16(128, BV, false, true);
+        const uint32_t kc = sbase + L::kKc + kb * 16384;
+        const uint32_t tps = sbase + L::kTP + s * 16384;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const uint64_t ad = sdesc_sw128(kc + k4 * 2048, 8192, 1024);
-          const uint64_t bd = sdesc_sw128(sbase + L::kEb + k4 * 2048, 8192, 1024);
-          mma_bf16(tmem + kD4, ad, bd, id, k4 > 0);
+          const uint64_t be = sdesc_sw128(sbase + L::kSb + k4 * 2048, 8192, 1024);
+          const uint64_t bv = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
+          mma_bf16(tmem + kAop0 + 64u * s, ad, be, id4, k4 > 0);
+          mma_bf16(tmem + kAop0 + 64u * s, ad, bv, id4, 1);
+          mma_bf16(tmem + kAcc0 + s * BV, sdesc_sw128(tps + k4 * 32, 16, 1024), be, ido, 1);
         }
         mma_commit(ctx.bar(kMmaS));
         ctx.wait(kMmaS, sph & 1);
-        mbar_arrive(ctx.bar(kKcFree0 + s));  // Kc[s] has been read
+        mbar_arrive(ctx.bar(kKcFree0 + kb));  // Kc[kb] has been read
+        mbar_arrive(ctx.bar(kEmptyV0 + s));   // the v tile has been read
       }
       ++sph;
       bar_sync(2, 128);
       tc_fence_after();
-      {
+      if (t >= 64) {  // output rows
+        float a[32];
+        const int i = t - 64;
+        __nv_bfloat16 *orow = p.out + ((size_t)(t0 + i) * H + h) * DV + tile * BV;
+#pragma unroll
+        for (int hh = 0; hh < BV / 32; ++hh) {
+          tmem_ld32(tmem + lane_base + kAcc0 + s * BV + 32 * hh, a);
+          if (i < len) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float v[8];
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) v[jj] = p.scale * a[8 * q + jj];
+              *reinterpret_cast<uint4 *>(orow + 32 * hh + 8 * q) = pack8(v);
+            }
+          }
+        }
+      }
+      {  // the state update, D4 from Aop[s]
         float a[32];
 #pragma unroll
         for (int hh = 0; hh < BV / 32; ++hh) {
-          tmem_ld32(tmem + lane_base + kD4 + 32 * hh, a);
+          tmem_ld32(tmem + lane_base + kAop0 + 64u * s + 32 * hh, a);
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) S[32 * hh + jj] = fmaf(gm, S[32 * hh + jj], gm * a[jj]);
         }
       }
+      tc_fence_before();
     }
     if (p.final_state) {
 #pragma unroll
