@@ -82,8 +82,8 @@ struct L {
   static constexpr uint32_t kSb = kTP + 2 * 16384;        // S in bf16 [DK rows][BV]; rows 0-63 then E - V
   static constexpr uint32_t kLtri = kSb + DK * BV * 2;    // bf16 [Ltri; Ltri], 128 x 64
   static constexpr uint32_t kBeta = kLtri + 16384;        // fp32 beta [2][64]
-  static constexpr uint32_t kGamma = kBeta + 512;         // fp32 e^Gl [2][128]
-  static constexpr uint32_t kBars = kGamma + 1024;        // mbarriers
+  static constexpr uint32_t kGlast = kBeta + 512;         // fp32 G_last [2][128]
+  static constexpr uint32_t kBars = kGlast + 1024;        // mbarriers
   static constexpr uint32_t kMisc = kBars + 256;          // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
@@ -98,9 +98,9 @@ enum : uint32_t {
   kFullQ0 = 0, kFullG0 = 2, kFullK0 = 4, kFullV0 = 6,        // part of stage s loaded
   kEmptyQ0 = 8, kEmptyG0 = 10, kEmptyK0 = 12, kEmptyV0 = 14,  // part of stage s released
   kReady0 = 16,   // K-side -> S-side: the chunk's state-independent operands are complete
-  kSDone0 = 18,   // S-side -> K-side: Aop[s], ACC[s] and TP[s] have been read
-  kGmRead0 = 20,  // S-side -> K-side: gamma[s] has been read
-  kKcFree0 = 22,  // S-side -> K-side: Kc[b] has been read (3 slots)
+  kSDone0 = 18,   // S-side -> K-side: Aop[s] and ACC[s] have been read
+  kGmRead0 = 20,  // S-side -> K-side: G_last[s] has been read
+  kKcFree0 = 22,  // S-side -> K-side: Kc[b] (and TP of that chunk) read (3 slots)
   kMmaK0 = 25, kMmaS = 27, kFinK0 = 28, kFinS = 30, kNever = 31, kNumBars = 32
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier area");
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   float *betas_all = reinterpret_cast<float *>(smem + L::kBeta);
-  float *gamma = reinterpret_cast<float *>(smem + L::kGamma);
+  float *glast = reinterpret_cast<float *>(smem + L::kGlast);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
 
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctx.wait(kFullK0 + s, cur);
         ctx.wait(kFullQ0 + s, cur);
         if (c >= 3) ctx.wait(kKcFree0 + kb, ((c / 3) - 1) & 1);  // chunk c - 3 is done with Kc[kb]
-        if (c >= 2) ctx.wait(kGmRead0 + s, prev);                  // chunk c - 2 is done with gamma[s]
+        if (c >= 2) ctx.wait(kGmRead0 + s, prev);                  // chunk c - 2 is done with G_last[s]
       }
       ++kph;
       bar_sync(bar_id, 128);
@@ -334,41 +334,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Each thread owns row r and 64 channels of the elementwise decay work.
       const int r = row & 63, half = row >> 6;
       const uint32_t kq = st + half * L::kKQ1;
-      const bool valid = r < len;  // rows past the sequence end write and decay nothing
-      const float vm = valid ? 1.f : 0.f;
+      // Rows past the sequence end are zeroed and get unit factors (G log2 e taken
+      // as 0), so no exp(-G) of the next sequence's decays can overflow there.
+      const bool valid = r < len;
+      const float lg2 = valid ? kLog2e : 0.f;
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float G[32];
         tmem_ld32(tm + lane_base + 64 * half + 32 * hh, G);
-        if (r == len - 1) {  // the chunk's last valid row: gamma = exp(G_last), range check
-          bool bad = false;
+        if (r == len - 1) {  // the chunk's last valid row: G_last for the state side
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            *reinterpret_cast<float4 *>(gamma + s * 128 + 64 * half + 32 * hh + j) =
-                make_float4(fast_exp2(G[j] * kLog2e), fast_exp2(G[j + 1] * kLog2e),
-                            fast_exp2(G[j + 2] * kLog2e), fast_exp2(G[j + 3] * kLog2e));
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) bad |= !(G[j + jj] >= kMinChunkLogDecay);
-          }
-          if (bad) atomicCAS(p.status, 0u, kStatusGateRange);
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(glast + s * 128 + 64 * half + 32 * hh + j) =
+                make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
         }
+        // bf16 pairs: exp(+-G) rounded to bf16, then one bf16 product per output pair
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t addr = kq + sw128(r, 4 * hh + q);
-          float kv[8], qv[8], kh[8], qh[8], kc[8];
-          unpack8(ld_shared_v4(addr), kv);
-          unpack8(ld_shared_v4(addr + L::kQoff), qv);
+          uint4 kw = ld_shared_v4(addr), qw = ld_shared_v4(addr + L::kQoff);
+          if (!valid) kw = qw = make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t kp[4] = {kw.x, kw.y, kw.z, kw.w}, qp[4] = {qw.x, qw.y, qw.z, qw.w};
+          uint32_t kh[4], qh[4], kc[4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float d = G[8 * q + j] * kLog2e;  // G log2 e, in [Gl log2 e, 0]
-            const float f = fast_exp2(d) * vm, fe = fast_exp2(-d) * vm;
-            kh[j] = kv[j] * f;
-            qh[j] = qv[j] * f;
-            kc[j] = kv[j] * fe;
+          for (int j = 0; j < 4; ++j) {
+            const float d0 = G[8 * q + 2 * j] * lg2, d1 = G[8 * q + 2 * j + 1] * lg2;
+            const uint32_t f = pack_bf16x2(fast_exp2(d0), fast_exp2(d1));
+            const uint32_t fe = pack_bf16x2(fast_exp2(-d0), fast_exp2(-d1));
+            kh[j] = mul_bf16x2(kp[j], f);
+            qh[j] = mul_bf16x2(qp[j], f);
+            kc[j] = mul_bf16x2(kp[j], fe);
           }
-          st8(addr, kh);
-          st8(addr + L::kQoff, qh);
-          st8(kcb + half * 8192 + sw128(r, 4 * hh + q), kc);
+          st_shared_v4(addr, kh[0], kh[1], kh[2], kh[3]);
+          st_shared_v4(addr + L::kQoff, qh[0], qh[1], qh[2], qh[3]);
+          st_shared_v4(kcb + half * 8192 + sw128(r, 4 * hh + q), kc[0], kc[1], kc[2], kc[3]);
         }
       }
       if (t < C) betas[t] = bnext;
@@ -388,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
-        if (c >= 2) ctx.wait(kSDone0 + s, prev);  // chunk c - 2 is done with TP[s], Aop[s], ACC[s]
+        // TP[s] was last read by chunk c - 2's output product, committed with its Kc release
+        if (c >= 2) ctx.wait(kKcFree0 + (c - 2) % 3, ((c - 2) / 3) & 1);
       }
       ++kph;
       bar_sync(bar_id, 128);
@@ -454,24 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int r2 = m + 1; r2 < 16; ++r2) acc[r2] = fmaf(Ab[r2 * kSdLd + m], x[m], acc[r2]);
           }
-        } else {
-          // meanwhile rows 64-127 copy Qh (bf16 pairs, all 128 channels of token
-          // row - 64) into Aop[s]: the lower half of the state product's A operand
-          const int i = row - 64;
-          const uint32_t rx = static_cast<uint32_t>(i & 7);
-#pragma unroll 1
-          for (int hq = 0; hq < 2; ++hq) {
-            const uint32_t base = st + hq * L::kKQ1 + L::kQoff + i * 128;
-            uint32_t pk[32];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 w = ld_shared_v4(base + ((static_cast<uint32_t>(q) ^ rx) << 4));
-              pk[4 * q] = w.x; pk[4 * q + 1] = w.y; pk[4 * q + 2] = w.z; pk[4 * q + 3] = w.w;
-            }
-            tmem_st32(aop + lane_base + 32 * hq, pk);
-          }
         }
-        tc_fence_before();
         bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
         if (t < 64) {
           float *Tb = Sd + sd_idx(I, 0, cc);
@@ -480,7 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       bar_sync(bar_id, 128);
-      if (t == 0) mbar_arrive(ctx.bar(kEmptyQ0 + s));  // the q area has been read by a2 and the copy
       // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
       // (16 x 8 tiles; TF32 operands rounded to nearest, fp32 accumulation).
       const int lg = (t & 31) >> 2, lc = t & 3;  // fragment coordinates of this lane
@@ -603,12 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       fence_async_smem();
+      if (t == 0) {
+        if (c >= 2) ctx.wait(kSDone0 + s, prev);  // chunk c - 2 is done with Aop[s] and ACC[s]
+        ctx.wait(kFullV0 + s, cur);
+      }
       bar_sync(bar_id, 128);
       if (t == 0) mbar_arrive(ctx.bar(kEmptyG0 + s));  // the g area (solve scratch) may be refilled
 
       // [Tb; A^qk] [Kh | V] -> D2 (rows 0-63: W) and ACC[s] (U | A^qk V)
       if (t == 0) {
-        ctx.wait(kFullV0 + s, cur);
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id_v = idesc_bf16(128, BV, false, true);
@@ -623,9 +608,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
         mbar_arrive(ctx.bar(kEmptyK0 + s));  // Kh (the k area) is no longer read
+      } else if (row >= 64) {
+        // while that runs, rows 64-127 copy Qh (bf16 pairs, all 128 channels of token
+        // row - 64) into Aop[s]: the lower half of the state product's A operand
+        const int i = row - 64;
+        const uint32_t rx = static_cast<uint32_t>(i & 7);
+#pragma unroll 1
+        for (int hq = 0; hq < 2; ++hq) {
+          const uint32_t base = st + hq * L::kKQ1 + L::kQoff + i * 128;
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 w = ld_shared_v4(base + ((static_cast<uint32_t>(q) ^ rx) << 4));
+            pk[4 * q] = w.x; pk[4 * q + 1] = w.y; pk[4 * q + 2] = w.z; pk[4 * q + 3] = w.w;
+          }
+          tmem_st32(aop + lane_base + 32 * hq, pk);
+        }
+        tc_fence_before();
       }
       ++kph;
       bar_sync(bar_id, 128);
+      if (t == 0) mbar_arrive(ctx.bar(kEmptyQ0 + s));  // the q area has been read by a2 and the copy
       tc_fence_after();
       if (row < 64) {  // -W (bf16 pairs) -> Aop[s] rows 0-63, from the fp32 W rows of D2
 #pragma unroll 1
@@ -692,7 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bar_sync(2, 128);
       tc_fence_after();
-      const float gm = gamma[s * 128 + t];
+      // gamma = exp(G_last) of this thread's key channel; a chunk whose total log decay
+      // is beyond the range the factors exp(+-G) are formed in is reported
+      const float gl = glast[s * 128 + t];
+      const float gm = fast_exp2(gl * kLog2e);
+      if (!(gl >= kMinChunkLogDecay)) atomicCAS(p.status, 0u, kStatusGateRange);
       // a4/a5: [E; X] = [U; A^qk V] + [-W; Qh] S, the A operand from Aop[s] in TMEM
       if (t == 0) {
         constexpr uint32_t id = idesc_bf16(128, BV, false, true);
@@ -702,11 +709,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_tmem_a(tmem + kAcc0 + s * BV, tmem + kAop0 + 64u * s + 8 * k8, bd, id, 1);
         }
         mma_commit(ctx.bar(kMmaS));
+      }
+      bar_sync(2, 128);  // while the product runs: every thread has read G_last[s]
+      if (t == 0) {
+        mbar_arrive(ctx.bar(kGmRead0 + s));
         ctx.wait(kMmaS, sph & 1);
       }
       ++sph;
       bar_sync(2, 128);
-      if (t == 0) mbar_arrive(ctx.bar(kGmRead0 + s));  // every thread has read gamma[s]
       tc_fence_after();
       if (t < 64) {  // E - V (rows 0-63) -> bf16 over the first half of Sb
 #pragma unroll
