@@ -74,3 +74,24 @@ def test_strong_decay_inside_range():
     ro, rs = run_oracle_prefill(x)
     assert rel_l2_per_head(out.float().cpu().numpy(), ro, x["cu_seqlens"].numpy()) <= TOL_BF16
     assert rel_l2_states(fin.cpu().numpy(), rs) <= TOL_BF16
+
+
+@pytest.mark.parametrize("algo", ["tensor", "simt"])
+def test_strong_decay_after_a_partial_chunk_stays_finite(algo):
+    """A sequence's partial last chunk shares its tile with the next sequence's
+    first tokens.  Here both decay at g = -2.4 for 32 tokens (each chunk's own
+    total, -76.8, is inside the range), so the rows past the first sequence's end
+    reach a cumulative decay of -153.6, where exp(-G) overflows fp32.  Those rows
+    must contribute nothing: outputs and states stay finite and match."""
+    spec = W.custom_prefill([96, 64], num_heads=2, d=128, seed=44)
+    x = W.prefill_inputs(spec)
+    g = torch.zeros_like(x["g"])
+    g[64:128] = -2.4  # the last 32 tokens of sequence 0 and the first 32 of sequence 1
+    x["g"] = g.to(x["g"].dtype)
+    d = to_dev(x)
+    out, fin = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                             d["init_state"], algo=algo, check=True)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fin).all()
+    ro, rs = run_oracle_prefill(x)
+    assert rel_l2_per_head(out.float().cpu().numpy(), ro, x["cu_seqlens"].numpy()) <= TOL_BF16
+    assert rel_l2_states(fin.cpu().numpy(), rs) <= TOL_BF16
