@@ -37,13 +37,20 @@ PREFILL_KERNELS = ("kda_chunk_tc_kernel", "kda_chunk_simt_kernel")
 
 
 # ----------------------------------------------------------------- helpers
-def algorithmic_prefill(token_heads: int, pairs: int, d_k: int, d_v: int, io_bytes: int, C=64):
+def gate_elems(gate: str, d_k: int) -> int:
+    """Elements of g read per token-head: one per key channel, one, or none."""
+    return {"channel": d_k, "scalar": 1, "none": 0}[gate]
+
+
+def algorithmic_prefill(token_heads: int, pairs: int, d_k: int, d_v: int, io_bytes: int, C=64,
+                        gate: str = "channel"):
     """Algorithmic bytes and flops of one prefill launch.
-    bytes: q, k, g (d_k each) and v (d_v) read, beta read, o (d_v) written per
-    token-head, plus the fp32 state read and written once per (sequence, head).
+    bytes: q, k (d_k each), g (see gate_elems) and v (d_v) read, beta read, o (d_v)
+    written per token-head, plus the fp32 state read and written once per
+    (sequence, head).
     flops: 3 state-sized GEMMs (2 d_k d_v each) + 5 chunk products (2 C d each)
     per token-head, the accounting 2Ld^2 + 2LCd of the chunked-attention cost."""
-    per_tok = io_bytes * (3 * d_k + 2 * d_v) + io_bytes
+    per_tok = io_bytes * (2 * d_k + gate_elems(gate, d_k) + 2 * d_v) + io_bytes
     state = 2 * 4 * d_k * d_v
     flops_tok = 2 * (d_k * d_v) * 3 + 2 * C * d_k * 5
     return token_heads * per_tok + pairs * state, token_heads * flops_tok
@@ -188,8 +195,14 @@ def oracle_cpu_baseline(x, pairs_limit=None):
     tokens processed, token-heads processed, threads, sample description)."""
     import oracle
     import numpy as np
+    import torch
     q, k, v, g, beta, cu, init = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu(),
                                   x["init_state"])
+    # the oracle takes one log alpha per key channel: repeat a per-token one, or zeros
+    if g is None:
+        g = torch.zeros_like(q)
+    elif g.dim() == 2:
+        g = g.unsqueeze(-1).expand_as(q)
     H = q.shape[1]
     if pairs_limit is not None and pairs_limit < H:
         q, k, v, g, beta = (t[:, :pairs_limit] for t in (q, k, v, g, beta))
@@ -218,6 +231,10 @@ def run_prefill(args, ws, rank, dev):
                          spec.init, rank_seed(spec.seed, rank))
     big = spec.total_tokens * spec.num_heads > 4_000_000
     x = W.prefill_inputs(spec, device=("cuda" if big else "cpu"))
+    if args.gate == "scalar":    # Gated DeltaNet: one log alpha per (token, head)
+        x["g"] = x["g"][..., 0].contiguous()
+    elif args.gate == "none":    # DeltaNet: alpha = 1, no g at all
+        x["g"] = None
     d = {kk: (vv.to(dev) if vv is not None else None) for kk, vv in x.items()}
     T, H, dk, dv, N = spec.total_tokens, spec.num_heads, spec.d_k, spec.d_v, spec.num_seqs
     io_bytes = 2 if spec.io_dtype == "bf16" else 4
@@ -291,7 +308,7 @@ def run_prefill(args, ws, rank, dev):
     e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, ws, dev)
 
     hbm, tflops, peak_src = measured_peaks()
-    alg_bytes, alg_flops = algorithmic_prefill(T * H, N * H, dk, dv, io_bytes)
+    alg_bytes, alg_flops = algorithmic_prefill(T * H, N * H, dk, dv, io_bytes, gate=args.gate)
     achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
     kind = "tensor" if tensor_path else "simt"
     res = {
@@ -300,11 +317,12 @@ def run_prefill(args, ws, rank, dev):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": N, "total_tokens": T, "num_heads": H,
-                   "d_k": dk, "d_v": dv, "chunk": 64, "io_dtype": spec.io_dtype,
+                   "d_k": dk, "d_v": dv, "chunk": 64, "io_dtype": spec.io_dtype, "gate": args.gate,
                    "kernel": kind, "l2": "inputs larger than L2 (%.0f MB read+written per step)" % (alg_bytes / 1e6),
                    "parallelism": f"replicas x{ws} (independent sequences per GPU)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": recorded_traffic(kind, args.workload),
+                     "frac": achieved / hbm, "traffic": recorded_traffic(kind, args.workload if args.gate == "channel" else
+                                                 f"{args.workload}:{args.gate}"),
                      "peak_source": f"{peak_src} hbm_gbs",
                      "tensor_tflops_algorithmic": alg_flops / (launch_ms * 1e-3) / 1e12,
                      "tensor_peak_tflops": tflops,
@@ -402,6 +420,10 @@ def main_reference(args):
     spec_name = args.workload if args.workload != "decode_bf16" else "prefill_bf16"
     spec = W.named(spec_name)
     x = W.prefill_inputs(spec)
+    if args.gate == "scalar":
+        x["g"] = x["g"][..., 0].contiguous()
+    elif args.gate == "none":
+        x["g"] = None
     H = spec.num_heads
     heads = args.cpu_heads or H
     times = []
@@ -417,7 +439,7 @@ def main_reference(args):
            "data": "synthetic",
            "config": {"workload": spec_name, "num_seqs": spec.num_seqs,
                       "total_tokens": spec.total_tokens, "num_heads": H, "d_k": spec.d_k,
-                      "d_v": spec.d_v},
+                      "d_v": spec.d_v, "gate": args.gate},
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                             "sample": f"{used} of {H} heads, all {tokens} tokens per step"},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -433,6 +455,8 @@ def main():
     ap.add_argument("--workload", default="prefill_bf16",
                     choices=["prefill_bf16", "long_prefill_bf16", "varlen_prefill_bf16", "decode_bf16"])
     ap.add_argument("--algo", default="auto", choices=["auto", "tensor", "simt"])
+    ap.add_argument("--gate", default="channel", choices=["channel", "scalar", "none"],
+                    help="decay per key channel (KDA), per token (Gated DeltaNet) or none (DeltaNet)")
     ap.add_argument("--cpu-heads", type=int, default=None,
                     help="heads of the workload the CPU oracle runs (default: all)")
     ap.add_argument("--no-decode", action="store_true")

@@ -5,7 +5,9 @@
  * and the five-line recurrence in the transposed d_k x d_v layout; "K3 架构图解"
  * Ch.08 column-vector form).  Per sequence and head, state S in R^{d_k x d_v}:
  *
- *   alpha_t = exp(g_t)                 (g_t = log alpha_t <= 0, one per key channel)
+ *   alpha_t = exp(g_t)                 (g_t = log alpha_t <= 0, one per key channel;
+ *                                       see kda_gate for the one-per-token form of
+ *                                       Gated DeltaNet and for DeltaNet, alpha = 1)
  *   S~_t    = Diag(alpha_t) S_{t-1}    forget
  *   e_t     = beta_t (v_t - S~_t^T k_t)  predict and correct (beta_t: one per token, head)
  *   S_t     = S~_t + k_t e_t^T         rank-one write
@@ -17,11 +19,13 @@
  *     `stream` (0 = legacy default stream) and enqueue kernels only.
  *   - Tensors are contiguous and row-major:
  *       q, k, g : [T_total, H, d_k]        v, out : [T_total, H, d_v]
+ *       (g is [T_total, H] with KDA_GATE_SCALAR and unused with KDA_GATE_NONE)
  *       beta    : [T_total, H]             states : [N, H, d_k, d_v] fp32
  *       cu_seqlens : int32 [N + 1] (device), nondecreasing, cu[0] = 0,
  *                    cu[N] = T_total; sequence n owns tokens [cu[n], cu[n+1]).
- *   - Alignment: states, workspace and (prefill) q, k, v, g, out start on a
- *     16-byte boundary; beta and (decode) q, k, v, g on their element size;
+ *   - Alignment: states, workspace and (prefill) q, k, v, out and a per-channel g
+ *     start on a 16-byte boundary; beta, a per-token g and (decode) q, k, v, g on
+ *     their element size;
  *     cu_seqlens on 4 bytes; the decode output on 4 elements.
  *   - q, k, v, g, beta and out have the I/O dtype (fp32 or bf16); states are
  *     always fp32.  q and k are used as given (normalisation belongs to the
@@ -61,6 +65,16 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  * d_k = d_v = 128 and SIMT otherwise. */
 typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_TENSOR = 1, KDA_ALGO_SIMT = 2 } kda_algo;
 
+/* How g carries the decay.  The recurrence is the same in all three; only the
+ * granularity of alpha_t differs ("Kimi Delta Attention (KDA)", the sections on
+ * DeltaNet, on Gated DeltaNet's single retention gate, and on KDA's gate per key
+ * channel):
+ *   KDA_GATE_CHANNEL  g [T_total, H, d_k]: one log alpha per key channel (KDA)
+ *   KDA_GATE_SCALAR   g [T_total, H]: one log alpha per (token, head), applied to
+ *                     every key channel (Gated DeltaNet)
+ *   KDA_GATE_NONE     alpha_t = 1 (DeltaNet); g is not read and may be NULL */
+typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_SCALAR = 1, KDA_GATE_NONE = 2 } kda_gate;
+
 typedef struct {
   int32_t num_seqs;     /* N >= 0 (sequences; for decode: independent sequences, one token each) */
   int32_t total_tokens; /* T_total = cu_seqlens[N]; for decode must equal num_seqs */
@@ -71,6 +85,7 @@ typedef struct {
   float scale;          /* output scale; <= 0 selects d_k^-1/2 */
   int32_t io_dtype;     /* kda_dtype of q, k, v, g, beta, out */
   int32_t algo;         /* kda_algo (prefill only) */
+  int32_t gate;         /* kda_gate: layout of g (0 = one per key channel) */
 } kda_shape;
 
 /*

@@ -23,6 +23,7 @@ int check_shape(const kda_shape *s, bool decode) {
   if (!((s->d_k == 64 || s->d_k == 128) && (s->d_v == 64 || s->d_v == 128))) return KDA_ERR_SHAPE;
   if (s->io_dtype != KDA_F32 && s->io_dtype != KDA_BF16) return KDA_ERR_SHAPE;
   if (!(s->scale == s->scale) || isinf(s->scale)) return KDA_ERR_SHAPE;
+  if (s->gate < KDA_GATE_CHANNEL || s->gate > KDA_GATE_NONE) return KDA_ERR_SHAPE;
   if (decode) {
     if (s->total_tokens != s->num_seqs) return KDA_ERR_SHAPE;
   } else {
@@ -102,12 +103,15 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
                   float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_shape(s, false);
   if (rc != KDA_OK) return rc;
-  if (s->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+  const bool need_g = s->gate != KDA_GATE_NONE;
+  if (!need_g) g = nullptr;  // not read
+  if (s->total_tokens > 0 && (!q || !k || !v || (need_g && !g) || !beta || !out)) return KDA_ERR_NULL;
   if (s->num_seqs > 0 && !cu_seqlens) return KDA_ERR_NULL;
   if (!workspace) return KDA_ERR_WORKSPACE;
   if (workspace_bytes < kda_chunk_fwd_workspace_bytes(s)) return KDA_ERR_WORKSPACE;
   const uintptr_t esz = s->io_dtype == KDA_BF16 ? 2 : 4;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned(beta, esz) ||
+  const bool g_ok = s->gate == KDA_GATE_CHANNEL ? aligned16(g) : aligned(g, esz);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !g_ok || !aligned(beta, esz) ||
       !aligned16(init_state) || !aligned(cu_seqlens, 4) || !aligned16(out) ||
       !aligned16(final_state) || !aligned16(workspace))
     return KDA_ERR_ALIGN;
@@ -130,6 +134,7 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
   a.scale = effective_scale(s);
   a.bf16 = s->io_dtype == KDA_BF16;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.gate = s->gate;
   a.init_state = init_state;
   a.cu_seqlens = cu_seqlens;
   a.out = out;
@@ -152,7 +157,9 @@ int kda_decode_step(const kda_shape *s, const void *q, const void *k, const void
   int rc = check_shape(s, true);
   if (rc != KDA_OK) return rc;
   if (s->num_seqs == 0) return KDA_OK;
-  if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_NULL;
+  if (s->gate == KDA_GATE_NONE) g = nullptr;  // not read
+  if (!q || !k || !v || (s->gate != KDA_GATE_NONE && !g) || !beta || !state || !out)
+    return KDA_ERR_NULL;
   const uintptr_t esz = s->io_dtype == KDA_BF16 ? 2 : 4;
   if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(g, esz) ||
       !aligned(beta, esz) || !aligned16(state) || !aligned(out, 4 * esz))
@@ -167,6 +174,7 @@ int kda_decode_step(const kda_shape *s, const void *q, const void *k, const void
   a.scale = effective_scale(s);
   a.bf16 = s->io_dtype == KDA_BF16;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.gate = s->gate;
   a.state = state;
   a.out = out;
   const cudaError_t err = kda::launch_decode(a, stream);

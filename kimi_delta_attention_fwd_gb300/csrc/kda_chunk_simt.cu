@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(NT)
                           const IO *__restrict__ v, const IO *__restrict__ g,
                           const IO *__restrict__ beta, const float *__restrict__ init_state,
                           const int32_t *__restrict__ cu_seqlens, IO *__restrict__ out,
-                          float *__restrict__ final_state, int H, int DV, float scale) {
+                          float *__restrict__ final_state, int H, int DV, float scale,
+                          int gate) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<DK> &sm = *reinterpret_cast<SimtSmem<DK> *>(smem_raw);
 
@@ -97,7 +98,9 @@ __global__ void __launch_bounds__(NT)
         const size_t o = ((size_t)(c0 + r) * H + h) * DK + j;
         kv = ld_f32(k + o);
         qv = ld_f32(q + o);
-        gv = ld_f32(g + o);
+        // g per key channel (KDA), one per token for every channel (Gated DeltaNet), or 0
+        if (gate == 0) gv = ld_f32(g + o);
+        else if (gate == 1) gv = ld_f32(g + (size_t)(c0 + r) * H + h);
       }
       sm.K[r][j] = kv;
       sm.Q[r][j] = qv;
@@ -212,7 +215,7 @@ cudaError_t launch_t(const ChunkArgs &a, cudaStream_t stream) {
   kern<<<grid, NT, smem, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
-      static_cast<IO *>(a.out), a.final_state, a.num_heads, a.d_v, a.scale);
+      static_cast<IO *>(a.out), a.final_state, a.num_heads, a.d_v, a.scale, a.gate);
   return cudaGetLastError();
 }
 

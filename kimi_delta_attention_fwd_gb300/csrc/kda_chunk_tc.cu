@@ -114,6 +114,8 @@ constexpr uint32_t kAop0 = 256, kAcc0 = 384;
 
 struct TcParams {
   const __nv_bfloat16 *beta;
+  const __nv_bfloat16 *g_tok;  // [T, H] log alpha per (token, head) when gate == 1
+  int gate;                    // 0: g per key channel (TMA), 1: per token (g_tok), 2: none
   const float *init_state;
   const int32_t *cu_seqlens;
   __nv_bfloat16 *out;
@@ -242,9 +244,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(st + L::kQoff, &tm_q, fb, 0, h, t0);
             tma_load_3d(st + L::kKQ1 + L::kQoff, &tm_q, fb, 64, h, t0);
           } else if (part == 1) {
-            mbar_arrive_expect_tx(fb, 16384);
-            tma_load_3d(st + L::kG, &tm_g, fb, 0, h, t0);
-            tma_load_3d(st + L::kG + 8192, &tm_g, fb, 64, h, t0);
+            if (p.gate == 0) {
+              mbar_arrive_expect_tx(fb, 16384);
+              tma_load_3d(st + L::kG, &tm_g, fb, 0, h, t0);
+              tma_load_3d(st + L::kG + 8192, &tm_g, fb, 64, h, t0);
+            } else {
+              mbar_arrive(fb);  // no g tile: the part's phase still completes
+            }
           } else if (part == 2) {
             mbar_arrive_expect_tx(fb, 16384);
             tma_load_3d(st, &tm_k, fb, 0, h, t0);
@@ -284,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Sl = So + 2 * 16 * kSdLd;                                            // [32][36]
     float *Ys = reinterpret_cast<float *>(smem + L::kTP + kw * 16384);          // TP rows 0-63
     const uint32_t mma_bar = ctx.bar(kMmaK0 + kw);
+    const bool chan = p.gate == 0;  // g per key channel: G by the cumsum product below
     // a1: G = [Ltri; Ltri] g on the tensor cores, straight from the TMA'd g tile:
     // the chunk-local inclusive cumsum per channel (rows 64-127 repeat rows 0-63)
     auto issue_cumsum = [&]() {
@@ -316,18 +323,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one thread polls the mbarriers, the others park on the named barrier
       const uint32_t prev = ((c >> 1) - 1) & 1;  // parity of chunk c - 2's release signals
       const uint32_t cur = (c >> 1) & 1;          // parity of this chunk's loads
-      if (t == 0) {
-        if (c < 2) {  // later chunks had their cumsum product issued at the end of chunk c - 2
-          ctx.wait(kFullG0 + s, cur);
-          issue_cumsum();
+      // a1 with one log alpha per (token, head): G_r is one inclusive scan over the
+      // chunk's rows (rows r and 32 + r of two per-warp scans), the same for every channel
+      float g_row = 0.f;
+      if (p.gate == 1) {
+        const int lane = t & 31;
+        float ga = lane < len ? __bfloat162float(p.g_tok[(size_t)(t0 + lane) * H + h]) : 0.f;
+        float gb = 32 + lane < len ? __bfloat162float(p.g_tok[(size_t)(t0 + 32 + lane) * H + h]) : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float xa = __shfl_up_sync(0xffffffffu, ga, o), xb = __shfl_up_sync(0xffffffffu, gb, o);
+          if (lane >= o) { ga += xa; gb += xb; }
         }
-        ctx.wait(kMmaK0 + kw, kph & 1);
+        g_row = (wq & 1) ? __shfl_sync(0xffffffffu, ga, 31) + gb : ga;  // row r = 32 (wq & 1) + lane
+      }
+      if (t == 0) {
+        if (chan) {
+          if (c < 2) {  // later chunks had their cumsum product issued at the end of chunk c - 2
+            ctx.wait(kFullG0 + s, cur);
+            issue_cumsum();
+          }
+          ctx.wait(kMmaK0 + kw, kph & 1);
+        }
         ctx.wait(kFullK0 + s, cur);
         ctx.wait(kFullQ0 + s, cur);
         if (c >= 3) ctx.wait(kKcFree0 + kb, ((c / 3) - 1) & 1);  // chunk c - 3 is done with Kc[kb]
         if (c >= 2) ctx.wait(kGmRead0 + s, prev);                  // chunk c - 2 is done with G_last[s]
       }
-      ++kph;
+      if (chan) ++kph;
       bar_sync(bar_id, 128);
       tc_fence_after();
 
@@ -341,7 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float G[32];
-        tmem_ld32(tm + lane_base + 64 * half + 32 * hh, G);
+        if (chan) {
+          tmem_ld32(tm + lane_base + 64 * half + 32 * hh, G);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) G[j] = g_row;
+        }
         if (r == len - 1) {  // the chunk's last valid row: G_last for the state side
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
@@ -645,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_sync(bar_id, 128);
       if (t == 0) {
         mbar_arrive(ctx.bar(kReady0 + s));
-        if (c + 2 < nchunks) {  // a1 of chunk c + 2: the group's TMEM columns are free again
+        if (chan && c + 2 < nchunks) {  // a1 of chunk c + 2: the group's TMEM columns are free again
           ctx.wait(kFullG0 + s, cur ^ 1);
           issue_cumsum();
         }
@@ -856,12 +884,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   if (a.total_tokens > 0) {
     if (!make_map(&mq, a.q, a.total_tokens, a.num_heads) ||
         !make_map(&mk, a.k, a.total_tokens, a.num_heads) ||
-        !make_map(&mg, a.g, a.total_tokens, a.num_heads) ||
+        !make_map(&mg, a.gate == 0 ? a.g : a.q, a.total_tokens, a.num_heads) ||
         !make_map(&mv, a.v, a.total_tokens, a.num_heads))
       return cudaErrorInvalidValue;
   }
   TcParams prm;
   prm.beta = static_cast<const __nv_bfloat16 *>(a.beta);
+  prm.g_tok = a.gate == 1 ? static_cast<const __nv_bfloat16 *>(a.g) : nullptr;
+  prm.gate = a.gate;
   prm.init_state = a.init_state;
   prm.cu_seqlens = a.cu_seqlens;
   prm.out = static_cast<__nv_bfloat16 *>(a.out);

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                       const IO *__restrict__ v, const IO *__restrict__ g,
                       const IO *__restrict__ beta, float *__restrict__ state,
-                      IO *__restrict__ out, float scale) {
+                      IO *__restrict__ out, float scale, int gate) {
   constexpr int TPR = DV / 4;               // threads covering one state row (float4 each)
   constexpr int RPP = kDecodeThreads / TPR;  // rows covered per pass of the block
   constexpr int RPT = DK / RPP;              // rows held by each thread
@@ -71,10 +71,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&S4[(size_t)(r0 + i * RPP) * TPR + c4]);
 
   const size_t koff = (size_t)pair * DK, voff = (size_t)pair * DV;
+  // alpha per key channel (KDA), one alpha for every channel (Gated DeltaNet), or 1 (DeltaNet)
+  const float a_tok = gate == 1 ? __expf(to_f32(g[pair])) : 1.f;
   for (int i = tid; i < DK; i += kDecodeThreads) {
     s_q[i] = to_f32(q[koff + i]);
     s_k[i] = to_f32(k[koff + i]);
-    s_a[i] = __expf(to_f32(g[koff + i]));
+    s_a[i] = gate == 0 ? __expf(to_f32(g[koff + i])) : a_tok;
   }
   for (int i = tid; i < DV; i += kDecodeThreads) s_v[i] = to_f32(v[voff + i]);
   if (tid == 0) s_beta = to_f32(beta[pair]);
@@ -143,7 +145,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
   kda_decode_kernel<IO, DK, DV><<<pairs, kDecodeThreads, 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.state,
-      static_cast<IO *>(a.out), a.scale);
+      static_cast<IO *>(a.out), a.scale, a.gate);
   return cudaGetLastError();
 }
 

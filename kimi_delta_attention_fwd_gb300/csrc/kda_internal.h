@@ -17,6 +17,7 @@ struct ChunkArgs {
   float scale;
   bool bf16;
   const void *q, *k, *v, *g, *beta;
+  int gate;           // kda_gate: 0 g per key channel, 1 per (token, head), 2 none (g unused)
   const float *init_state;
   const int32_t *cu_seqlens;
   void *out;
@@ -33,6 +34,7 @@ struct DecodeArgs {
   float scale;
   bool bf16;
   const void *q, *k, *v, *g, *beta;
+  int gate;           // kda_gate, as in ChunkArgs
   float *state;
   void *out;
 };

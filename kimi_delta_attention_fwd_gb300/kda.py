@@ -17,6 +17,7 @@ from . import build as _build
 
 KDA_OK = 0
 KDA_F32, KDA_BF16 = 0, 1
+KDA_GATE_CHANNEL, KDA_GATE_SCALAR, KDA_GATE_NONE = 0, 1, 2
 _ALGOS = {"auto": 0, "tensor": 1, "simt": 2}
 _DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
 
@@ -31,7 +32,7 @@ class kda_shape(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("io_dtype", ctypes.c_int32), ("algo", ctypes.c_int32)]
+                ("io_dtype", ctypes.c_int32), ("algo", ctypes.c_int32), ("gate", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -89,9 +90,19 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _make_shape(num_seqs, total_tokens, H, dk, dv, scale, io, algo="auto"):
+def _make_shape(num_seqs, total_tokens, H, dk, dv, scale, io, algo="auto", gate=0):
     return kda_shape(int(num_seqs), int(total_tokens), int(H), int(dk), int(dv), 64,
-                     float(scale) if scale is not None else 0.0, io, _ALGOS[algo])
+                     float(scale) if scale is not None else 0.0, io, _ALGOS[algo], int(gate))
+
+
+def _gate_of(g, lead, H, dk):
+    """kda_gate of g: None -> no gate (DeltaNet), [lead, H] -> one log alpha per
+    (token, head) (Gated DeltaNet), [lead, H, d_k] -> one per key channel (KDA)."""
+    if g is None:
+        return KDA_GATE_NONE, None
+    if g.dim() == 2:
+        return KDA_GATE_SCALAR, (lead, H)
+    return KDA_GATE_CHANNEL, (lead, H, dk)
 
 
 def _check_io(name, t, shape, dtype, device):
@@ -129,7 +140,9 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
                   check=False):
     """Chunkwise prefill over packed sequences (see include/kda.h).
 
-    q, k, g: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (one dtype: bf16 or fp32, CUDA);
+    q, k: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (one dtype: bf16 or fp32, CUDA);
+    g: [T, H, d_k] (one log alpha per key channel), [T, H] (one per token and head,
+    Gated DeltaNet) or None (alpha = 1, DeltaNet);
     cu_seqlens: int32 [N+1] (CUDA); init_state: fp32 [N, H, d_k, d_v] or None.
     final_state may be the init_state tensor itself (in-place update).
     Returns (out, final_state or None).  With check=True the call synchronises and
@@ -144,9 +157,11 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
     dt = q.dtype
     if dt not in _DTYPES:
         raise TypeError(f"unsupported I/O dtype {dt}")
-    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, (T, H, dk)),
+    gate, gshape = _gate_of(g, T, H, dk)
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, gshape),
                          ("v", v, (T, H, dv)), ("beta", beta, (T, H))):
-        _check_io(name, t, shp, dt, dev)
+        if t is not None:
+            _check_io(name, t, shp, dt, dev)
     _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
     if init_state is not None:
         _check_io("init_state", init_state, (N, H, dk, dv), torch.float32, dev)
@@ -157,7 +172,7 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     if final_state is not None:
         _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
-    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], algo)
+    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], algo, gate)
     lib = load_library()
     need = int(lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(shape)))
     if workspace is None:
@@ -182,8 +197,9 @@ def kda_workspace_status(workspace, stream=None) -> int:
 
 
 def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=None):
-    """One single-token step for N sequences: q, k, g [N, H, d_k]; v [N, H, d_v];
-    beta [N, H]; state fp32 [N, H, d_k, d_v] updated in place.  Returns out [N, H, d_v]."""
+    """One single-token step for N sequences: q, k [N, H, d_k]; v [N, H, d_v];
+    g [N, H, d_k], [N, H] or None (as for kda_chunk_fwd); beta [N, H];
+    state fp32 [N, H, d_k, d_v] updated in place.  Returns out [N, H, d_v]."""
     N, H, dk = q.shape
     dv = v.shape[2]
     dev, dt = q.device, q.dtype
@@ -191,14 +207,16 @@ def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=Non
         raise ValueError("kda_decode_step runs on CUDA tensors only")
     if dt not in _DTYPES:
         raise TypeError(f"unsupported I/O dtype {dt}")
-    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)),
+    gate, gshape = _gate_of(g, N, H, dk)
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, gshape),
                          ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
-        _check_io(name, t, shp, dt, dev)
+        if t is not None:
+            _check_io(name, t, shp, dt, dev)
     _check_io("state", state, (N, H, dk, dv), torch.float32, dev)
     if out is None:
         out = torch.empty((N, H, dv), dtype=dt, device=dev)
     _check_io("out", out, (N, H, dv), dt, dev)
-    shape = _make_shape(N, N, H, dk, dv, scale, _DTYPES[dt])
+    shape = _make_shape(N, N, H, dk, dv, scale, _DTYPES[dt], gate=gate)
     rc = load_library().kda_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                         _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
     if rc != KDA_OK:

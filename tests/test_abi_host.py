@@ -76,7 +76,7 @@ def test_workspace_size(lib):
 
 @pytest.mark.parametrize("bad", [dict(d_k=96), dict(d_v=32), dict(num_heads=0), dict(num_seqs=-1),
                                  dict(chunk_size=128), dict(io_dtype=5), dict(algo=9),
-                                 dict(total_tokens=-3)])
+                                 dict(total_tokens=-3), dict(gate=3), dict(gate=-1)])
 def test_rejects_bad_shapes(lib, bad):
     assert _chunk(lib, _shape(**bad)) == -2
 
@@ -117,3 +117,28 @@ def test_status_strings(lib):
     assert lib.kda_status_string(-99).decode() == "unknown status"
     assert lib.kda_workspace_status(None, None) == -1
     assert lib.kda_version() >= 1000
+
+
+def test_gate_modes_validation(lib):
+    """g is required (and 16-byte aligned for the prefill) with one log alpha per key
+    channel, required on its element size with one per token, and not read at all
+    without a gate (DeltaNet): NULL and odd addresses then pass validation, which
+    reaches the device check (-6, no GPU here)."""
+    p = ctypes.c_void_p(FAKE)
+    s_chan, s_tok, s_none = _shape(gate=0), _shape(gate=1), _shape(gate=2)
+
+    def chunk_g(shape, g):
+        ws = lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(shape))
+        return lib.kda_chunk_fwd(ctypes.byref(shape), p, p, p, g, p, None, p, p, p, p, ws, None)
+
+    assert chunk_g(s_chan, None) == -1
+    assert chunk_g(s_tok, None) == -1
+    assert chunk_g(s_chan, ctypes.c_void_p(FAKE + 2)) == -3   # per channel: 16-byte aligned
+    assert chunk_g(s_tok, ctypes.c_void_p(FAKE + 2)) == -6    # per token: element aligned
+    assert chunk_g(s_tok, ctypes.c_void_p(FAKE + 1)) == -3
+    assert chunk_g(s_none, None) == -6
+    assert chunk_g(s_none, ctypes.c_void_p(FAKE + 1)) == -6   # not read
+    d = _shape(total_tokens=2, gate=2)
+    assert lib.kda_decode_step(ctypes.byref(d), p, p, p, None, p, p, p, None) == -6
+    d = _shape(total_tokens=2, gate=1)
+    assert lib.kda_decode_step(ctypes.byref(d), p, p, p, None, p, p, p, None) == -1
