@@ -156,6 +156,7 @@ __device__ __forceinline__ void st8(uint32_t addr, const float (&f)[8]) {
   const uint4 p = pack8(f);
   st_shared_v4(addr, p.x, p.y, p.z, p.w);
 }
+__device__ __forceinline__ uint32_t tf32_bits(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -492,19 +493,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bar_sync(bar_id, 128);
       // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
-      // (16 x 8 tiles; TF32 operands rounded to nearest, fp32 accumulation).
+      // (16 x 8 tiles; fp32 operands enter as TF32, their low 13 mantissa bits
+      // dropped: a relative error below 2^-10, under the bf16 rounding T gets next).
       const int lg = (t & 31) >> 2, lc = t & 3;  // fragment coordinates of this lane
       {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y
         const int b = wq >> 1, n0 = 8 * (wq & 1);  // warp: block b, 8 output columns
         float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k0 = 0; k0 < 16; k0 += 8) {
-          const uint32_t a[4] = {to_tf32(So[so_idx(b, lg, k0 + lc)]),
-                                 to_tf32(So[so_idx(b, lg + 8, k0 + lc)]),
-                                 to_tf32(So[so_idx(b, lg, k0 + lc + 4)]),
-                                 to_tf32(So[so_idx(b, lg + 8, k0 + lc + 4)])};
-          const uint32_t bb[2] = {to_tf32(Sd[sd_idx(2 * b, k0 + lc, n0 + lg)]),
-                                  to_tf32(Sd[sd_idx(2 * b, k0 + lc + 4, n0 + lg)])};
+          const uint32_t a[4] = {tf32_bits(So[so_idx(b, lg, k0 + lc)]),
+                                 tf32_bits(So[so_idx(b, lg + 8, k0 + lc)]),
+                                 tf32_bits(So[so_idx(b, lg, k0 + lc + 4)]),
+                                 tf32_bits(So[so_idx(b, lg + 8, k0 + lc + 4)])};
+          const uint32_t bb[2] = {tf32_bits(Sd[sd_idx(2 * b, k0 + lc, n0 + lg)]),
+                                  tf32_bits(Sd[sd_idx(2 * b, k0 + lc + 4, n0 + lg)])};
           mma_tf32_16x8x8(y, a, bb);
         }
         float *yb = Ys + b * 16 * 20;
@@ -514,12 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k0 = 0; k0 < 16; k0 += 8) {
-          const uint32_t a[4] = {to_tf32(Sd[sd_idx(2 * b + 1, lg, k0 + lc)]),
-                                 to_tf32(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc)]),
-                                 to_tf32(Sd[sd_idx(2 * b + 1, lg, k0 + lc + 4)]),
-                                 to_tf32(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc + 4)])};
-          const uint32_t bb[2] = {to_tf32(yb[(k0 + lc) * 20 + n0 + lg]),
-                                  to_tf32(yb[(k0 + lc + 4) * 20 + n0 + lg])};
+          const uint32_t a[4] = {tf32_bits(Sd[sd_idx(2 * b + 1, lg, k0 + lc)]),
+                                 tf32_bits(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc)]),
+                                 tf32_bits(Sd[sd_idx(2 * b + 1, lg, k0 + lc + 4)]),
+                                 tf32_bits(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc + 4)])};
+          const uint32_t bb[2] = {tf32_bits(yb[(k0 + lc) * 20 + n0 + lg]),
+                                  tf32_bits(yb[(k0 + lc + 4) * 20 + n0 + lg])};
           mma_tf32_16x8x8(z, a, bb);
         }
         *reinterpret_cast<float2 *>(So + so_idx(b, lg, n0 + 2 * lc)) = make_float2(-z[0], -z[1]);
@@ -535,15 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k0 = 0; k0 < 32; k0 += 8) {
           if (ch == 1 && k0 < 16) continue;
           const int ra = 16 * rh + lg;
-          const uint32_t a[4] = {to_tf32(Sl[sl_idx(ra, k0 + lc)]), to_tf32(Sl[sl_idx(ra + 8, k0 + lc)]),
-                                 to_tf32(Sl[sl_idx(ra, k0 + lc + 4)]),
-                                 to_tf32(Sl[sl_idx(ra + 8, k0 + lc + 4)])};
+          const uint32_t a[4] = {tf32_bits(Sl[sl_idx(ra, k0 + lc)]), tf32_bits(Sl[sl_idx(ra + 8, k0 + lc)]),
+                                 tf32_bits(Sl[sl_idx(ra, k0 + lc + 4)]),
+                                 tf32_bits(Sl[sl_idx(ra + 8, k0 + lc + 4)])};
           auto tlo = [&](int k, int c) -> float {  // T[k][16 ch + c], k in 0..31, c in 0..15
             if (ch == 0) return k < 16 ? Sd[sd_idx(0, k, c)] : So[so_idx(0, k - 16, c)];
             return Sd[sd_idx(1, k - 16, c)];
           };
-          const uint32_t b0[2] = {to_tf32(tlo(k0 + lc, lg)), to_tf32(tlo(k0 + lc + 4, lg))};
-          const uint32_t b1[2] = {to_tf32(tlo(k0 + lc, 8 + lg)), to_tf32(tlo(k0 + lc + 4, 8 + lg))};
+          const uint32_t b0[2] = {tf32_bits(tlo(k0 + lc, lg)), tf32_bits(tlo(k0 + lc + 4, lg))};
+          const uint32_t b1[2] = {tf32_bits(tlo(k0 + lc, 8 + lg)), tf32_bits(tlo(k0 + lc + 4, 8 + lg))};
           mma_tf32_16x8x8(y0, a, b0);
           mma_tf32_16x8x8(y1, a, b1);
         }
@@ -565,12 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rh == 0) return Sd[sd_idx(2, r, k)];
             return k < 16 ? So[so_idx(1, r, k)] : Sd[sd_idx(3, r, k - 16)];
           };
-          const uint32_t a[4] = {to_tf32(thi(lg, k0 + lc)), to_tf32(thi(lg + 8, k0 + lc)),
-                                 to_tf32(thi(lg, k0 + lc + 4)), to_tf32(thi(lg + 8, k0 + lc + 4))};
+          const uint32_t a[4] = {tf32_bits(thi(lg, k0 + lc)), tf32_bits(thi(lg + 8, k0 + lc)),
+                                 tf32_bits(thi(lg, k0 + lc + 4)), tf32_bits(thi(lg + 8, k0 + lc + 4))};
           const float *yk0 = Ys + (k0 + lc) * 36 + 16 * ch + lg;
           const float *yk1 = Ys + (k0 + lc + 4) * 36 + 16 * ch + lg;
-          const uint32_t b0[2] = {to_tf32(yk0[0]), to_tf32(yk1[0])};
-          const uint32_t b1[2] = {to_tf32(yk0[8]), to_tf32(yk1[8])};
+          const uint32_t b0[2] = {tf32_bits(yk0[0]), tf32_bits(yk1[0])};
+          const uint32_t b1[2] = {tf32_bits(yk0[8]), tf32_bits(yk1[8])};
           mma_tf32_16x8x8(z0, a, b0);
           mma_tf32_16x8x8(z1, a, b1);
         }
