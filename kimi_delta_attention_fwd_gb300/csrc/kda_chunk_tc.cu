@@ -432,16 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         float a[32];
         tmem_ld32(tm + lane_base + 32 * hh, a);
         if (row < 64) {  // A^kk row (beta_row, strictly lower)
+          // Entries on and above the diagonal of a diagonal block are stored unmasked:
+          // the substitution below reads only the strictly lower ones and then
+          // overwrites each block with its inverse.
           const float bi = betas[row];
           const int I = row >> 4, rl = row & 15;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const int j = 32 * hh + 4 * q;  // global column of this float4
-            float4 v;
-            v.x = j + 0 < row ? bi * a[4 * q + 0] : 0.f;
-            v.y = j + 1 < row ? bi * a[4 * q + 1] : 0.f;
-            v.z = j + 2 < row ? bi * a[4 * q + 2] : 0.f;
-            v.w = j + 3 < row ? bi * a[4 * q + 3] : 0.f;
+            const float4 v = make_float4(bi * a[4 * q + 0], bi * a[4 * q + 1], bi * a[4 * q + 2],
+                                         bi * a[4 * q + 3]);
             const int J = j >> 4;  // block column (compile-time)
             if (J == I) *reinterpret_cast<float4 *>(Sd + sd_idx(I, rl, j & 15)) = v;
             if ((I == 1 && J == 0) || (I == 3 && J == 2))
@@ -607,9 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4 b0 = *reinterpret_cast<const float4 *>(betas + j0);
           const float4 b1 = *reinterpret_cast<const float4 *>(betas + j0 + 4);
           const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-          float v[8];
+          float v[8];  // T is exactly lower triangular (zeros above the diagonal)
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) v[jj] = j0 + jj <= i ? tv[jj] * bv[jj] : 0.f;
+          for (int jj = 0; jj < 8; ++jj) v[jj] = tv[jj] * bv[jj];
           st8(tp + sw128(i, 4 * hh + q), v);
         }
       }
