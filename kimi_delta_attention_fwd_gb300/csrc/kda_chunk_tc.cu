@@ -473,15 +473,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         float x[16];
         const int I = t >> 4, cc = t & 15;
         if (t < 64) {
+          // left-looking: x[r2] = -(row r2 of the block) . x[0 .. r2-1], rows read as
+          // float4s, four partial sums per row (x[m] = 0 above column cc)
           const float *Ab = Sd + sd_idx(I, 0, 0);
-          float acc[16];
 #pragma unroll
-          for (int r2 = 0; r2 < 16; ++r2) acc[r2] = 0.f;
+          for (int r2 = 0; r2 < 16; ++r2) {
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            x[m] = m == cc ? 1.f : (m > cc ? -acc[m] : 0.f);
+            for (int m4 = 0; m4 < r2; m4 += 4) {
+              const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r2 * kSdLd + m4);
+              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-            for (int r2 = m + 1; r2 < 16; ++r2) acc[r2] = fmaf(Ab[r2 * kSdLd + m], x[m], acc[r2]);
+              for (int e = 0; e < 4; ++e)
+                if (m4 + e < r2) s4[e] = fmaf(av[e], x[m4 + e], s4[e]);
+            }
+            x[r2] = r2 == cc ? 1.f : (r2 > cc ? -((s4[0] + s4[1]) + (s4[2] + s4[3])) : 0.f);
           }
         }
         bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
