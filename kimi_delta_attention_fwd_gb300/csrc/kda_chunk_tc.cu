@@ -43,6 +43,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "kda_internal.h"
 #include "kda_tc_ptx.cuh"
 
@@ -362,6 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // as 0), so no exp(-G) of the next sequence's decays can overflow there.
       const bool valid = r < len;
       const float lg2 = valid ? kLog2e : 0.f;
+      uint32_t f_row = 0u, fe_row = 0u;  // exp(+-G) of the row, when G is one per row
+      if (!chan) {
+        const float dr = g_row * lg2;
+        const float er = fast_exp2(dr), ier = fast_exp2(-dr);
+        f_row = pack_bf16x2(er, er);
+        fe_row = pack_bf16x2(ier, ier);
+      }
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float G[32];
@@ -377,27 +386,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4 *>(glast + s * 128 + 64 * half + 32 * hh + j) =
                 make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
         }
-        // bf16 pairs: exp(+-G) rounded to bf16, then one bf16 product per output pair
+        // bf16 pairs: exp(+-G) rounded to bf16, then one bf16 product per output pair.
+        // With one G per row (a per-token gate, or none) the two factors are the
+        // row's own, formed once before the loop.
+        auto products = [&](auto per_channel) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t addr = kq + sw128(r, 4 * hh + q);
-          uint4 kw = ld_shared_v4(addr), qw = ld_shared_v4(addr + L::kQoff);
-          if (!valid) kw = qw = make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t kp[4] = {kw.x, kw.y, kw.z, kw.w}, qp[4] = {qw.x, qw.y, qw.z, qw.w};
-          uint32_t kh[4], qh[4], kc[4];
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t addr = kq + sw128(r, 4 * hh + q);
+            uint4 kw = ld_shared_v4(addr), qw = ld_shared_v4(addr + L::kQoff);
+            if (!valid) kw = qw = make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t kp[4] = {kw.x, kw.y, kw.z, kw.w}, qp[4] = {qw.x, qw.y, qw.z, qw.w};
+            uint32_t kh[4], qh[4], kc[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float d0 = G[8 * q + 2 * j] * lg2, d1 = G[8 * q + 2 * j + 1] * lg2;
-            const uint32_t f = pack_bf16x2(fast_exp2(d0), fast_exp2(d1));
-            const uint32_t fe = pack_bf16x2(fast_exp2(-d0), fast_exp2(-d1));
-            kh[j] = mul_bf16x2(kp[j], f);
-            qh[j] = mul_bf16x2(qp[j], f);
-            kc[j] = mul_bf16x2(kp[j], fe);
+            for (int j = 0; j < 4; ++j) {
+              uint32_t f = f_row, fe = fe_row;
+              if constexpr (decltype(per_channel)::value) {
+                const float d0 = G[8 * q + 2 * j] * lg2, d1 = G[8 * q + 2 * j + 1] * lg2;
+                f = pack_bf16x2(fast_exp2(d0), fast_exp2(d1));
+                fe = pack_bf16x2(fast_exp2(-d0), fast_exp2(-d1));
+              }
+              kh[j] = mul_bf16x2(kp[j], f);
+              qh[j] = mul_bf16x2(qp[j], f);
+              kc[j] = mul_bf16x2(kp[j], fe);
+            }
+            st_shared_v4(addr, kh[0], kh[1], kh[2], kh[3]);
+            st_shared_v4(addr + L::kQoff, qh[0], qh[1], qh[2], qh[3]);
+            st_shared_v4(kcb + half * 8192 + sw128(r, 4 * hh + q), kc[0], kc[1], kc[2], kc[3]);
           }
-          st_shared_v4(addr, kh[0], kh[1], kh[2], kh[3]);
-          st_shared_v4(addr + L::kQoff, qh[0], qh[1], qh[2], qh[3]);
-          st_shared_v4(kcb + half * 8192 + sw128(r, 4 * hh + q), kc[0], kc[1], kc[2], kc[3]);
-        }
+        };
+        if (chan) products(std::true_type{});
+        else products(std::false_type{});
       }
       if (t < C) betas[t] = bnext;
       fence_async_smem();
