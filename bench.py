@@ -430,11 +430,19 @@ def main_ours(args):
         if not args.no_decode and args.workload == "prefill_bf16":
             res["decode"] = run_decode(args, ws, rank, dev)
     if rank == 0 and not args.no_cpu_baseline and x is not None:
-        dt, tokens, th, threads, heads = oracle_cpu_baseline(x, pairs_limit=args.cpu_heads)
+        # repeat the sample until about --cpu-seconds of oracle time have accumulated
+        reps, total = 0, 0.0
+        while True:
+            dt, tokens, th, threads, heads = oracle_cpu_baseline(x, pairs_limit=args.cpu_heads)
+            reps, total = reps + 1, total + dt
+            if total >= args.cpu_seconds or reps >= 50:
+                break
+        dt = total / reps
         res["cpu_baseline"] = {"value": th / dt / x["q"].shape[1],
                                "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                "sample": f"{args.workload}: all {tokens} tokens of {heads} of {x['q'].shape[1]} heads "
-                                         f"({th} token-heads, {dt:.1f} s), scaled to tokens/s over all heads"}
+                                         f"({th} token-heads per run, {reps} runs, {total:.1f} s in all), "
+                                         f"scaled to tokens/s over all heads"}
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -492,6 +500,8 @@ def main():
                     help="heads of the workload the CPU oracle runs (default: all)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle time to accumulate for the CPU baseline (whole runs of the sample)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
