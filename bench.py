@@ -492,7 +492,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_bf16",
-                    choices=["prefill_bf16", "long_prefill_bf16", "varlen_prefill_bf16", "decode_bf16"])
+                    choices=["prefill_bf16", "long_prefill_bf16", "long_prefill_16k_bf16",
+                             "varlen_prefill_bf16", "decode_bf16"])
     ap.add_argument("--algo", default="auto", choices=["auto", "tensor", "simt"])
     ap.add_argument("--gate", default="channel", choices=["channel", "scalar", "none"],
                     help="decay per key channel (KDA), per token (Gated DeltaNet) or none (DeltaNet)")

@@ -103,10 +103,12 @@ typedef struct {
  *   out         : [T_total, H, d_v] (io dtype), written for every token.
  *   final_state : [N, H, d_k, d_v] fp32 or NULL; may alias init_state exactly
  *                 (in-place update); no other overlap is allowed.
- *   workspace   : device scratch of at least kda_chunk_fwd_workspace_bytes()
- *                 bytes (16-byte aligned).  It holds the device status block
- *                 read by kda_workspace_status(); calls that share one
- *                 workspace must be ordered on one stream.
+ *   workspace   : device scratch (16-byte aligned) of at least 256 bytes: the
+ *                 device status block read by kda_workspace_status().  With
+ *                 kda_chunk_fwd_workspace_bytes() bytes every schedule can run;
+ *                 a smaller workspace selects the schedule that fits (results
+ *                 agree to rounding).  Calls that share one workspace must be
+ *                 ordered on one stream.
  * Zero sequences or zero tokens are valid (nothing but the status reset is enqueued).
  * Sequences must be at most 2^31 - 1 tokens long in total; an empty sequence
  * copies its initial state to final_state.
@@ -116,8 +118,10 @@ int kda_chunk_fwd(const kda_shape *shape, const void *q, const void *k, const vo
                   const int32_t *cu_seqlens, void *out, float *final_state, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream);
 
-/* Bytes of workspace kda_chunk_fwd needs for this shape (always > 0), or 0 if
- * the shape is invalid. */
+/* Bytes of workspace with which kda_chunk_fwd can run every schedule for this
+ * shape (always >= 256), or 0 if the shape is invalid.  Few sequence-heads on
+ * the tensor-core path add a ring through which extra CTAs hand over the
+ * chunk solve (4 x 16 KiB + 32 bytes per sequence-head). */
 size_t kda_chunk_fwd_workspace_bytes(const kda_shape *shape);
 
 /* The prefill kernel a call with this shape runs: KDA_ALGO_TENSOR or
@@ -146,9 +150,10 @@ int kda_decode_step(const kda_shape *shape, const void *q, const void *k, const 
  *
  * Same arguments and results as kda_chunk_fwd, without the workspace: the
  * scratch comes from a 256 KiB buffer compiled into the library, which every
- * GPU that loads the library holds until the process exits.  Shapes whose
- * kda_chunk_fwd_workspace_bytes() exceeds 256 KiB are rejected with
- * KDA_ERR_NOALLOC_LIMIT.  Nothing is allocated or freed.  The first call on a
+ * GPU that loads the library holds until the process exits.  The schedule
+ * that fits the buffer runs; a shape whose minimum workspace exceeds 256 KiB
+ * would be rejected with KDA_ERR_NOALLOC_LIMIT (no current schedule needs more
+ * than the 256-byte status block).  Nothing is allocated or freed.  The first call on a
  * device (made while that device is current) looks the buffer's address up,
  * so make that first call before any stream capture.  All calls on one device
  * share the buffer and it keeps the last call's contents (each call clears the

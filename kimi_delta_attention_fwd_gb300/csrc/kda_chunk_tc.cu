@@ -64,6 +64,20 @@ constexpr float kMinChunkLogDecay = -80.f;
 constexpr uint32_t kStatusTimeout = 7;      // -KDA_ERR_DEVICE_TIMEOUT
 constexpr uint32_t kStatusGateRange = 8;    // -KDA_ERR_GATE_RANGE
 
+// Solve helpers (few sequence-heads).  With at most 38 (sequence, head) pairs and
+// room for the ring, the launch is cooperative (all CTAs resident) and each pair
+// gets two helper CTAs beside its two d_v tiles: K-side group kw of helper hp
+// solves the chunks c = hp + 2 kw + 4 i (the state-independent [T diag(beta); A^qk])
+// and hands each to both tiles through a ring in the workspace, slot c % 4
+// holding chunk c's 16 KiB shared-memory image.  Each slot has two words: the
+// last chunk published + 1 (a release store after the image) and the number of
+// reads so far (a release add by each tile once its copy is in shared memory);
+// a helper overwrites a slot when both tiles have read the chunk four before.
+// Every wait on these words is bounded.
+constexpr int kRingSlots = 4;
+constexpr uint32_t kRingSlotBytes = 16384;
+constexpr int kHelperMaxPairs = 38;  // 4 CTAs per sequence-head, one per SM, all resident
+
 // Compact fp32 layout of the 64 x 64 unit-lower-triangular solve (12 KB):
 // the four 16 x 16 diagonal blocks, the sub-diagonal blocks (1,0) and (3,2), and
 // the lower-left 32 x 32 block; row strides keep 16-byte alignment and spread
@@ -126,7 +140,23 @@ struct TcParams {
   int H;
   float scale;
   int flags;  // bit 0: test hook, wait once on a barrier nothing arrives on
+  int npairs;                // P, the number of (sequence, head) pairs
+  uint8_t *ring;             // [P][kRingSlots][kRingSlotBytes]
+  uint32_t *ring_flags;      // [P][kRingSlots][2]: chunk + 1 published, consumptions (zeroed)
 };
+
+// Global-memory hand-over between CTAs of one launch (all resident: cooperative launch).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 struct Ctx {
   uint32_t bars;
@@ -138,6 +168,21 @@ struct Ctx {
     if (!mbar_wait(bar(i), parity, kWaitCycles)) {
       *abort = 1;
       atomicCAS(status, 0u, kStatusTimeout);
+    }
+  }
+  // Bounded wait until the global word *w (written by another CTA) reaches target;
+  // a timeout anywhere in the launch (the status word) ends it at once.
+  __device__ __forceinline__ void wait_global(const uint32_t *w, uint32_t target) const {
+    if (*abort) return;
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(w) < target) {
+      if (*reinterpret_cast<volatile uint32_t *>(status) == kStatusTimeout ||
+          clock64() - t0 > kWaitCycles) {
+        *abort = 1;
+        atomicCAS(status, 0u, kStatusTimeout);
+        return;
+      }
+      __nanosleep(64);
     }
   }
 };
@@ -165,6 +210,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// kSched = false: every CTA is a d_v tile that solves its own chunks (the plain
+// schedule); true: CTAs 2 P .. 4 P - 1 are solve helpers for the first 2 P.
+template <bool kSched>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -182,8 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   constexpr int kTiles = DV / BV;
-  const int tile = blockIdx.x % kTiles;
-  const int pair = blockIdx.x / kTiles;
+  // roles: a d_v-tile CTA (pair, tile) runs everything, or with helpers takes each
+  // chunk's [Tb; A^qk] from the ring; a helper (pair, parity hp) runs the chunk
+  // solve of the chunks c = hp mod 2 and publishes it
+  const bool helper = kSched && (int)blockIdx.x >= 2 * p.npairs;
+  const bool fed = kSched && !helper;
+  const int hb = (int)blockIdx.x - 2 * p.npairs;
+  const int hp = helper ? (hb & 1) : 0;
+  const int tile = helper ? 0 : (int)blockIdx.x % kTiles;
+  const int pair = helper ? (hb >> 1) : (int)blockIdx.x / kTiles;
+  // the chunks a stage / K-side group takes: c = c_first + i * c_step, phase i & 1
+  const int c_step = helper ? 4 : 2;
+  const int c_shift = helper ? 2 : 1;
+  uint32_t *rflags = kSched ? p.ring_flags + (size_t)pair * kRingSlots * 2 : nullptr;
+  uint8_t *rdata = kSched ? p.ring + (size_t)pair * kRingSlots * kRingSlotBytes : nullptr;
   const int H = p.H;
   const int n = pair / H, h = pair % H;
   const int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
@@ -223,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of a stage are released at different points of the chunk (q after the
     // state-product operand has been copied out, g after the solve, k after the
     // W / U product, v after the state side's last product) and each is refilled
-    // for chunk c + 2 as soon as it is free.
+    // for chunk c + 2 as soon as it is free.  In a helper, stage s holds the chunks
+    // hp + 2 s + 4 i and no v; q and k are released after [Kh; Qh] Kc^T.
     if ((tid & 31) == 0) {
       const int s = warp - 12;
       if (s == 0) {
@@ -234,12 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t st = sbase + s * L::kStageBytes;
       int last[4] = {-1, -1, -1, -1};  // last chunk loaded, per part
-      for (int c = s; c < nchunks && !*abort_flag; c += 2) {
-        const uint32_t prev = ((c >> 1) - 1) & 1;
+      const int c_first = helper ? hp + 2 * s : s;
+      const int nparts = helper ? 3 : 4;  // a helper reads no v
+      for (int c = c_first; c < nchunks && !*abort_flag; c += c_step) {
+        const int it = c >> c_shift;
+        const uint32_t prev = (it - 1) & 1;
         const int t0 = bos + c * C;
 #pragma unroll 1
-        for (int part = 0; part < 4; ++part) {  // q, g, k, v: the order they are released in
-          if (c >= 2) ctx.wait(kEmptyQ0 + 2 * part + s, prev);
+        for (int part = 0; part < nparts; ++part) {  // q, g, k, v: the order they are released in
+          if (it >= 1) ctx.wait(kEmptyQ0 + 2 * part + s, prev);
           if (*abort_flag) break;
           const uint32_t fb = ctx.bar(kFullQ0 + 2 * part + s);
           if (part == 0) {
@@ -268,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // never leave a copy in flight: wait (bounded) for the last load of every part
       for (int part = 0; part < 4; ++part)
         if (last[part] >= 0)
-          mbar_wait(ctx.bar(kFullQ0 + 2 * part + s), (last[part] >> 1) & 1, kWaitCycles);
+          mbar_wait(ctx.bar(kFullQ0 + 2 * part + s), (last[part] >> c_shift) & 1, kWaitCycles);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ K-side
@@ -276,6 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // owns stage kw, TP[kw], beta[kw], Aop[kw], ACC[kw] and TMEM columns
     // [128 kw, 128 kw + 128), so the dependent chain of one chunk overlaps the
     // other group's chunk.  Kc rotates over three slots (chunk % 3).
+    // A helper's groups take c = hp + 2 kw + 4 i, run the gate, a2 and the solve, and
+    // publish [Tb; A^qk]; a tile fed by helpers runs the gate and takes [Tb; A^qk]
+    // from the ring in place of a2 and the solve.
     const int kw = warp >> 2;
     const int t = tid & 127;            // thread within the group
     const int wq = warp & 3;            // TMEM lane quarter of this warp
@@ -315,17 +382,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     uint32_t kph = 0;
-    for (int c = kw; c < nchunks; c += 2) {
-      const int s = kw;  // == c & 1
+    // chunks of this group: c = kw, kw + 2, ...; in a helper c = hp + 2 kw + 4 i
+    for (int c = helper ? hp + 2 * kw : kw; c < nchunks; c += c_step) {
+      const int s = kw;
       const int t0 = bos + c * C;
       const int len = min(C, eos - t0);
-      const int kb = c % 3;  // Kc slot
+      const int kb = helper ? kw : c % 3;  // Kc slot (a helper's own two are read by its a2 only)
       const uint32_t kcb = sbase + L::kKc + kb * 16384;
+      const int slot = c & (kRingSlots - 1);  // ring slot of this chunk's [Tb; A^qk]
       float bnext = 0.f;  // beta of this chunk, loaded early to hide the global latency
-      if (t < C && t < len) bnext = __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]);
+      if (!fed && t < C && t < len) bnext = __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]);
       // one thread polls the mbarriers, the others park on the named barrier
-      const uint32_t prev = ((c >> 1) - 1) & 1;  // parity of chunk c - 2's release signals
-      const uint32_t cur = (c >> 1) & 1;          // parity of this chunk's loads
+      const int it = c >> c_shift;                // this group's it-th chunk
+      const uint32_t prev = (it - 1) & 1;         // parity of the group's previous release signals
+      const uint32_t cur = it & 1;                // parity of this chunk's loads
       // a1 with one log alpha per (token, head): G_r is one inclusive scan over the
       // chunk's rows (rows r and 32 + r of two per-warp scans), the same for every channel
       float g_row = 0.f;
@@ -342,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (t == 0) {
         if (chan) {
-          if (c < 2) {  // later chunks had their cumsum product issued at the end of chunk c - 2
+          if (it == 0) {  // later chunks had their cumsum product issued at the end of the previous one
             ctx.wait(kFullG0 + s, cur);
             issue_cumsum();
           }
@@ -350,8 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ctx.wait(kFullK0 + s, cur);
         ctx.wait(kFullQ0 + s, cur);
-        if (c >= 3) ctx.wait(kKcFree0 + kb, ((c / 3) - 1) & 1);  // chunk c - 3 is done with Kc[kb]
-        if (c >= 2) ctx.wait(kGmRead0 + s, prev);                  // chunk c - 2 is done with G_last[s]
+        if (!helper) {
+          if (c >= 3) ctx.wait(kKcFree0 + kb, ((c / 3) - 1) & 1);  // chunk c - 3 is done with Kc[kb]
+          if (c >= 2) ctx.wait(kGmRead0 + s, prev);                  // chunk c - 2 is done with G_last[s]
+        }
+      } else if (fed && t == 32) {
+        // meanwhile another thread acquires the chunk's ring slot (published by a helper);
+        // the barrier below orders every thread's later reads of it after this
+        ctx.wait_global(rflags + 2 * slot, static_cast<uint32_t>(c + 1));
       }
       if (chan) ++kph;
       bar_sync(bar_id, 128);
@@ -422,221 +498,266 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       bar_sync(bar_id, 128);
 
-      // a2: [Kh; Qh] Kc^T -> D1 (rows 0-63: A^kk / beta, rows 64-127: A^qk)
-      if (t == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+      if (fed) {
+        // The chunk's [Tb; A^qk] comes from a helper through ring slot c % 4 (acquired
+        // above): it is read into registers while TP[s] is still being read by chunk
+        // c - 2's output product, then stored there.  The read is counted while the
+        // W / U product runs.
+        if (t == 0) mbar_arrive(ctx.bar(kEmptyG0 + s));  // g was read by the cumsum product only
+        const uint4 *src = reinterpret_cast<const uint4 *>(rdata + slot * kRingSlotBytes);
+        uint4 w[8];
 #pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {
-          const uint64_t ad = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kcb + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
-          mma_bf16(tm, ad, bd, id, k8 > 0);
-        }
-        mma_commit(mma_bar);
-        ctx.wait(kMmaK0 + kw, kph & 1);
-        // TP[s] was last read by chunk c - 2's output product, committed with its Kc release
-        if (c >= 2) ctx.wait(kKcFree0 + (c - 2) % 3, ((c - 2) / 3) & 1);
-      }
-      ++kph;
-      bar_sync(bar_id, 128);
-      tc_fence_after();
-      // A^kk (fp32, strictly lower, beta applied) goes to the stage's g area, which
-      // the cumsum product has finished reading, in the compact solve layout
-      // (diagonal 16-blocks, the two 16-wide sub-diagonal blocks, the lower-left
-      // 32 x 32 block; the zero blocks above the diagonal are not stored).  T is
-      // then computed in place there.
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        float a[32];
-        tmem_ld32(tm + lane_base + 32 * hh, a);
-        if (row < 64) {  // A^kk row (beta_row, strictly lower)
-          // Entries on and above the diagonal of a diagonal block are stored unmasked:
-          // the substitution below reads only the strictly lower ones and then
-          // overwrites each block with its inverse.
-          const float bi = betas[row];
-          const int I = row >> 4, rl = row & 15;
+        for (int j = 0; j < 8; ++j) w[j] = __ldcg(src + 128 * j + t);
+        if (t == 0 && c >= 2) ctx.wait(kKcFree0 + (c - 2) % 3, ((c - 2) / 3) & 1);
+        bar_sync(bar_id, 128);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int j = 32 * hh + 4 * q;  // global column of this float4
-            const float4 v = make_float4(bi * a[4 * q + 0], bi * a[4 * q + 1], bi * a[4 * q + 2],
-                                         bi * a[4 * q + 3]);
-            const int J = j >> 4;  // block column (compile-time)
-            if (J == I) *reinterpret_cast<float4 *>(Sd + sd_idx(I, rl, j & 15)) = v;
-            if ((I == 1 && J == 0) || (I == 3 && J == 2))
-              *reinterpret_cast<float4 *>(So + so_idx(I >> 1, rl, j & 15)) = v;
-            if (row >= 32 && j < 32) *reinterpret_cast<float4 *>(Sl + sl_idx(row - 32, j)) = v;
+        for (int j = 0; j < 8; ++j) st_shared_v4(tp + 16 * (128 * j + t), w[j].x, w[j].y, w[j].z, w[j].w);
+      } else {
+        // a2: [Kh; Qh] Kc^T -> D1 (rows 0-63: A^kk / beta, rows 64-127: A^qk)
+        if (t == 0) {
+          tc_fence_after();
+          constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) {
+            const uint64_t ad = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kcb + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
+            mma_bf16(tm, ad, bd, id, k8 > 0);
           }
-        } else {  // A^qk row (lower, diagonal included) -> bf16 TP rows 64-127
-          const int i = row - 64;
+          mma_commit(mma_bar);
+          ctx.wait(kMmaK0 + kw, kph & 1);
+          if (helper) {  // Kh and Qh are read by a2 only in a helper
+            mbar_arrive(ctx.bar(kEmptyQ0 + s));
+            mbar_arrive(ctx.bar(kEmptyK0 + s));
+          } else if (c >= 2) {
+            // TP[s] was last read by chunk c - 2's output product, committed with its Kc release
+            ctx.wait(kKcFree0 + (c - 2) % 3, ((c - 2) / 3) & 1);
+          }
+        }
+        ++kph;
+        bar_sync(bar_id, 128);
+        tc_fence_after();
+        // A^kk (fp32, strictly lower, beta applied) goes to the stage's g area, which
+        // the cumsum product has finished reading, in the compact solve layout
+        // (diagonal 16-blocks, the two 16-wide sub-diagonal blocks, the lower-left
+        // 32 x 32 block; the zero blocks above the diagonal are not stored).  T is
+        // then computed in place there.
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float a[32];
+          tmem_ld32(tm + lane_base + 32 * hh, a);
+          if (row < 64) {  // A^kk row (beta_row, strictly lower)
+            // Entries on and above the diagonal of a diagonal block are stored unmasked:
+            // the substitution below reads only the strictly lower ones and then
+            // overwrites each block with its inverse.
+            const float bi = betas[row];
+            const int I = row >> 4, rl = row & 15;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int j = 32 * hh + 4 * q;  // global column of this float4
+              const float4 v = make_float4(bi * a[4 * q + 0], bi * a[4 * q + 1], bi * a[4 * q + 2],
+                                           bi * a[4 * q + 3]);
+              const int J = j >> 4;  // block column (compile-time)
+              if (J == I) *reinterpret_cast<float4 *>(Sd + sd_idx(I, rl, j & 15)) = v;
+              if ((I == 1 && J == 0) || (I == 3 && J == 2))
+                *reinterpret_cast<float4 *>(So + so_idx(I >> 1, rl, j & 15)) = v;
+              if (row >= 32 && j < 32) *reinterpret_cast<float4 *>(Sl + sl_idx(row - 32, j)) = v;
+            }
+          } else {  // A^qk row (lower, diagonal included) -> bf16 TP rows 64-127
+            const int i = row - 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float v[8];
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int j = 32 * hh + 8 * q + jj;
+                v[jj] = j <= i ? a[8 * q + jj] : 0.f;
+              }
+              st8(tp + sw128(row, 4 * hh + q), v);
+            }
+          }
+        }
+        tc_fence_before();
+        bar_sync(bar_id, 128);
+
+        // a3: T = (I + A^kk)^-1 in place, by recursive doubling of the block inverse
+        //   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
+        // 16 x 16 diagonal blocks first (left-looking substitution, one column
+        // per thread), then the 16-wide and the 32-wide off-diagonal blocks.
+        {
+          float x[16];
+          const int I = t >> 4, cc = t & 15;
+          if (t < 64) {
+            // left-looking: x[r2] = -(row r2 of the block) . x[0 .. r2-1], rows read as
+            // float4s, four partial sums per row (x[m] = 0 above column cc)
+            const float *Ab = Sd + sd_idx(I, 0, 0);
+#pragma unroll
+            for (int r2 = 0; r2 < 16; ++r2) {
+              float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int m4 = 0; m4 < r2; m4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r2 * kSdLd + m4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (m4 + e < r2) s4[e] = fmaf(av[e], x[m4 + e], s4[e]);
+              }
+              x[r2] = r2 == cc ? 1.f : (r2 > cc ? -((s4[0] + s4[1]) + (s4[2] + s4[3])) : 0.f);
+            }
+          }
+          bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
+          if (t < 64) {
+            float *Tb = Sd + sd_idx(I, 0, cc);
+#pragma unroll
+            for (int r2 = 0; r2 < 16; ++r2) Tb[r2 * kSdLd] = x[r2];
+          }
+        }
+        bar_sync(bar_id, 128);
+        // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
+        // (16 x 8 tiles; fp32 operands enter as TF32, their low 13 mantissa bits
+        // dropped: a relative error below 2^-10, under the bf16 rounding T gets next).
+        const int lg = (t & 31) >> 2, lc = t & 3;  // fragment coordinates of this lane
+        {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y
+          const int b = wq >> 1, n0 = 8 * (wq & 1);  // warp: block b, 8 output columns
+          float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k0 = 0; k0 < 16; k0 += 8) {
+            const uint32_t a[4] = {tf32_bits(So[so_idx(b, lg, k0 + lc)]),
+                                   tf32_bits(So[so_idx(b, lg + 8, k0 + lc)]),
+                                   tf32_bits(So[so_idx(b, lg, k0 + lc + 4)]),
+                                   tf32_bits(So[so_idx(b, lg + 8, k0 + lc + 4)])};
+            const uint32_t bb[2] = {tf32_bits(Sd[sd_idx(2 * b, k0 + lc, n0 + lg)]),
+                                    tf32_bits(Sd[sd_idx(2 * b, k0 + lc + 4, n0 + lg)])};
+            mma_tf32_16x8x8(y, a, bb);
+          }
+          float *yb = Ys + b * 16 * 20;
+          *reinterpret_cast<float2 *>(yb + lg * 20 + n0 + 2 * lc) = make_float2(y[0], y[1]);
+          *reinterpret_cast<float2 *>(yb + (lg + 8) * 20 + n0 + 2 * lc) = make_float2(y[2], y[3]);
+          bar_sync(bar_id, 128);
+          float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k0 = 0; k0 < 16; k0 += 8) {
+            const uint32_t a[4] = {tf32_bits(Sd[sd_idx(2 * b + 1, lg, k0 + lc)]),
+                                   tf32_bits(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc)]),
+                                   tf32_bits(Sd[sd_idx(2 * b + 1, lg, k0 + lc + 4)]),
+                                   tf32_bits(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc + 4)])};
+            const uint32_t bb[2] = {tf32_bits(yb[(k0 + lc) * 20 + n0 + lg]),
+                                    tf32_bits(yb[(k0 + lc + 4) * 20 + n0 + lg])};
+            mma_tf32_16x8x8(z, a, bb);
+          }
+          *reinterpret_cast<float2 *>(So + so_idx(b, lg, n0 + 2 * lc)) = make_float2(-z[0], -z[1]);
+          *reinterpret_cast<float2 *>(So + so_idx(b, lg + 8, n0 + 2 * lc)) = make_float2(-z[2], -z[3]);
+        }
+        bar_sync(bar_id, 128);
+        {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
+          // warp: rows 16 rh .. 16 rh + 15, columns 16 ch .. 16 ch + 15 (two 8-wide tiles)
+          const int ch = wq & 1, rh = wq >> 1;
+          float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
+          // T[0:32, 0:16] = [T_00; T_10];  T[0:32, 16:32] = [0; T_11]
+#pragma unroll
+          for (int k0 = 0; k0 < 32; k0 += 8) {
+            if (ch == 1 && k0 < 16) continue;
+            const int ra = 16 * rh + lg;
+            const uint32_t a[4] = {tf32_bits(Sl[sl_idx(ra, k0 + lc)]), tf32_bits(Sl[sl_idx(ra + 8, k0 + lc)]),
+                                   tf32_bits(Sl[sl_idx(ra, k0 + lc + 4)]),
+                                   tf32_bits(Sl[sl_idx(ra + 8, k0 + lc + 4)])};
+            auto tlo = [&](int k, int c) -> float {  // T[k][16 ch + c], k in 0..31, c in 0..15
+              if (ch == 0) return k < 16 ? Sd[sd_idx(0, k, c)] : So[so_idx(0, k - 16, c)];
+              return Sd[sd_idx(1, k - 16, c)];
+            };
+            const uint32_t b0[2] = {tf32_bits(tlo(k0 + lc, lg)), tf32_bits(tlo(k0 + lc + 4, lg))};
+            const uint32_t b1[2] = {tf32_bits(tlo(k0 + lc, 8 + lg)), tf32_bits(tlo(k0 + lc + 4, 8 + lg))};
+            mma_tf32_16x8x8(y0, a, b0);
+            mma_tf32_16x8x8(y1, a, b1);
+          }
+          {
+            float *yr0 = Ys + (16 * rh + lg) * 36 + 16 * ch + 2 * lc;
+            float *yr1 = Ys + (16 * rh + lg + 8) * 36 + 16 * ch + 2 * lc;
+            *reinterpret_cast<float2 *>(yr0) = make_float2(y0[0], y0[1]);
+            *reinterpret_cast<float2 *>(yr1) = make_float2(y0[2], y0[3]);
+            *reinterpret_cast<float2 *>(yr0 + 8) = make_float2(y1[0], y1[1]);
+            *reinterpret_cast<float2 *>(yr1 + 8) = make_float2(y1[2], y1[3]);
+          }
+          bar_sync(bar_id, 128);
+          float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+          // T[32:48, 32:64] = [T_22, 0];  T[48:64, 32:64] = [T_32, T_33]
+#pragma unroll
+          for (int k0 = 0; k0 < 32; k0 += 8) {
+            if (rh == 0 && k0 >= 16) continue;
+            auto thi = [&](int r, int k) -> float {  // T[32 + 16 rh + r][32 + k]
+              if (rh == 0) return Sd[sd_idx(2, r, k)];
+              return k < 16 ? So[so_idx(1, r, k)] : Sd[sd_idx(3, r, k - 16)];
+            };
+            const uint32_t a[4] = {tf32_bits(thi(lg, k0 + lc)), tf32_bits(thi(lg + 8, k0 + lc)),
+                                   tf32_bits(thi(lg, k0 + lc + 4)), tf32_bits(thi(lg + 8, k0 + lc + 4))};
+            const float *yk0 = Ys + (k0 + lc) * 36 + 16 * ch + lg;
+            const float *yk1 = Ys + (k0 + lc + 4) * 36 + 16 * ch + lg;
+            const uint32_t b0[2] = {tf32_bits(yk0[0]), tf32_bits(yk1[0])};
+            const uint32_t b1[2] = {tf32_bits(yk0[8]), tf32_bits(yk1[8])};
+            mma_tf32_16x8x8(z0, a, b0);
+            mma_tf32_16x8x8(z1, a, b1);
+          }
+          // only Ys, Sd and So are read in this stage, so the lower-left block can be overwritten
+          float *s0 = Sl + sl_idx(16 * rh + lg, 16 * ch + 2 * lc);
+          float *s1 = Sl + sl_idx(16 * rh + lg + 8, 16 * ch + 2 * lc);
+          *reinterpret_cast<float2 *>(s0) = make_float2(-z0[0], -z0[1]);
+          *reinterpret_cast<float2 *>(s1) = make_float2(-z0[2], -z0[3]);
+          *reinterpret_cast<float2 *>(s0 + 8) = make_float2(-z1[0], -z1[1]);
+          *reinterpret_cast<float2 *>(s1 + 8) = make_float2(-z1[2], -z1[3]);
+        }
+        bar_sync(bar_id, 128);
+        {  // Tb = T diag(beta) -> TP rows 0-63, 32 columns per thread
+          const int i = t & 63, hh = t >> 6, I = i >> 4, il = i & 15;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float v[8];
+            const int j0 = 32 * hh + 8 * q, J = j0 >> 4, jl = j0 & 15;
+            const float *src = nullptr;  // 8 consecutive T entries of row i, or zeros
+            if (J == I) src = Sd + sd_idx(I, il, jl);
+            else if ((I == 1 && J == 0) || (I == 3 && J == 2)) src = So + so_idx(I >> 1, il, jl);
+            else if (I >= 2 && J <= 1) src = Sl + sl_idx(i - 32, j0);
+            float tv[8];
+            if (src) {
+              const float4 t0v = *reinterpret_cast<const float4 *>(src);
+              const float4 t1v = *reinterpret_cast<const float4 *>(src + 4);
+              tv[0] = t0v.x; tv[1] = t0v.y; tv[2] = t0v.z; tv[3] = t0v.w;
+              tv[4] = t1v.x; tv[5] = t1v.y; tv[6] = t1v.z; tv[7] = t1v.w;
+            } else {
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int j = 32 * hh + 8 * q + jj;
-              v[jj] = j <= i ? a[8 * q + jj] : 0.f;
+              for (int jj = 0; jj < 8; ++jj) tv[jj] = 0.f;
             }
-            st8(tp + sw128(row, 4 * hh + q), v);
+            const float4 b0 = *reinterpret_cast<const float4 *>(betas + j0);
+            const float4 b1 = *reinterpret_cast<const float4 *>(betas + j0 + 4);
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float v[8];  // T is exactly lower triangular (zeros above the diagonal)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) v[jj] = tv[jj] * bv[jj];
+            st8(tp + sw128(i, 4 * hh + q), v);
           }
         }
-      }
-      tc_fence_before();
-      bar_sync(bar_id, 128);
 
-      // a3: T = (I + A^kk)^-1 in place, by recursive doubling of the block inverse
-      //   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
-      // 16 x 16 diagonal blocks first (right-looking substitution, one column
-      // per thread), then the 16-wide and the 32-wide off-diagonal blocks.
-      {
-        float x[16];
-        const int I = t >> 4, cc = t & 15;
-        if (t < 64) {
-          // left-looking: x[r2] = -(row r2 of the block) . x[0 .. r2-1], rows read as
-          // float4s, four partial sums per row (x[m] = 0 above column cc)
-          const float *Ab = Sd + sd_idx(I, 0, 0);
+        if (helper) {
+          // publish: once both d_v tiles have read chunk c - 4 out of the slot, copy
+          // TP (16 KiB, the shared-memory image) there and release chunk c + 1
+          bar_sync(bar_id, 128);
+          if (t == 0) {
+            mbar_arrive(ctx.bar(kEmptyG0 + s));  // the solve scratch is no longer read
+            ctx.wait_global(rflags + 2 * slot + 1, static_cast<uint32_t>(2 * (c >> 2)));
+          }
+          bar_sync(bar_id, 128);
+          uint4 *dst = reinterpret_cast<uint4 *>(rdata + slot * kRingSlotBytes);
 #pragma unroll
-          for (int r2 = 0; r2 < 16; ++r2) {
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m4 = 0; m4 < r2; m4 += 4) {
-              const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r2 * kSdLd + m4);
-              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (m4 + e < r2) s4[e] = fmaf(av[e], x[m4 + e], s4[e]);
+          for (int j = 0; j < 8; ++j) __stcg(dst + 128 * j + t, ld_shared_v4(tp + 16 * (128 * j + t)));
+          __threadfence();
+          bar_sync(bar_id, 128);
+          if (t == 0) {
+            st_release_gpu(rflags + 2 * slot, static_cast<uint32_t>(c + 1));
+            if (chan && c + c_step < nchunks) {  // a1 of the group's next chunk
+              ctx.wait(kFullG0 + s, cur ^ 1);
+              issue_cumsum();
             }
-            x[r2] = r2 == cc ? 1.f : (r2 > cc ? -((s4[0] + s4[1]) + (s4[2] + s4[3])) : 0.f);
           }
+          continue;
         }
-        bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
-        if (t < 64) {
-          float *Tb = Sd + sd_idx(I, 0, cc);
-#pragma unroll
-          for (int r2 = 0; r2 < 16; ++r2) Tb[r2 * kSdLd] = x[r2];
-        }
-      }
-      bar_sync(bar_id, 128);
-      // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
-      // (16 x 8 tiles; fp32 operands enter as TF32, their low 13 mantissa bits
-      // dropped: a relative error below 2^-10, under the bf16 rounding T gets next).
-      const int lg = (t & 31) >> 2, lc = t & 3;  // fragment coordinates of this lane
-      {  // T_10 and T_32: Y = L_{b+1,b} T_bb, then T_{b+1,b} = -T_{b+1,b+1} Y
-        const int b = wq >> 1, n0 = 8 * (wq & 1);  // warp: block b, 8 output columns
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8) {
-          const uint32_t a[4] = {tf32_bits(So[so_idx(b, lg, k0 + lc)]),
-                                 tf32_bits(So[so_idx(b, lg + 8, k0 + lc)]),
-                                 tf32_bits(So[so_idx(b, lg, k0 + lc + 4)]),
-                                 tf32_bits(So[so_idx(b, lg + 8, k0 + lc + 4)])};
-          const uint32_t bb[2] = {tf32_bits(Sd[sd_idx(2 * b, k0 + lc, n0 + lg)]),
-                                  tf32_bits(Sd[sd_idx(2 * b, k0 + lc + 4, n0 + lg)])};
-          mma_tf32_16x8x8(y, a, bb);
-        }
-        float *yb = Ys + b * 16 * 20;
-        *reinterpret_cast<float2 *>(yb + lg * 20 + n0 + 2 * lc) = make_float2(y[0], y[1]);
-        *reinterpret_cast<float2 *>(yb + (lg + 8) * 20 + n0 + 2 * lc) = make_float2(y[2], y[3]);
-        bar_sync(bar_id, 128);
-        float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8) {
-          const uint32_t a[4] = {tf32_bits(Sd[sd_idx(2 * b + 1, lg, k0 + lc)]),
-                                 tf32_bits(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc)]),
-                                 tf32_bits(Sd[sd_idx(2 * b + 1, lg, k0 + lc + 4)]),
-                                 tf32_bits(Sd[sd_idx(2 * b + 1, lg + 8, k0 + lc + 4)])};
-          const uint32_t bb[2] = {tf32_bits(yb[(k0 + lc) * 20 + n0 + lg]),
-                                  tf32_bits(yb[(k0 + lc + 4) * 20 + n0 + lg])};
-          mma_tf32_16x8x8(z, a, bb);
-        }
-        *reinterpret_cast<float2 *>(So + so_idx(b, lg, n0 + 2 * lc)) = make_float2(-z[0], -z[1]);
-        *reinterpret_cast<float2 *>(So + so_idx(b, lg + 8, n0 + 2 * lc)) = make_float2(-z[2], -z[3]);
-      }
-      bar_sync(bar_id, 128);
-      {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
-        // warp: rows 16 rh .. 16 rh + 15, columns 16 ch .. 16 ch + 15 (two 8-wide tiles)
-        const int ch = wq & 1, rh = wq >> 1;
-        float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
-        // T[0:32, 0:16] = [T_00; T_10];  T[0:32, 16:32] = [0; T_11]
-#pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8) {
-          if (ch == 1 && k0 < 16) continue;
-          const int ra = 16 * rh + lg;
-          const uint32_t a[4] = {tf32_bits(Sl[sl_idx(ra, k0 + lc)]), tf32_bits(Sl[sl_idx(ra + 8, k0 + lc)]),
-                                 tf32_bits(Sl[sl_idx(ra, k0 + lc + 4)]),
-                                 tf32_bits(Sl[sl_idx(ra + 8, k0 + lc + 4)])};
-          auto tlo = [&](int k, int c) -> float {  // T[k][16 ch + c], k in 0..31, c in 0..15
-            if (ch == 0) return k < 16 ? Sd[sd_idx(0, k, c)] : So[so_idx(0, k - 16, c)];
-            return Sd[sd_idx(1, k - 16, c)];
-          };
-          const uint32_t b0[2] = {tf32_bits(tlo(k0 + lc, lg)), tf32_bits(tlo(k0 + lc + 4, lg))};
-          const uint32_t b1[2] = {tf32_bits(tlo(k0 + lc, 8 + lg)), tf32_bits(tlo(k0 + lc + 4, 8 + lg))};
-          mma_tf32_16x8x8(y0, a, b0);
-          mma_tf32_16x8x8(y1, a, b1);
-        }
-        {
-          float *yr0 = Ys + (16 * rh + lg) * 36 + 16 * ch + 2 * lc;
-          float *yr1 = Ys + (16 * rh + lg + 8) * 36 + 16 * ch + 2 * lc;
-          *reinterpret_cast<float2 *>(yr0) = make_float2(y0[0], y0[1]);
-          *reinterpret_cast<float2 *>(yr1) = make_float2(y0[2], y0[3]);
-          *reinterpret_cast<float2 *>(yr0 + 8) = make_float2(y1[0], y1[1]);
-          *reinterpret_cast<float2 *>(yr1 + 8) = make_float2(y1[2], y1[3]);
-        }
-        bar_sync(bar_id, 128);
-        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
-        // T[32:48, 32:64] = [T_22, 0];  T[48:64, 32:64] = [T_32, T_33]
-#pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8) {
-          if (rh == 0 && k0 >= 16) continue;
-          auto thi = [&](int r, int k) -> float {  // T[32 + 16 rh + r][32 + k]
-            if (rh == 0) return Sd[sd_idx(2, r, k)];
-            return k < 16 ? So[so_idx(1, r, k)] : Sd[sd_idx(3, r, k - 16)];
-          };
-          const uint32_t a[4] = {tf32_bits(thi(lg, k0 + lc)), tf32_bits(thi(lg + 8, k0 + lc)),
-                                 tf32_bits(thi(lg, k0 + lc + 4)), tf32_bits(thi(lg + 8, k0 + lc + 4))};
-          const float *yk0 = Ys + (k0 + lc) * 36 + 16 * ch + lg;
-          const float *yk1 = Ys + (k0 + lc + 4) * 36 + 16 * ch + lg;
-          const uint32_t b0[2] = {tf32_bits(yk0[0]), tf32_bits(yk1[0])};
-          const uint32_t b1[2] = {tf32_bits(yk0[8]), tf32_bits(yk1[8])};
-          mma_tf32_16x8x8(z0, a, b0);
-          mma_tf32_16x8x8(z1, a, b1);
-        }
-        // only Ys, Sd and So are read in this stage, so the lower-left block can be overwritten
-        float *s0 = Sl + sl_idx(16 * rh + lg, 16 * ch + 2 * lc);
-        float *s1 = Sl + sl_idx(16 * rh + lg + 8, 16 * ch + 2 * lc);
-        *reinterpret_cast<float2 *>(s0) = make_float2(-z0[0], -z0[1]);
-        *reinterpret_cast<float2 *>(s1) = make_float2(-z0[2], -z0[3]);
-        *reinterpret_cast<float2 *>(s0 + 8) = make_float2(-z1[0], -z1[1]);
-        *reinterpret_cast<float2 *>(s1 + 8) = make_float2(-z1[2], -z1[3]);
-      }
-      bar_sync(bar_id, 128);
-      {  // Tb = T diag(beta) -> TP rows 0-63, 32 columns per thread
-        const int i = t & 63, hh = t >> 6, I = i >> 4, il = i & 15;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j0 = 32 * hh + 8 * q, J = j0 >> 4, jl = j0 & 15;
-          const float *src = nullptr;  // 8 consecutive T entries of row i, or zeros
-          if (J == I) src = Sd + sd_idx(I, il, jl);
-          else if ((I == 1 && J == 0) || (I == 3 && J == 2)) src = So + so_idx(I >> 1, il, jl);
-          else if (I >= 2 && J <= 1) src = Sl + sl_idx(i - 32, j0);
-          float tv[8];
-          if (src) {
-            const float4 t0v = *reinterpret_cast<const float4 *>(src);
-            const float4 t1v = *reinterpret_cast<const float4 *>(src + 4);
-            tv[0] = t0v.x; tv[1] = t0v.y; tv[2] = t0v.z; tv[3] = t0v.w;
-            tv[4] = t1v.x; tv[5] = t1v.y; tv[6] = t1v.z; tv[7] = t1v.w;
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) tv[jj] = 0.f;
-          }
-          const float4 b0 = *reinterpret_cast<const float4 *>(betas + j0);
-          const float4 b1 = *reinterpret_cast<const float4 *>(betas + j0 + 4);
-          const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-          float v[8];  // T is exactly lower triangular (zeros above the diagonal)
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) v[jj] = tv[jj] * bv[jj];
-          st8(tp + sw128(i, 4 * hh + q), v);
-        }
-      }
+      }  // !fed
 
       fence_async_smem();
       if (t == 0) {
@@ -644,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctx.wait(kFullV0 + s, cur);
       }
       bar_sync(bar_id, 128);
-      if (t == 0) mbar_arrive(ctx.bar(kEmptyG0 + s));  // the g area (solve scratch) may be refilled
+      if (t == 0 && !fed) mbar_arrive(ctx.bar(kEmptyG0 + s));  // the g area (solve scratch) may be refilled
 
       // [Tb; A^qk] [Kh | V] -> D2 (rows 0-63: W) and ACC[s] (U | A^qk V)
       if (t == 0) {
@@ -662,6 +783,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
         mbar_arrive(ctx.bar(kEmptyK0 + s));  // Kh (the k area) is no longer read
+      } else if (fed && t == 32) {
+        // every thread's ring loads have completed (their values are in TP[s]): count
+        // the read (a gpu-scope release, kept off the issuing thread)
+        red_release_gpu_add(rflags + 2 * slot + 1, 1u);
       } else if (row >= 64) {
         // while that runs, rows 64-127 copy Qh (bf16 pairs, all 128 channels of token
         // row - 64) into Aop[s]: the lower half of the state product's A operand
@@ -709,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(ctx.bar(kFinK0 + kw));
       mbar_wait(ctx.bar(kFinK0 + kw), 0, kWaitCycles);
     }
-  } else {
+  } else if (!helper) {
     // ------------------------------------------------------------ S-side
     const int t = tid - 256;  // key channel of the state row this thread holds
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp - 8)) << 16;
@@ -894,10 +1019,18 @@ bool make_map(CUtensorMap *m, const void *base, int T, int H) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Ring of the helper schedule: [P][kRingSlots] slot images, then [P][kRingSlots][2] words.
+size_t ring_bytes(long long pairs) {
+  return static_cast<size_t>(pairs) * kRingSlots * (kRingSlotBytes + 2 * sizeof(uint32_t));
+}
+
 }  // namespace
 
 bool chunk_tc_supported(int d_k, int d_v, bool bf16) { return bf16 && d_k == 128 && d_v == 128; }
-size_t chunk_tc_scratch_bytes(int, int, int, int) { return 0; }
+size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int, int) {
+  const long long pairs = (long long)num_seqs * num_heads;
+  return pairs >= 1 && pairs <= kHelperMaxPairs ? ring_bytes(pairs) : 0;
+}
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   if (!chunk_tc_supported(a.d_k, a.d_v, a.bf16)) return cudaErrorInvalidValue;
@@ -926,12 +1059,39 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.H = a.num_heads;
   prm.scale = a.scale;
   prm.flags = a.test_flags;
-  const long long blocks = (long long)a.num_seqs * a.num_heads * (DV / BV);
+  prm.ring = nullptr;
+  prm.ring_flags = nullptr;
+  const long long pairs = (long long)a.num_seqs * a.num_heads;
+  prm.npairs = static_cast<int>(pairs);
+  const long long blocks = pairs * (DV / BV);
   if (blocks == 0) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel,
+  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (err != cudaSuccess) return err;
-  kda_chunk_tc_kernel<<<(unsigned)blocks, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, prm);
+  // Few sequence-heads leave most SMs idle: with room for the ring, two solve helpers
+  // per sequence-head join the two d_v tiles in one cooperative launch (every CTA
+  // resident, as the hand-over through global memory needs).
+  int dev = 0, coop = 0;
+  if (pairs <= kHelperMaxPairs && 4 * pairs <= a.num_sms && a.scratch &&
+      a.scratch_bytes >= ring_bytes(pairs) && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
+    err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (err != cudaSuccess) return err;
+    prm.ring = static_cast<uint8_t *>(a.scratch);
+    prm.ring_flags = reinterpret_cast<uint32_t *>(prm.ring + pairs * kRingSlots * kRingSlotBytes);
+    err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
+    if (err != cudaSuccess) return err;
+    void *args[] = {&mq, &mk, &mg, &mv, &prm};
+    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true>),
+                                      dim3(static_cast<unsigned>(4 * pairs)), dim3(kThreads), args,
+                                      L::kAlloc, stream);
+    if (err != cudaErrorCooperativeLaunchTooLarge) return err;
+    (void)cudaGetLastError();  // not all resident (SMs taken): the plain schedule below
+    prm.ring = nullptr;
+    prm.ring_flags = nullptr;
+  }
+  kda_chunk_tc_kernel<false><<<(unsigned)blocks, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, prm);
   return cudaGetLastError();
 }
 

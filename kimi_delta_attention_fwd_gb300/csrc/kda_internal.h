@@ -45,6 +45,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
 bool chunk_tc_supported(int d_k, int d_v, bool bf16);
+// Scratch that lets the tensor-core path run every schedule (0 = none needed).
 size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int d_k, int d_v);
 
 }  // namespace kda

@@ -28,6 +28,7 @@
 namespace {
 
 constexpr size_t kScratchBytes = 256 * 1024;
+constexpr size_t kMinWorkspaceBytes = 256;  // the device status block
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char kda_noalloc_scratch[kScratchBytes];
@@ -55,9 +56,9 @@ extern "C" int kda_chunk_fwd_noalloc(const kda_shape *shape, const void *q, cons
                                      const void *v, const void *g, const void *beta,
                                      const float *init_state, const int32_t *cu_seqlens,
                                      void *out, float *final_state, cudaStream_t stream) {
-  const size_t need = kda_chunk_fwd_workspace_bytes(shape);
-  if (need == 0) return shape ? KDA_ERR_SHAPE : KDA_ERR_NULL;
-  if (need > kScratchBytes) return KDA_ERR_NOALLOC_LIMIT;
+  if (kda_chunk_fwd_workspace_bytes(shape) == 0) return shape ? KDA_ERR_SHAPE : KDA_ERR_NULL;
+  // every schedule needs the status block; kda_chunk_fwd runs the one that fits the rest
+  if (kMinWorkspaceBytes > kScratchBytes) return KDA_ERR_NOALLOC_LIMIT;
   void *scratch = scratch_on_current_device();
   if (!scratch) return KDA_ERR_DEVICE;
   return kda_chunk_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state, scratch,

@@ -19,6 +19,9 @@ Named workloads (sizes as stated for the KDA forward benchmarks):
   tiny_fp32            1 seq x 256 tokens, H=2, d=64, fp32 I/O, zero state, seed 0
   prefill_bf16         4 seqs x 4096 tokens, H=16, d=128, bf16 I/O, seed 1
   long_prefill_bf16    1 seq x 65536 tokens, H=32, d=128, mixed gate, seed 2
+  long_prefill_16k_bf16  1 seq x 16384 tokens, otherwise as long_prefill_bf16: the same
+                       32 sequence-heads (and schedule) at a quarter of the tokens, small
+                       enough for a full profiler capture
   decode_bf16          256 seqs x H=32, d=128, 128 consecutive single-token steps, seed 3
   varlen_prefill_bf16  64 seqs, lengths ~ U[512, 16384], H=32, d=128, seed 4
 """
@@ -77,6 +80,8 @@ def named(name: str):
         return PrefillSpec((4096,) * 4, 16, 128, 128, "bf16", "std", "normal", 1)
     if name == "long_prefill_bf16":
         return PrefillSpec((65536,), 32, 128, 128, "bf16", "mixed", "normal", 2)
+    if name == "long_prefill_16k_bf16":
+        return PrefillSpec((16384,), 32, 128, 128, "bf16", "mixed", "normal", 2)
     if name == "decode_bf16":
         return DecodeSpec(256, 32, 128, 128, 128, "bf16", "std", 3)
     if name == "varlen_prefill_bf16":
@@ -85,8 +90,8 @@ def named(name: str):
     raise KeyError(name)
 
 
-NAMES = ("tiny_fp32", "prefill_bf16", "long_prefill_bf16", "decode_bf16",
-         "varlen_prefill_bf16")
+NAMES = ("tiny_fp32", "prefill_bf16", "long_prefill_bf16", "long_prefill_16k_bf16",
+         "decode_bf16", "varlen_prefill_bf16")
 
 
 def torch_dtype(io: str):

@@ -74,6 +74,24 @@ def test_workspace_size(lib):
     assert lib.kda_chunk_fwd_workspace_bytes(None) == 0
 
 
+def test_workspace_holds_the_solve_helper_ring_for_few_sequence_heads(lib):
+    """Tensor-core path with at most 38 sequence-heads: the status block plus a
+    ring of 4 x 16 KiB and 32 bytes per sequence-head; otherwise the status block."""
+    ws = lambda **kw: lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(**kw)))
+    assert ws(num_seqs=1, num_heads=1) == 256 + 65568
+    assert ws(num_seqs=19, num_heads=2) == 256 + 38 * 65568
+    assert ws(num_seqs=13, num_heads=3) == 256            # 39 sequence-heads
+    assert ws(num_seqs=1, num_heads=32) == 256 + 32 * 65568
+    assert ws(num_seqs=1, num_heads=1, algo=K._ALGOS["simt"]) == 256
+    assert ws(num_seqs=1, num_heads=1, io_dtype=K.KDA_F32) == 256  # CUDA-core path
+
+
+def test_status_block_alone_is_an_accepted_workspace(lib):
+    """256 bytes select the plain schedule; fewer are rejected before any device call."""
+    s = _shape(num_seqs=1, num_heads=1)
+    assert _chunk(lib, s, ws_bytes=255) == -4
+
+
 @pytest.mark.parametrize("bad", [dict(d_k=96), dict(d_v=32), dict(num_heads=0), dict(num_seqs=-1),
                                  dict(chunk_size=128), dict(io_dtype=5), dict(algo=9),
                                  dict(total_tokens=-3), dict(gate=3), dict(gate=-1)])
