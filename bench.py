@@ -208,8 +208,8 @@ def oracle_cpu_baseline(x, pairs_limit=None):
         q, k, v, g, beta = (t[:, :pairs_limit] for t in (q, k, v, g, beta))
         init = None if init is None else init[:, :pairs_limit]
     # widen once outside the timed call (the oracle's input is fp64)
-    q, k, v, g, beta = (t.float().numpy().astype(np.float64) for t in (q, k, v, g, beta))
-    init = None if init is None else init.numpy().astype(np.float64)
+    q, k, v, g, beta = (t.float().cpu().numpy().astype(np.float64) for t in (q, k, v, g, beta))
+    init = None if init is None else init.cpu().numpy().astype(np.float64)
     threads = oracle.default_threads()
     t0 = time.perf_counter()
     oracle.kda_fwd(q, k, v, g, beta, cu.numpy(), init_state=init, threads=threads)
@@ -430,10 +430,15 @@ def main_ours(args):
         if not args.no_decode and args.workload == "prefill_bf16":
             res["decode"] = run_decode(args, ws, rank, dev)
     if rank == 0 and not args.no_cpu_baseline and x is not None:
+        # a bounded sample: on the largest workloads (over 4 M token-heads) an eighth
+        # of the heads, so that one oracle run stays within seconds
+        limit = args.cpu_heads
+        if limit is None and x["q"].shape[0] * x["q"].shape[1] > 4_000_000:
+            limit = max(1, x["q"].shape[1] // 8)
         # repeat the sample until about --cpu-seconds of oracle time have accumulated
         reps, total = 0, 0.0
         while True:
-            dt, tokens, th, threads, heads = oracle_cpu_baseline(x, pairs_limit=args.cpu_heads)
+            dt, tokens, th, threads, heads = oracle_cpu_baseline(x, pairs_limit=limit)
             reps, total = reps + 1, total + dt
             if total >= args.cpu_seconds or reps >= 50:
                 break
@@ -498,7 +503,8 @@ def main():
     ap.add_argument("--gate", default="channel", choices=["channel", "scalar", "none"],
                     help="decay per key channel (KDA), per token (Gated DeltaNet) or none (DeltaNet)")
     ap.add_argument("--cpu-heads", type=int, default=None,
-                    help="heads of the workload the CPU oracle runs (default: all)")
+                    help="heads of the workload the CPU oracle runs (default: all; an eighth on "
+                         "workloads over 4 M token-heads)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

@@ -56,6 +56,29 @@ def test_noalloc_matches_kda_chunk_fwd_on_two_calls():
         assert np.isfinite(out.float().cpu().numpy()).all()
 
 
+def test_noalloc_runs_the_schedule_that_fits_its_buffer():
+    """Up to 3 sequence-heads the solve helpers' ring fits the 256 KiB buffer and the
+    helper schedule runs; with more the plain one does.  Both give the results of
+    kda_chunk_fwd's plain schedule (a 256-byte workspace) bit for bit."""
+    kbuild.build()
+    lib = K.load_library()
+    lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(K.kda_shape)] + [ctypes.c_void_p] * 10
+    assert K.kda_chunk_fwd_workspace_bytes(1, 700, 3, 128, 128) <= 256 * 1024  # ring fits: helpers
+    assert K.kda_chunk_fwd_workspace_bytes(1, 700, 4, 128, 128) > 256 * 1024   # plain
+    for H in (3, 4):
+        x = W.prefill_inputs(W.custom_prefill([700], num_heads=H, d=128, gate="mixed", seed=53 + H))
+        d = to_dev(x)
+        ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+        ref_o, ref_f = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                     d["init_state"], workspace=ws, check=True)
+        out = torch.full_like(ref_o, float("nan"))
+        fin = torch.full_like(ref_f, float("nan"))
+        assert _noalloc(lib, d, out, fin) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_o) and torch.equal(fin, ref_f)
+
+
 def test_noalloc_rejects_bad_shapes_without_launching():
     kbuild.build()
     lib = K.load_library()
