@@ -407,6 +407,50 @@ def run_decode(args, ws, rank, dev, name="decode_bf16"):
             "gpu_launches": reps * spec.steps, "clocks": clk.summary()}
 
 
+def run_verify(args, ws, rank, dev, drafts=4, name="decode_bf16"):
+    """Speculative verification on the decode workload's sequences: `drafts`
+    consecutive tokens per sequence through kda_recurrent_fwd in one call (outputs
+    of every token, the state advanced in place), against `drafts` decode steps."""
+    import torch
+    from kimi_delta_attention_fwd_gb300 import kda_recurrent_fwd
+    from kimi_delta_attention_fwd_gb300 import workloads as W
+    spec = W.named(name)
+    spec = W.DecodeSpec(spec.num_seqs, spec.num_heads, spec.d_k, spec.d_v, drafts, spec.io_dtype,
+                        spec.gate, rank_seed(spec.seed, rank))
+    y = W.decode_inputs(spec, device=str(dev))
+    N, H = spec.num_seqs, spec.num_heads
+    pack = lambda t: t.transpose(0, 1).reshape(N * drafts, *t.shape[2:]).contiguous()
+    q, k, v, g, beta = (pack(y[n]) for n in ("q", "k", "v", "g", "beta"))
+    cu = torch.arange(N + 1, dtype=torch.int32, device=dev) * drafts
+    st = y["state"].clone()
+    out = torch.empty((N * drafts, H, spec.d_v), dtype=q.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+    call = lambda: kda_recurrent_fwd(q, k, v, g, beta, cu, st, out=out, final_state=st, stream=stream)
+    for _ in range(max(1, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        a.record(stream)
+        for _ in range(reps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / reps, ws, dev)
+    io_bytes = 2 if spec.io_dtype == "bf16" else 4
+    per_tok = io_bytes * (3 * spec.d_k + 2 * spec.d_v) + io_bytes
+    by = N * H * (drafts * per_tok + 2 * 4 * spec.d_k * spec.d_v)
+    hbm, _, src = measured_peaks()
+    ach = by / (ms * 1e-3) / 1e9
+    return {"workload": f"{name} sequences, {drafts} draft tokens each (kda_recurrent_fwd)",
+            "value": aggregate_throughput(N * drafts, ws, ms), "unit": "tokens/s", "ms_per_call": ms,
+            "reps": reps,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "traffic": None, "peak_source": f"{src} hbm_gbs"},
+            "gpu_launches": reps, "clocks": clk.summary()}
+
+
 def main_ours(args):
     import torch
     ws, rank, local = dist_info()
@@ -429,6 +473,7 @@ def main_ours(args):
         res, x = run_prefill(args, ws, rank, dev)
         if not args.no_decode and args.workload == "prefill_bf16":
             res["decode"] = run_decode(args, ws, rank, dev)
+            res["verify"] = run_verify(args, ws, rank, dev)
     if rank == 0 and not args.no_cpu_baseline and x is not None:
         # a bounded sample: on the largest workloads (over 4 M token-heads) an eighth
         # of the heads, so that one oracle run stays within seconds

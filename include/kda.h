@@ -24,9 +24,10 @@
  *       cu_seqlens : int32 [N + 1] (device), nondecreasing, cu[0] = 0,
  *                    cu[N] = T_total; sequence n owns tokens [cu[n], cu[n+1]).
  *   - Alignment: states, workspace and (prefill) q, k, v, out and a per-channel g
- *     start on a 16-byte boundary; beta, a per-token g and (decode) q, k, v, g on
- *     their element size;
- *     cu_seqlens on 4 bytes; the decode output on 4 elements.
+ *     start on a 16-byte boundary; beta, a per-token g and (decode, recurrent)
+ *     q, k, v, g on their element size;
+ *     cu_seqlens and accepted on 4 bytes; the decode and recurrent outputs on 4
+ *     elements.
  *   - q, k, v, g, beta and out have the I/O dtype (fp32 or bf16); states are
  *     always fp32.  q and k are used as given (normalisation belongs to the
  *     caller).  g must be finite and <= 0.
@@ -139,6 +140,37 @@ int kda_chunk_fwd_selected_algo(const kda_shape *shape);
 int kda_decode_step(const kda_shape *shape, const void *q, const void *k, const void *v,
                     const void *g, const void *beta, float *state, void *out,
                     cudaStream_t stream);
+
+/*
+ * The recurrence token by token over short packed sequences: the "fused
+ * recurrent" schedule of "Kimi Delta Attention (KDA)" (one program per sequence
+ * and head that walks its tokens with the state held on chip), here with the
+ * state read once and written once per call.  For speculative decoding ("K3
+ * 架构图解", the section on speculative decoding: a recurrent state must roll
+ * back the rejected drafts):
+ *   1. verify: the draft tokens of each sequence as one packed sequence, with
+ *      out and final_state = NULL: the outputs of every draft, state untouched;
+ *   2. commit: the same call with out = NULL, final_state = the state (may alias
+ *      init_state) and accepted[n] = the drafts sequence n keeps: the state
+ *      advances over exactly those tokens.
+ * Both can be combined in one call when the counts are known in advance.
+ *
+ *   q, k, v, g, beta, init_state, cu_seqlens : as for kda_chunk_fwd (device).
+ *   accepted    : int32 [N] on the device, or NULL (= every token).  final_state
+ *                 of sequence n is the state after its first accepted[n] tokens
+ *                 (clamped to [0, length]).
+ *   out         : [T_total, H, d_v] (io dtype) or NULL; when given, every token's
+ *                 output is written.
+ *   final_state : [N, H, d_k, d_v] fp32 or NULL; may alias init_state exactly.
+ * chunk_size and algo are ignored.  Every (sequence, head) takes one pass over
+ * its tokens, so this suits sequences of a few to a few dozen tokens; longer
+ * ones belong to kda_chunk_fwd.  With out and final_state both NULL nothing is
+ * enqueued.
+ */
+int kda_recurrent_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
+                      const void *g, const void *beta, const float *init_state,
+                      const int32_t *cu_seqlens, const int32_t *accepted, void *out,
+                      float *final_state, cudaStream_t stream);
 
 /*
  * kda_chunk_fwd for callers that cannot allocate device memory.  The method

@@ -152,6 +152,43 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
   return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
+int kda_recurrent_fwd(const kda_shape *s, const void *q, const void *k, const void *v,
+                      const void *g, const void *beta, const float *init_state,
+                      const int32_t *cu_seqlens, const int32_t *accepted, void *out,
+                      float *final_state, cudaStream_t stream) {
+  int rc = check_shape(s, false);
+  if (rc != KDA_OK) return rc;
+  const bool need_g = s->gate != KDA_GATE_NONE;
+  if (!need_g) g = nullptr;  // not read
+  if (!out && !final_state) return KDA_OK;  // nothing to produce
+  if (s->total_tokens > 0 && (!q || !k || !v || (need_g && !g) || !beta)) return KDA_ERR_NULL;
+  if (s->num_seqs > 0 && !cu_seqlens) return KDA_ERR_NULL;
+  const uintptr_t esz = s->io_dtype == KDA_BF16 ? 2 : 4;
+  if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(g, esz) ||
+      !aligned(beta, esz) || !aligned16(init_state) || !aligned(cu_seqlens, 4) ||
+      !aligned(accepted, 4) || !aligned(out, 4 * esz) || !aligned16(final_state))
+    return KDA_ERR_ALIGN;
+  rc = check_device(nullptr);
+  if (rc != KDA_OK) return rc;
+  if (s->num_seqs == 0) return KDA_OK;
+  kda::RecurrentArgs a;
+  a.num_seqs = s->num_seqs;
+  a.num_heads = s->num_heads;
+  a.d_k = s->d_k;
+  a.d_v = s->d_v;
+  a.scale = effective_scale(s);
+  a.bf16 = s->io_dtype == KDA_BF16;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.gate = s->gate;
+  a.init_state = init_state;
+  a.cu_seqlens = cu_seqlens;
+  a.accepted = accepted;
+  a.out = out;
+  a.final_state = final_state;
+  const cudaError_t err = kda::launch_recurrent(a, stream);
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 int kda_decode_step(const kda_shape *s, const void *q, const void *k, const void *v, const void *g,
                     const void *beta, float *state, void *out, cudaStream_t stream) {
   int rc = check_shape(s, true);

@@ -33,6 +33,8 @@
 //                and runs the state-dependent products per chunk
 //   warps 12-13  TMA producers, one per stage: the q, g, k and v parts of a stage
 //                are refilled as soon as each is released; warp 12 owns the TMEM
+// With few sequence-heads, two more CTAs per sequence-head run the solve of its
+// chunks for both d_v tiles ("Solve helpers" below).
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // KDA_ERR_DEVICE_TIMEOUT in the status word and runs to completion without
 // waiting again (outputs are then undefined, nothing blocks or faults).

@@ -1,5 +1,6 @@
 // Single-token KDA decode step (the "fused recurrent" schedule of
-// "Kimi Delta Attention (KDA)", brain.bigb.es, with one token per sequence):
+// "Kimi Delta Attention (KDA)", brain.bigb.es, with one token per sequence), and
+// the same schedule over a few consecutive tokens per sequence (below):
 //
 //   S~ = Diag(exp(g)) S,  e = beta (v - S~^T k),  S <- S~ + k e^T,
 //   o  = scale * S^T q = scale * (S~^T q + e (k . q))
@@ -138,6 +139,162 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   }
 }
 
+// Several consecutive tokens per sequence (the same fused recurrent schedule over a
+// short packed sequence, for speculative verification: "K3 架构图解", the section on
+// speculative decoding and the rollback a recurrent state needs after a rejected
+// draft).  One CTA per (sequence, head) walks the sequence's tokens in order with
+// the state in registers, read once and written once: the state after the first
+// `acc` tokens goes to final_state (acc = accepted[n], clamped to the length, or
+// the length), and the outputs of all tokens to out.  The inputs of kTokBlock
+// tokens at a time are loaded into shared memory together (the first block while
+// the state loads), so the per-token loop has no global loads on its path.
+constexpr int kTokBlock = 8;
+
+template <typename IO, int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+    kda_recurrent_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
+                         const IO *__restrict__ v, const IO *__restrict__ g,
+                         const IO *__restrict__ beta, const float *init_state,
+                         const int32_t *__restrict__ cu_seqlens,
+                         const int32_t *__restrict__ accepted, IO *__restrict__ out,
+                         float *final_state, int H, float scale, int gate) {
+  constexpr int TPR = DV / 4;
+  constexpr int RPP = kDecodeThreads / TPR;
+  constexpr int RPT = DK / RPP;
+  static_assert(RPT * RPP == DK, "row split");
+
+  __shared__ float s_q[kTokBlock][DK], s_k[kTokBlock][DK], s_a[kTokBlock][DK];
+  __shared__ float s_v[kTokBlock][DV], s_beta[kTokBlock];
+  __shared__ float4 s_red[2][RPP][TPR];
+  __shared__ float4 s_e[TPR];
+  __shared__ float s_kq;
+
+  const int pair = blockIdx.x;  // n * H + h
+  const int n = pair / H, h = pair % H;
+  const int tid = threadIdx.x;
+  const int c4 = tid % TPR;
+  const int r0 = tid / TPR;
+  const int bos = cu_seqlens[n], len = cu_seqlens[n + 1] - bos;
+  const int acc = accepted ? min(max(accepted[n], 0), len) : len;
+  const int steps = out ? len : acc;  // outputs need every token, the state only the first acc
+
+  const size_t soff = (size_t)pair * DK * DV;
+  constexpr int RS = DV / 4;  // float4s per state row
+  float4 s[RPT];
+  if (init_state) {
+    const float4 *I4 = reinterpret_cast<const float4 *>(init_state + soff);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&I4[(size_t)(r0 + i * RPP) * RS + c4]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float4 *F4 = final_state ? reinterpret_cast<float4 *>(final_state + soff) : nullptr;
+  auto store_state = [&]() {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) __stcs(&F4[(size_t)(r0 + i * RPP) * RS + c4], s[i]);
+  };
+  if (final_state && acc == 0) store_state();
+
+  for (int tb = 0; tb < steps; tb += kTokBlock) {
+    const int nb = min(kTokBlock, steps - tb);
+    // the block's inputs, once every thread is done with the previous block's
+    if (tb > 0) __syncthreads();
+    for (int idx = tid; idx < nb * DK; idx += kDecodeThreads) {
+      const int j = idx / DK, i = idx % DK;
+      const size_t row = (size_t)(bos + tb + j) * H + h;
+      s_q[j][i] = to_f32(q[row * DK + i]);
+      s_k[j][i] = to_f32(k[row * DK + i]);
+      s_a[j][i] = gate == 0 ? __expf(to_f32(g[row * DK + i]))
+                            : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
+    }
+    for (int idx = tid; idx < nb * DV; idx += kDecodeThreads) {
+      const int j = idx / DV, i = idx % DV;
+      s_v[j][i] = to_f32(v[((size_t)(bos + tb + j) * H + h) * DV + i]);
+    }
+    if (tid < nb) s_beta[tid] = to_f32(beta[(size_t)(bos + tb + tid) * H + h]);
+    __syncthreads();
+
+    for (int j = 0; j < nb; ++j) {
+      const int t = tb + j;
+      if (tid < 32) {  // k . q
+        float a = 0.f;
+        for (int i = tid; i < DK; i += 32) a += s_k[j][i] * s_q[j][i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (tid == 0) s_kq = a;
+      }
+      // forget, then partial sums of S~^T k and S~^T q over this thread's rows
+      float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int r = r0 + i * RPP;
+        const float a = s_a[j][r], qr = s_q[j][r], kr = s_k[j][r];
+        s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+        pk.x += s[i].x * kr; pk.y += s[i].y * kr; pk.z += s[i].z * kr; pk.w += s[i].w * kr;
+        pq.x += s[i].x * qr; pq.y += s[i].y * qr; pq.z += s[i].z * qr; pq.w += s[i].w * qr;
+      }
+      s_red[0][r0][c4] = pk;
+      s_red[1][r0][c4] = pq;
+      __syncthreads();
+      if (tid < TPR) {
+        float4 P = s_red[0][0][tid], R = s_red[1][0][tid];
+#pragma unroll
+        for (int jj = 1; jj < RPP; ++jj) {
+          const float4 a = s_red[0][jj][tid], c = s_red[1][jj][tid];
+          P.x += a.x; P.y += a.y; P.z += a.z; P.w += a.w;
+          R.x += c.x; R.y += c.y; R.z += c.z; R.w += c.w;
+        }
+        const float bt = s_beta[j], kq = s_kq;
+        const int c = 4 * tid;
+        float4 e;
+        e.x = bt * (s_v[j][c + 0] - P.x);
+        e.y = bt * (s_v[j][c + 1] - P.y);
+        e.z = bt * (s_v[j][c + 2] - P.z);
+        e.w = bt * (s_v[j][c + 3] - P.w);
+        s_e[tid] = e;
+        if (out) {
+          float4 o;
+          o.x = scale * (R.x + e.x * kq);
+          o.y = scale * (R.y + e.y * kq);
+          o.z = scale * (R.z + e.z * kq);
+          o.w = scale * (R.w + e.w * kq);
+          store4<IO>(out + ((size_t)(bos + t) * H + h) * DV + c, o);
+        }
+      }
+      __syncthreads();
+      // rank-one write
+      const float4 e = s_e[c4];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const float kr = s_k[j][r0 + i * RPP];
+        s[i].x += kr * e.x; s[i].y += kr * e.y; s[i].z += kr * e.z; s[i].w += kr * e.w;
+      }
+      if (final_state && t == acc - 1) store_state();
+    }
+  }
+}
+
+template <typename IO, int DK, int DV>
+cudaError_t launch_recurrent_t(const RecurrentArgs &a, cudaStream_t stream) {
+  const long long pairs = (long long)a.num_seqs * a.num_heads;
+  if (pairs == 0 || (!a.out && !a.final_state)) return cudaSuccess;
+  kda_recurrent_kernel<IO, DK, DV><<<(unsigned)pairs, kDecodeThreads, 0, stream>>>(
+      static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
+      static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
+      a.accepted, static_cast<IO *>(a.out), a.final_state, a.num_heads, a.scale, a.gate);
+  return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_recurrent_io(const RecurrentArgs &a, cudaStream_t stream) {
+  if (a.d_k == 128 && a.d_v == 128) return launch_recurrent_t<IO, 128, 128>(a, stream);
+  if (a.d_k == 128 && a.d_v == 64) return launch_recurrent_t<IO, 128, 64>(a, stream);
+  if (a.d_k == 64 && a.d_v == 128) return launch_recurrent_t<IO, 64, 128>(a, stream);
+  if (a.d_k == 64 && a.d_v == 64) return launch_recurrent_t<IO, 64, 64>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
 template <typename IO, int DK, int DV>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
   const int pairs = a.num_seqs * a.num_heads;
@@ -162,6 +319,11 @@ cudaError_t launch_decode_io(const DecodeArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   return a.bf16 ? launch_decode_io<__nv_bfloat16>(a, stream) : launch_decode_io<float>(a, stream);
+}
+
+cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream) {
+  return a.bf16 ? launch_recurrent_io<__nv_bfloat16>(a, stream)
+                : launch_recurrent_io<float>(a, stream);
 }
 
 }  // namespace kda

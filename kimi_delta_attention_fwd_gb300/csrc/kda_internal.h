@@ -39,9 +39,23 @@ struct DecodeArgs {
   void *out;
 };
 
+struct RecurrentArgs {
+  int num_seqs, num_heads, d_k, d_v;
+  float scale;
+  bool bf16;
+  const void *q, *k, *v, *g, *beta;
+  int gate;                   // kda_gate, as in ChunkArgs
+  const float *init_state;    // or NULL (zeros)
+  const int32_t *cu_seqlens;  // device [N + 1]
+  const int32_t *accepted;    // device [N] or NULL: tokens whose state final_state keeps
+  void *out;                  // or NULL
+  float *final_state;         // or NULL; may alias init_state
+};
+
 // Each returns cudaSuccess or the launch error; a shape the launcher does not
 // handle returns cudaErrorInvalidValue without launching.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
 bool chunk_tc_supported(int d_k, int d_v, bool bf16);

@@ -62,6 +62,8 @@ def load_library():
         lib.kda_chunk_fwd_workspace_bytes.argtypes = [sp]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.kda_recurrent_fwd.restype = ctypes.c_int
+        lib.kda_recurrent_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.kda_workspace_status.restype = ctypes.c_int
         lib.kda_workspace_status.argtypes = [vp, vp]
         lib.kda_status_string.restype = ctypes.c_char_p
@@ -222,3 +224,53 @@ def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=Non
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
     return out
+
+
+def kda_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, accepted=None, out=None,
+                      final_state=None, output=True, output_final_state=True, scale=None,
+                      stream=None):
+    """The recurrence token by token over short packed sequences (see include/kda.h):
+    the same tensors as kda_chunk_fwd, plus accepted (int32 [N], CUDA, or None): the
+    state returned for sequence n is the one after its first accepted[n] tokens.
+    output=False skips the outputs (the commit of a speculative step);
+    output_final_state=False leaves every state untouched (the verify).
+    final_state may be the init_state tensor itself.  Returns (out or None,
+    final_state or None)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    dev, dt = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("kda_recurrent_fwd runs on CUDA tensors only")
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    gate, gshape = _gate_of(g, T, H, dk)
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, gshape),
+                         ("v", v, (T, H, dv)), ("beta", beta, (T, H))):
+        if t is not None:
+            _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    if accepted is not None:
+        _check_io("accepted", accepted, (N,), torch.int32, dev)
+    if init_state is not None:
+        _check_io("init_state", init_state, (N, H, dk, dv), torch.float32, dev)
+    if output:
+        if out is None:
+            out = torch.empty((T, H, dv), dtype=dt, device=dev)
+        _check_io("out", out, (T, H, dv), dt, dev)
+    else:
+        out = None
+    if output_final_state:
+        if final_state is None:
+            final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+        _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
+    else:
+        final_state = None
+    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], gate=gate)
+    rc = load_library().kda_recurrent_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                          _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+                                          _ptr(accepted), _ptr(out), _ptr(final_state),
+                                          _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_recurrent_fwd")
+    return out, final_state

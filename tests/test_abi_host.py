@@ -110,6 +110,27 @@ def test_rejects_null_and_small_workspace_and_misalignment(lib):
     assert _chunk(lib, s, ws=FAKE + 8) == -3               # misaligned workspace
 
 
+def test_recurrent_validation(lib):
+    """kda_recurrent_fwd rejects bad arguments before touching the device, and with
+    neither outputs nor a final state there is nothing to do."""
+    s = _shape()
+    p = ctypes.c_void_p(FAKE)
+
+    def rec(shape, q=p, init=None, cu=p, acc=None, out=p, fin=p):
+        return lib.kda_recurrent_fwd(ctypes.byref(shape) if shape is not None else None, q, q, q, q,
+                                     q, init, cu, acc, out, fin, None)
+    assert rec(None) == -1
+    assert rec(_shape(d_k=96)) == -2
+    assert rec(_shape(gate=5)) == -2
+    assert rec(s, out=None, fin=None) == 0                      # nothing to produce: no launch
+    assert rec(s, q=None) == -1
+    assert rec(s, cu=None) == -1
+    assert rec(s, q=ctypes.c_void_p(FAKE + 1)) == -3           # q not on its element size
+    assert rec(s, fin=ctypes.c_void_p(FAKE + 8)) == -3         # states on 16 bytes
+    assert rec(s, acc=ctypes.c_void_p(FAKE + 2)) == -3         # accepted on 4 bytes
+    assert rec(s, out=ctypes.c_void_p(FAKE + 2)) == -3         # outputs on 4 elements
+
+
 def test_decode_validation(lib):
     s = _shape(total_tokens=2)
     p = ctypes.c_void_p(FAKE)
