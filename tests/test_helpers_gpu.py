@@ -13,7 +13,8 @@ import numpy as np
 import pytest
 import torch
 
-from kimi_delta_attention_fwd_gb300 import kda_chunk_fwd, kda_chunk_fwd_workspace_bytes
+from kimi_delta_attention_fwd_gb300 import (kda_chunk_fwd, kda_chunk_fwd_workspace_bytes,
+                                            kda_workspace_status)
 from kimi_delta_attention_fwd_gb300 import workloads as W
 
 from parity import TOL_BF16, rel_l2_per_head, rel_l2_states, run_oracle_prefill, to_dev
@@ -104,6 +105,31 @@ def test_helper_schedule_is_repeatable_on_one_workspace():
     for _ in range(3):
         again = _run(dv, dv["g"], ws)
         assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+
+
+def test_helper_schedule_on_concurrent_streams():
+    """Calls on two streams, each with its own workspace, may run at the same time
+    (each cooperative grid is resident as a whole); every result and status is
+    that of a lone call."""
+    spec = W.custom_prefill([900, 300, 65], num_heads=2, d=128, gate="mixed", seed=69)
+    x = W.prefill_inputs(spec)
+    dv = to_dev(x)
+    ref = _run(dv, dv["g"], _full_workspace(x, 2)[0])
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [_full_workspace(x, 2)[0] for _ in streams]
+    outs = []
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for st, ws in zip(streams, wss):
+            with torch.cuda.stream(st):
+                outs.append(kda_chunk_fwd(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"],
+                                          dv["cu_seqlens"], dv["init_state"], workspace=ws,
+                                          algo="tensor", stream=st))
+    torch.cuda.synchronize()
+    for o, f in outs:
+        assert torch.equal(o, ref[0]) and torch.equal(f, ref[1])
+    for ws in wss:
+        assert kda_workspace_status(ws) == 0
 
 
 def test_more_pairs_than_helpers_use_the_plain_schedule():
