@@ -145,54 +145,60 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 // draft).  One CTA per (sequence, head) walks the sequence's tokens in order with
 // the state in registers, read once and written once: the state after the first
 // `acc` tokens goes to final_state (acc = accepted[n], clamped to the length, or
-// the length), and the outputs of all tokens to out.  The inputs of kTokBlock
-// tokens at a time are loaded into shared memory together (the first block while
-// the state loads), so the per-token loop has no global loads on its path.
+// the length), and the outputs of all tokens to out.
+//
+// Layout: warp w owns the state columns [CW w, CW w + CW) as CG groups of four;
+// lane l holds column group l % CG of the rows l / CG + RG i.  Per token a lane
+// forms the partial sums of S~^T k and S~^T q for its four columns over its rows,
+// and an all-reduce over the RG lanes of its column group (xor shuffles) gives
+// every lane its columns' sums: e, the output and the rank-one write follow in
+// registers, with no barrier and no shared-memory reduction per token.  The
+// inputs of kTokBlock tokens at a time are loaded into shared memory together
+// (the first block while the state loads).
 constexpr int kTokBlock = 8;
+constexpr int kRecThreads = 256;  // 512 (8 columns per warp) measured slower
 
 template <typename IO, int DK, int DV>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+__global__ void __launch_bounds__(kRecThreads, 2)
     kda_recurrent_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                          const IO *__restrict__ v, const IO *__restrict__ g,
                          const IO *__restrict__ beta, const float *init_state,
                          const int32_t *__restrict__ cu_seqlens,
                          const int32_t *__restrict__ accepted, IO *__restrict__ out,
                          float *final_state, int H, float scale, int gate) {
-  constexpr int TPR = DV / 4;
-  constexpr int RPP = kDecodeThreads / TPR;
-  constexpr int RPT = DK / RPP;
-  static_assert(RPT * RPP == DK, "row split");
+  constexpr int kWarps = kRecThreads / 32;
+  constexpr int CW = DV / kWarps;  // columns per warp (16 or 8)
+  constexpr int CG = CW / 4;       // column groups of four per warp
+  constexpr int RG = 32 / CG;      // lanes per column group = row stride
+  constexpr int RPL = DK / RG;     // rows per lane
+  static_assert(CW % 4 == 0 && RPL * RG == DK, "warp layout");
 
   __shared__ float s_q[kTokBlock][DK], s_k[kTokBlock][DK], s_a[kTokBlock][DK];
   __shared__ float s_v[kTokBlock][DV], s_beta[kTokBlock];
-  __shared__ float4 s_red[2][RPP][TPR];
-  __shared__ float4 s_e[TPR];
-  __shared__ float s_kq;
 
   const int pair = blockIdx.x;  // n * H + h
   const int n = pair / H, h = pair % H;
-  const int tid = threadIdx.x;
-  const int c4 = tid % TPR;
-  const int r0 = tid / TPR;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int cg = lane % CG, rg = lane / CG;
+  const int col = CW * w + 4 * cg;  // this lane's four columns
   const int bos = cu_seqlens[n], len = cu_seqlens[n + 1] - bos;
   const int acc = accepted ? min(max(accepted[n], 0), len) : len;
   const int steps = out ? len : acc;  // outputs need every token, the state only the first acc
 
-  const size_t soff = (size_t)pair * DK * DV;
-  constexpr int RS = DV / 4;  // float4s per state row
-  float4 s[RPT];
+  const size_t soff = (size_t)pair * DK * DV + col;
+  float4 s[RPL];
   if (init_state) {
-    const float4 *I4 = reinterpret_cast<const float4 *>(init_state + soff);
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&I4[(size_t)(r0 + i * RPP) * RS + c4]);
+    for (int i = 0; i < RPL; ++i)
+      s[i] = __ldcs(reinterpret_cast<const float4 *>(init_state + soff + (size_t)(rg + RG * i) * DV));
   } else {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < RPL; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  float4 *F4 = final_state ? reinterpret_cast<float4 *>(final_state + soff) : nullptr;
   auto store_state = [&]() {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) __stcs(&F4[(size_t)(r0 + i * RPP) * RS + c4], s[i]);
+    for (int i = 0; i < RPL; ++i)
+      __stcs(reinterpret_cast<float4 *>(final_state + soff + (size_t)(rg + RG * i) * DV), s[i]);
   };
   if (final_state && acc == 0) store_state();
 
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     const int nb = min(kTokBlock, steps - tb);
     // the block's inputs, once every thread is done with the previous block's
     if (tb > 0) __syncthreads();
-    for (int idx = tid; idx < nb * DK; idx += kDecodeThreads) {
+    for (int idx = tid; idx < nb * DK; idx += kRecThreads) {
       const int j = idx / DK, i = idx % DK;
       const size_t row = (size_t)(bos + tb + j) * H + h;
       s_q[j][i] = to_f32(q[row * DK + i]);
@@ -208,67 +214,64 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       s_a[j][i] = gate == 0 ? __expf(to_f32(g[row * DK + i]))
                             : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
     }
-    for (int idx = tid; idx < nb * DV; idx += kDecodeThreads) {
+    for (int idx = tid; idx < nb * DV; idx += kRecThreads) {
       const int j = idx / DV, i = idx % DV;
       s_v[j][i] = to_f32(v[((size_t)(bos + tb + j) * H + h) * DV + i]);
     }
     if (tid < nb) s_beta[tid] = to_f32(beta[(size_t)(bos + tb + tid) * H + h]);
     __syncthreads();
 
-    for (int j = 0; j < nb; ++j) {
-      const int t = tb + j;
-      if (tid < 32) {  // k . q
-        float a = 0.f;
-        for (int i = tid; i < DK; i += 32) a += s_k[j][i] * s_q[j][i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (tid == 0) s_kq = a;
-      }
-      // forget, then partial sums of S~^T k and S~^T q over this thread's rows
+    for (int jt = 0; jt < nb; ++jt) {
+      const int t = tb + jt;
+      // forget, then this lane's partial sums of S~^T k, S~^T q (4 columns) and k . q
       float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+      float kq = 0.f;
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        const int r = r0 + i * RPP;
-        const float a = s_a[j][r], qr = s_q[j][r], kr = s_k[j][r];
-        s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
-        pk.x += s[i].x * kr; pk.y += s[i].y * kr; pk.z += s[i].z * kr; pk.w += s[i].w * kr;
-        pq.x += s[i].x * qr; pq.y += s[i].y * qr; pq.z += s[i].z * qr; pq.w += s[i].w * qr;
+      for (int i = 0; i < RPL; ++i) {
+        const int r = rg + RG * i;
+        const float a = s_a[jt][r], kr = s_k[jt][r], qr = s_q[jt][r];
+        float4 &u = s[i];
+        u.x *= a; u.y *= a; u.z *= a; u.w *= a;
+        pk.x = fmaf(u.x, kr, pk.x); pk.y = fmaf(u.y, kr, pk.y);
+        pk.z = fmaf(u.z, kr, pk.z); pk.w = fmaf(u.w, kr, pk.w);
+        pq.x = fmaf(u.x, qr, pq.x); pq.y = fmaf(u.y, qr, pq.y);
+        pq.z = fmaf(u.z, qr, pq.z); pq.w = fmaf(u.w, qr, pq.w);
+        kq = fmaf(kr, qr, kq);
       }
-      s_red[0][r0][c4] = pk;
-      s_red[1][r0][c4] = pq;
-      __syncthreads();
-      if (tid < TPR) {
-        float4 P = s_red[0][0][tid], R = s_red[1][0][tid];
+      // all-reduce over the lanes of this column group (they differ in rg: xor CG, 2 CG, ...)
 #pragma unroll
-        for (int jj = 1; jj < RPP; ++jj) {
-          const float4 a = s_red[0][jj][tid], c = s_red[1][jj][tid];
-          P.x += a.x; P.y += a.y; P.z += a.z; P.w += a.w;
-          R.x += c.x; R.y += c.y; R.z += c.z; R.w += c.w;
-        }
-        const float bt = s_beta[j], kq = s_kq;
-        const int c = 4 * tid;
-        float4 e;
-        e.x = bt * (s_v[j][c + 0] - P.x);
-        e.y = bt * (s_v[j][c + 1] - P.y);
-        e.z = bt * (s_v[j][c + 2] - P.z);
-        e.w = bt * (s_v[j][c + 3] - P.w);
-        s_e[tid] = e;
-        if (out) {
-          float4 o;
-          o.x = scale * (R.x + e.x * kq);
-          o.y = scale * (R.y + e.y * kq);
-          o.z = scale * (R.z + e.z * kq);
-          o.w = scale * (R.w + e.w * kq);
-          store4<IO>(out + ((size_t)(bos + t) * H + h) * DV + c, o);
-        }
+      for (int o = CG; o < 32; o <<= 1) {
+        pk.x += __shfl_xor_sync(0xffffffffu, pk.x, o);
+        pk.y += __shfl_xor_sync(0xffffffffu, pk.y, o);
+        pk.z += __shfl_xor_sync(0xffffffffu, pk.z, o);
+        pk.w += __shfl_xor_sync(0xffffffffu, pk.w, o);
+        pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o);
+        pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
+        pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o);
+        pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
+        kq += __shfl_xor_sync(0xffffffffu, kq, o);
       }
-      __syncthreads();
+      const float bt = s_beta[jt];
+      float4 e;
+      e.x = bt * (s_v[jt][col + 0] - pk.x);
+      e.y = bt * (s_v[jt][col + 1] - pk.y);
+      e.z = bt * (s_v[jt][col + 2] - pk.z);
+      e.w = bt * (s_v[jt][col + 3] - pk.w);
+      if (out && rg == 0) {
+        float4 o;
+        o.x = scale * (pq.x + e.x * kq);
+        o.y = scale * (pq.y + e.y * kq);
+        o.z = scale * (pq.z + e.z * kq);
+        o.w = scale * (pq.w + e.w * kq);
+        store4<IO>(out + ((size_t)(bos + t) * H + h) * DV + col, o);
+      }
       // rank-one write
-      const float4 e = s_e[c4];
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        const float kr = s_k[j][r0 + i * RPP];
-        s[i].x += kr * e.x; s[i].y += kr * e.y; s[i].z += kr * e.z; s[i].w += kr * e.w;
+      for (int i = 0; i < RPL; ++i) {
+        const float kr = s_k[jt][rg + RG * i];
+        float4 &u = s[i];
+        u.x = fmaf(kr, e.x, u.x); u.y = fmaf(kr, e.y, u.y);
+        u.z = fmaf(kr, e.z, u.z); u.w = fmaf(kr, e.w, u.w);
       }
       if (final_state && t == acc - 1) store_state();
     }
@@ -279,7 +282,7 @@ template <typename IO, int DK, int DV>
 cudaError_t launch_recurrent_t(const RecurrentArgs &a, cudaStream_t stream) {
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   if (pairs == 0 || (!a.out && !a.final_state)) return cudaSuccess;
-  kda_recurrent_kernel<IO, DK, DV><<<(unsigned)pairs, kDecodeThreads, 0, stream>>>(
+  kda_recurrent_kernel<IO, DK, DV><<<(unsigned)pairs, kRecThreads, 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
       a.accepted, static_cast<IO *>(a.out), a.final_state, a.num_heads, a.scale, a.gate);
