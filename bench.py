@@ -71,7 +71,8 @@ def measured_peaks():
 
 
 def kernel_source_hash(kind: str) -> str:
-    name = {"tensor": "kda_chunk_tc.cu", "simt": "kda_chunk_simt.cu", "decode": "kda_decode.cu"}[kind]
+    name = {"tensor": "kda_chunk_tc.cu", "simt": "kda_chunk_simt.cu", "decode": "kda_decode.cu",
+            "recurrent": "kda_decode.cu"}[kind]
     p = os.path.join(ROOT, "kimi_delta_attention_fwd_gb300", "csrc", name)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
@@ -447,7 +448,8 @@ def run_verify(args, ws, rank, dev, drafts=4, name="decode_bf16"):
             "value": aggregate_throughput(N * drafts, ws, ms), "unit": "tokens/s", "ms_per_call": ms,
             "reps": reps,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                         "traffic": None, "peak_source": f"{src} hbm_gbs"},
+                         "traffic": recorded_traffic("recurrent", f"verify{drafts}:{name}"),
+                         "peak_source": f"{src} hbm_gbs"},
             "gpu_launches": reps, "clocks": clk.summary()}
 
 
