@@ -207,7 +207,7 @@ int kda_workspace_status(const void *workspace, cudaStream_t stream);
 /* Static English description of a status code. */
 const char *kda_status_string(int status);
 
-/* Library ABI version (major * 1000 + minor). */
+/* Library ABI version (major * 1000 + minor); 1001 added kda_recurrent_fwd. */
 int kda_version(void);
 
 #ifdef __cplusplus

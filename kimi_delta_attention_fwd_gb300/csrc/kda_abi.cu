@@ -64,7 +64,7 @@ bool use_tensor_path(const kda_shape *s) {
 
 extern "C" {
 
-int kda_version(void) { return 1000; }
+int kda_version(void) { return 1001; }  // 1.1: kda_recurrent_fwd
 
 const char *kda_status_string(int status) {
   switch (status) {

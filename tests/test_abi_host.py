@@ -155,7 +155,7 @@ def test_status_strings(lib):
     assert len(seen) == 10
     assert lib.kda_status_string(-99).decode() == "unknown status"
     assert lib.kda_workspace_status(None, None) == -1
-    assert lib.kda_version() >= 1000
+    assert lib.kda_version() >= 1001  # 1.1 added kda_recurrent_fwd
 
 
 def test_gate_modes_validation(lib):
