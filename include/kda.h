@@ -107,9 +107,9 @@ typedef struct {
  *   workspace   : device scratch (16-byte aligned) of at least 256 bytes: the
  *                 device status block read by kda_workspace_status().  With
  *                 kda_chunk_fwd_workspace_bytes() bytes every schedule can run;
- *                 a smaller workspace selects the schedule that fits (results
- *                 agree to rounding).  Calls that share one workspace must be
- *                 ordered on one stream.
+ *                 a smaller workspace selects the schedule that fits.  The
+ *                 schedules give bit-identical results.  Calls that share one
+ *                 workspace must be ordered on one stream.
  * Zero sequences or zero tokens are valid (nothing but the status reset is enqueued).
  * Sequences must be at most 2^31 - 1 tokens long in total; an empty sequence
  * copies its initial state to final_state.
