@@ -4,21 +4,24 @@
 // (brain.bigb.es, section on the two schedules) in the WY / UT form of the
 // chunked DeltaNet section of "22580: от GPT-2 до Kimi K3", for the d_k x d_v
 // state layout.  For a chunk of C = 64 rows with incoming state S, G = the
-// chunk-local inclusive cumsum of g (per key channel) and gamma = exp(G_last):
+// chunk-local inclusive cumsum of g (per key channel) and gamma = exp(G_last),
+// the write strengths beta folded into the rows of K and V:
 //
-//   Kh  = K * exp(G)     Qh = Q * exp(G)     Kc = K * exp(-G)
-//   [Kh; Qh] Kc^T              -> rows: A^kk / beta_i (j < i), A^qk (j <= i)
-//   T   = (I + A^kk)^-1,  Tb = T diag(beta)            (fp32 triangular solve)
-//   [Tb; A^qk] [Kh | V]        -> rows 0-63: W = Tb Kh, U = Tb V;  rows 64-127: A^qk V
-//   [E; X] = [U; A^qk V] + [-W; Qh] S                  (state-dependent; E = U - W S)
-//   O / s  = X + A^qk (E - V) = Qh S + A^qk E          (state-dependent)
-//   S  <- gamma * S + gamma * (Kc^T (E - V) + Kc^T V)   (state-dependent)
+//   Kb  = diag(beta) K * exp(G)   Qh = Q * exp(G)   Kc = K * exp(-G)   Vb = diag(beta) V
+//   [Kb; Qh] Kc^T              -> rows: A^kk (j < i, beta_i included), A^qk (j <= i)
+//   T   = (I + A^kk)^-1                                (fp32 triangular solve)
+//   [T; A^qk] [Kb | Vb]        -> rows 0-63: W = T Kb, U = T Vb;  rows 64-127: A^qk Vb
+//   [E; X] = [U; A^qk Vb] + [-W; Qh] S                 (state-dependent; E = U - W S)
+//   O / s  = X + A^qk (E - Vb) = Qh S + A^qk E         (state-dependent)
+//   S  <- gamma * S + gamma * (Kc^T (E - Vb) + Kc^T Vb) (state-dependent)
 //
 // The output is the inter-chunk term Qh S plus the masked intra-chunk product
-// A^qk applied to the new values E.  E - V is the operand the state side rounds
-// to bf16 for both of its last two products: the A^qk V and Kc^T V terms it is
-// combined with were formed from V itself, so they add back exactly what was
-// subtracted.
+// A^qk applied to the new values E.  E - Vb is the operand the state side rounds
+// to bf16 for both of its last two products: the A^qk Vb and Kc^T Vb terms it is
+// combined with were formed from Vb itself, so they add back what was
+// subtracted.  E - Vb = (T - I) Vb - W S scales with beta like E does, so its
+// bf16 rounding stays small against E for small write strengths too (E - V would
+// be about -V there, and its rounding large against E).
 //
 // exp(G) <= 1 and exp(-G) <= exp(-G_last); every factor stays finite as long
 // as a chunk's total log decay per channel is above -80 (checked; beyond it
@@ -69,7 +72,7 @@ constexpr uint32_t kStatusGateRange = 8;    // -KDA_ERR_GATE_RANGE
 // Solve helpers (few sequence-heads).  With at most 38 (sequence, head) pairs and
 // room for the ring, the launch is cooperative (all CTAs resident) and each pair
 // gets two helper CTAs beside its two d_v tiles: K-side group kw of helper hp
-// solves the chunks c = hp + 2 kw + 4 i (the state-independent [T diag(beta); A^qk])
+// solves the chunks c = hp + 2 kw + 4 i (the state-independent [T; A^qk])
 // and hands each to both tiles through a ring in the workspace, slot c % 4
 // holding chunk c's 16 KiB shared-memory image.  Each slot has two words: the
 // last chunk published + 1 (a release store after the image) and the number of
@@ -96,11 +99,10 @@ struct L {
   static constexpr uint32_t kKQ1 = 16384, kQoff = 8192, kG = 32768, kV = 49152;
   static constexpr uint32_t kStageBytes = 49152 + C * BV * 2;
   static constexpr uint32_t kKc = 2 * kStageBytes;      // 3 x Kc [ch0-63 | ch64-127], slot = chunk % 3
-  static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [Tb rows 0-63 | A^qk rows 64-127]
-  static constexpr uint32_t kSb = kTP + 2 * 16384;        // S in bf16 [DK rows][BV]; rows 0-63 then E - V
+  static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [T rows 0-63 | A^qk rows 64-127]
+  static constexpr uint32_t kSb = kTP + 2 * 16384;        // S in bf16 [DK rows][BV]; rows 0-63 then E - Vb
   static constexpr uint32_t kLtri = kSb + DK * BV * 2;    // bf16 [Ltri; Ltri], 128 x 64
-  static constexpr uint32_t kBeta = kLtri + 16384;        // fp32 beta [2][64]
-  static constexpr uint32_t kGlast = kBeta + 512;         // fp32 G_last [2][128]
+  static constexpr uint32_t kGlast = kLtri + 16384;       // fp32 G_last [2][128]
   static constexpr uint32_t kBars = kGlast + 1024;        // mbarriers
   static constexpr uint32_t kMisc = kBars + 256;          // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
@@ -224,7 +226,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  float *betas_all = reinterpret_cast<float *>(smem + L::kBeta);
   float *glast = reinterpret_cast<float *>(smem + L::kGlast);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   constexpr int kTiles = DV / BV;
   // roles: a d_v-tile CTA (pair, tile) runs everything, or with helpers takes each
-  // chunk's [Tb; A^qk] from the ring; a helper (pair, parity hp) runs the chunk
+  // chunk's [T; A^qk] from the ring; a helper (pair, parity hp) runs the chunk
   // solve of the chunks c = hp mod 2 and publishes it
   const bool helper = kSched && (int)blockIdx.x >= 2 * p.npairs;
   const bool fed = kSched && !helper;
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // state-product operand has been copied out, g after the solve, k after the
     // W / U product, v after the state side's last product) and each is refilled
     // for chunk c + 2 as soon as it is free.  In a helper, stage s holds the chunks
-    // hp + 2 s + 4 i and no v; q and k are released after [Kh; Qh] Kc^T.
+    // hp + 2 s + 4 i and no v; q and k are released after [Kb; Qh] Kc^T.
     if ((tid & 31) == 0) {
       const int s = warp - 12;
       if (s == 0) {
@@ -339,11 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     // ------------------------------------------------------------ K-side
     // Two groups of 4 warps; group kw takes the chunks c = kw, kw + 2, ... and
-    // owns stage kw, TP[kw], beta[kw], Aop[kw], ACC[kw] and TMEM columns
+    // owns stage kw, TP[kw], Aop[kw], ACC[kw] and TMEM columns
     // [128 kw, 128 kw + 128), so the dependent chain of one chunk overlaps the
     // other group's chunk.  Kc rotates over three slots (chunk % 3).
     // A helper's groups take c = hp + 2 kw + 4 i, run the gate, a2 and the solve, and
-    // publish [Tb; A^qk]; a tile fed by helpers runs the gate and takes [Tb; A^qk]
+    // publish [T; A^qk]; a tile fed by helpers runs the gate and takes [T; A^qk]
     // from the ring in place of a2 and the solve.
     const int kw = warp >> 2;
     const int t = tid & 127;            // thread within the group
@@ -355,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t aop = tmem + kAop0 + 64u * kw;  // [-W; Qh] for the state product
     const uint32_t st = sbase + kw * L::kStageBytes;
     const uint32_t tp = sbase + L::kTP + kw * 16384;
-    float *betas = betas_all + kw * 64;
     // compact fp32 solve layout in the stage's g area (after the cumsum product has read g)
     float *Sd = reinterpret_cast<float *>(smem + kw * L::kStageBytes + L::kG);  // [4][16][20]
     float *So = Sd + 4 * 16 * kSdLd;                                            // [2][16][20]
@@ -391,9 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int len = min(C, eos - t0);
       const int kb = helper ? kw : c % 3;  // Kc slot (a helper's own two are read by its a2 only)
       const uint32_t kcb = sbase + L::kKc + kb * 16384;
-      const int slot = c & (kRingSlots - 1);  // ring slot of this chunk's [Tb; A^qk]
-      float bnext = 0.f;  // beta of this chunk, loaded early to hide the global latency
-      if (!fed && t < C && t < len) bnext = __bfloat162float(p.beta[(size_t)(t0 + t) * H + h]);
+      const int slot = c & (kRingSlots - 1);  // ring slot of this chunk's [T; A^qk]
+      // beta of this thread's row (row t mod 64 of the chunk; 0 past the sequence end),
+      // folded into Kb and Vb; loaded early to hide the global latency
+      const int rb = t & 63;
+      const float brow = rb < len ? __bfloat162float(p.beta[(size_t)(t0 + rb) * H + h]) : 0.f;
       // one thread polls the mbarriers, the others park on the named barrier
       const int it = c >> c_shift;                // this group's it-th chunk
       const uint32_t prev = (it - 1) & 1;         // parity of the group's previous release signals
@@ -442,11 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // as 0), so no exp(-G) of the next sequence's decays can overflow there.
       const bool valid = r < len;
       const float lg2 = valid ? kLog2e : 0.f;
-      uint32_t f_row = 0u, fe_row = 0u;  // exp(+-G) of the row, when G is one per row
+      // exp(G), beta exp(G) and exp(-G) of the row, when G is one per row
+      uint32_t f_row = 0u, fk_row = 0u, fe_row = 0u;
       if (!chan) {
         const float dr = g_row * lg2;
         const float er = fast_exp2(dr), ier = fast_exp2(-dr);
         f_row = pack_bf16x2(er, er);
+        fk_row = pack_bf16x2(brow * er, brow * er);
         fe_row = pack_bf16x2(ier, ier);
       }
 #pragma unroll 1
@@ -464,9 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4 *>(glast + s * 128 + 64 * half + 32 * hh + j) =
                 make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
         }
-        // bf16 pairs: exp(+-G) rounded to bf16, then one bf16 product per output pair.
-        // With one G per row (a per-token gate, or none) the two factors are the
-        // row's own, formed once before the loop.
+        // bf16 pairs: exp(+-G) (and beta exp(G) for Kb) rounded to bf16, then one bf16
+        // product per output pair.  With one G per row (a per-token gate, or none) the
+        // factors are the row's own, formed once before the loop.
         auto products = [&](auto per_channel) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -477,13 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t kh[4], qh[4], kc[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              uint32_t f = f_row, fe = fe_row;
+              uint32_t f = f_row, fk = fk_row, fe = fe_row;
               if constexpr (decltype(per_channel)::value) {
                 const float d0 = G[8 * q + 2 * j] * lg2, d1 = G[8 * q + 2 * j + 1] * lg2;
-                f = pack_bf16x2(fast_exp2(d0), fast_exp2(d1));
+                const float e0 = fast_exp2(d0), e1 = fast_exp2(d1);
+                f = pack_bf16x2(e0, e1);
+                fk = pack_bf16x2(brow * e0, brow * e1);
                 fe = pack_bf16x2(fast_exp2(-d0), fast_exp2(-d1));
               }
-              kh[j] = mul_bf16x2(kp[j], f);
+              kh[j] = mul_bf16x2(kp[j], fk);
               qh[j] = mul_bf16x2(qp[j], f);
               kc[j] = mul_bf16x2(kp[j], fe);
             }
@@ -495,13 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (chan) products(std::true_type{});
         else products(std::false_type{});
       }
-      if (t < C) betas[t] = bnext;
       fence_async_smem();
       tc_fence_before();
       bar_sync(bar_id, 128);
 
       if (fed) {
-        // The chunk's [Tb; A^qk] comes from a helper through ring slot c % 4 (acquired
+        // The chunk's [T; A^qk] comes from a helper through ring slot c % 4 (acquired
         // above): it is read into registers while TP[s] is still being read by chunk
         // c - 2's output product, then stored there.  The read is counted while the
         // W / U product runs.
@@ -515,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) st_shared_v4(tp + 16 * (128 * j + t), w[j].x, w[j].y, w[j].z, w[j].w);
       } else {
-        // a2: [Kh; Qh] Kc^T -> D1 (rows 0-63: A^kk / beta, rows 64-127: A^qk)
+        // a2: [Kb; Qh] Kc^T -> D1 (rows 0-63: A^kk, rows 64-127: A^qk)
         if (t == 0) {
           tc_fence_after();
           constexpr uint32_t id = idesc_bf16(128, 64, false, false);
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(mma_bar);
           ctx.wait(kMmaK0 + kw, kph & 1);
-          if (helper) {  // Kh and Qh are read by a2 only in a helper
+          if (helper) {  // Kb and Qh are read by a2 only in a helper
             mbar_arrive(ctx.bar(kEmptyQ0 + s));
             mbar_arrive(ctx.bar(kEmptyK0 + s));
           } else if (c >= 2) {
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++kph;
         bar_sync(bar_id, 128);
         tc_fence_after();
-        // A^kk (fp32, strictly lower, beta applied) goes to the stage's g area, which
+        // A^kk (fp32, strictly lower; beta is in Kb) goes to the stage's g area, which
         // the cumsum product has finished reading, in the compact solve layout
         // (diagonal 16-blocks, the two 16-wide sub-diagonal blocks, the lower-left
         // 32 x 32 block; the zero blocks above the diagonal are not stored).  T is
@@ -547,17 +552,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < 2; ++hh) {
           float a[32];
           tmem_ld32(tm + lane_base + 32 * hh, a);
-          if (row < 64) {  // A^kk row (beta_row, strictly lower)
+          if (row < 64) {  // A^kk row (strictly lower)
             // Entries on and above the diagonal of a diagonal block are stored unmasked:
             // the substitution below reads only the strictly lower ones and then
             // overwrites each block with its inverse.
-            const float bi = betas[row];
             const int I = row >> 4, rl = row & 15;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const int j = 32 * hh + 4 * q;  // global column of this float4
-              const float4 v = make_float4(bi * a[4 * q + 0], bi * a[4 * q + 1], bi * a[4 * q + 2],
-                                           bi * a[4 * q + 3]);
+              const float4 v = make_float4(a[4 * q + 0], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
               const int J = j >> 4;  // block column (compile-time)
               if (J == I) *reinterpret_cast<float4 *>(Sd + sd_idx(I, rl, j & 15)) = v;
               if ((I == 1 && J == 0) || (I == 3 && J == 2))
@@ -707,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float2 *>(s1 + 8) = make_float2(-z1[2], -z1[3]);
         }
         bar_sync(bar_id, 128);
-        {  // Tb = T diag(beta) -> TP rows 0-63, 32 columns per thread
+        {  // T -> TP rows 0-63 (bf16), 32 columns per thread
           const int i = t & 63, hh = t >> 6, I = i >> 4, il = i & 15;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -726,13 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) tv[jj] = 0.f;
             }
-            const float4 b0 = *reinterpret_cast<const float4 *>(betas + j0);
-            const float4 b1 = *reinterpret_cast<const float4 *>(betas + j0 + 4);
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-            float v[8];  // T is exactly lower triangular (zeros above the diagonal)
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) v[jj] = tv[jj] * bv[jj];
-            st8(tp + sw128(i, 4 * hh + q), v);
+            st8(tp + sw128(i, 4 * hh + q), tv);  // T is exactly lower triangular
           }
         }
 
@@ -761,15 +758,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }  // !fed
 
-      fence_async_smem();
-      if (t == 0) {
-        if (c >= 2) ctx.wait(kSDone0 + s, prev);  // chunk c - 2 is done with Aop[s] and ACC[s]
-        ctx.wait(kFullV0 + s, cur);
+      // Vb = diag(beta) V in place, each thread its part (row t mod 64, half t / 64 of
+      // its columns) once the v tile has landed; one barrier covers it and the waits
+      ctx.wait(kFullV0 + s, cur);
+      {
+        const uint32_t fb = pack_bf16x2(brow, brow);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t addr = st + L::kV + sw128(rb, 4 * (t >> 6) + q);
+          const uint4 w = ld_shared_v4(addr);
+          st_shared_v4(addr, mul_bf16x2(w.x, fb), mul_bf16x2(w.y, fb), mul_bf16x2(w.z, fb),
+                       mul_bf16x2(w.w, fb));
+        }
       }
+      fence_async_smem();
+      if (t == 0 && c >= 2) ctx.wait(kSDone0 + s, prev);  // chunk c - 2 is done with Aop[s] and ACC[s]
       bar_sync(bar_id, 128);
       if (t == 0 && !fed) mbar_arrive(ctx.bar(kEmptyG0 + s));  // the g area (solve scratch) may be refilled
 
-      // [Tb; A^qk] [Kh | V] -> D2 (rows 0-63: W) and ACC[s] (U | A^qk V)
+      // [T; A^qk] [Kb | Vb] -> D2 (rows 0-63: W) and ACC[s] (U | A^qk Vb)
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
@@ -784,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
-        mbar_arrive(ctx.bar(kEmptyK0 + s));  // Kh (the k area) is no longer read
+        mbar_arrive(ctx.bar(kEmptyK0 + s));  // Kb (the k area) is no longer read
       } else if (fed && t == 32) {
         // every thread's ring loads have completed (their values are in TP[s]): count
         // the read (a gpu-scope release, kept off the issuing thread)
@@ -899,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++sph;
       bar_sync(2, 128);
       tc_fence_after();
-      if (t < 64) {  // E - V (rows 0-63) -> bf16 over the first half of Sb
+      if (t < 64) {  // E - Vb (rows 0-63) -> bf16 over the first half of Sb
 #pragma unroll
         for (int hh = 0; hh < BV / 32; ++hh) {
           float a[32];
@@ -917,8 +924,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       tc_fence_before();
       bar_sync(2, 128);
-      // a4: D4 = Kc^T (E - V) + Kc^T V over Aop[s] (read by the product above);
-      // a5: ACC[s] += [Tb; A^qk] (E - V), which turns rows 64-127 into O / s
+      // a4: D4 = Kc^T (E - Vb) + Kc^T Vb over Aop[s] (read by the product above);
+      // a5: ACC[s] += [T; A^qk] (E - Vb), which turns rows 64-127 into O / s
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id4 = idesc_bf16(128, BV, true, true);

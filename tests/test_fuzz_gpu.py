@@ -1,0 +1,99 @@
+"""Seeded random configurations through every prefill path and the recurrent pass,
+each against the oracle (the recurrence of "Kimi Delta Attention (KDA)" in fp64).
+
+Each case draws the number of sequences, their lengths (0, 1, chunk boundaries
+and ragged tails included), the heads, the gate form (per channel, per token,
+none), whether an initial state is given, and for fp32 I/O the head size.  The
+tensor-core cases run both schedules (solve helpers and plain) and require them
+to agree bit for bit.
+
+Conditioning: random cases include sequences of a single token with a zero
+initial state, whose output scale * beta (q . k) v can be far below the terms
+that form it (q . k near 0 while |q| = |k| = 1).  bf16 operands carry an error
+of about 2^-9 |q_i k_i| per channel, so for bf16 I/O the relative L2 of such a
+(sequence, head) is measured against at least 2^-6 |scale v| instead of an
+output that cancelled to nearly nothing.  fp32 I/O keeps the plain relative L2."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_fwd_gb300 import kda_chunk_fwd, kda_recurrent_fwd
+from kimi_delta_attention_fwd_gb300 import workloads as W
+
+from parity import TOL_BF16, TOL_F32, rel_l2_per_head, rel_l2_states, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _rel_l2_floored(out, ref, v, cu, scale, floor):
+    """max over (sequence, head) of ||out - ref|| / max(||ref||, floor ||scale v||)."""
+    out, ref, v = (np.asarray(a, dtype=np.float64) for a in (out, ref, v))
+    worst = 0.0
+    for n in range(len(cu) - 1):
+        a, b, w = out[cu[n]:cu[n + 1]], ref[cu[n]:cu[n + 1]], v[cu[n]:cu[n + 1]]
+        if a.shape[0] == 0:
+            continue
+        num = np.sqrt(((a - b) ** 2).sum(axis=(0, 2)))
+        den = np.maximum(np.sqrt((b ** 2).sum(axis=(0, 2))), floor * scale * np.sqrt((w ** 2).sum(axis=(0, 2))))
+        worst = max(worst, float((num / np.maximum(den, 1e-300)).max()))
+    return worst
+
+
+def _case(seed):
+    r = random.Random(seed)
+    n = r.randint(1, 5)
+    lens = [r.choice([0, 1, 2, 63, 64, 65, 127, 128, 129, r.randint(1, 300)]) for _ in range(n)]
+    io = r.choice(["bf16", "bf16", "f32"])
+    d = 128 if io == "bf16" else r.choice([64, 128])
+    return dict(lens=lens, H=r.randint(1, 4), io=io, d=d, gate=r.choice(["channel", "scalar", "none"]),
+                init=r.choice(["normal", "zeros"]), seed=seed)
+
+
+def _gates(x, mode):
+    if mode == "channel":
+        return x["g"], x["g"]
+    if mode == "scalar":
+        g_tok = x["g"][..., 0].contiguous()
+        return g_tok, g_tok.unsqueeze(-1).expand_as(x["g"]).contiguous()
+    return None, torch.zeros_like(x["g"])
+
+
+@pytest.mark.parametrize("seed", range(1000, 1024))
+def test_random_configuration_on_every_path(seed):
+    c = _case(seed)
+    spec = W.custom_prefill(c["lens"], num_heads=c["H"], d=c["d"], io=c["io"], gate="mixed",
+                            init=c["init"], seed=c["seed"])
+    x = W.prefill_inputs(spec)
+    g_gpu, g_ref = _gates(x, c["gate"])
+    dv = to_dev(x)
+    gd = None if g_gpu is None else g_gpu.cuda()
+    init = dv["init_state"] if c["init"] == "normal" else None
+    ro, rs = oracle.kda_fwd(x["q"], x["k"], x["v"], g_ref, x["beta"], x["cu_seqlens"],
+                            x["init_state"] if c["init"] == "normal" else None)
+    cu = x["cu_seqlens"].numpy()
+    tol = TOL_BF16 if c["io"] == "bf16" else TOL_F32
+    runs = {}
+    if c["io"] == "bf16":
+        runs["tensor"] = kda_chunk_fwd(dv["q"], dv["k"], dv["v"], gd, dv["beta"], dv["cu_seqlens"], init,
+                                       algo="tensor", check=True)
+        ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+        runs["tensor-plain"] = kda_chunk_fwd(dv["q"], dv["k"], dv["v"], gd, dv["beta"], dv["cu_seqlens"],
+                                             init, algo="tensor", workspace=ws, check=True)
+    runs["simt"] = kda_chunk_fwd(dv["q"], dv["k"], dv["v"], gd, dv["beta"], dv["cu_seqlens"], init,
+                                 algo="simt", check=True)
+    runs["recurrent"] = kda_recurrent_fwd(dv["q"], dv["k"], dv["v"], gd, dv["beta"], dv["cu_seqlens"], init)
+    torch.cuda.synchronize()
+    if "tensor" in runs:
+        assert torch.equal(runs["tensor"][0], runs["tensor-plain"][0])
+        assert torch.equal(runs["tensor"][1], runs["tensor-plain"][1])
+    scale = 1.0 / np.sqrt(c["d"])
+    for name, (o, s) in runs.items():
+        if c["io"] == "bf16":
+            eo = _rel_l2_floored(o.float().cpu().numpy(), ro, x["v"].float().numpy(), cu, scale, 2.0 ** -6)
+        else:
+            eo = rel_l2_per_head(o.float().cpu().numpy(), ro, cu)
+        es = rel_l2_states(s.cpu().numpy(), rs)
+        assert eo <= tol and es <= tol, (name, c, eo, es)
