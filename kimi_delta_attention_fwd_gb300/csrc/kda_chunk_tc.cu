@@ -582,16 +582,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        bar_sync(bar_id, 128);
+        // The diagonal 16 x 16 blocks below are inverted by the warp that read their
+        // rows out (warp 0: rows 0-31, warp 1: rows 32-63), so warps 0-1 go on after
+        // a warp-level sync while warps 2-3 finish A^qk; the group meets again after.
+        __syncwarp();
 
         // a3: T = (I + A^kk)^-1 in place, by recursive doubling of the block inverse
         //   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
         // 16 x 16 diagonal blocks first (left-looking substitution, one column
         // per thread), then the 16-wide and the 32-wide off-diagonal blocks.
-        {
+        if (t < 64) {
           float x[16];
           const int I = t >> 4, cc = t & 15;
-          if (t < 64) {
+          {
             // left-looking: x[r2] = -(row r2 of the block) . x[0 .. r2-1], rows read as
             // float4s, four partial sums per row (x[m] = 0 above column cc)
             const float *Ab = Sd + sd_idx(I, 0, 0);
@@ -609,12 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               x[r2] = r2 == cc ? 1.f : (r2 > cc ? -((s4[0] + s4[1]) + (s4[2] + s4[3])) : 0.f);
             }
           }
-          bar_sync(bar_id, 128);  // every read of the diagonal blocks is done
-          if (t < 64) {
-            float *Tb = Sd + sd_idx(I, 0, cc);
+          __syncwarp();  // every read of this warp's diagonal blocks is done
+          float *Tb = Sd + sd_idx(I, 0, cc);
 #pragma unroll
-            for (int r2 = 0; r2 < 16; ++r2) Tb[r2 * kSdLd] = x[r2];
-          }
+          for (int r2 = 0; r2 < 16; ++r2) Tb[r2 * kSdLd] = x[r2];
         }
         bar_sync(bar_id, 128);
         // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
