@@ -283,11 +283,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 12) {
     // ------------------------------------------------------------ producers
     // warp 12 fills stage 0 (even chunks), warp 13 stage 1 (odd chunks).  The parts
-    // of a stage are released at different points of the chunk (q after the
-    // state-product operand has been copied out, g after the solve, k after the
-    // W / U product, v after the state side's last product) and each is refilled
-    // for chunk c + 2 as soon as it is free.  In a helper, stage s holds the chunks
-    // hp + 2 s + 4 i and no v; q and k are released after [Kb; Qh] Kc^T.
+    // of a stage are released at different points of the chunk (g after the solve,
+    // or after the gate in a tile fed by helpers; q after the state-product operand
+    // has been copied out; k after the W / U product; v after the state side's last
+    // product) and each is refilled for chunk c + 2 in that order, so the g tile the
+    // next cumsum product reads is in flight while the chunk's W / U product runs.
+    // In a helper, stage s holds the chunks hp + 2 s + 4 i and no v; q and k are
+    // released after [Kb; Qh] Kc^T, g after the solve, and are refilled in that order.
     if ((tid & 31) == 0) {
       const int s = warp - 12;
       if (s == 0) {
@@ -305,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t prev = (it - 1) & 1;
         const int t0 = bos + c * C;
 #pragma unroll 1
-        for (int part = 0; part < nparts; ++part) {  // q, g, k, v: the order they are released in
+        for (int pi = 0; pi < nparts; ++pi) {
+          // part 0 q, 1 g, 2 k, 3 v; loaded in the order they are released
+          const int part = helper ? (pi == 0 ? 0 : pi == 1 ? 2 : 1) : (pi == 0 ? 1 : pi == 1 ? 0 : pi);
           if (it >= 1) ctx.wait(kEmptyQ0 + 2 * part + s, prev);
           if (*abort_flag) break;
           const uint32_t fb = ctx.bar(kFullQ0 + 2 * part + s);
