@@ -87,7 +87,7 @@ constexpr int kHelperMaxPairs = 38;  // 4 CTAs per sequence-head, one per SM, al
 // the four 16 x 16 diagonal blocks, the sub-diagonal blocks (1,0) and (3,2), and
 // the lower-left 32 x 32 block; row strides keep 16-byte alignment and spread
 // the rows of a column over the shared-memory banks.
-constexpr int kSdLd = 20, kSlLd = 36;
+constexpr int kSdLd = 20, kSlLd = 36, kYLd = 40;
 __device__ __forceinline__ int sd_idx(int blk, int r, int c) { return (blk * 16 + r) * kSdLd + c; }
 __device__ __forceinline__ int so_idx(int blk, int r, int c) { return (blk * 16 + r) * kSdLd + c; }
 __device__ __forceinline__ int sl_idx(int r, int c) { return r * kSlLd + c; }
@@ -639,10 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tf32_bits(Sd[sd_idx(2 * b, k0 + lc + 4, n0 + lg)])};
             mma_tf32_16x8x8(y, a, bb);
           }
+          // column n of T_{b+1,b} needs column n of Y only: this warp's own columns
           float *yb = Ys + b * 16 * 20;
           *reinterpret_cast<float2 *>(yb + lg * 20 + n0 + 2 * lc) = make_float2(y[0], y[1]);
           *reinterpret_cast<float2 *>(yb + (lg + 8) * 20 + n0 + 2 * lc) = make_float2(y[2], y[3]);
-          bar_sync(bar_id, 128);
+          __syncwarp();
           float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int k0 = 0; k0 < 16; k0 += 8) {
@@ -658,72 +659,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float2 *>(So + so_idx(b, lg + 8, n0 + 2 * lc)) = make_float2(-z[2], -z[3]);
         }
         bar_sync(bar_id, 128);
-        {  // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y
-          // warp: rows 16 rh .. 16 rh + 15, columns 16 ch .. 16 ch + 15 (two 8-wide tiles)
-          const int ch = wq & 1, rh = wq >> 1;
-          float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
+        // rows 32-63, columns 0-31: Y = L[32:64, 0:32] T[0:32, 0:32], then -T[32:64, 32:64] Y.
+        // Warp wq takes columns 8 wq .. 8 wq + 7 of all 32 rows, so the second product
+        // reads only its own columns of Y; the result stays in registers until T is
+        // converted to bf16 below (L[32:64, 0:32] is read by every warp meanwhile).
+        const int n0 = 8 * wq;
+        float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
           // T[0:32, 0:16] = [T_00; T_10];  T[0:32, 16:32] = [0; T_11]
 #pragma unroll
           for (int k0 = 0; k0 < 32; k0 += 8) {
-            if (ch == 1 && k0 < 16) continue;
-            const int ra = 16 * rh + lg;
-            const uint32_t a[4] = {tf32_bits(Sl[sl_idx(ra, k0 + lc)]), tf32_bits(Sl[sl_idx(ra + 8, k0 + lc)]),
-                                   tf32_bits(Sl[sl_idx(ra, k0 + lc + 4)]),
-                                   tf32_bits(Sl[sl_idx(ra + 8, k0 + lc + 4)])};
-            auto tlo = [&](int k, int c) -> float {  // T[k][16 ch + c], k in 0..31, c in 0..15
-              if (ch == 0) return k < 16 ? Sd[sd_idx(0, k, c)] : So[so_idx(0, k - 16, c)];
-              return Sd[sd_idx(1, k - 16, c)];
+            if (wq >= 2 && k0 < 16) continue;
+            auto tlo = [&](int k, int cl) -> float {  // T[k][n0 + cl], k in 0..31, cl in 0..7
+              if (wq < 2) return k < 16 ? Sd[sd_idx(0, k, n0 + cl)] : So[so_idx(0, k - 16, n0 + cl)];
+              return Sd[sd_idx(1, k - 16, n0 - 16 + cl)];
             };
-            const uint32_t b0[2] = {tf32_bits(tlo(k0 + lc, lg)), tf32_bits(tlo(k0 + lc + 4, lg))};
-            const uint32_t b1[2] = {tf32_bits(tlo(k0 + lc, 8 + lg)), tf32_bits(tlo(k0 + lc + 4, 8 + lg))};
-            mma_tf32_16x8x8(y0, a, b0);
-            mma_tf32_16x8x8(y1, a, b1);
+            const uint32_t bb[2] = {tf32_bits(tlo(k0 + lc, lg)), tf32_bits(tlo(k0 + lc + 4, lg))};
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              const int ra = 16 * mt + lg;
+              const uint32_t a[4] = {tf32_bits(Sl[sl_idx(ra, k0 + lc)]), tf32_bits(Sl[sl_idx(ra + 8, k0 + lc)]),
+                                     tf32_bits(Sl[sl_idx(ra, k0 + lc + 4)]),
+                                     tf32_bits(Sl[sl_idx(ra + 8, k0 + lc + 4)])};
+              mma_tf32_16x8x8(y[mt], a, bb);
+            }
           }
-          {
-            float *yr0 = Ys + (16 * rh + lg) * 36 + 16 * ch + 2 * lc;
-            float *yr1 = Ys + (16 * rh + lg + 8) * 36 + 16 * ch + 2 * lc;
-            *reinterpret_cast<float2 *>(yr0) = make_float2(y0[0], y0[1]);
-            *reinterpret_cast<float2 *>(yr1) = make_float2(y0[2], y0[3]);
-            *reinterpret_cast<float2 *>(yr0 + 8) = make_float2(y1[0], y1[1]);
-            *reinterpret_cast<float2 *>(yr1 + 8) = make_float2(y1[2], y1[3]);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            float *yr = Ys + (16 * mt + lg) * kYLd + n0 + 2 * lc;
+            *reinterpret_cast<float2 *>(yr) = make_float2(y[mt][0], y[mt][1]);
+            *reinterpret_cast<float2 *>(yr + 8 * kYLd) = make_float2(y[mt][2], y[mt][3]);
           }
-          bar_sync(bar_id, 128);
-          float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+          __syncwarp();
           // T[32:48, 32:64] = [T_22, 0];  T[48:64, 32:64] = [T_32, T_33]
 #pragma unroll
           for (int k0 = 0; k0 < 32; k0 += 8) {
-            if (rh == 0 && k0 >= 16) continue;
-            auto thi = [&](int r, int k) -> float {  // T[32 + 16 rh + r][32 + k]
-              if (rh == 0) return Sd[sd_idx(2, r, k)];
-              return k < 16 ? So[so_idx(1, r, k)] : Sd[sd_idx(3, r, k - 16)];
-            };
-            const uint32_t a[4] = {tf32_bits(thi(lg, k0 + lc)), tf32_bits(thi(lg + 8, k0 + lc)),
-                                   tf32_bits(thi(lg, k0 + lc + 4)), tf32_bits(thi(lg + 8, k0 + lc + 4))};
-            const float *yk0 = Ys + (k0 + lc) * 36 + 16 * ch + lg;
-            const float *yk1 = Ys + (k0 + lc + 4) * 36 + 16 * ch + lg;
-            const uint32_t b0[2] = {tf32_bits(yk0[0]), tf32_bits(yk1[0])};
-            const uint32_t b1[2] = {tf32_bits(yk0[8]), tf32_bits(yk1[8])};
-            mma_tf32_16x8x8(z0, a, b0);
-            mma_tf32_16x8x8(z1, a, b1);
+            const uint32_t bb[2] = {tf32_bits(Ys[(k0 + lc) * kYLd + n0 + lg]),
+                                    tf32_bits(Ys[(k0 + lc + 4) * kYLd + n0 + lg])};
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              if (mt == 0 && k0 >= 16) continue;
+              auto thi = [&](int r2, int k) -> float {  // T[32 + 16 mt + r2][32 + k]
+                if (mt == 0) return Sd[sd_idx(2, r2, k)];
+                return k < 16 ? So[so_idx(1, r2, k)] : Sd[sd_idx(3, r2, k - 16)];
+              };
+              const uint32_t a[4] = {tf32_bits(thi(lg, k0 + lc)), tf32_bits(thi(lg + 8, k0 + lc)),
+                                     tf32_bits(thi(lg, k0 + lc + 4)), tf32_bits(thi(lg + 8, k0 + lc + 4))};
+              mma_tf32_16x8x8(z[mt], a, bb);
+            }
           }
-          // only Ys, Sd and So are read in this stage, so the lower-left block can be overwritten
-          float *s0 = Sl + sl_idx(16 * rh + lg, 16 * ch + 2 * lc);
-          float *s1 = Sl + sl_idx(16 * rh + lg + 8, 16 * ch + 2 * lc);
-          *reinterpret_cast<float2 *>(s0) = make_float2(-z0[0], -z0[1]);
-          *reinterpret_cast<float2 *>(s1) = make_float2(-z0[2], -z0[3]);
-          *reinterpret_cast<float2 *>(s0 + 8) = make_float2(-z1[0], -z1[1]);
-          *reinterpret_cast<float2 *>(s1 + 8) = make_float2(-z1[2], -z1[3]);
         }
         bar_sync(bar_id, 128);
-        {  // T -> TP rows 0-63 (bf16), 32 columns per thread
+        {  // T -> TP rows 0-63 (bf16), 32 columns per thread; rows 32-63, columns 0-31
+           // come from the fragments above
           const int i = t & 63, hh = t >> 6, I = i >> 4, il = i & 15;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int j0 = 32 * hh + 8 * q, J = j0 >> 4, jl = j0 & 15;
+            if (I >= 2 && J <= 1) continue;
             const float *src = nullptr;  // 8 consecutive T entries of row i, or zeros
             if (J == I) src = Sd + sd_idx(I, il, jl);
             else if ((I == 1 && J == 0) || (I == 3 && J == 2)) src = So + so_idx(I >> 1, il, jl);
-            else if (I >= 2 && J <= 1) src = Sl + sl_idx(i - 32, j0);
             float tv[8];
             if (src) {
               const float4 t0v = *reinterpret_cast<const float4 *>(src);
@@ -736,6 +733,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             st8(tp + sw128(i, 4 * hh + q), tv);  // T is exactly lower triangular
           }
+          uint8_t *tpg = smem + L::kTP + kw * 16384;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ri = 32 + 16 * mt + lg + 8 * e, cj = n0 + 2 * lc;
+              *reinterpret_cast<uint32_t *>(tpg + sw128(ri, cj >> 3) + 2 * (cj & 7)) =
+                  pack_bf16x2(-z[mt][2 * e], -z[mt][2 * e + 1]);
+            }
         }
 
         if (helper) {
