@@ -102,9 +102,9 @@ struct L {
   static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [T rows 0-63 | A^qk rows 64-127]
   static constexpr uint32_t kSb = kTP + 2 * 16384;        // S in bf16 [DK rows][BV]; rows 0-63 then E - Vb
   static constexpr uint32_t kLtri = kSb + DK * BV * 2;    // bf16 [Ltri; Ltri], 128 x 64
-  static constexpr uint32_t kGlast = kLtri + 16384;       // fp32 G_last [2][128]
-  static constexpr uint32_t kBars = kGlast + 1024;        // mbarriers
-  static constexpr uint32_t kMisc = kBars + 256;          // tmem slot, abort flag
+  static constexpr uint32_t kGlast = kLtri + 16384;       // fp32 G_last [3][128] (2 slots used unfed)
+  static constexpr uint32_t kBars = kGlast + 1536;        // mbarriers
+  static constexpr uint32_t kMisc = kBars + 272;          // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
@@ -119,11 +119,11 @@ enum : uint32_t {
   kEmptyQ0 = 8, kEmptyG0 = 10, kEmptyK0 = 12, kEmptyV0 = 14,  // part of stage s released
   kReady0 = 16,   // K-side -> S-side: the chunk's state-independent operands are complete
   kSDone0 = 18,   // S-side -> K-side: Aop[s] and ACC[s] have been read
-  kGmRead0 = 20,  // S-side -> K-side: G_last[s] has been read
-  kKcFree0 = 22,  // S-side -> K-side: Kc[b] (and TP of that chunk) read (3 slots)
-  kMmaK0 = 25, kMmaS = 27, kFinK0 = 28, kFinS = 30, kNever = 31, kNumBars = 32
+  kGmRead0 = 20,  // S-side -> K-side: G_last[b] has been read (up to 3 slots)
+  kKcFree0 = 23,  // S-side -> K-side: Kc[b] (and TP of that chunk) read (3 slots)
+  kMmaK0 = 26, kMmaS = 28, kFinK0 = 29, kFinS = 31, kNever = 32, kNumBars = 33
 };
-static_assert(kNumBars * 8 <= 256, "mbarrier area");
+static_assert(kNumBars * 8 <= 272, "mbarrier area");
 
 // TMEM columns
 //   [128 kw, +128)   K-side group kw: G, then D1 (+0), then D2
@@ -245,6 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the chunks a stage / K-side group takes: c = c_first + i * c_step, phase i & 1
   const int c_step = helper ? 4 : 2;
   const int c_shift = helper ? 2 : 1;
+  // G_last slots: with helpers the tiles run ahead of the state side, so a third slot
+  // lets a tile's gate wait for the state side of chunk c - 3 instead of c - 2
+  constexpr int kGl = kSched ? 3 : 2;
   uint32_t *rflags = kSched ? p.ring_flags + (size_t)pair * kRingSlots * 2 : nullptr;
   uint8_t *rdata = kSched ? p.ring + (size_t)pair * kRingSlots * kRingSlotBytes : nullptr;
   const int H = p.H;
@@ -430,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctx.wait(kFullQ0 + s, cur);
         if (!helper) {
           if (c >= 3) ctx.wait(kKcFree0 + kb, ((c / 3) - 1) & 1);  // chunk c - 3 is done with Kc[kb]
-          if (c >= 2) ctx.wait(kGmRead0 + s, prev);                  // chunk c - 2 is done with G_last[s]
+          // chunk c - kGl is done with G_last[c % kGl]
+          if (c >= kGl) ctx.wait(kGmRead0 + c % kGl, ((c / kGl) - 1) & 1);
         }
       } else if (fed && t == 32) {
         // meanwhile another thread acquires the chunk's ring slot (published by a helper);
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r == len - 1) {  // the chunk's last valid row: G_last for the state side
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4 *>(glast + s * 128 + 64 * half + 32 * hh + j) =
+            *reinterpret_cast<float4 *>(glast + (c % kGl) * 128 + 64 * half + 32 * hh + j) =
                 make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
         }
         // bf16 pairs: exp(+-G) (and beta exp(G) for Kb) rounded to bf16, then one bf16
@@ -896,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // gamma = exp(G_last) of this thread's key channel; a chunk whose total log decay
       // is beyond the range the factors exp(+-G) are formed in is reported
-      const float gl = glast[s * 128 + t];
+      const float gl = glast[(c % kGl) * 128 + t];
       const float gm = fast_exp2(gl * kLog2e);
       if (!(gl >= kMinChunkLogDecay)) atomicCAS(p.status, 0u, kStatusGateRange);
       // a4/a5: [E; X] = [U; A^qk V] + [-W; Qh] S, the A operand from Aop[s] in TMEM
@@ -909,9 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(ctx.bar(kMmaS));
       }
-      bar_sync(2, 128);  // while the product runs: every thread has read G_last[s]
+      bar_sync(2, 128);  // while the product runs: every thread has read G_last[c % kGl]
       if (t == 0) {
-        mbar_arrive(ctx.bar(kGmRead0 + s));
+        mbar_arrive(ctx.bar(kGmRead0 + c % kGl));
         ctx.wait(kMmaS, sph & 1);
       }
       ++sph;
