@@ -117,6 +117,31 @@ def kda_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, scale=None,
     return out, fin
 
 
+def preprocess(q, k, beta, qk_silu=False, qk_l2norm=False, beta_sigmoid=False):
+    """The weight-free input steps of the module around the recurrence, in fp64.
+
+    "22580: от GPT-2 до Kimi K3" (temp07.ru), section "DeltaNet, или Fast Weight
+    Programmers", the forward with a per-token write strength: q and k go through
+    SiLU and are then L2-normalised over the key dimension of each (token, head)
+    (F.normalize: x / max(||x||_2, 1e-12)), and beta is the sigmoid of a logit.
+    "K3 架构图解" Ch.08 notes that the real KDA module also has these
+    normalisations.  Each step is optional, in that order: silu, then the norm.
+
+    q, k: [..., d_k]; beta: any shape.  Returns float64 (q, k, beta).
+    """
+    q, k, beta = map(_f64, (q, k, beta))
+    with np.errstate(over="ignore"):
+        if qk_silu:  # silu(x) = x * sigmoid(x) = x / (1 + e^-x)
+            q = q / (1.0 + np.exp(-q))
+            k = k / (1.0 + np.exp(-k))
+        if beta_sigmoid:
+            beta = 1.0 / (1.0 + np.exp(-beta))
+    if qk_l2norm:
+        q = q / np.maximum(np.sqrt(np.sum(q * q, axis=-1, keepdims=True)), 1e-12)
+        k = k / np.maximum(np.sqrt(np.sum(k * k, axis=-1, keepdims=True)), 1e-12)
+    return q, k, beta
+
+
 def kda_decode_steps(q, k, v, g, beta, state, scale=None, threads=None):
     """Consecutive single-token steps for N independent sequences.
 
