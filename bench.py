@@ -231,7 +231,9 @@ def run_prefill(args, ws, rank, dev):
     spec = W.PrefillSpec(spec.seqlens, spec.num_heads, spec.d_k, spec.d_v, spec.io_dtype, spec.gate,
                          spec.init, rank_seed(spec.seed, rank))
     big = spec.total_tokens * spec.num_heads > 4_000_000
-    x = W.prefill_inputs(spec, device=("cuda" if big else "cpu"))
+    # --prep: q, k and beta as drawn before the input steps, which the kernels then apply
+    x = W.prefill_inputs(spec, device=("cuda" if big else "cpu"), raw=args.prep)
+    prep = dict(qk_silu=args.prep, qk_l2norm=args.prep, beta_sigmoid=args.prep)
     if args.gate == "scalar":    # Gated DeltaNet: one log alpha per (token, head)
         x["g"] = x["g"][..., 0].contiguous()
     elif args.gate == "none":    # DeltaNet: alpha = 1, no g at all
@@ -248,7 +250,7 @@ def run_prefill(args, ws, rank, dev):
 
     def step(o=out, f=fin):
         kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"],
-                      out=o, final_state=f, workspace=work, algo=args.algo, stream=stream)
+                      out=o, final_state=f, workspace=work, algo=args.algo, stream=stream, **prep)
 
     for _ in range(args.warmup):
         step()
@@ -318,7 +320,7 @@ def run_prefill(args, ws, rank, dev):
                 di = b["din"]
                 kda_chunk_fwd(di["q"], di["k"], di["v"], di["g"], di["beta"], di["cu_seqlens"],
                               di["init_state"], out=b["out"], final_state=b["fin"], workspace=b["work"],
-                              algo=args.algo, stream=s_cmp)
+                              algo=args.algo, stream=s_cmp, **prep)
                 ev_cmp[i].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_cmp[i])
@@ -349,11 +351,14 @@ def run_prefill(args, ws, rank, dev):
         "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": N, "total_tokens": T, "num_heads": H,
                    "d_k": dk, "d_v": dv, "chunk": 64, "io_dtype": spec.io_dtype, "gate": args.gate,
+                   "prep": "silu + l2norm of q, k; sigmoid of beta" if args.prep else "none",
                    "kernel": kind, "l2": "inputs larger than L2 (%.0f MB read+written per step)" % (alg_bytes / 1e6),
                    "parallelism": f"replicas x{ws} (independent sequences per GPU)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": recorded_traffic(kind, args.workload if args.gate == "channel" else
-                                                 f"{args.workload}:{args.gate}"),
+                     "frac": achieved / hbm,
+                     "traffic": recorded_traffic(kind, (args.workload if args.gate == "channel" else
+                                                        f"{args.workload}:{args.gate}")
+                                                 + (":prep" if args.prep else "")),
                      "peak_source": f"{peak_src} hbm_gbs",
                      "tensor_tflops_algorithmic": alg_flops / (launch_ms * 1e-3) / 1e12,
                      "tensor_peak_tflops": tflops,
@@ -473,10 +478,10 @@ def main_ours(args):
         x = None
     else:
         res, x = run_prefill(args, ws, rank, dev)
-        if not args.no_decode and args.workload == "prefill_bf16":
+        if not args.no_decode and not args.prep and args.workload == "prefill_bf16":
             res["decode"] = run_decode(args, ws, rank, dev)
             res["verify"] = run_verify(args, ws, rank, dev)
-    if rank == 0 and not args.no_cpu_baseline and x is not None:
+    if rank == 0 and not args.no_cpu_baseline and not args.prep and x is not None:
         # a bounded sample: on the largest workloads (over 4 M token-heads) an eighth
         # of the heads, so that one oracle run stays within seconds
         limit = args.cpu_heads
@@ -552,6 +557,9 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=None,
                     help="heads of the workload the CPU oracle runs (default: all; an eighth on "
                          "workloads over 4 M token-heads)")
+    ap.add_argument("--prep", action="store_true",
+                    help="raw q, k and beta logits; the kernels apply silu and the L2 norm to q, k "
+                         "and the sigmoid to beta (no CPU baseline, no decode block)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

@@ -30,7 +30,7 @@
  *     elements.
  *   - q, k, v, g, beta and out have the I/O dtype (fp32 or bf16); states are
  *     always fp32.  q and k are used as given (normalisation belongs to the
- *     caller).  g must be finite and <= 0.
+ *     caller, or to the KDA_PREP_* steps below).  g must be finite and <= 0.
  *   - Return value: KDA_OK or a negative KDA_ERR_* code; on error nothing was
  *     enqueued.  No C++ exception crosses the ABI.
  */
@@ -76,6 +76,20 @@ typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_TENSOR = 1, KDA_ALGO_SIMT = 2 } kda_a
  *   KDA_GATE_NONE     alpha_t = 1 (DeltaNet); g is not read and may be NULL */
 typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_SCALAR = 1, KDA_GATE_NONE = 2 } kda_gate;
 
+/* Weight-free input steps the kernels apply on the fly, as bits of
+ * kda_shape.prep ("22580: от GPT-2 до Kimi K3", section "DeltaNet, или Fast
+ * Weight Programmers", the forward with a per-token write strength; "K3 架构图解"
+ * Ch.08 notes the real module normalises too):
+ *   KDA_PREP_QK_SILU      q and k pass through silu(x) = x sigmoid(x)
+ *   KDA_PREP_QK_L2NORM    then each (token, head) row of q and of k is divided
+ *                         by max(||row||_2, 1e-12) over d_k
+ *   KDA_PREP_BETA_SIGMOID beta holds logits; the write strength is sigmoid(beta)
+ * The tensors in memory are left as they are.  0 = every input used as given
+ * (the default, and the form of the benchmark workloads).  The fp32 paths
+ * compute the SiLU in fp32; the tensor-core path (bf16 I/O) computes it on bf16
+ * pairs with the hardware tanh, about 0.3 % relative error over a row. */
+enum { KDA_PREP_QK_SILU = 1, KDA_PREP_QK_L2NORM = 2, KDA_PREP_BETA_SIGMOID = 4 };
+
 typedef struct {
   int32_t num_seqs;     /* N >= 0 (sequences; for decode: independent sequences, one token each) */
   int32_t total_tokens; /* T_total = cu_seqlens[N]; for decode must equal num_seqs */
@@ -87,6 +101,7 @@ typedef struct {
   int32_t io_dtype;     /* kda_dtype of q, k, v, g, beta, out */
   int32_t algo;         /* kda_algo (prefill only) */
   int32_t gate;         /* kda_gate: layout of g (0 = one per key channel) */
+  int32_t prep;         /* KDA_PREP_* bits (0 = none); added in ABI 1.2 */
 } kda_shape;
 
 /*
@@ -207,7 +222,8 @@ int kda_workspace_status(const void *workspace, cudaStream_t stream);
 /* Static English description of a status code. */
 const char *kda_status_string(int status);
 
-/* Library ABI version (major * 1000 + minor); 1001 added kda_recurrent_fwd. */
+/* Library ABI version (major * 1000 + minor); 1001 added kda_recurrent_fwd,
+ * 1002 the kda_shape.prep field. */
 int kda_version(void);
 
 #ifdef __cplusplus

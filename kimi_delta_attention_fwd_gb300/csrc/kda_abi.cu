@@ -24,6 +24,7 @@ int check_shape(const kda_shape *s, bool decode) {
   if (s->io_dtype != KDA_F32 && s->io_dtype != KDA_BF16) return KDA_ERR_SHAPE;
   if (!(s->scale == s->scale) || isinf(s->scale)) return KDA_ERR_SHAPE;
   if (s->gate < KDA_GATE_CHANNEL || s->gate > KDA_GATE_NONE) return KDA_ERR_SHAPE;
+  if (s->prep & ~(KDA_PREP_QK_SILU | KDA_PREP_QK_L2NORM | KDA_PREP_BETA_SIGMOID)) return KDA_ERR_SHAPE;
   if (decode) {
     if (s->total_tokens != s->num_seqs) return KDA_ERR_SHAPE;
   } else {
@@ -64,7 +65,7 @@ bool use_tensor_path(const kda_shape *s) {
 
 extern "C" {
 
-int kda_version(void) { return 1001; }  // 1.1: kda_recurrent_fwd
+int kda_version(void) { return 1002; }  // 1.1: kda_recurrent_fwd; 1.2: kda_shape.prep
 
 const char *kda_status_string(int status) {
   switch (status) {
@@ -135,6 +136,7 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
   a.bf16 = s->io_dtype == KDA_BF16;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate = s->gate;
+  a.prep = s->prep;
   a.init_state = init_state;
   a.cu_seqlens = cu_seqlens;
   a.out = out;
@@ -180,6 +182,7 @@ int kda_recurrent_fwd(const kda_shape *s, const void *q, const void *k, const vo
   a.bf16 = s->io_dtype == KDA_BF16;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate = s->gate;
+  a.prep = s->prep;
   a.init_state = init_state;
   a.cu_seqlens = cu_seqlens;
   a.accepted = accepted;
@@ -212,6 +215,7 @@ int kda_decode_step(const kda_shape *s, const void *q, const void *k, const void
   a.bf16 = s->io_dtype == KDA_BF16;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate = s->gate;
+  a.prep = s->prep;
   a.state = state;
   a.out = out;
   const cudaError_t err = kda::launch_decode(a, stream);

@@ -47,6 +47,11 @@ __device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16 *p, float x) 
   *p = __float2bfloat16_rn(x);
 }
 
+// Input steps of kda_shape.prep in fp32 (see kda.h): silu(x) = x / (1 + e^-x), the
+// sigmoid of a write-strength logit, and 1 / max(||x||, 1e-12) = rsqrt(max(||x||^2, 1e-24)).
+__device__ __forceinline__ float silu_f32(float x) { return x / (1.f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid_f32(float x) { return 1.f / (1.f + __expf(-x)); }
+
 template <int DK>
 struct SimtSmem {
   static constexpr int LK = DK + 1;  // padded row length (conflict-free column walks)
@@ -70,7 +75,7 @@ __global__ void __launch_bounds__(NT)
                           const IO *__restrict__ beta, const float *__restrict__ init_state,
                           const int32_t *__restrict__ cu_seqlens, IO *__restrict__ out,
                           float *__restrict__ final_state, int H, int DV, float scale,
-                          int gate) {
+                          int gate, int prep) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<DK> &sm = *reinterpret_cast<SimtSmem<DK> *>(smem_raw);
 
@@ -98,6 +103,10 @@ __global__ void __launch_bounds__(NT)
         const size_t o = ((size_t)(c0 + r) * H + h) * DK + j;
         kv = ld_f32(k + o);
         qv = ld_f32(q + o);
+        if (prep & kPrepSilu) {
+          kv = silu_f32(kv);
+          qv = silu_f32(qv);
+        }
         // g per key channel (KDA), one per token for every channel (Gated DeltaNet), or 0
         if (gate == 0) gv = ld_f32(g + o);
         else if (gate == 1) gv = ld_f32(g + (size_t)(c0 + r) * H + h);
@@ -110,8 +119,30 @@ __global__ void __launch_bounds__(NT)
       const int r = idx / BV, c = idx % BV;
       sm.V[r][c] = r < len ? ld_f32(v + ((size_t)(c0 + r) * H + h) * DV + col0 + c) : 0.f;
     }
-    if (tid < C) sm.beta[tid] = tid < len ? ld_f32(beta + (size_t)(c0 + tid) * H + h) : 0.f;
+    if (tid < C) {
+      float b = 0.f;  // rows past the end write nothing, with or without the sigmoid
+      if (tid < len) {
+        b = ld_f32(beta + (size_t)(c0 + tid) * H + h);
+        if (prep & kPrepBetaSigmoid) b = sigmoid_f32(b);
+      }
+      sm.beta[tid] = b;
+    }
     __syncthreads();
+
+    // optional L2 norm of each row of K and Q (zero rows stay zero), warp per row;
+    // it overlaps the cumsum below, which reads G only
+    if (prep & kPrepL2) {
+      const int lane = tid & 31;
+      for (int rr = tid >> 5; rr < 2 * C; rr += NT / 32) {
+        float *x = rr < C ? sm.K[rr] : sm.Q[rr - C];
+        float acc = 0.f;
+        for (int j = lane; j < DK; j += 32) acc = fmaf(x[j], x[j], acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const float rn = rsqrtf(fmaxf(acc, 1e-24f));
+        for (int j = lane; j < DK; j += 32) x[j] *= rn;
+      }
+    }
 
     // a1: per-channel inclusive cumulative sum of g inside the chunk ------
     for (int j = tid; j < DK; j += NT) {
@@ -215,7 +246,7 @@ cudaError_t launch_t(const ChunkArgs &a, cudaStream_t stream) {
   kern<<<grid, NT, smem, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
-      static_cast<IO *>(a.out), a.final_state, a.num_heads, a.d_v, a.scale, a.gate);
+      static_cast<IO *>(a.out), a.final_state, a.num_heads, a.d_v, a.scale, a.gate, a.prep);
   return cudaGetLastError();
 }
 

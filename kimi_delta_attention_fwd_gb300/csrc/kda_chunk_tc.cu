@@ -136,6 +136,7 @@ struct TcParams {
   const __nv_bfloat16 *beta;
   const __nv_bfloat16 *g_tok;  // [T, H] log alpha per (token, head) when gate == 1
   int gate;                    // 0: g per key channel (TMA), 1: per token (g_tok), 2: none
+  int prep;                    // KDA_PREP_* bits: silu / L2 norm of q and k, sigmoid of beta
   const float *init_state;
   const int32_t *cu_seqlens;
   __nv_bfloat16 *out;
@@ -213,10 +214,40 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// silu(x) = x sigmoid(x) = x (1 + tanh(x / 2)) / 2 on a bf16 pair, every step in bf16
+// (the hardware tanh and three bf16x2 operations: a relative error of a few 2^-9 per
+// element, about 0.3 % over a row, against the 2 % tolerance of bf16 I/O)
+__device__ __forceinline__ uint32_t silu_bf16x2(uint32_t x) {
+  constexpr uint32_t kHalf2 = 0x3F003F00u;  // (0.5, 0.5) in bf16
+  uint32_t t, sg;
+  asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t) : "r"(mul_bf16x2(x, kHalf2)));
+  asm("fma.rn.bf16x2 %0, %1, %2, %2;" : "=r"(sg) : "r"(t), "r"(kHalf2));
+  return mul_bf16x2(x, sg);
+}
+// The optional input steps on 8 bf16 values of a q or k row: silu in place when asked;
+// with the norm, returns the sum of squares (fp32) of the values the products will use.
+__device__ __forceinline__ float prep_row8(uint4 &w, bool silu, bool norm) {
+  if (silu) w = make_uint4(silu_bf16x2(w.x), silu_bf16x2(w.y), silu_bf16x2(w.z), silu_bf16x2(w.w));
+  float ss = 0.f;
+  if (norm) {
+    float f[8];
+    unpack8(w, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  return ss;
+}
 
 // kSched = false: every CTA is a d_v tile that solves its own chunks (the plain
 // schedule); true: CTAs 2 P .. 4 P - 1 are solve helpers for the first 2 P.
-template <bool kSched>
+// kPrep: the input steps of TcParams::prep are compiled in (a call without them runs
+// the instantiation that has none of their code).
+template <bool kSched, bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -402,7 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // beta of this thread's row (row t mod 64 of the chunk; 0 past the sequence end),
       // folded into Kb and Vb; loaded early to hide the global latency
       const int rb = t & 63;
-      const float brow = rb < len ? __bfloat162float(p.beta[(size_t)(t0 + rb) * H + h]) : 0.f;
+      const float braw = rb < len ? __bfloat162float(p.beta[(size_t)(t0 + rb) * H + h]) : 0.f;
+      // beta given as a logit: sigmoid (rows past the end keep 0)
+      const float brow = kPrep && (p.prep & kPrepBetaSigmoid) && rb < len
+                             ? 1.f / (1.f + fast_exp2(-kLog2e * braw)) : braw;
       // one thread polls the mbarriers, the others park on the named barrier
       const int it = c >> c_shift;                // this group's it-th chunk
       const uint32_t prev = (it - 1) & 1;         // parity of the group's previous release signals
@@ -452,14 +486,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       // as 0), so no exp(-G) of the next sequence's decays can overflow there.
       const bool valid = r < len;
       const float lg2 = valid ? kLog2e : 0.f;
+      // Optional input steps on the row's q and k: silu in place, then the norms.  The
+      // two halves of a row meet in the stage's g area (read by the cumsum product
+      // already, written by the solve only after the next barrier).  1 / ||k|| goes into
+      // the factors of Kb and Kc, 1 / ||q|| into those of Qh.
+      const bool norm = kPrep && (p.prep & kPrepL2);
+      float rk = 1.f, rq = 1.f, lk = 0.f;  // 1 / ||k_row||, 1 / ||q_row||, log2(rk)
+      if (kPrep && (p.prep & (kPrepSilu | kPrepL2))) {
+        const bool silu = p.prep & kPrepSilu;
+        float ssk = 0.f, ssq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t addr = kq + sw128(r, j);
+          uint4 kw4 = ld_shared_v4(addr), qw4 = ld_shared_v4(addr + L::kQoff);
+          ssk += prep_row8(kw4, silu, norm);
+          ssq += prep_row8(qw4, silu, norm);
+          if (silu) {
+            st_shared_v4(addr, kw4.x, kw4.y, kw4.z, kw4.w);
+            st_shared_v4(addr + L::kQoff, qw4.x, qw4.y, qw4.z, qw4.w);
+          }
+        }
+        if (norm) {
+          float *xch = Sd;
+          xch[t] = ssk;
+          xch[128 + t] = ssq;
+          bar_sync(bar_id, 128);
+          ssk += xch[t ^ 64];
+          ssq += xch[128 + (t ^ 64)];
+          // 1 / max(||x||, 1e-12) = 2^(-log2(max(||x||^2, 1e-24)) / 2)
+          lk = -0.5f * fast_log2(fmaxf(ssk, 1e-24f));
+          rk = fast_exp2(lk);
+          rq = fast_exp2(-0.5f * fast_log2(fmaxf(ssq, 1e-24f)));
+        }
+      }
+      const float bk = kPrep ? brow * rk : brow;  // Kb's row factor
       // exp(G), beta exp(G) and exp(-G) of the row, when G is one per row
       uint32_t f_row = 0u, fk_row = 0u, fe_row = 0u;
       if (!chan) {
         const float dr = g_row * lg2;
         const float er = fast_exp2(dr), ier = fast_exp2(-dr);
-        f_row = pack_bf16x2(er, er);
-        fk_row = pack_bf16x2(brow * er, brow * er);
-        fe_row = pack_bf16x2(ier, ier);
+        if constexpr (kPrep) {
+          f_row = pack_bf16x2(rq * er, rq * er);
+          fk_row = pack_bf16x2(bk * er, bk * er);
+          fe_row = pack_bf16x2(rk * ier, rk * ier);
+        } else {
+          f_row = pack_bf16x2(er, er);
+          fk_row = pack_bf16x2(brow * er, brow * er);
+          fe_row = pack_bf16x2(ier, ier);
+        }
       }
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
@@ -479,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bf16 pairs: exp(+-G) (and beta exp(G) for Kb) rounded to bf16, then one bf16
         // product per output pair.  With one G per row (a per-token gate, or none) the
         // factors are the row's own, formed once before the loop.
-        auto products = [&](auto per_channel) {
+        auto products = [&](auto per_channel, auto normed) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t addr = kq + sw128(r, 4 * hh + q);
@@ -493,9 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (decltype(per_channel)::value) {
                 const float d0 = G[8 * q + 2 * j] * lg2, d1 = G[8 * q + 2 * j + 1] * lg2;
                 const float e0 = fast_exp2(d0), e1 = fast_exp2(d1);
-                f = pack_bf16x2(e0, e1);
-                fk = pack_bf16x2(brow * e0, brow * e1);
-                fe = pack_bf16x2(fast_exp2(-d0), fast_exp2(-d1));
+                if constexpr (decltype(normed)::value) {
+                  f = pack_bf16x2(rq * e0, rq * e1);
+                  fk = pack_bf16x2(bk * e0, bk * e1);
+                  fe = pack_bf16x2(fast_exp2(lk - d0), fast_exp2(lk - d1));
+                } else {
+                  f = pack_bf16x2(e0, e1);
+                  fk = pack_bf16x2(brow * e0, brow * e1);
+                  fe = pack_bf16x2(fast_exp2(-d0), fast_exp2(-d1));
+                }
               }
               kh[j] = mul_bf16x2(kp[j], fk);
               qh[j] = mul_bf16x2(qp[j], f);
@@ -506,8 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_shared_v4(kcb + half * 8192 + sw128(r, 4 * hh + q), kc[0], kc[1], kc[2], kc[3]);
           }
         };
-        if (chan) products(std::true_type{});
-        else products(std::false_type{});
+        if (!chan) {
+          products(std::false_type{}, std::false_type{});
+        } else if constexpr (kPrep) {
+          if (norm) products(std::true_type{}, std::true_type{});
+          else products(std::true_type{}, std::false_type{});
+        } else {
+          products(std::true_type{}, std::false_type{});
+        }
       }
       fence_async_smem();
       tc_fence_before();
@@ -1056,6 +1142,42 @@ size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int, int) {
   return pairs >= 1 && pairs <= kHelperMaxPairs ? ring_bytes(pairs) : 0;
 }
 
+// The launch of one instantiation: the solve-helper schedule when it fits (cooperative),
+// otherwise the plain one.
+template <bool kPrep>
+static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
+                      CUtensorMap &mg, CUtensorMap &mv, TcParams &prm, long long pairs,
+                      long long blocks) {
+  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false, kPrep>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (err != cudaSuccess) return err;
+  // Few sequence-heads leave most SMs idle: with room for the ring, two solve helpers
+  // per sequence-head join the two d_v tiles in one cooperative launch (every CTA
+  // resident, as the hand-over through global memory needs).
+  int dev = 0, coop = 0;
+  if (pairs <= kHelperMaxPairs && 4 * pairs <= a.num_sms && a.scratch &&
+      a.scratch_bytes >= ring_bytes(pairs) && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
+    err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true, kPrep>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (err != cudaSuccess) return err;
+    prm.ring = static_cast<uint8_t *>(a.scratch);
+    prm.ring_flags = reinterpret_cast<uint32_t *>(prm.ring + pairs * kRingSlots * kRingSlotBytes);
+    err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
+    if (err != cudaSuccess) return err;
+    void *args[] = {&mq, &mk, &mg, &mv, &prm};
+    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true, kPrep>),
+                                      dim3(static_cast<unsigned>(4 * pairs)), dim3(kThreads), args,
+                                      L::kAlloc, stream);
+    if (err != cudaErrorCooperativeLaunchTooLarge) return err;
+    (void)cudaGetLastError();  // not all resident (SMs taken): the plain schedule below
+    prm.ring = nullptr;
+    prm.ring_flags = nullptr;
+  }
+  kda_chunk_tc_kernel<false, kPrep><<<(unsigned)blocks, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, prm);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   if (!chunk_tc_supported(a.d_k, a.d_v, a.bf16)) return cudaErrorInvalidValue;
   if (!encode_fn()) return cudaErrorNotSupported;
@@ -1075,6 +1197,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.beta = static_cast<const __nv_bfloat16 *>(a.beta);
   prm.g_tok = a.gate == 1 ? static_cast<const __nv_bfloat16 *>(a.g) : nullptr;
   prm.gate = a.gate;
+  prm.prep = a.prep;
   prm.init_state = a.init_state;
   prm.cu_seqlens = a.cu_seqlens;
   prm.out = static_cast<__nv_bfloat16 *>(a.out);
@@ -1089,34 +1212,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.npairs = static_cast<int>(pairs);
   const long long blocks = pairs * (DV / BV);
   if (blocks == 0) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-  if (err != cudaSuccess) return err;
-  // Few sequence-heads leave most SMs idle: with room for the ring, two solve helpers
-  // per sequence-head join the two d_v tiles in one cooperative launch (every CTA
-  // resident, as the hand-over through global memory needs).
-  int dev = 0, coop = 0;
-  if (pairs <= kHelperMaxPairs && 4 * pairs <= a.num_sms && a.scratch &&
-      a.scratch_bytes >= ring_bytes(pairs) && cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
-    err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (err != cudaSuccess) return err;
-    prm.ring = static_cast<uint8_t *>(a.scratch);
-    prm.ring_flags = reinterpret_cast<uint32_t *>(prm.ring + pairs * kRingSlots * kRingSlotBytes);
-    err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
-    if (err != cudaSuccess) return err;
-    void *args[] = {&mq, &mk, &mg, &mv, &prm};
-    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true>),
-                                      dim3(static_cast<unsigned>(4 * pairs)), dim3(kThreads), args,
-                                      L::kAlloc, stream);
-    if (err != cudaErrorCooperativeLaunchTooLarge) return err;
-    (void)cudaGetLastError();  // not all resident (SMs taken): the plain schedule below
-    prm.ring = nullptr;
-    prm.ring_flags = nullptr;
-  }
-  kda_chunk_tc_kernel<false><<<(unsigned)blocks, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, prm);
-  return cudaGetLastError();
+  return a.prep ? launch_tc<true>(a, stream, mq, mk, mg, mv, prm, pairs, blocks)
+                : launch_tc<false>(a, stream, mq, mk, mg, mv, prm, pairs, blocks);
 }
 
 }  // namespace kda

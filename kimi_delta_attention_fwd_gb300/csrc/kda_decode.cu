@@ -42,6 +42,20 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v
   *reinterpret_cast<uint2 *>(p) = u;
 }
 
+// Input steps of kda_shape.prep, in fp32: silu(x) = x / (1 + e^-x) (saturates to x
+// and -0 without overflow), the logistic sigmoid of a write-strength logit, and
+// 1 / max(||x||, 1e-12) as rsqrt(max(||x||^2, 1e-24)).
+__device__ __forceinline__ float silu_f32(float x) { return x / (1.f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid_f32(float x) { return 1.f / (1.f + __expf(-x)); }
+__device__ __forceinline__ float inv_norm_f32(float sumsq) { return rsqrtf(fmaxf(sumsq, 1e-24f)); }
+
+// Sum over the 32 lanes of a warp, every lane gets the total.
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
 constexpr int kDecodeThreads = 256;
 
 template <typename IO, int DK, int DV>
@@ -49,7 +63,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                       const IO *__restrict__ v, const IO *__restrict__ g,
                       const IO *__restrict__ beta, float *__restrict__ state,
-                      IO *__restrict__ out, float scale, int gate) {
+                      IO *__restrict__ out, float scale, int gate, int prep) {
   constexpr int TPR = DV / 4;               // threads covering one state row (float4 each)
   constexpr int RPP = kDecodeThreads / TPR;  // rows covered per pass of the block
   constexpr int RPT = DK / RPP;              // rows held by each thread
@@ -58,7 +72,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   __shared__ float s_q[DK], s_k[DK], s_a[DK], s_v[DV];
   __shared__ float4 s_red[2][RPP][TPR];
   __shared__ float4 s_e[TPR];
-  __shared__ float s_kq, s_beta;
+  __shared__ float s_kq, s_beta, s_rn[2];
 
   const int pair = blockIdx.x;  // n * H + h
   const int tid = threadIdx.x;
@@ -74,14 +88,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const size_t koff = (size_t)pair * DK, voff = (size_t)pair * DV;
   // alpha per key channel (KDA), one alpha for every channel (Gated DeltaNet), or 1 (DeltaNet)
   const float a_tok = gate == 1 ? __expf(to_f32(g[pair])) : 1.f;
+  const bool silu = prep & kPrepSilu;
   for (int i = tid; i < DK; i += kDecodeThreads) {
-    s_q[i] = to_f32(q[koff + i]);
-    s_k[i] = to_f32(k[koff + i]);
+    const float qi = to_f32(q[koff + i]), ki = to_f32(k[koff + i]);
+    s_q[i] = silu ? silu_f32(qi) : qi;
+    s_k[i] = silu ? silu_f32(ki) : ki;
     s_a[i] = gate == 0 ? __expf(to_f32(g[koff + i])) : a_tok;
   }
   for (int i = tid; i < DV; i += kDecodeThreads) s_v[i] = to_f32(v[voff + i]);
-  if (tid == 0) s_beta = to_f32(beta[pair]);
+  if (tid == 0) {
+    const float b = to_f32(beta[pair]);
+    s_beta = (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
+  }
   __syncthreads();
+  if (prep & kPrepL2) {  // warp 0: 1 / ||k||, warp 1: 1 / ||q||; then both rows scaled
+    if (tid < 64) {
+      const float *x = tid < 32 ? s_k : s_q;
+      float acc = 0.f;
+      for (int i = tid & 31; i < DK; i += 32) acc = fmaf(x[i], x[i], acc);
+      acc = warp_sum(acc);
+      if ((tid & 31) == 0) s_rn[tid >> 5] = inv_norm_f32(acc);
+    }
+    __syncthreads();
+    for (int i = tid; i < DK; i += kDecodeThreads) {
+      s_k[i] *= s_rn[0];
+      s_q[i] *= s_rn[1];
+    }
+    __syncthreads();
+  }
 
   if (tid < 32) {  // k . q
     float acc = 0.f;
@@ -165,8 +199,9 @@ __global__ void __launch_bounds__(kRecThreads, 2)
                          const IO *__restrict__ beta, const float *init_state,
                          const int32_t *__restrict__ cu_seqlens,
                          const int32_t *__restrict__ accepted, IO *__restrict__ out,
-                         float *final_state, int H, float scale, int gate) {
+                         float *final_state, int H, float scale, int gate, int prep) {
   constexpr int kWarps = kRecThreads / 32;
+  static_assert(kTokBlock <= kWarps, "one warp per token of a block normalises its q and k");
   constexpr int CW = DV / kWarps;  // columns per warp (16 or 8)
   constexpr int CG = CW / 4;       // column groups of four per warp
   constexpr int RG = 32 / CG;      // lanes per column group = row stride
@@ -209,8 +244,9 @@ __global__ void __launch_bounds__(kRecThreads, 2)
     for (int idx = tid; idx < nb * DK; idx += kRecThreads) {
       const int j = idx / DK, i = idx % DK;
       const size_t row = (size_t)(bos + tb + j) * H + h;
-      s_q[j][i] = to_f32(q[row * DK + i]);
-      s_k[j][i] = to_f32(k[row * DK + i]);
+      const float qi = to_f32(q[row * DK + i]), ki = to_f32(k[row * DK + i]);
+      s_q[j][i] = (prep & kPrepSilu) ? silu_f32(qi) : qi;
+      s_k[j][i] = (prep & kPrepSilu) ? silu_f32(ki) : ki;
       s_a[j][i] = gate == 0 ? __expf(to_f32(g[row * DK + i]))
                             : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
     }
@@ -218,8 +254,27 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       const int j = idx / DV, i = idx % DV;
       s_v[j][i] = to_f32(v[((size_t)(bos + tb + j) * H + h) * DV + i]);
     }
-    if (tid < nb) s_beta[tid] = to_f32(beta[(size_t)(bos + tb + tid) * H + h]);
+    if (tid < nb) {
+      const float b = to_f32(beta[(size_t)(bos + tb + tid) * H + h]);
+      s_beta[tid] = (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
+    }
     __syncthreads();
+    if (prep & kPrepL2) {  // warp w divides token w's k and q by their norms
+      if (w < nb) {
+        float sk = 0.f, sq = 0.f;
+        for (int i = lane; i < DK; i += 32) {
+          sk = fmaf(s_k[w][i], s_k[w][i], sk);
+          sq = fmaf(s_q[w][i], s_q[w][i], sq);
+        }
+        sk = inv_norm_f32(warp_sum(sk));
+        sq = inv_norm_f32(warp_sum(sq));
+        for (int i = lane; i < DK; i += 32) {
+          s_k[w][i] *= sk;
+          s_q[w][i] *= sq;
+        }
+      }
+      __syncthreads();
+    }
 
     for (int jt = 0; jt < nb; ++jt) {
       const int t = tb + jt;
@@ -285,7 +340,7 @@ cudaError_t launch_recurrent_t(const RecurrentArgs &a, cudaStream_t stream) {
   kda_recurrent_kernel<IO, DK, DV><<<(unsigned)pairs, kRecThreads, 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
-      a.accepted, static_cast<IO *>(a.out), a.final_state, a.num_heads, a.scale, a.gate);
+      a.accepted, static_cast<IO *>(a.out), a.final_state, a.num_heads, a.scale, a.gate, a.prep);
   return cudaGetLastError();
 }
 
@@ -305,7 +360,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
   kda_decode_kernel<IO, DK, DV><<<pairs, kDecodeThreads, 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.state,
-      static_cast<IO *>(a.out), a.scale, a.gate);
+      static_cast<IO *>(a.out), a.scale, a.gate, a.prep);
   return cudaGetLastError();
 }
 

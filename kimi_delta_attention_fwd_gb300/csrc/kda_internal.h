@@ -8,6 +8,9 @@
 
 namespace kda {
 
+// KDA_PREP_* bits of kda_shape.prep (include/kda.h), for the kernels
+constexpr int kPrepSilu = 1, kPrepL2 = 2, kPrepBetaSigmoid = 4;
+
 // Status block at the start of the workspace, written by the prefill kernels.
 // word 0: first error code recorded (0 = none), word 1: detail (where).
 constexpr size_t kStatusBytes = 256;
@@ -18,6 +21,7 @@ struct ChunkArgs {
   bool bf16;
   const void *q, *k, *v, *g, *beta;
   int gate;           // kda_gate: 0 g per key channel, 1 per (token, head), 2 none (g unused)
+  int prep;           // KDA_PREP_* bits: SiLU / L2 norm of q and k, sigmoid of beta
   const float *init_state;
   const int32_t *cu_seqlens;
   void *out;
@@ -35,6 +39,7 @@ struct DecodeArgs {
   bool bf16;
   const void *q, *k, *v, *g, *beta;
   int gate;           // kda_gate, as in ChunkArgs
+  int prep;           // KDA_PREP_* bits, as in ChunkArgs
   float *state;
   void *out;
 };
@@ -45,6 +50,7 @@ struct RecurrentArgs {
   bool bf16;
   const void *q, *k, *v, *g, *beta;
   int gate;                   // kda_gate, as in ChunkArgs
+  int prep;                   // KDA_PREP_* bits, as in ChunkArgs
   const float *init_state;    // or NULL (zeros)
   const int32_t *cu_seqlens;  // device [N + 1]
   const int32_t *accepted;    // device [N] or NULL: tokens whose state final_state keeps

@@ -18,6 +18,7 @@ from . import build as _build
 KDA_OK = 0
 KDA_F32, KDA_BF16 = 0, 1
 KDA_GATE_CHANNEL, KDA_GATE_SCALAR, KDA_GATE_NONE = 0, 1, 2
+KDA_PREP_QK_SILU, KDA_PREP_QK_L2NORM, KDA_PREP_BETA_SIGMOID = 1, 2, 4
 _ALGOS = {"auto": 0, "tensor": 1, "simt": 2}
 _DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
 
@@ -32,7 +33,8 @@ class kda_shape(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("io_dtype", ctypes.c_int32), ("algo", ctypes.c_int32), ("gate", ctypes.c_int32)]
+                ("io_dtype", ctypes.c_int32), ("algo", ctypes.c_int32), ("gate", ctypes.c_int32),
+                ("prep", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -92,9 +94,16 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _make_shape(num_seqs, total_tokens, H, dk, dv, scale, io, algo="auto", gate=0):
+def _make_shape(num_seqs, total_tokens, H, dk, dv, scale, io, algo="auto", gate=0, prep=0):
     return kda_shape(int(num_seqs), int(total_tokens), int(H), int(dk), int(dv), 64,
-                     float(scale) if scale is not None else 0.0, io, _ALGOS[algo], int(gate))
+                     float(scale) if scale is not None else 0.0, io, _ALGOS[algo], int(gate),
+                     int(prep))
+
+
+def _prep_bits(qk_silu, qk_l2norm, beta_sigmoid):
+    """KDA_PREP_* bits of the optional input steps (see include/kda.h)."""
+    return ((KDA_PREP_QK_SILU if qk_silu else 0) | (KDA_PREP_QK_L2NORM if qk_l2norm else 0)
+            | (KDA_PREP_BETA_SIGMOID if beta_sigmoid else 0))
 
 
 def _gate_of(g, lead, H, dk):
@@ -139,7 +148,7 @@ def kda_chunk_fwd_selected_algo(num_seqs, total_tokens, num_heads, d_k, d_v, io_
 
 def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, final_state=None,
                   output_final_state=True, workspace=None, scale=None, algo="auto", stream=None,
-                  check=False):
+                  check=False, qk_silu=False, qk_l2norm=False, beta_sigmoid=False):
     """Chunkwise prefill over packed sequences (see include/kda.h).
 
     q, k: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (one dtype: bf16 or fp32, CUDA);
@@ -147,6 +156,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
     Gated DeltaNet) or None (alpha = 1, DeltaNet);
     cu_seqlens: int32 [N+1] (CUDA); init_state: fp32 [N, H, d_k, d_v] or None.
     final_state may be the init_state tensor itself (in-place update).
+    qk_silu, qk_l2norm, beta_sigmoid: the kernels apply silu and then the L2 norm
+    to each (token, head) row of q and k, and read beta as logits (KDA_PREP_*).
     Returns (out, final_state or None).  With check=True the call synchronises and
     raises if a kernel recorded a device-side error in the workspace.
     """
@@ -174,7 +185,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     if final_state is not None:
         _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
-    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], algo, gate)
+    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], algo, gate,
+                        _prep_bits(qk_silu, qk_l2norm, beta_sigmoid))
     lib = load_library()
     need = int(lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(shape)))
     if workspace is None:
@@ -198,10 +210,12 @@ def kda_workspace_status(workspace, stream=None) -> int:
     return int(load_library().kda_workspace_status(_ptr(workspace), _stream(stream)))
 
 
-def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=None):
+def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=None, qk_silu=False,
+                    qk_l2norm=False, beta_sigmoid=False):
     """One single-token step for N sequences: q, k [N, H, d_k]; v [N, H, d_v];
     g [N, H, d_k], [N, H] or None (as for kda_chunk_fwd); beta [N, H];
-    state fp32 [N, H, d_k, d_v] updated in place.  Returns out [N, H, d_v]."""
+    state fp32 [N, H, d_k, d_v] updated in place.  The input steps as for
+    kda_chunk_fwd.  Returns out [N, H, d_v]."""
     N, H, dk = q.shape
     dv = v.shape[2]
     dev, dt = q.device, q.dtype
@@ -218,7 +232,8 @@ def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=Non
     if out is None:
         out = torch.empty((N, H, dv), dtype=dt, device=dev)
     _check_io("out", out, (N, H, dv), dt, dev)
-    shape = _make_shape(N, N, H, dk, dv, scale, _DTYPES[dt], gate=gate)
+    shape = _make_shape(N, N, H, dk, dv, scale, _DTYPES[dt], gate=gate,
+                        prep=_prep_bits(qk_silu, qk_l2norm, beta_sigmoid))
     rc = load_library().kda_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                         _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
     if rc != KDA_OK:
@@ -228,14 +243,14 @@ def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=Non
 
 def kda_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, accepted=None, out=None,
                       final_state=None, output=True, output_final_state=True, scale=None,
-                      stream=None):
+                      stream=None, qk_silu=False, qk_l2norm=False, beta_sigmoid=False):
     """The recurrence token by token over short packed sequences (see include/kda.h):
     the same tensors as kda_chunk_fwd, plus accepted (int32 [N], CUDA, or None): the
     state returned for sequence n is the one after its first accepted[n] tokens.
     output=False skips the outputs (the commit of a speculative step);
     output_final_state=False leaves every state untouched (the verify).
-    final_state may be the init_state tensor itself.  Returns (out or None,
-    final_state or None)."""
+    final_state may be the init_state tensor itself.  The input steps as for
+    kda_chunk_fwd.  Returns (out or None, final_state or None)."""
     T, H, dk = q.shape
     dv = v.shape[2]
     N = cu_seqlens.shape[0] - 1
@@ -266,7 +281,8 @@ def kda_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, accepted
         _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
     else:
         final_state = None
-    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], gate=gate)
+    shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], gate=gate,
+                        prep=_prep_bits(qk_silu, qk_l2norm, beta_sigmoid))
     rc = load_library().kda_recurrent_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                           _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
                                           _ptr(accepted), _ptr(out), _ptr(final_state),

@@ -15,6 +15,10 @@ drawn in fp32 from one torch generator per workload in the fixed order
 q, k, v, g, beta, state, then rounded (round-to-nearest-even) to the I/O dtype.
 Both the CUDA path and the oracle receive the rounded values.
 
+With raw=True the same draws are kept before the two input steps the library can
+apply itself (kda_shape.prep): q and k stay N(0, 1) * qk_scale (not normalised)
+and beta stays its N(0, 1) logit.
+
 Named workloads (sizes as stated for the KDA forward benchmarks):
   tiny_fp32            1 seq x 256 tokens, H=2, d=64, fp32 I/O, zero state, seed 0
   prefill_bf16         4 seqs x 4096 tokens, H=16, d=128, bf16 I/O, seed 1
@@ -112,18 +116,31 @@ def _unit_normal(shape, gen, device):
     return x / x.norm(dim=-1, keepdim=True)
 
 
-def prefill_inputs(spec: PrefillSpec, device: str = "cpu") -> dict:
+def _qk(shape, gen, device, raw, qk_scale):
+    if raw:
+        return torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * qk_scale
+    return _unit_normal(shape, gen, device)
+
+
+def _beta(shape, gen, device, raw):
+    x = torch.randn(shape, generator=gen, device=device)
+    return x if raw else torch.sigmoid(x)
+
+
+def prefill_inputs(spec: PrefillSpec, device: str = "cpu", raw: bool = False,
+                   qk_scale: float = 1.0) -> dict:
     """Inputs of one prefill call, laid out as the library expects:
     q, k, g [T, H, d_k]; v [T, H, d_v]; beta [T, H] (all io dtype);
-    cu_seqlens int32 [N+1]; init_state fp32 [N, H, d_k, d_v] or None."""
+    cu_seqlens int32 [N+1]; init_state fp32 [N, H, d_k, d_v] or None.
+    raw=True: q, k and beta before the input steps (module docstring)."""
     gen = torch.Generator(device=device).manual_seed(spec.seed)
     T, H, dk, dv = spec.total_tokens, spec.num_heads, spec.d_k, spec.d_v
     dt = torch_dtype(spec.io_dtype)
-    q = _unit_normal((T, H, dk), gen, device).to(dt)
-    k = _unit_normal((T, H, dk), gen, device).to(dt)
+    q = _qk((T, H, dk), gen, device, raw, qk_scale).to(dt)
+    k = _qk((T, H, dk), gen, device, raw, qk_scale).to(dt)
     v = torch.randn((T, H, dv), generator=gen, device=device).to(dt)
     g = _gate((T, H, dk), spec.gate, gen, device).to(dt)
-    beta = torch.sigmoid(torch.randn((T, H), generator=gen, device=device)).to(dt)
+    beta = _beta((T, H), gen, device, raw).to(dt)
     if spec.init == "normal":
         init = torch.randn((spec.num_seqs, H, dk, dv), generator=gen, device=device) * 0.02
     elif spec.init == "zeros":
@@ -136,17 +153,19 @@ def prefill_inputs(spec: PrefillSpec, device: str = "cpu") -> dict:
     return dict(q=q, k=k, v=v, g=g, beta=beta, cu_seqlens=cu.to(device), init_state=init)
 
 
-def decode_inputs(spec: DecodeSpec, device: str = "cpu") -> dict:
+def decode_inputs(spec: DecodeSpec, device: str = "cpu", raw: bool = False,
+                  qk_scale: float = 1.0) -> dict:
     """Inputs of `steps` consecutive decode steps: q, k, g [steps, N, H, d_k];
-    v [steps, N, H, d_v]; beta [steps, N, H]; state fp32 [N, H, d_k, d_v]."""
+    v [steps, N, H, d_v]; beta [steps, N, H]; state fp32 [N, H, d_k, d_v].
+    raw=True: q, k and beta before the input steps (module docstring)."""
     gen = torch.Generator(device=device).manual_seed(spec.seed)
     S, N, H, dk, dv = spec.steps, spec.num_seqs, spec.num_heads, spec.d_k, spec.d_v
     dt = torch_dtype(spec.io_dtype)
-    q = _unit_normal((S, N, H, dk), gen, device).to(dt)
-    k = _unit_normal((S, N, H, dk), gen, device).to(dt)
+    q = _qk((S, N, H, dk), gen, device, raw, qk_scale).to(dt)
+    k = _qk((S, N, H, dk), gen, device, raw, qk_scale).to(dt)
     v = torch.randn((S, N, H, dv), generator=gen, device=device).to(dt)
     g = _gate((S, N, H, dk), spec.gate, gen, device).to(dt)
-    beta = torch.sigmoid(torch.randn((S, N, H), generator=gen, device=device)).to(dt)
+    beta = _beta((S, N, H), gen, device, raw).to(dt)
     state = torch.randn((N, H, dk, dv), generator=gen, device=device) * 0.02
     return dict(q=q, k=k, v=v, g=g, beta=beta, state=state)
 

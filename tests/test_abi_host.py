@@ -181,3 +181,27 @@ def test_gate_modes_validation(lib):
     assert lib.kda_decode_step(ctypes.byref(d), p, p, p, None, p, p, p, None) == -6
     d = _shape(total_tokens=2, gate=1)
     assert lib.kda_decode_step(ctypes.byref(d), p, p, p, None, p, p, p, None) == -1
+
+
+def test_prep_bits_validation(lib):
+    """kda_shape.prep takes the three KDA_PREP_* bits in any combination; any other
+    bit is a shape error on every entry point (before the device check, -6 here)."""
+    assert lib.kda_version() >= 1002  # 1.2 added kda_shape.prep
+    assert ctypes.sizeof(K.kda_shape) == 44
+    p = ctypes.c_void_p(FAKE)
+    for bits in range(8):
+        s = _shape(prep=bits)
+        ws = lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(s))
+        assert ws >= 256
+        assert lib.kda_chunk_fwd(ctypes.byref(s), p, p, p, p, p, None, p, p, p, p, ws, None) == -6
+        d = _shape(total_tokens=2, prep=bits)
+        assert lib.kda_decode_step(ctypes.byref(d), p, p, p, p, p, p, p, None) == -6
+    for bits in (8, 16, -1):
+        s = _shape(prep=bits)
+        assert lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(s)) == 0
+        assert lib.kda_chunk_fwd(ctypes.byref(s), p, p, p, p, p, None, p, p, p, p, 256, None) == -2
+        d = _shape(total_tokens=2, prep=bits)
+        assert lib.kda_decode_step(ctypes.byref(d), p, p, p, p, p, p, p, None) == -2
+        assert lib.kda_recurrent_fwd(ctypes.byref(s), p, p, p, p, p, None, p, None, p, None,
+                                     None) == -2
+    assert K._prep_bits(True, True, True) == 7 and K._prep_bits(False, True, False) == 2
