@@ -58,7 +58,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 constexpr int kDecodeThreads = 256;
 
-template <typename IO, int DK, int DV>
+// kPrep: the input steps of `prep` are compiled in (a call without them runs the
+// instantiation that has none of their code).
+template <typename IO, int DK, int DV, bool kPrep>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                       const IO *__restrict__ v, const IO *__restrict__ g,
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const size_t koff = (size_t)pair * DK, voff = (size_t)pair * DV;
   // alpha per key channel (KDA), one alpha for every channel (Gated DeltaNet), or 1 (DeltaNet)
   const float a_tok = gate == 1 ? __expf(to_f32(g[pair])) : 1.f;
-  const bool silu = prep & kPrepSilu;
+  const bool silu = kPrep && (prep & kPrepSilu);
   for (int i = tid; i < DK; i += kDecodeThreads) {
     const float qi = to_f32(q[koff + i]), ki = to_f32(k[koff + i]);
     s_q[i] = silu ? silu_f32(qi) : qi;
@@ -98,10 +100,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   for (int i = tid; i < DV; i += kDecodeThreads) s_v[i] = to_f32(v[voff + i]);
   if (tid == 0) {
     const float b = to_f32(beta[pair]);
-    s_beta = (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
+    s_beta = kPrep && (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
   }
   __syncthreads();
-  if (prep & kPrepL2) {  // warp 0: 1 / ||k||, warp 1: 1 / ||q||; then both rows scaled
+  if (kPrep && (prep & kPrepL2)) {  // warp 0: 1 / ||k||, warp 1: 1 / ||q||; then both rows scaled
     if (tid < 64) {
       const float *x = tid < 32 ? s_k : s_q;
       float acc = 0.f;
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 constexpr int kTokBlock = 8;
 constexpr int kRecThreads = 256;  // 512 (8 columns per warp) measured slower
 
-template <typename IO, int DK, int DV>
+template <typename IO, int DK, int DV, bool kPrep>
 __global__ void __launch_bounds__(kRecThreads, 2)
     kda_recurrent_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                          const IO *__restrict__ v, const IO *__restrict__ g,
@@ -245,8 +247,8 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       const int j = idx / DK, i = idx % DK;
       const size_t row = (size_t)(bos + tb + j) * H + h;
       const float qi = to_f32(q[row * DK + i]), ki = to_f32(k[row * DK + i]);
-      s_q[j][i] = (prep & kPrepSilu) ? silu_f32(qi) : qi;
-      s_k[j][i] = (prep & kPrepSilu) ? silu_f32(ki) : ki;
+      s_q[j][i] = kPrep && (prep & kPrepSilu) ? silu_f32(qi) : qi;
+      s_k[j][i] = kPrep && (prep & kPrepSilu) ? silu_f32(ki) : ki;
       s_a[j][i] = gate == 0 ? __expf(to_f32(g[row * DK + i]))
                             : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
     }
@@ -256,10 +258,10 @@ __global__ void __launch_bounds__(kRecThreads, 2)
     }
     if (tid < nb) {
       const float b = to_f32(beta[(size_t)(bos + tb + tid) * H + h]);
-      s_beta[tid] = (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
+      s_beta[tid] = kPrep && (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
     }
     __syncthreads();
-    if (prep & kPrepL2) {  // warp w divides token w's k and q by their norms
+    if (kPrep && (prep & kPrepL2)) {  // warp w divides token w's k and q by their norms
       if (w < nb) {
         float sk = 0.f, sq = 0.f;
         for (int i = lane; i < DK; i += 32) {
@@ -337,7 +339,8 @@ template <typename IO, int DK, int DV>
 cudaError_t launch_recurrent_t(const RecurrentArgs &a, cudaStream_t stream) {
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   if (pairs == 0 || (!a.out && !a.final_state)) return cudaSuccess;
-  kda_recurrent_kernel<IO, DK, DV><<<(unsigned)pairs, kRecThreads, 0, stream>>>(
+  auto kern = a.prep ? kda_recurrent_kernel<IO, DK, DV, true> : kda_recurrent_kernel<IO, DK, DV, false>;
+  kern<<<(unsigned)pairs, kRecThreads, 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
       a.accepted, static_cast<IO *>(a.out), a.final_state, a.num_heads, a.scale, a.gate, a.prep);
@@ -357,7 +360,8 @@ template <typename IO, int DK, int DV>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
   const int pairs = a.num_seqs * a.num_heads;
   if (pairs == 0) return cudaSuccess;
-  kda_decode_kernel<IO, DK, DV><<<pairs, kDecodeThreads, 0, stream>>>(
+  auto kern = a.prep ? kda_decode_kernel<IO, DK, DV, true> : kda_decode_kernel<IO, DK, DV, false>;
+  kern<<<pairs, kDecodeThreads, 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.state,
       static_cast<IO *>(a.out), a.scale, a.gate, a.prep);
