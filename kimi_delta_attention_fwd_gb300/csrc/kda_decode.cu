@@ -210,7 +210,10 @@ __global__ void __launch_bounds__(kRecThreads, 2)
   constexpr int RPL = DK / RG;     // rows per lane
   static_assert(CW % 4 == 0 && RPL * RG == DK, "warp layout");
 
-  __shared__ float s_q[kTokBlock][DK], s_k[kTokBlock][DK], s_a[kTokBlock][DK];
+  // q, k and the decay of a token are stored with the key channels permuted, channel
+  // r at (r % RG) RPL + r / RG, so that the RPL rows a lane holds (rg + RG i) are
+  // contiguous and read as float4s
+  __shared__ __align__(16) float s_q[kTokBlock][DK], s_k[kTokBlock][DK], s_a[kTokBlock][DK];
   __shared__ float s_v[kTokBlock][DV], s_beta[kTokBlock];
 
   const int pair = blockIdx.x;  // n * H + h
@@ -247,10 +250,11 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       const int j = idx / DK, i = idx % DK;
       const size_t row = (size_t)(bos + tb + j) * H + h;
       const float qi = to_f32(q[row * DK + i]), ki = to_f32(k[row * DK + i]);
-      s_q[j][i] = kPrep && (prep & kPrepSilu) ? silu_f32(qi) : qi;
-      s_k[j][i] = kPrep && (prep & kPrepSilu) ? silu_f32(ki) : ki;
-      s_a[j][i] = gate == 0 ? __expf(to_f32(g[row * DK + i]))
-                            : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
+      const int pi = (i % RG) * RPL + i / RG;
+      s_q[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(qi) : qi;
+      s_k[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(ki) : ki;
+      s_a[j][pi] = gate == 0 ? __expf(to_f32(g[row * DK + i]))
+                             : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
     }
     for (int idx = tid; idx < nb * DV; idx += kRecThreads) {
       const int j = idx / DV, i = idx % DV;
@@ -283,17 +287,25 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       // forget, then this lane's partial sums of S~^T k, S~^T q (4 columns) and k . q
       float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
       float kq = 0.f;
+      const float4 *a4 = reinterpret_cast<const float4 *>(&s_a[jt][rg * RPL]);
+      const float4 *k4 = reinterpret_cast<const float4 *>(&s_k[jt][rg * RPL]);
+      const float4 *q4 = reinterpret_cast<const float4 *>(&s_q[jt][rg * RPL]);
 #pragma unroll
-      for (int i = 0; i < RPL; ++i) {
-        const int r = rg + RG * i;
-        const float a = s_a[jt][r], kr = s_k[jt][r], qr = s_q[jt][r];
-        float4 &u = s[i];
-        u.x *= a; u.y *= a; u.z *= a; u.w *= a;
-        pk.x = fmaf(u.x, kr, pk.x); pk.y = fmaf(u.y, kr, pk.y);
-        pk.z = fmaf(u.z, kr, pk.z); pk.w = fmaf(u.w, kr, pk.w);
-        pq.x = fmaf(u.x, qr, pq.x); pq.y = fmaf(u.y, qr, pq.y);
-        pq.z = fmaf(u.z, qr, pq.z); pq.w = fmaf(u.w, qr, pq.w);
-        kq = fmaf(kr, qr, kq);
+      for (int i4 = 0; i4 < RPL / 4; ++i4) {
+        const float4 av = a4[i4], kv = k4[i4], qv = q4[i4];
+        const float aa[4] = {av.x, av.y, av.z, av.w}, ka[4] = {kv.x, kv.y, kv.z, kv.w},
+                    qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {  // row rg + RG (4 i4 + e)
+          const float a = aa[e], kr = ka[e], qr = qa[e];
+          float4 &u = s[4 * i4 + e];
+          u.x *= a; u.y *= a; u.z *= a; u.w *= a;
+          pk.x = fmaf(u.x, kr, pk.x); pk.y = fmaf(u.y, kr, pk.y);
+          pk.z = fmaf(u.z, kr, pk.z); pk.w = fmaf(u.w, kr, pk.w);
+          pq.x = fmaf(u.x, qr, pq.x); pq.y = fmaf(u.y, qr, pq.y);
+          pq.z = fmaf(u.z, qr, pq.z); pq.w = fmaf(u.w, qr, pq.w);
+          kq = fmaf(kr, qr, kq);
+        }
       }
       // all-reduce over the lanes of this column group (they differ in rg: xor CG, 2 CG, ...)
 #pragma unroll
@@ -309,26 +321,31 @@ __global__ void __launch_bounds__(kRecThreads, 2)
         kq += __shfl_xor_sync(0xffffffffu, kq, o);
       }
       const float bt = s_beta[jt];
-      float4 e;
-      e.x = bt * (s_v[jt][col + 0] - pk.x);
-      e.y = bt * (s_v[jt][col + 1] - pk.y);
-      e.z = bt * (s_v[jt][col + 2] - pk.z);
-      e.w = bt * (s_v[jt][col + 3] - pk.w);
+      float4 e4;
+      e4.x = bt * (s_v[jt][col + 0] - pk.x);
+      e4.y = bt * (s_v[jt][col + 1] - pk.y);
+      e4.z = bt * (s_v[jt][col + 2] - pk.z);
+      e4.w = bt * (s_v[jt][col + 3] - pk.w);
       if (out && rg == 0) {
         float4 o;
-        o.x = scale * (pq.x + e.x * kq);
-        o.y = scale * (pq.y + e.y * kq);
-        o.z = scale * (pq.z + e.z * kq);
-        o.w = scale * (pq.w + e.w * kq);
+        o.x = scale * (pq.x + e4.x * kq);
+        o.y = scale * (pq.y + e4.y * kq);
+        o.z = scale * (pq.z + e4.z * kq);
+        o.w = scale * (pq.w + e4.w * kq);
         store4<IO>(out + ((size_t)(bos + t) * H + h) * DV + col, o);
       }
       // rank-one write
 #pragma unroll
-      for (int i = 0; i < RPL; ++i) {
-        const float kr = s_k[jt][rg + RG * i];
-        float4 &u = s[i];
-        u.x = fmaf(kr, e.x, u.x); u.y = fmaf(kr, e.y, u.y);
-        u.z = fmaf(kr, e.z, u.z); u.w = fmaf(kr, e.w, u.w);
+      for (int i4 = 0; i4 < RPL / 4; ++i4) {
+        const float4 kv = k4[i4];
+        const float ka[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float kr = ka[e];
+          float4 &u = s[4 * i4 + e];
+          u.x = fmaf(kr, e4.x, u.x); u.y = fmaf(kr, e4.y, u.y);
+          u.z = fmaf(kr, e4.z, u.z); u.w = fmaf(kr, e4.w, u.w);
+        }
       }
       if (final_state && t == acc - 1) store_state();
     }
