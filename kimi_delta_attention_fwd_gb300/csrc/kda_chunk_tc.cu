@@ -216,6 +216,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -231,18 +236,56 @@ __device__ __forceinline__ uint32_t silu_bf16x2(uint32_t x) {
   asm("fma.rn.bf16x2 %0, %1, %2, %2;" : "=r"(sg) : "r"(t), "r"(kHalf2));
   return mul_bf16x2(x, sg);
 }
-// The optional input steps on 8 bf16 values of a q or k row: silu in place when asked;
-// with the norm, returns the sum of squares (fp32) of the values the products will use.
-__device__ __forceinline__ float prep_row8(uint4 &w, bool silu, bool norm) {
-  if (silu) w = make_uint4(silu_bf16x2(w.x), silu_bf16x2(w.y), silu_bf16x2(w.z), silu_bf16x2(w.w));
-  float ss = 0.f;
-  if (norm) {
-    float f[8];
-    unpack8(w, f);
+// Sums of squares of the 32 rows rbase .. rbase + 31 of two 64-row bf16 tiles (k and q)
+// in the stage layout (two 64-channel halves kKQ1 apart, 128-byte rows, 128-byte
+// swizzle), as the diagonals of X X^T on the warp-level tensor instructions: per tile
+// and 16-row block, eight 16 x 16 slices of X, each one ldmatrix and two MMAs whose B
+// operand is the slice's own rows; the four accumulator chains are interleaved.  Exact
+// bf16 products, fp32 sums.  Lane l gets the sums of row rbase + l.
+__device__ __forceinline__ void row_sumsq32x2(uint32_t tk, uint32_t tq, int rbase, int lane,
+                                              float &ssk, float &ssq) {
+  const int m = lane >> 3, rr = lane & 7;  // ldmatrix: this lane addresses row rr of matrix m
+  const int g = lane >> 2;                 // MMA fragment row of this lane
+  float d[2][2][2][4];                     // [tile][block][column half][fragment]
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[i][b][h][e] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {  // 16 channels per step
+    const uint32_t chunk = static_cast<uint32_t>(2 * (ks & 3) + (m >> 1));
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t row = static_cast<uint32_t>(rbase + 16 * b + rr + 8 * (m & 1));
+      const uint32_t off = (ks >> 2) * L::kKQ1 + sw128(row, chunk);
+      uint32_t ak[4], aq[4];
+      ldmatrix_x4(ak, tk + off);
+      ldmatrix_x4(aq, tq + off);
+      mma_bf16_16x8x16(d[0][b][0], ak, ak[0], ak[2]);  // columns = rows 0-7 of the block
+      mma_bf16_16x8x16(d[0][b][1], ak, ak[1], ak[3]);  // columns = rows 8-15
+      mma_bf16_16x8x16(d[1][b][0], aq, aq[0], aq[2]);
+      mma_bf16_16x8x16(d[1][b][1], aq, aq[1], aq[3]);
+    }
   }
-  return ss;
+  // the diagonal: lane 4 g + g / 2 holds rows g (column half 0) and g + 8 (half 1)
+  const int want = lane & 15, gw = want & 7, src = 4 * gw + (gw >> 1), bw = lane >> 4;
+  float out[2] = {0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const float lo = (g & 1) ? d[i][b][0][1] : d[i][b][0][0];
+      const float hi = (g & 1) ? d[i][b][1][3] : d[i][b][1][2];
+      const float vlo = __shfl_sync(0xffffffffu, lo, src);
+      const float vhi = __shfl_sync(0xffffffffu, hi, src);
+      if (bw == b) out[i] = want >= 8 ? vhi : vlo;
+    }
+  ssk = out[0];
+  ssq = out[1];
 }
 
 // kSched = false: every CTA is a d_v tile that solves its own chunks (the plain
@@ -438,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float braw = rb < len ? __bfloat162float(p.beta[(size_t)(t0 + rb) * H + h]) : 0.f;
       // beta given as a logit: sigmoid (rows past the end keep 0)
       const float brow = kPrep && (p.prep & kPrepBetaSigmoid) && rb < len
-                             ? 1.f / (1.f + fast_exp2(-kLog2e * braw)) : braw;
+                             ? fast_rcp(1.f + fast_exp2(-kLog2e * braw)) : braw;
       // one thread polls the mbarriers, the others park on the named barrier
       const int it = c >> c_shift;                // this group's it-th chunk
       const uint32_t prev = (it - 1) & 1;         // parity of the group's previous release signals
@@ -488,24 +531,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // as 0), so no exp(-G) of the next sequence's decays can overflow there.
       const bool valid = r < len;
       const float lg2 = valid ? kLog2e : 0.f;
-      // Optional input steps on the row's q and k: silu in place, then the norms.  The
-      // two halves of a row meet in the stage's g area (read by the cumsum product
-      // already, written by the solve only after the next barrier).  1 / ||k|| goes into
-      // the factors of Kb and Kc, 1 / ||q|| into those of Qh.
+      // Optional input steps on the row's q and k: silu in place, then the norms.  With the
+      // silu the sums of squares come from the values already in registers (the two halves
+      // of a row meet in the stage's g area, read by the cumsum product already and written
+      // by the solve only after the next barrier); without it, from the warp-level tensor
+      // instructions (row_sumsq32x2), which needs no exchange.  1 / ||k|| goes into the
+      // factors of Kb and Kc, 1 / ||q|| into those of Qh.
       const bool norm = kPrep && (p.prep & kPrepL2);
       float rk = 1.f, rq = 1.f, lk = 0.f;  // 1 / ||k_row||, 1 / ||q_row||, log2(rk)
-      if (kPrep && (p.prep & (kPrepSilu | kPrepL2))) {
-        const bool silu = p.prep & kPrepSilu;
-        float ssk = 0.f, ssq = 0.f;
+      float ssk = 0.f, ssq = 0.f;
+      if (kPrep && (p.prep & kPrepSilu)) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t addr = kq + sw128(r, j);
-          uint4 kw4 = ld_shared_v4(addr), qw4 = ld_shared_v4(addr + L::kQoff);
-          ssk += prep_row8(kw4, silu, norm);
-          ssq += prep_row8(qw4, silu, norm);
-          if (silu) {
-            st_shared_v4(addr, kw4.x, kw4.y, kw4.z, kw4.w);
-            st_shared_v4(addr + L::kQoff, qw4.x, qw4.y, qw4.z, qw4.w);
+          const uint4 kw4 = ld_shared_v4(addr), qw4 = ld_shared_v4(addr + L::kQoff);
+          const uint4 ks4 = make_uint4(silu_bf16x2(kw4.x), silu_bf16x2(kw4.y), silu_bf16x2(kw4.z),
+                                       silu_bf16x2(kw4.w));
+          const uint4 qs4 = make_uint4(silu_bf16x2(qw4.x), silu_bf16x2(qw4.y), silu_bf16x2(qw4.z),
+                                       silu_bf16x2(qw4.w));
+          st_shared_v4(addr, ks4.x, ks4.y, ks4.z, ks4.w);
+          st_shared_v4(addr + L::kQoff, qs4.x, qs4.y, qs4.z, qs4.w);
+          if (norm) {
+            float fk[8], fq[8];
+            unpack8(ks4, fk);
+            unpack8(qs4, fq);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              ssk = fmaf(fk[e], fk[e], ssk);
+              ssq = fmaf(fq[e], fq[e], ssq);
+            }
           }
         }
         if (norm) {
@@ -515,11 +569,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           bar_sync(bar_id, 128);
           ssk += xch[t ^ 64];
           ssq += xch[128 + (t ^ 64)];
-          // 1 / max(||x||, 1e-12) = 2^(-log2(max(||x||^2, 1e-24)) / 2)
-          lk = -0.5f * fast_log2(fmaxf(ssk, 1e-24f));
-          rk = fast_exp2(lk);
-          rq = fast_exp2(-0.5f * fast_log2(fmaxf(ssq, 1e-24f)));
         }
+      } else if (norm) {
+        row_sumsq32x2(st, st + L::kQoff, 32 * (wq & 1), t & 31, ssk, ssq);  // row r = 32 (wq & 1) + lane
+      }
+      if (norm) {
+        // 1 / max(||x||, 1e-12) = 2^(-log2(max(||x||^2, 1e-24)) / 2)
+        lk = -0.5f * fast_log2(fmaxf(ssk, 1e-24f));
+        rk = fast_exp2(lk);
+        rq = fast_exp2(-0.5f * fast_log2(fmaxf(ssq, 1e-24f)));
       }
       const float bk = kPrep ? brow * rk : brow;  // Kb's row factor
       // exp(G), beta exp(G) and exp(-G) of the row, when G is one per row
@@ -591,8 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!chan) {
           products(std::false_type{}, std::false_type{});
         } else if constexpr (kPrep) {
-          if (norm) products(std::true_type{}, std::true_type{});
-          else products(std::true_type{}, std::false_type{});
+          // one variant for every combination of steps (factors 1 and 0 without the
+          // norm), which keeps a single copy of this loop in the instruction cache
+          products(std::true_type{}, std::true_type{});
         } else {
           products(std::true_type{}, std::false_type{});
         }
