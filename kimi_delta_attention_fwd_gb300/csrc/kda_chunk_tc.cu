@@ -104,7 +104,7 @@ struct L {
   static constexpr uint32_t kLtri = kSb + DK * BV * 2;    // bf16 [Ltri; Ltri], 128 x 64
   static constexpr uint32_t kGlast = kLtri + 16384;       // fp32 G_last [3][128] (2 slots used unfed)
   static constexpr uint32_t kBars = kGlast + 1536;        // mbarriers
-  static constexpr uint32_t kMisc = kBars + 288;          // tmem slot, abort flag
+  static constexpr uint32_t kMisc = kBars + 272;          // tmem slot, abort flag
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
@@ -121,11 +121,9 @@ enum : uint32_t {
   kSDone0 = 18,   // S-side -> K-side: Aop[s] and ACC[s] have been read
   kGmRead0 = 20,  // S-side -> K-side: G_last[b] has been read (up to 3 slots)
   kKcFree0 = 23,  // S-side -> K-side: Kc[b] (and TP of that chunk) read (3 slots)
-  kMmaK0 = 26, kMmaS = 28, kFinK0 = 29, kFinS = 31, kNever = 32,
-  kMmaU0 = 33,    // K-side group: the U / A^qk Vb half of the W / U product is complete
-  kNumBars = 35
+  kMmaK0 = 26, kMmaS = 28, kFinK0 = 29, kFinS = 31, kNever = 32, kNumBars = 33
 };
-static_assert(kNumBars * 8 <= 288, "mbarrier area");
+static_assert(kNumBars * 8 <= 272, "mbarrier area");
 
 // TMEM columns
 //   [128 kw, +128)   K-side group kw: G, then D1 (+0), then D2
@@ -771,20 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           float *Tb = Sd + sd_idx(I, 0, cc);
 #pragma unroll
           for (int r2 = 0; r2 < 16; ++r2) Tb[r2 * kSdLd] = x[r2];
-        } else if (!helper) {
-          // meanwhile warps 2-3 form Vb = diag(beta) V in place once the v tile has
-          // landed (a helper loads no v): thread t takes all of row t - 64 (whose beta
-          // it holds)
-          ctx.wait(kFullV0 + s, cur);
-          const uint32_t fb = pack_bf16x2(brow, brow);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t addr = st + L::kV + sw128(rb, q);
-            const uint4 w = ld_shared_v4(addr);
-            st_shared_v4(addr, mul_bf16x2(w.x, fb), mul_bf16x2(w.y, fb), mul_bf16x2(w.z, fb),
-                         mul_bf16x2(w.w, fb));
-          }
-          fence_async_smem();
         }
         bar_sync(bar_id, 128);
         // The off-diagonal blocks are small dense products: warp-level TF32 MMAs
@@ -934,11 +918,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }  // !fed
 
-      // Vb = diag(beta) V in place (a tile fed by helpers; the solving schedules form it
-      // during the diagonal-block inverses above), each thread its part (row t mod 64,
-      // half t / 64 of its columns) once the v tile has landed
-      if (fed) {
-        ctx.wait(kFullV0 + s, cur);
+      // Vb = diag(beta) V in place, each thread its part (row t mod 64, half t / 64 of
+      // its columns) once the v tile has landed; one barrier covers it and the waits
+      ctx.wait(kFullV0 + s, cur);
+      {
         const uint32_t fb = pack_bf16x2(brow, brow);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -947,8 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_shared_v4(addr, mul_bf16x2(w.x, fb), mul_bf16x2(w.y, fb), mul_bf16x2(w.z, fb),
                        mul_bf16x2(w.w, fb));
         }
-        fence_async_smem();
       }
+      fence_async_smem();
       if (t == 0 && c >= 2) ctx.wait(kSDone0 + s, prev);  // chunk c - 2 is done with Aop[s] and ACC[s]
       bar_sync(bar_id, 128);
       if (t == 0 && !fed) mbar_arrive(ctx.bar(kEmptyG0 + s));  // the g area (solve scratch) may be refilled
@@ -958,35 +941,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id_v = idesc_bf16(128, BV, false, true);
-        if constexpr (!kSched) {
-          // W first, with its own commit, so that its readout below overlaps the U half
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
-            const uint64_t bk = sdesc_sw128(st + k4 * 2048, L::kKQ1, 1024);
-            mma_bf16(tm, ad, bk, id_k, k4 > 0);
-          }
-          mma_commit(mma_bar);
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
-            const uint64_t bv = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
-            mma_bf16(tmem + kAcc0 + s * BV, ad, bv, id_v, k4 > 0);
-          }
-          mma_commit(ctx.bar(kMmaU0 + kw));
-        } else {
-          // a tile fed by helpers is bound by its state side: one commit, the two halves
-          // interleaved (measured faster there)
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
-            const uint64_t bk = sdesc_sw128(st + k4 * 2048, L::kKQ1, 1024);
-            const uint64_t bv = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
-            mma_bf16(tm, ad, bk, id_k, k4 > 0);
-            mma_bf16(tmem + kAcc0 + s * BV, ad, bv, id_v, k4 > 0);
-          }
-          mma_commit(mma_bar);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
+          const uint64_t bk = sdesc_sw128(st + k4 * 2048, L::kKQ1, 1024);
+          const uint64_t bv = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
+          mma_bf16(tm, ad, bk, id_k, k4 > 0);
+          mma_bf16(tmem + kAcc0 + s * BV, ad, bv, id_v, k4 > 0);
         }
+        mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
         mbar_arrive(ctx.bar(kEmptyK0 + s));  // Kb (the k area) is no longer read
       } else if (fed && t == 32) {
@@ -1029,7 +992,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       bar_sync(bar_id, 128);
       if (t == 0) {
-        if constexpr (!kSched) ctx.wait(kMmaU0 + kw, cur);  // U and A^qk Vb are in ACC[s]
         mbar_arrive(ctx.bar(kReady0 + s));
         if (chan && c + 2 < nchunks) {  // a1 of chunk c + 2: the group's TMEM columns are free again
           ctx.wait(kFullG0 + s, cur ^ 1);
