@@ -141,3 +141,26 @@ def test_recurrent_input_steps(io, tol):
     ro, rs = _oracle_prefill(x, x["g"], ALL)
     assert rel_l2_per_head(out.float().cpu().numpy(), ro, x["cu_seqlens"].numpy()) <= tol
     assert rel_l2_states(fin.cpu().numpy(), rs) <= tol
+
+
+@pytest.mark.parametrize("name,pairs", [("prefill_bf16", [(0, 0), (1, 7), (2, 11), (3, 15)]),
+                                        ("long_prefill_16k_bf16", [(0, 0), (0, 31)])])
+def test_input_steps_at_full_size_sampled(name, pairs):
+    """The benchmark workloads (4 x 4096 x 16 heads, plain schedule; 1 x 16384 x 32 heads,
+    solve helpers) from raw inputs with all three steps, sampled (sequence, head) pairs
+    against the oracle."""
+    x = W.prefill_inputs(W.named(name), device="cuda", raw=True)
+    out, fin = kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
+                             x["init_state"], check=True, **ALL)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fin).all()
+    cu = x["cu_seqlens"].cpu().tolist()
+    for n, h in pairs:
+        a, b = cu[n], cu[n + 1]
+        sl = lambda t: t[a:b, h:h + 1].cpu()
+        q, k, beta = oracle.preprocess(sl(x["q"]), sl(x["k"]), sl(x["beta"]), **ALL)
+        ro, rs = oracle.kda_fwd(q, k, sl(x["v"]), sl(x["g"]), beta, np.array([0, b - a]),
+                                x["init_state"][n:n + 1, h:h + 1].cpu())
+        eo = rel_l2_per_head(out[a:b, h:h + 1].float().cpu().numpy(), ro, [0, b - a])
+        es = rel_l2_states(fin[n:n + 1, h:h + 1].cpu().numpy(), rs)
+        assert eo <= TOL_BF16 and es <= TOL_BF16, (n, h, eo, es)
