@@ -175,6 +175,7 @@ int kda_recurrent_fwd(const kda_shape *s, const void *q, const void *k, const vo
   if (s->num_seqs == 0) return KDA_OK;
   kda::RecurrentArgs a;
   a.num_seqs = s->num_seqs;
+  a.total_tokens = s->total_tokens;
   a.num_heads = s->num_heads;
   a.d_k = s->d_k;
   a.d_v = s->d_v;

@@ -45,7 +45,7 @@ struct DecodeArgs {
 };
 
 struct RecurrentArgs {
-  int num_seqs, num_heads, d_k, d_v;
+  int num_seqs, total_tokens, num_heads, d_k, d_v;
   float scale;
   bool bf16;
   const void *q, *k, *v, *g, *beta;
