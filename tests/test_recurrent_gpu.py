@@ -133,3 +133,34 @@ def test_recurrent_zero_init_and_empty_inputs():
     o, f = kda_recurrent_fwd(e, e, e, e, torch.zeros((0, 1), device="cuda"),
                              torch.zeros(1, dtype=torch.int32, device="cuda"))
     assert o.shape == (0, 1, 64) and f.shape == (0, 1, 64, 64)
+
+
+@pytest.mark.parametrize("mode", ["channel", "none"])
+@pytest.mark.parametrize("io,d,tol", [("bf16", 128, TOL_BF16), ("f32", 64, TOL_F32)])
+def test_persistent_launch_matches_oracle(mode, io, d, tol):
+    """More sequence-heads than two CTAs per SM, with two or more tokens per sequence on
+    average: the launch takes persistent CTAs that stage each next sequence-head's state
+    in shared memory while they run the current one.  Ragged lengths (0 to 9 tokens),
+    accepted counts, the state updated in place, against the oracle."""
+    n = 2 * torch.cuda.get_device_properties(0).multi_processor_count + 37  # > 2 CTAs per SM
+    gen = torch.Generator().manual_seed(86)
+    lens = [int(x) for x in torch.randint(0, 10, (n,), generator=gen)]
+    lens[0] = 9
+    assert sum(lens) >= 2 * n
+    spec = W.custom_prefill(lens, num_heads=1, d=d, io=io, gate="mixed", seed=86)
+    x = W.prefill_inputs(spec)
+    g_gpu, g_ref = _gates(x, mode)
+    dv = to_dev(x)
+    acc = [int(a) for a in torch.randint(0, 11, (n,), generator=gen)]
+    acc_t = torch.tensor(acc, dtype=torch.int32, device="cuda")
+    st = dv["init_state"].clone()
+    out, fin = kda_recurrent_fwd(dv["q"], dv["k"], dv["v"], None if g_gpu is None else g_gpu.cuda(),
+                                 dv["beta"], dv["cu_seqlens"], st, accepted=acc_t, final_state=st)
+    torch.cuda.synchronize()
+    ro, _ = oracle.kda_fwd(x["q"], x["k"], x["v"], g_ref, x["beta"], x["cu_seqlens"], x["init_state"])
+    cu = x["cu_seqlens"].numpy()
+    assert rel_l2_per_head(out.float().cpu().numpy(), ro, cu) <= tol
+    kept = [min(a, L) for a, L in zip(acc, lens)]
+    t = _truncate(x, g_ref, kept)
+    _, rs = oracle.kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], t["init_state"])
+    assert rel_l2_states(fin.cpu().numpy(), rs) <= tol
