@@ -201,7 +201,10 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// waits until at most the most recently committed group of this thread is in flight
+__device__ __forceinline__ void cp_async_wait_but_last() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 template <typename IO, int DK, int DV, bool kPrep>
 __global__ void __launch_bounds__(kRecThreads, 2)
@@ -235,12 +238,47 @@ __global__ void __launch_bounds__(kRecThreads, 2)
   const int cg = lane % CG, rg = lane / CG;
   const int col = CW * w + 4 * cg;  // this lane's four columns
   auto prefetch = [&](int p) {
-    const float *src = init_state + (size_t)p * DK * DV + col;
+    if (init_state) {
+      const float *src = init_state + (size_t)p * DK * DV + col;
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) cp_async16(&s_next[i * kRecThreads + tid], src + (size_t)(rg + RG * i) * DV);
+      for (int i = 0; i < RPL; ++i) cp_async16(&s_next[i * kRecThreads + tid], src + (size_t)(rg + RG * i) * DV);
+    }
+    cp_async_commit();  // one group per pair, empty without an initial state
+  };
+  // The raw q, k, g (per key channel) and v rows of the first kTokBlock tokens of the
+  // next pair follow in shared memory, [kTokBlock][q | k | g | v] in the I/O type, copied
+  // in 16-byte pieces (the launch only stages with 16-byte aligned tensors).
+  constexpr int kRawRow = 3 * DK + DV;  // elements per token
+  IO *s_raw = reinterpret_cast<IO *>(s_next + RPL * kRecThreads);
+  auto pair_steps = [&](int p, int &pbos) {
+    const int pn = p / H;
+    pbos = cu_seqlens[pn];
+    const int plen = cu_seqlens[pn + 1] - pbos;
+    const int pacc = accepted ? min(max(accepted[pn], 0), plen) : plen;
+    return out ? plen : pacc;
+  };
+  auto prefetch_inputs = [&](int p) {
+    int pbos = 0;
+    const int nb = min(kTokBlock, pair_steps(p, pbos));
+    const int ph = p % H;
+    constexpr int kPer = 16 / sizeof(IO);  // elements per 16-byte piece
+    constexpr int kPieces = kRawRow / kPer;
+    for (int ci = tid; ci < nb * kPieces; ci += kRecThreads) {
+      const int j = ci / kPieces, e = (ci % kPieces) * kPer;  // token, element in the raw row
+      const size_t row = (size_t)(pbos + j) * H + ph;
+      const IO *src = nullptr;  // the g part only with one log alpha per key channel
+      if (e < DK) src = q + row * DK + e;
+      else if (e < 2 * DK) src = k + row * DK + (e - DK);
+      else if (e < 3 * DK) src = gate == 0 ? g + row * DK + (e - 2 * DK) : nullptr;
+      else src = v + row * DV + (e - 3 * DK);
+      if (src) cp_async16(s_raw + j * kRawRow + e, src);
+    }
     cp_async_commit();
   };
-  if (staged && init_state && (int)blockIdx.x < npairs) prefetch(blockIdx.x);
+  if (staged && (int)blockIdx.x < npairs) {
+    prefetch(blockIdx.x);
+    prefetch_inputs(blockIdx.x);
+  }
 
   for (int pair = blockIdx.x; pair < npairs; pair += gridDim.x) {  // pair = n * H + h
   const int n = pair / H, h = pair % H;
@@ -250,11 +288,13 @@ __global__ void __launch_bounds__(kRecThreads, 2)
 
   const size_t soff = (size_t)pair * DK * DV + col;
   float4 s[RPL];
+  // staged: in flight are [state(pair)], [inputs(pair)], so waiting for all but the
+  // last group gives this pair's state; its inputs are waited for below
+  const bool more = staged && pair + (int)gridDim.x < npairs;
+  if (staged) cp_async_wait_but_last();
   if (init_state && staged) {
-    cp_async_wait_all();
 #pragma unroll
     for (int i = 0; i < RPL; ++i) s[i] = s_next[i * kRecThreads + tid];
-    if (pair + (int)gridDim.x < npairs) prefetch(pair + gridDim.x);  // this thread's slots are free again
   } else if (init_state) {  // one pair per CTA: straight into registers
 #pragma unroll
     for (int i = 0; i < RPL; ++i)
@@ -263,19 +303,50 @@ __global__ void __launch_bounds__(kRecThreads, 2)
 #pragma unroll
     for (int i = 0; i < RPL; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // this thread's state slots are free again: the next pair's state streams in (the
+  // last pair commits an empty group, so that "all but the last group" below still
+  // covers this pair's inputs)
+  if (more) prefetch(pair + gridDim.x);
+  else if (staged) cp_async_commit();
   auto store_state = [&]() {
 #pragma unroll
     for (int i = 0; i < RPL; ++i)
       __stcs(reinterpret_cast<float4 *>(final_state + soff + (size_t)(rg + RG * i) * DV), s[i]);
   };
   if (final_state && acc == 0) store_state();
+  if (more && steps == 0) {  // nothing reads this pair's staged inputs
+    cp_async_wait_but_last();  // they have landed before the next pair's overwrite them
+    prefetch_inputs(pair + gridDim.x);
+  }
 
   for (int tb = 0; tb < steps; tb += kTokBlock) {
     const int nb = min(kTokBlock, steps - tb);
     // the block's inputs, once every thread is done with the previous block's (of this
     // pair or of the CTA's previous pair)
     if (tb > 0 || pair != (int)blockIdx.x) __syncthreads();
+    const bool from_raw = staged && tb == 0;  // the first block was staged
+    if (from_raw) {
+      cp_async_wait_but_last();  // [inputs(pair)] done; [state(next)] may be in flight
+      __syncthreads();           // every thread's pieces
+    }
     for (int idx = tid; idx < nb * DK; idx += kRecThreads) {
+      const int j = idx / DK, i = idx % DK;
+      if (!from_raw) break;
+      const IO *rr = s_raw + j * kRawRow;
+      const float qi = to_f32(rr[i]), ki = to_f32(rr[DK + i]);
+      const int pi = (i % RG) * RPL + i / RG;
+      s_q[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(qi) : qi;
+      s_k[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(ki) : ki;
+      s_a[j][pi] = gate == 0 ? __expf(to_f32(rr[2 * DK + i]))
+                             : (gate == 1 ? __expf(to_f32(g[(size_t)(bos + tb + j) * H + h])) : 1.f);
+    }
+    for (int idx = tid; idx < nb * DV; idx += kRecThreads) {
+      if (!from_raw) break;
+      const int j = idx / DV, i = idx % DV;
+      s_v[j][i] = to_f32(s_raw[j * kRawRow + 3 * DK + i]);
+    }
+    for (int idx = tid; idx < nb * DK; idx += kRecThreads) {
+      if (from_raw) break;
       const int j = idx / DK, i = idx % DK;
       const size_t row = (size_t)(bos + tb + j) * H + h;
       const float qi = to_f32(q[row * DK + i]), ki = to_f32(k[row * DK + i]);
@@ -286,6 +357,7 @@ __global__ void __launch_bounds__(kRecThreads, 2)
                              : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
     }
     for (int idx = tid; idx < nb * DV; idx += kRecThreads) {
+      if (from_raw) break;
       const int j = idx / DV, i = idx % DV;
       s_v[j][i] = to_f32(v[((size_t)(bos + tb + j) * H + h) * DV + i]);
     }
@@ -294,6 +366,8 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       s_beta[tid] = kPrep && (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
     }
     __syncthreads();
+    // the raw rows have been read by every thread: the next pair's may stream in
+    if (more && tb == 0) prefetch_inputs(pair + gridDim.x);
     if (kPrep && (prep & kPrepL2)) {  // warp w divides token w's k and q by their norms
       if (w < nb) {
         float sk = 0.f, sq = 0.f;
@@ -395,10 +469,12 @@ cudaError_t launch_recurrent_t(const RecurrentArgs &a, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidDevice;
-  const int smem = DK * DV * 4;
+  const int smem = DK * DV * 4 + kTokBlock * (3 * DK + DV) * (int)sizeof(IO);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const bool staged = (long long)a.total_tokens >= 2LL * a.num_seqs && pairs > 2LL * sms;
+  auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  const bool staged = (long long)a.total_tokens >= 2LL * a.num_seqs && pairs > 2LL * sms &&
+                      al16(a.q) && al16(a.k) && al16(a.v) && (a.gate != 0 || al16(a.g));
   const long long grid = staged ? 2LL * sms : pairs;
   kern<<<(unsigned)grid, kRecThreads, staged ? smem : 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),

@@ -154,9 +154,15 @@ def test_persistent_launch_matches_oracle(mode, io, d, tol):
     acc = [int(a) for a in torch.randint(0, 11, (n,), generator=gen)]
     acc_t = torch.tensor(acc, dtype=torch.int32, device="cuda")
     st = dv["init_state"].clone()
-    out, fin = kda_recurrent_fwd(dv["q"], dv["k"], dv["v"], None if g_gpu is None else g_gpu.cuda(),
-                                 dv["beta"], dv["cu_seqlens"], st, accepted=acc_t, final_state=st)
+    gd = None if g_gpu is None else g_gpu.cuda()
+    out, fin = kda_recurrent_fwd(dv["q"], dv["k"], dv["v"], gd, dv["beta"], dv["cu_seqlens"], st,
+                                 accepted=acc_t, final_state=st)
+    # the commit alone (no outputs: each sequence-head runs only its accepted tokens)
+    st2 = dv["init_state"].clone()
+    _, fin2 = kda_recurrent_fwd(dv["q"], dv["k"], dv["v"], gd, dv["beta"], dv["cu_seqlens"], st2,
+                                accepted=acc_t, output=False, final_state=st2)
     torch.cuda.synchronize()
+    assert torch.equal(fin2, fin)
     ro, _ = oracle.kda_fwd(x["q"], x["k"], x["v"], g_ref, x["beta"], x["cu_seqlens"], x["init_state"])
     cu = x["cu_seqlens"].numpy()
     assert rel_l2_per_head(out.float().cpu().numpy(), ro, cu) <= tol
