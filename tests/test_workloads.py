@@ -43,3 +43,22 @@ def test_seeded_and_deterministic():
         assert torch.equal(a[key], b[key])
     d = W.decode_inputs(W.DecodeSpec(4, 2, 64, 64, 3))
     assert d["q"].shape == (3, 4, 2, 64) and d["state"].shape == (4, 2, 64, 64)
+
+
+def test_raw_inputs_are_the_same_draws_before_the_input_steps():
+    """raw=True keeps q, k (times qk_scale) and beta as drawn, before the L2 norm and the
+    sigmoid of the recipe; every other tensor is the same."""
+    spec = W.custom_prefill([70, 33], num_heads=2, d=64, io="f32", seed=7)
+    a = W.prefill_inputs(spec)
+    b = W.prefill_inputs(spec, raw=True, qk_scale=0.5)
+    for key in ("v", "g", "init_state", "cu_seqlens"):
+        assert torch.equal(a[key], b[key])
+    torch.testing.assert_close(b["k"] / b["k"].norm(dim=-1, keepdim=True), a["k"], rtol=1e-6, atol=1e-6)
+    torch.testing.assert_close(b["q"] / b["q"].norm(dim=-1, keepdim=True), a["q"], rtol=1e-6, atol=1e-6)
+    torch.testing.assert_close(torch.sigmoid(b["beta"]), a["beta"], rtol=1e-6, atol=1e-7)
+    c = W.prefill_inputs(spec, raw=True)
+    torch.testing.assert_close(b["q"], 0.5 * c["q"], rtol=0, atol=0)
+    d = W.decode_inputs(W.DecodeSpec(3, 2, 64, 64, 4, "f32", "std", 5))
+    e = W.decode_inputs(W.DecodeSpec(3, 2, 64, 64, 4, "f32", "std", 5), raw=True)
+    assert torch.equal(d["v"], e["v"]) and torch.equal(d["state"], e["state"])
+    torch.testing.assert_close(torch.sigmoid(e["beta"]), d["beta"], rtol=1e-6, atol=1e-7)
