@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kRecThreads, 2)
   // r at (r % RG) RPL + r / RG, so that the RPL rows a lane holds (rg + RG i) are
   // contiguous and read as float4s
   __shared__ __align__(16) float s_q[kTokBlock][DK], s_k[kTokBlock][DK], s_a[kTokBlock][DK];
-  __shared__ float s_v[kTokBlock][DV], s_beta[kTokBlock];
+  __shared__ float s_v[kTokBlock][DV], s_beta[kTokBlock], s_alpha_tok[kTokBlock];
 
   // This thread's RPL state float4s of the next pair wait in shared memory, interleaved
   // over the block (float4 i of thread t at i * kRecThreads + t, so a warp's reads are
@@ -257,10 +257,17 @@ __global__ void __launch_bounds__(kRecThreads, 2)
     const int pacc = accepted ? min(max(accepted[pn], 0), plen) : plen;
     return out ? plen : pacc;
   };
+  // beta and a per-token log alpha of the next pair's first block wait in registers of
+  // threads 0 .. kTokBlock - 1 (one token each)
+  float beta_pre = 0.f, gtok_pre = 0.f;
   auto prefetch_inputs = [&](int p) {
     int pbos = 0;
     const int nb = min(kTokBlock, pair_steps(p, pbos));
     const int ph = p % H;
+    if (tid < nb) {
+      beta_pre = to_f32(beta[(size_t)(pbos + tid) * H + ph]);
+      if (gate == 1) gtok_pre = to_f32(g[(size_t)(pbos + tid) * H + ph]);
+    }
     constexpr int kPer = 16 / sizeof(IO);  // elements per 16-byte piece
     constexpr int kPieces = kRawRow / kPer;
     for (int ci = tid; ci < nb * kPieces; ci += kRecThreads) {
@@ -326,6 +333,10 @@ __global__ void __launch_bounds__(kRecThreads, 2)
     if (tb > 0 || pair != (int)blockIdx.x) __syncthreads();
     const bool from_raw = staged && tb == 0;  // the first block was staged
     if (from_raw) {
+      if (tid < nb) {
+        s_beta[tid] = kPrep && (prep & kPrepBetaSigmoid) ? sigmoid_f32(beta_pre) : beta_pre;
+        if (gate == 1) s_alpha_tok[tid] = __expf(gtok_pre);
+      }
       cp_async_wait_but_last();  // [inputs(pair)] done; [state(next)] may be in flight
       __syncthreads();           // every thread's pieces
     }
@@ -337,8 +348,7 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       const int pi = (i % RG) * RPL + i / RG;
       s_q[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(qi) : qi;
       s_k[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(ki) : ki;
-      s_a[j][pi] = gate == 0 ? __expf(to_f32(rr[2 * DK + i]))
-                             : (gate == 1 ? __expf(to_f32(g[(size_t)(bos + tb + j) * H + h])) : 1.f);
+      s_a[j][pi] = gate == 0 ? __expf(to_f32(rr[2 * DK + i])) : (gate == 1 ? s_alpha_tok[j] : 1.f);
     }
     for (int idx = tid; idx < nb * DV; idx += kRecThreads) {
       if (!from_raw) break;
@@ -361,7 +371,7 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       const int j = idx / DV, i = idx % DV;
       s_v[j][i] = to_f32(v[((size_t)(bos + tb + j) * H + h) * DV + i]);
     }
-    if (tid < nb) {
+    if (tid < nb && !from_raw) {
       const float b = to_f32(beta[(size_t)(bos + tb + tid) * H + h]);
       s_beta[tid] = kPrep && (prep & kPrepBetaSigmoid) ? sigmoid_f32(b) : b;
     }

@@ -135,7 +135,7 @@ def test_recurrent_zero_init_and_empty_inputs():
     assert o.shape == (0, 1, 64) and f.shape == (0, 1, 64, 64)
 
 
-@pytest.mark.parametrize("mode", ["channel", "none"])
+@pytest.mark.parametrize("mode", ["channel", "scalar", "none"])
 @pytest.mark.parametrize("io,d,tol", [("bf16", 128, TOL_BF16), ("f32", 64, TOL_F32)])
 def test_persistent_launch_matches_oracle(mode, io, d, tol):
     """More sequence-heads than two CTAs per SM, with two or more tokens per sequence on
