@@ -1,4 +1,5 @@
-"""Bitwise repeatability of the tensor-core prefill under repeated calls.
+"""Bitwise repeatability of the tensor-core prefill and of the persistent recurrent pass
+under repeated calls.
 
 Both schedules (plain, and the solve helpers with their ring in the workspace) are
 deterministic: the same inputs must give the same bits on every call.  A race in
@@ -10,7 +11,8 @@ development failed this check in about one call in twenty."""
 import pytest
 import torch
 
-from kimi_delta_attention_fwd_gb300 import kda_chunk_fwd, kda_chunk_fwd_workspace_bytes
+from kimi_delta_attention_fwd_gb300 import (kda_chunk_fwd, kda_chunk_fwd_workspace_bytes,
+                                            kda_recurrent_fwd)
 from kimi_delta_attention_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -34,6 +36,34 @@ def test_repeated_calls_are_bitwise_identical(mode, schedule):
     differing = 0
     for _ in range(REPS):
         o, f = kda_chunk_fwd(*args, workspace=ws, algo="tensor")
+        differing += not (torch.equal(o, o0) and torch.equal(f, f0))
+    torch.cuda.synchronize()
+    assert differing == 0, f"{differing} of {REPS} calls differ from the first"
+
+
+@pytest.mark.parametrize("gate", ["channel", "scalar", "none"])
+def test_persistent_recurrent_pass_is_bitwise_repeatable(gate):
+    """The multi-token recurrent pass on 256 x 32 sequence-heads (persistent CTAs staging
+    each next sequence-head's state and first token block through cp.async): repeated
+    calls give the same bits."""
+    drafts, N, H = 4, 256, 32
+    y = W.decode_inputs(W.DecodeSpec(N, H, 128, 128, drafts, "bf16", "std", 3), device="cuda")
+    pack = lambda t: t.transpose(0, 1).reshape(N * drafts, *t.shape[2:]).contiguous()
+    q, k, v, g, beta = (pack(y[n]) for n in ("q", "k", "v", "g", "beta"))
+    g = g if gate == "channel" else (g[..., 0].contiguous() if gate == "scalar" else None)
+    cu = torch.arange(N + 1, dtype=torch.int32, device="cuda") * drafts
+    acc = torch.randint(0, drafts + 1, (N,), dtype=torch.int32, device="cuda",
+                        generator=torch.Generator(device="cuda").manual_seed(5))
+
+    def run():
+        st = y["state"].clone()
+        o, f = kda_recurrent_fwd(q, k, v, g, beta, cu, st, accepted=acc, final_state=st)
+        return o.clone(), f.clone()
+
+    o0, f0 = run()
+    differing = 0
+    for _ in range(REPS):
+        o, f = run()
         differing += not (torch.equal(o, o0) and torch.equal(f, f0))
     torch.cuda.synchronize()
     assert differing == 0, f"{differing} of {REPS} calls differ from the first"
