@@ -97,7 +97,7 @@ class ClockSampler:
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks",
                0x1: "gpu_idle"}
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
+    def __init__(self, device_index: int, period_s: float = 0.0005):
         self.samples, self.reasons, self.max_mhz = [], set(), None
         self.period = period_s
         self._stop = threading.Event()
