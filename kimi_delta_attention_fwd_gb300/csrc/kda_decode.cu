@@ -201,6 +201,7 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // waits until at most the most recently committed group of this thread is in flight
 __device__ __forceinline__ void cp_async_wait_but_last() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(kRecThreads, 2)
     }
   }
   }  // pairs
+  if (staged) cp_async_wait_all();  // no copy in flight when the CTA leaves (a last pair without tokens)
 }
 
 template <typename IO, int DK, int DV>
