@@ -127,6 +127,23 @@ def _check_io(name, t, shape, dtype, device):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _check_workspace(ws, device):
+    """The caller's prefill workspace: device memory on the tensors' device, contiguous."""
+    if ws.device != device:
+        raise ValueError(f"workspace is on {ws.device}, expected {device}")
+    if not ws.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+
+
+def _check_ranks(where, **tensors):
+    """Each named tensor (None allowed where the entry point allows it) has the rank
+    given with it, checked before any shape is unpacked."""
+    for name, (t, ranks) in tensors.items():
+        if t is not None and t.dim() not in ranks:
+            want = " or ".join(str(r) for r in ranks)
+            raise ValueError(f"{where}: {name} has {t.dim()} dimensions, expected {want}")
+
+
 def kda_chunk_fwd_workspace_bytes(num_seqs, total_tokens, num_heads, d_k, d_v, io_dtype=torch.bfloat16,
                                   algo="auto") -> int:
     shape = _make_shape(num_seqs, total_tokens, num_heads, d_k, d_v, None, _DTYPES[io_dtype], algo)
@@ -161,6 +178,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
     Returns (out, final_state or None).  With check=True the call synchronises and
     raises if a kernel recorded a device-side error in the workspace.
     """
+    _check_ranks("kda_chunk_fwd", q=(q, (3,)), k=(k, (3,)), v=(v, (3,)), g=(g, (2, 3)),
+                 beta=(beta, (2,)), cu_seqlens=(cu_seqlens, (1,)))
     T, H, dk = q.shape
     dv = v.shape[2]
     N = cu_seqlens.shape[0] - 1
@@ -191,6 +210,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
     need = int(lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(shape)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    else:
+        _check_workspace(workspace, dev)
     rc = lib.kda_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                            _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
                            _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -207,6 +228,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
 def kda_workspace_status(workspace, stream=None) -> int:
     """Synchronises the stream and returns the device status of the last
     kda_chunk_fwd that used this workspace."""
+    if workspace.device.type != "cuda":
+        raise ValueError("kda_workspace_status reads a CUDA workspace only")
     return int(load_library().kda_workspace_status(_ptr(workspace), _stream(stream)))
 
 
@@ -216,6 +239,8 @@ def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=Non
     g [N, H, d_k], [N, H] or None (as for kda_chunk_fwd); beta [N, H];
     state fp32 [N, H, d_k, d_v] updated in place.  The input steps as for
     kda_chunk_fwd.  Returns out [N, H, d_v]."""
+    _check_ranks("kda_decode_step", q=(q, (3,)), k=(k, (3,)), v=(v, (3,)), g=(g, (2, 3)),
+                 beta=(beta, (2,)), state=(state, (4,)))
     N, H, dk = q.shape
     dv = v.shape[2]
     dev, dt = q.device, q.dtype
@@ -251,6 +276,8 @@ def kda_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, accepted
     output_final_state=False leaves every state untouched (the verify).
     final_state may be the init_state tensor itself.  The input steps as for
     kda_chunk_fwd.  Returns (out or None, final_state or None)."""
+    _check_ranks("kda_recurrent_fwd", q=(q, (3,)), k=(k, (3,)), v=(v, (3,)), g=(g, (2, 3)),
+                 beta=(beta, (2,)), cu_seqlens=(cu_seqlens, (1,)))
     T, H, dk = q.shape
     dv = v.shape[2]
     N = cu_seqlens.shape[0] - 1
