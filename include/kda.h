@@ -23,6 +23,10 @@
  *       beta    : [T_total, H]             states : [N, H, d_k, d_v] fp32
  *       cu_seqlens : int32 [N + 1] (device), nondecreasing, cu[0] = 0,
  *                    cu[N] = T_total; sequence n owns tokens [cu[n], cu[n+1]).
+ *                    The kernels read it on the device and do not check it:
+ *                    offsets that decrease or pass T_total make them read and
+ *                    write out of range (the Python binding's check=True reads it
+ *                    back and checks it on the host first).
  *   - Alignment: states, workspace and (prefill) q, k, v, out and a per-channel g
  *     start on a 16-byte boundary; beta, a per-token g and (decode, recurrent)
  *     q, k, v, g on their element size;

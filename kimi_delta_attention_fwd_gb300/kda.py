@@ -144,6 +144,19 @@ def _check_ranks(where, **tensors):
             raise ValueError(f"{where}: {name} has {t.dim()} dimensions, expected {want}")
 
 
+def _check_cu_seqlens(cu, total_tokens):
+    """Host check of packed-sequence offsets (a CPU int32 [N + 1] tensor): they start at
+    0, never decrease and stay within the token count, so that no kernel indexes past
+    the buffers (the library itself reads them on the device only, unchecked)."""
+    c = [int(x) for x in cu.tolist()]
+    if not c or c[0] != 0:
+        raise ValueError("cu_seqlens must start at 0")
+    if any(b < a for a, b in zip(c, c[1:])):
+        raise ValueError("cu_seqlens must be nondecreasing")
+    if c[-1] > total_tokens:
+        raise ValueError(f"cu_seqlens ends at {c[-1]}, beyond the {total_tokens} tokens")
+
+
 def kda_chunk_fwd_workspace_bytes(num_seqs, total_tokens, num_heads, d_k, d_v, io_dtype=torch.bfloat16,
                                   algo="auto") -> int:
     shape = _make_shape(num_seqs, total_tokens, num_heads, d_k, d_v, None, _DTYPES[io_dtype], algo)
@@ -175,7 +188,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
     final_state may be the init_state tensor itself (in-place update).
     qk_silu, qk_l2norm, beta_sigmoid: the kernels apply silu and then the L2 norm
     to each (token, head) row of q and k, and read beta as logits (KDA_PREP_*).
-    Returns (out, final_state or None).  With check=True the call synchronises and
+    Returns (out, final_state or None).  With check=True the call first reads
+    cu_seqlens back and checks it on the host, then synchronises after the launch and
     raises if a kernel recorded a device-side error in the workspace.
     """
     _check_ranks("kda_chunk_fwd", q=(q, (3,)), k=(k, (3,)), v=(v, (3,)), g=(g, (2, 3)),
@@ -195,6 +209,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
         if t is not None:
             _check_io(name, t, shp, dt, dev)
     _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    if check:
+        _check_cu_seqlens(cu_seqlens.cpu(), T)
     if init_state is not None:
         _check_io("init_state", init_state, (N, H, dk, dv), torch.float32, dev)
     if out is None:

@@ -93,3 +93,16 @@ def test_workspace_checks():
         kda._check_workspace(ws, torch.device("cuda", 0))
     with pytest.raises(ValueError, match="contiguous"):
         kda._check_workspace(ws[::2], torch.device("cpu"))
+
+
+def test_sequence_offsets_check():
+    ok = torch.tensor([0, 0, 3, 7, 7], dtype=torch.int32)
+    kda._check_cu_seqlens(ok, 7)
+    kda._check_cu_seqlens(ok, 9)  # trailing tokens belong to no sequence
+    kda._check_cu_seqlens(torch.tensor([0], dtype=torch.int32), 0)
+    with pytest.raises(ValueError, match="start at 0"):
+        kda._check_cu_seqlens(torch.tensor([1, 3], dtype=torch.int32), 3)
+    with pytest.raises(ValueError, match="nondecreasing"):
+        kda._check_cu_seqlens(torch.tensor([0, 5, 4], dtype=torch.int32), 5)
+    with pytest.raises(ValueError, match="beyond the 6 tokens"):
+        kda._check_cu_seqlens(torch.tensor([0, 3, 7], dtype=torch.int32), 6)
