@@ -1,13 +1,16 @@
 """Benchmark of the KDA forward hot path on GB300.
 
-Default line: chunkwise prefill on 4 sequences x 4096 tokens, H=16,
-d_k=d_v=128, chunk 64, bf16 I/O with fp32 state; one step = one
-kda_chunk_fwd call over the whole batch.  The same run also times the decode
-workload (256 sequences x 32 heads, 128 consecutive steps, 512 MiB state updated
-in place) and reports it under "decode".
+Default line: chunkwise prefill of the largest single-GPU workload, 64 packed
+sequences of seeded lengths uniform in [512, 16384] (about 540 K tokens), H=32,
+d_k=d_v=128, chunk 64, bf16 I/O with fp32 state; one step = one kda_chunk_fwd
+call over the whole batch.  The same run times the other prefill workloads
+(4 x 4096 tokens with H=16, and 1 x 65536 tokens with H=32) under their own names,
+the decode workload (256 sequences x 32 heads, 128 consecutive steps, 512 MiB state
+updated in place) under "decode", and a 4-token speculative verification under
+"verify".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload prefill_bf16|long_prefill_bf16|varlen_prefill_bf16|decode_bf16]
+                  [--workload varlen_prefill_bf16|prefill_bf16|long_prefill_bf16|decode_bf16]
 
 Under torchrun each rank runs its own copy of the workload on its own GPU
 (independent problems, no collective on the data path); the timing is the max
@@ -34,6 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA tokens/sec on 1 GB300 (prefill & decode) and % of roofline"
 D_FLOP_CONST = 180_224          # 6 d^2 + 10 C d flops per token-head at d=128, C=64
 PREFILL_KERNELS = ("kda_chunk_tc_kernel", "kda_chunk_simt_kernel")
+DEFAULT_WORKLOAD = "varlen_prefill_bf16"  # the largest workload that fits one GPU
 
 
 # ----------------------------------------------------------------- helpers
@@ -221,13 +225,17 @@ def oracle_cpu_baseline(x, pairs_limit=None):
 
 
 # ------------------------------------------------------------- our arm
-def run_prefill(args, ws, rank, dev):
+def run_prefill(args, ws, rank, dev, workload, e2e=True, steps=None):
+    """Times `steps` kda_chunk_fwd calls on the named workload (inputs resident in HBM),
+    and with e2e=True the same calls end to end from pinned host memory.  Returns the
+    result block and the inputs (for the CPU baseline)."""
     import torch
     from kimi_delta_attention_fwd_gb300 import kda_chunk_fwd, kda_chunk_fwd_workspace_bytes
     from kimi_delta_attention_fwd_gb300 import workloads as W
     from kimi_delta_attention_fwd_gb300 import kda as K
 
-    spec = W.named(args.workload)
+    steps = args.steps if steps is None else steps
+    spec = W.named(workload)
     spec = W.PrefillSpec(spec.seqlens, spec.num_heads, spec.d_k, spec.d_v, spec.io_dtype, spec.gate,
                          spec.init, rank_seed(spec.seed, rank))
     big = spec.total_tokens * spec.num_heads > 4_000_000
@@ -261,7 +269,7 @@ def run_prefill(args, ws, rank, dev):
         raise RuntimeError(f"device status {status} after warm-up")
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -269,7 +277,7 @@ def run_prefill(args, ws, rank, dev):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -279,13 +287,37 @@ def run_prefill(args, ws, rank, dev):
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    ms_step = max_over_ranks(total_ms / args.steps, ws, dev)
+    ms_step = max_over_ranks(total_ms / steps, ws, dev)
+    hbm, tflops, peak_src = measured_peaks()
+    alg_bytes, alg_flops = algorithmic_prefill(T * H, N * H, dk, dv, io_bytes, gate=args.gate)
+    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+    kind = "tensor" if tensor_path else "simt"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm,
+                "traffic": recorded_traffic(kind, (workload if args.gate == "channel" else
+                                                   f"{workload}:{args.gate}")
+                                            + (":prep" if args.prep else "")),
+                "peak_source": f"{peak_src} hbm_gbs",
+                "tensor_tflops_algorithmic": alg_flops / (launch_ms * 1e-3) / 1e12,
+                "tensor_peak_tflops": tflops,
+                "kernel_ms": launch_ms,
+                "roofline_ms": max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12)) * 1e3}
+    config = {"workload": workload, "num_seqs": N, "total_tokens": T, "num_heads": H,
+              "d_k": dk, "d_v": dv, "chunk": 64, "io_dtype": spec.io_dtype, "gate": args.gate,
+              "prep": "silu + l2norm of q, k; sigmoid of beta" if args.prep else "none",
+              "kernel": kind, "l2": "inputs larger than L2 (%.0f MB read+written per step)" % (alg_bytes / 1e6),
+              "parallelism": f"replicas x{ws} (independent sequences per GPU)"}
+    if not e2e:
+        del d, out, fin, work
+        return {"workload": workload, "value": aggregate_throughput(T, ws, ms_step), "unit": "tokens/s",
+                "ms_per_step": ms_step, "steps": steps, "config": config, "roofline": roofline,
+                "gpu_launches": steps, "clocks": clk.summary()}, x
 
     # e2e through the public API: every step copies its inputs from pinned host memory,
     # runs kda_chunk_fwd and reads its outputs and final states back.  Steps are
     # double-buffered on three streams (copy in, compute, copy out), so step i + 1's
     # inputs cross the host link while step i computes and its results come back.
-    e2e_steps = max(2, min(args.steps, 10))
+    e2e_steps = max(2, min(steps, 10))
     host_in = {kk: (vv.to("cpu").pin_memory() if vv is not None else None) for kk, vv in x.items()}
     h2d = sum(vv.numel() * vv.element_size() for vv in host_in.values() if vv is not None)
     sets = []
@@ -340,36 +372,19 @@ def run_prefill(args, ws, rank, dev):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b_end) / e2e_steps, ws, dev)
 
-    hbm, tflops, peak_src = measured_peaks()
-    alg_bytes, alg_flops = algorithmic_prefill(T * H, N * H, dk, dv, io_bytes, gate=args.gate)
-    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
-    kind = "tensor" if tensor_path else "simt"
     res = {
         "metric": METRIC, "value": aggregate_throughput(T, ws, ms_step), "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "num_seqs": N, "total_tokens": T, "num_heads": H,
-                   "d_k": dk, "d_v": dv, "chunk": 64, "io_dtype": spec.io_dtype, "gate": args.gate,
-                   "prep": "silu + l2norm of q, k; sigmoid of beta" if args.prep else "none",
-                   "kernel": kind, "l2": "inputs larger than L2 (%.0f MB read+written per step)" % (alg_bytes / 1e6),
-                   "parallelism": f"replicas x{ws} (independent sequences per GPU)"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm,
-                     "traffic": recorded_traffic(kind, (args.workload if args.gate == "channel" else
-                                                        f"{args.workload}:{args.gate}")
-                                                 + (":prep" if args.prep else "")),
-                     "peak_source": f"{peak_src} hbm_gbs",
-                     "tensor_tflops_algorithmic": alg_flops / (launch_ms * 1e-3) / 1e12,
-                     "tensor_peak_tflops": tflops,
-                     "kernel_ms": launch_ms,
-                     "roofline_ms": max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12)) * 1e3},
+        "config": config, "roofline": roofline,
         "e2e": {"value": aggregate_throughput(T, ws, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "schedule": "double-buffered: a step's host-to-device copies overlap the previous step's kernel and device-to-host copies"},
-        "gpu_launches": args.steps,
+        "gpu_launches": steps,
         "clocks": clk.summary(),
     }
+    del sets, host_in, d, out, fin, work
     return res, x
 
 
@@ -477,10 +492,7 @@ def main_ours(args):
                "roofline": dec["roofline"], "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"]}
         x = None
     else:
-        res, x = run_prefill(args, ws, rank, dev)
-        if not args.no_decode and not args.prep and args.workload == "prefill_bf16":
-            res["decode"] = run_decode(args, ws, rank, dev)
-            res["verify"] = run_verify(args, ws, rank, dev)
+        res, x = run_prefill(args, ws, rank, dev, args.workload)
     if rank == 0 and not args.no_cpu_baseline and not args.prep and x is not None:
         # a bounded sample: on the largest workloads (over 4 M token-heads) an eighth
         # of the heads, so that one oracle run stays within seconds
@@ -500,6 +512,18 @@ def main_ours(args):
                                "sample": f"{args.workload}: all {tokens} tokens of {heads} of {x['q'].shape[1]} heads "
                                          f"({th} token-heads per run, {reps} runs, {total:.1f} s in all), "
                                          f"scaled to tokens/s over all heads"}
+    x = None
+    torch.cuda.empty_cache()
+    if args.workload == DEFAULT_WORKLOAD and not args.prep:
+        # the other prefill workloads, each timed the same way on the device (no e2e leg)
+        if not args.no_extra:
+            for name in ("prefill_bf16", "long_prefill_bf16"):
+                blk, _ = run_prefill(args, ws, rank, dev, name, e2e=False, steps=min(args.steps, 10))
+                res[name] = blk
+                torch.cuda.empty_cache()
+        if not args.no_decode:
+            res["decode"] = run_decode(args, ws, rank, dev)
+            res["verify"] = run_verify(args, ws, rank, dev)
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -512,16 +536,29 @@ def main_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
         return
+    import torch
     from kimi_delta_attention_fwd_gb300 import workloads as W
-    spec_name = args.workload if args.workload != "decode_bf16" else "prefill_bf16"
+    spec_name = args.workload if args.workload != "decode_bf16" else DEFAULT_WORKLOAD
     spec = W.named(spec_name)
-    x = W.prefill_inputs(spec)
+    H = spec.num_heads
+    # each step runs a bounded sample: every token of `heads` heads (one head on the
+    # workloads over 4 M token-heads, all heads otherwise)
+    heads = args.cpu_heads or (1 if spec.total_tokens * H > 4_000_000 else H)
+    if torch.cuda.is_available():
+        # the same inputs as our arm, drawn on the device; the sampled heads go to the host
+        x = W.prefill_inputs(spec, device="cuda")
+        drawn = "the workload's own inputs"
+    else:
+        # no device to draw the whole workload on: the same recipe and lengths, drawn
+        # for the sampled heads only
+        spec = W.PrefillSpec(spec.seqlens, heads, spec.d_k, spec.d_v, spec.io_dtype, spec.gate,
+                             spec.init, spec.seed)
+        x = W.prefill_inputs(spec)
+        drawn = "inputs of the same recipe drawn for the sampled heads"
     if args.gate == "scalar":
         x["g"] = x["g"][..., 0].contiguous()
     elif args.gate == "none":
         x["g"] = None
-    H = spec.num_heads
-    heads = args.cpu_heads or H
     times = []
     for i in range(args.warmup + args.steps):
         dt, tokens, th, threads, used = oracle_cpu_baseline(x, pairs_limit=heads)
@@ -537,7 +574,8 @@ def main_reference(args):
                       "total_tokens": spec.total_tokens, "num_heads": H, "d_k": spec.d_k,
                       "d_v": spec.d_v, "gate": args.gate},
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                            "sample": f"{used} of {H} heads, all {tokens} tokens per step"},
+                            "sample": f"{used} of {H} heads, all {tokens} tokens per step ({drawn}), "
+                                      f"scaled to tokens/s over all heads"},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res))
 
@@ -548,7 +586,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="prefill_bf16",
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["prefill_bf16", "long_prefill_bf16", "long_prefill_16k_bf16",
                              "varlen_prefill_bf16", "decode_bf16"])
     ap.add_argument("--algo", default="auto", choices=["auto", "tensor", "simt"])
@@ -561,6 +599,8 @@ def main():
                     help="raw q, k and beta logits; the kernels apply silu and the L2 norm to q, k "
                          "and the sigmoid to beta (no CPU baseline, no decode block)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the 4 x 4096 and 1 x 65536 prefill blocks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle time to accumulate for the CPU baseline (whole runs of the sample)")

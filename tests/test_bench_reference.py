@@ -1,5 +1,6 @@
 """bench.py --impl reference: the oracle timed on the host cores, printed as one JSON
-line with the keys of the bench contract (CPU only, a one-head sample)."""
+line with the keys of the bench contract (CPU only, a one-head sample of the default,
+largest workload)."""
 import json
 import os
 import subprocess
@@ -18,7 +19,7 @@ def test_reference_arm_prints_one_contract_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] and d["unit"] == "tokens/s"
     assert d["value"] > 0 and d["higher_is_better"] is True and d["n_gpus"] == 1
-    assert d["config"]["workload"] == "prefill_bf16"
+    assert d["config"]["workload"] == "varlen_prefill_bf16"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
