@@ -17,7 +17,9 @@ Both the CUDA path and the oracle receive the rounded values.
 
 With raw=True the same draws are kept before the two input steps the library can
 apply itself (kda_shape.prep): q and k stay N(0, 1) * qk_scale (not normalised)
-and beta stays its N(0, 1) logit.
+and beta stays its N(0, 1) logit.  With raw_gate=True g holds the gate logits x
+(std: the N(0, 1) draw, mixed: the draw - 2) from which the recipe's log alpha is
+-c softplus(x), c = gate_scale(spec) (0.1 std, 1 mixed).
 
 Named workloads (sizes as stated for the KDA forward benchmarks):
   tiny_fp32            1 seq x 256 tokens, H=2, d=64, fp32 I/O, zero state, seed 0
@@ -102,13 +104,18 @@ def torch_dtype(io: str):
     return {"bf16": torch.bfloat16, "f32": torch.float32}[io]
 
 
-def _gate(shape, kind, gen, device):
+def _gate(shape, kind, gen, device, raw=False):
     x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
     if kind == "std":
-        return -F.softplus(x) * 0.1
+        return x if raw else -F.softplus(x) * 0.1
     if kind == "mixed":
-        return -F.softplus(x - 2.0)
+        return x - 2.0 if raw else -F.softplus(x - 2.0)
     raise ValueError(kind)
+
+
+def gate_scale(spec) -> float:
+    """c of the recipe's log alpha = -c softplus(logit) (see raw_gate)."""
+    return {"std": 0.1, "mixed": 1.0}[spec.gate]
 
 
 def _unit_normal(shape, gen, device):
@@ -128,18 +135,19 @@ def _beta(shape, gen, device, raw):
 
 
 def prefill_inputs(spec: PrefillSpec, device: str = "cpu", raw: bool = False,
-                   qk_scale: float = 1.0) -> dict:
+                   qk_scale: float = 1.0, raw_gate: bool = False) -> dict:
     """Inputs of one prefill call, laid out as the library expects:
     q, k, g [T, H, d_k]; v [T, H, d_v]; beta [T, H] (all io dtype);
     cu_seqlens int32 [N+1]; init_state fp32 [N, H, d_k, d_v] or None.
-    raw=True: q, k and beta before the input steps (module docstring)."""
+    raw=True: q, k and beta before the input steps; raw_gate=True: g as gate logits
+    (module docstring)."""
     gen = torch.Generator(device=device).manual_seed(spec.seed)
     T, H, dk, dv = spec.total_tokens, spec.num_heads, spec.d_k, spec.d_v
     dt = torch_dtype(spec.io_dtype)
     q = _qk((T, H, dk), gen, device, raw, qk_scale).to(dt)
     k = _qk((T, H, dk), gen, device, raw, qk_scale).to(dt)
     v = torch.randn((T, H, dv), generator=gen, device=device).to(dt)
-    g = _gate((T, H, dk), spec.gate, gen, device).to(dt)
+    g = _gate((T, H, dk), spec.gate, gen, device, raw_gate).to(dt)
     beta = _beta((T, H), gen, device, raw).to(dt)
     if spec.init == "normal":
         init = torch.randn((spec.num_seqs, H, dk, dv), generator=gen, device=device) * 0.02
@@ -154,7 +162,7 @@ def prefill_inputs(spec: PrefillSpec, device: str = "cpu", raw: bool = False,
 
 
 def decode_inputs(spec: DecodeSpec, device: str = "cpu", raw: bool = False,
-                  qk_scale: float = 1.0) -> dict:
+                  qk_scale: float = 1.0, raw_gate: bool = False) -> dict:
     """Inputs of `steps` consecutive decode steps: q, k, g [steps, N, H, d_k];
     v [steps, N, H, d_v]; beta [steps, N, H]; state fp32 [N, H, d_k, d_v].
     raw=True: q, k and beta before the input steps (module docstring)."""
@@ -164,7 +172,7 @@ def decode_inputs(spec: DecodeSpec, device: str = "cpu", raw: bool = False,
     q = _qk((S, N, H, dk), gen, device, raw, qk_scale).to(dt)
     k = _qk((S, N, H, dk), gen, device, raw, qk_scale).to(dt)
     v = torch.randn((S, N, H, dv), generator=gen, device=device).to(dt)
-    g = _gate((S, N, H, dk), spec.gate, gen, device).to(dt)
+    g = _gate((S, N, H, dk), spec.gate, gen, device, raw_gate).to(dt)
     beta = _beta((S, N, H), gen, device, raw).to(dt)
     state = torch.randn((N, H, dk, dv), generator=gen, device=device) * 0.02
     return dict(q=q, k=k, v=v, g=g, beta=beta, state=state)

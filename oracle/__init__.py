@@ -142,6 +142,20 @@ def preprocess(q, k, beta, qk_silu=False, qk_l2norm=False, beta_sigmoid=False):
     return q, k, beta
 
 
+def gate_from_logits(x, gate_scale=1.0):
+    """log alpha from gate logits, in fp64: -c * softplus(x), softplus(x) = log(1 + e^x),
+    taken in the overflow-free form max(x, 0) + log1p(e^-|x|).
+
+    The pages give the decay only as alpha_t in [0, 1] per key channel ("Kimi Delta
+    Attention (KDA)", Gated DeltaNet and KDA sections: alpha = 1 keeps, alpha = 0
+    clears memory); the workloads draw it as exp(-c * softplus(x)) of a normal x, a
+    positive decay rate made so by softplus.  This is that map, for the kernels'
+    optional gate step (KDA_PREP_G_SOFTPLUS).  x: any shape.  Returns float64.
+    """
+    x = _f64(x)
+    return -float(gate_scale) * (np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x))))
+
+
 def kda_decode_steps(q, k, v, g, beta, state, scale=None, threads=None):
     """Consecutive single-token steps for N independent sequences.
 

@@ -107,3 +107,39 @@ def test_very_negative_write_logit_only_decays():
     _, fin = oracle.kda_fwd(q, k, v, g, b, np.array([0, T]), init_state=S0)
     decay = np.exp(np.sum(g, axis=0))  # [H, d]
     np.testing.assert_allclose(fin[0], decay[:, :, None] * S0[0], rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- the gate step
+# log alpha = -c softplus(x): the decay alpha in [0, 1] per key channel of "Kimi Delta
+# Attention (KDA)" (alpha = 1 keeps, alpha = 0 clears) as the workloads draw it.
+def test_gate_closed_forms():
+    ln2 = math.log(2.0)
+    x = np.array([0.0, math.log(3.0), -math.log(3.0), 40.0, -40.0, 800.0, -800.0])
+    g = oracle.gate_from_logits(x)
+    # softplus(0) = ln 2; softplus(ln 3) = ln 4; softplus(-ln 3) = ln(4 / 3)
+    np.testing.assert_allclose(g[:3], [-ln2, -2 * ln2, -math.log(4.0 / 3.0)], rtol=1e-15)
+    # no overflow or loss at the ends: softplus(x) -> x, softplus(-x) -> e^-x
+    assert np.all(np.isfinite(g))
+    np.testing.assert_allclose(g[[3, 5]], [-40.0, -800.0], rtol=1e-15)
+    np.testing.assert_allclose(g[4], -math.exp(-40.0), rtol=1e-14)
+    assert g[6] == 0.0 or abs(g[6]) < 1e-300
+
+
+def test_gate_identities_and_range():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((200, 3, 16)) * 6
+    c = 0.37
+    gp, gm = oracle.gate_from_logits(x, c), oracle.gate_from_logits(-x, c)
+    # softplus(x) - softplus(-x) = x
+    np.testing.assert_allclose(gp - gm, -c * x, rtol=1e-13, atol=1e-13)
+    # alpha = e^g in (0, 1], decreasing in x, and linear in the scale c
+    assert np.all(gp <= 0.0) and np.all(np.exp(gp) > 0.0)
+    xs = np.sort(x.ravel())
+    assert np.all(np.diff(oracle.gate_from_logits(xs, c)) <= 0.0)
+    np.testing.assert_allclose(oracle.gate_from_logits(x, 2 * c), 2 * gp, rtol=1e-15)
+    # the recipe of the workloads: -0.1 softplus of a draw equals the stored log decay
+    import torch
+    t = torch.from_numpy(x[:, 0]).float()
+    np.testing.assert_allclose(oracle.gate_from_logits(t, 0.1),
+                               (-torch.nn.functional.softplus(t) * 0.1).double().numpy(),
+                               rtol=2e-6, atol=1e-7)
