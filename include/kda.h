@@ -23,10 +23,12 @@
  *       beta    : [T_total, H]             states : [N, H, d_k, d_v] fp32
  *       cu_seqlens : int32 [N + 1] (device), nondecreasing, cu[0] = 0,
  *                    cu[N] = T_total; sequence n owns tokens [cu[n], cu[n+1]).
- *                    The kernels read it on the device and do not check it:
- *                    offsets that decrease or pass T_total make them read and
- *                    write out of range (the Python binding's check=True reads it
- *                    back and checks it on the host first).
+ *                    The kernels check each sequence's pair of offsets on the
+ *                    device before any access they guide: a sequence whose
+ *                    offsets decrease or leave [0, T_total] is skipped (nothing
+ *                    read or written for it, its final state left as it was) and
+ *                    KDA_ERR_SEQLENS is recorded (kda_workspace_status for the
+ *                    prefill, kda_last_device_status for kda_recurrent_fwd).
  *   - Alignment: states, workspace and (prefill) q, k, v, out and a per-channel g
  *     start on a 16-byte boundary; beta, a per-token g and (decode, recurrent)
  *     q, k, v, g on their element size;
@@ -61,7 +63,8 @@ enum {
   KDA_ERR_DEVICE_TIMEOUT = -7, /* (device-reported) a bounded wait in a kernel gave up */
   KDA_ERR_GATE_RANGE = -8,     /* (device-reported) a chunk's decay exceeded the tensor-core path's range */
   KDA_ERR_UNSUPPORTED = -9,    /* the requested algorithm does not support this dtype or size */
-  KDA_ERR_NOALLOC_LIMIT = -10  /* the shape needs more scratch than kda_chunk_fwd_noalloc's built-in buffer */
+  KDA_ERR_NOALLOC_LIMIT = -10, /* the shape needs more scratch than kda_chunk_fwd_noalloc's built-in buffer */
+  KDA_ERR_SEQLENS = -11        /* (device-reported) cu_seqlens offsets decrease or leave [0, T_total] */
 };
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -88,11 +91,17 @@ typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_SCALAR = 1, KDA_GATE_NONE = 2 } kd
  *   KDA_PREP_QK_L2NORM    then each (token, head) row of q and of k is divided
  *                         by max(||row||_2, 1e-12) over d_k
  *   KDA_PREP_BETA_SIGMOID beta holds logits; the write strength is sigmoid(beta)
+ *   KDA_PREP_G_SOFTPLUS   g holds gate logits x; the log decay is
+ *                         log alpha = -c softplus(x) = -c log(1 + e^x) <= 0, with
+ *                         c = kda_shape.gate_scale (<= 0 selects 1): a decay rate made
+ *                         positive by softplus, as the benchmark workloads draw it
  * The tensors in memory are left as they are.  0 = every input used as given
  * (the default, and the form of the benchmark workloads).  The fp32 paths
  * compute the SiLU in fp32; the tensor-core path (bf16 I/O) computes it on bf16
- * pairs with the hardware tanh, about 0.3 % relative error over a row. */
-enum { KDA_PREP_QK_SILU = 1, KDA_PREP_QK_L2NORM = 2, KDA_PREP_BETA_SIGMOID = 4 };
+ * pairs with the hardware tanh, about 0.3 % relative error over a row, and rounds
+ * a per-channel -c softplus(x) to bf16 before its chunk cumsum. */
+enum { KDA_PREP_QK_SILU = 1, KDA_PREP_QK_L2NORM = 2, KDA_PREP_BETA_SIGMOID = 4,
+       KDA_PREP_G_SOFTPLUS = 8 };
 
 typedef struct {
   int32_t num_seqs;     /* N >= 0 (sequences; for decode: independent sequences, one token each) */
@@ -106,6 +115,7 @@ typedef struct {
   int32_t algo;         /* kda_algo (prefill only) */
   int32_t gate;         /* kda_gate: layout of g (0 = one per key channel) */
   int32_t prep;         /* KDA_PREP_* bits (0 = none); added in ABI 1.2 */
+  float gate_scale;     /* c of KDA_PREP_G_SOFTPLUS (<= 0 selects 1); added in ABI 1.4 */
 } kda_shape;
 
 /*
@@ -129,6 +139,14 @@ typedef struct {
  *                 a smaller workspace selects the schedule that fits.  The
  *                 schedules give bit-identical results.  Calls that share one
  *                 workspace must be ordered on one stream.
+ * The tensor-core kernel forms its decay factors relative to each chunk's start, so
+ * they stay finite while a chunk's total log decay per key channel is above -80.  A
+ * sequence-head with a chunk beyond that (a very fast decay, alpha -> 0) is marked in
+ * one flag word per sequence-head after the status block, and a second kernel of the
+ * same call recomputes it token by token with exact decays (status word 3 counts such
+ * sequence-heads).  That needs 256 + 4 N H bytes (rounded up to 256) of workspace,
+ * included in kda_chunk_fwd_workspace_bytes(); with less, such a call reports
+ * KDA_ERR_GATE_RANGE and its results are undefined.
  * Zero sequences or zero tokens are valid (nothing but the status reset is enqueued).
  * Sequences must be at most 2^31 - 1 tokens long in total; an empty sequence
  * copies its initial state to final_state.
@@ -139,8 +157,9 @@ int kda_chunk_fwd(const kda_shape *shape, const void *q, const void *k, const vo
                   size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of workspace with which kda_chunk_fwd can run every schedule for this
- * shape (always >= 256), or 0 if the shape is invalid.  Few sequence-heads on
- * the tensor-core path add a ring through which extra CTAs hand over the
+ * shape (always >= 256), or 0 if the shape is invalid: the status block, on the
+ * tensor-core path with a gate one flag word per sequence-head (rounded up to 256
+ * bytes), and for few sequence-heads a ring through which extra CTAs hand over the
  * chunk solve (4 x 16 KiB + 32 bytes per sequence-head). */
 size_t kda_chunk_fwd_workspace_bytes(const kda_shape *shape);
 
@@ -201,33 +220,55 @@ int kda_recurrent_fwd(const kda_shape *shape, const void *q, const void *k, cons
  *
  * Same arguments and results as kda_chunk_fwd, without the workspace: the
  * scratch comes from a 256 KiB buffer compiled into the library, which every
- * GPU that loads the library holds until the process exits.  The schedule
- * that fits the buffer runs; a shape whose minimum workspace exceeds 256 KiB
- * would be rejected with KDA_ERR_NOALLOC_LIMIT (no current schedule needs more
- * than the 256-byte status block).  Nothing is allocated or freed.  The first call on a
- * device (made while that device is current) looks the buffer's address up,
- * so make that first call before any stream capture.  All calls on one device
- * share the buffer and it keeps the last call's contents (each call clears the
- * status block it needs); calls whose kernels overlap on the GPU race on it, so
- * order them on one stream.
+ * GPU that loads the library holds until the process exits.  The status block
+ * and the recomputation flags (4 bytes per sequence-head) must fit in it: a shape
+ * of more than 65,472 sequence-heads is rejected with KDA_ERR_NOALLOC_LIMIT.  The
+ * schedule that fits the rest runs.  Nothing is allocated or freed.  The first
+ * call on a device (made while that device is current) looks the buffer's
+ * address up, again after a cudaDeviceReset, so make that first call before any
+ * stream capture.  All calls on one device share the buffer and it keeps the
+ * last call's contents (each call clears the status block and flags it needs);
+ * calls whose kernels overlap on the GPU race on it, so order them on one stream.
+ * kda_noalloc_status() reads the device status of the last call.
  */
 int kda_chunk_fwd_noalloc(const kda_shape *shape, const void *q, const void *k, const void *v,
                           const void *g, const void *beta, const float *init_state,
                           const int32_t *cu_seqlens, void *out, float *final_state,
                           cudaStream_t stream);
 
+/* Synchronises `stream` and returns the device status of the last
+ * kda_chunk_fwd_noalloc on the current device (as kda_workspace_status does for a
+ * caller workspace); with `words` non-NULL also copies the first four words of its
+ * status block there (see kda_workspace_status).  The method has no counterpart to
+ * this; it serves the callers of kda_chunk_fwd_noalloc, which own no workspace to
+ * read. */
+int kda_noalloc_status(uint32_t *words, cudaStream_t stream);
+
 /*
  * Synchronises `stream`, then reads the status block that the kernels of the
- * last kda_chunk_fwd on this workspace wrote: KDA_OK, KDA_ERR_DEVICE_TIMEOUT
- * or KDA_ERR_GATE_RANGE.  A CUDA error while reading returns KDA_ERR_LAUNCH.
+ * last kda_chunk_fwd on this workspace wrote: KDA_OK, KDA_ERR_DEVICE_TIMEOUT,
+ * KDA_ERR_SEQLENS or KDA_ERR_GATE_RANGE.  A CUDA error while reading returns
+ * KDA_ERR_LAUNCH.  Word 2 of the block holds the tensor-core schedule that ran
+ * (1 plain, 2 with solve helpers), word 3 the sequence-heads recomputed token by
+ * token.
  */
 int kda_workspace_status(const void *workspace, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the first error the kernels of
+ * kda_recurrent_fwd recorded on the current device since the last read: KDA_OK or
+ * KDA_ERR_SEQLENS.  A CUDA error while reading returns KDA_ERR_LAUNCH.
+ */
+int kda_last_device_status(cudaStream_t stream);
 
 /* Static English description of a status code. */
 const char *kda_status_string(int status);
 
 /* Library ABI version (major * 1000 + minor); 1001 added kda_recurrent_fwd,
- * 1002 the kda_shape.prep field. */
+ * 1002 the kda_shape.prep field, 1003 the device check of cu_seqlens
+ * (KDA_ERR_SEQLENS, kda_last_device_status), the exact recomputation beyond the
+ * tensor-core decay range and kda_noalloc_status, 1004 KDA_PREP_G_SOFTPLUS and
+ * kda_shape.gate_scale. */
 int kda_version(void);
 
 #ifdef __cplusplus

@@ -24,7 +24,9 @@ int check_shape(const kda_shape *s, bool decode) {
   if (s->io_dtype != KDA_F32 && s->io_dtype != KDA_BF16) return KDA_ERR_SHAPE;
   if (!(s->scale == s->scale) || isinf(s->scale)) return KDA_ERR_SHAPE;
   if (s->gate < KDA_GATE_CHANNEL || s->gate > KDA_GATE_NONE) return KDA_ERR_SHAPE;
-  if (s->prep & ~(KDA_PREP_QK_SILU | KDA_PREP_QK_L2NORM | KDA_PREP_BETA_SIGMOID)) return KDA_ERR_SHAPE;
+  if (s->prep & ~(KDA_PREP_QK_SILU | KDA_PREP_QK_L2NORM | KDA_PREP_BETA_SIGMOID | KDA_PREP_G_SOFTPLUS))
+    return KDA_ERR_SHAPE;
+  if (!(s->gate_scale == s->gate_scale) || isinf(s->gate_scale)) return KDA_ERR_SHAPE;
   if (decode) {
     if (s->total_tokens != s->num_seqs) return KDA_ERR_SHAPE;
   } else {
@@ -39,6 +41,7 @@ int check_shape(const kda_shape *s, bool decode) {
 float effective_scale(const kda_shape *s) {
   return s->scale > 0.f ? s->scale : 1.0f / sqrtf((float)s->d_k);
 }
+float effective_gate_scale(const kda_shape *s) { return s->gate_scale > 0.f ? s->gate_scale : 1.0f; }
 
 // The library carries sm_103a code only.
 int check_device(int *num_sms) {
@@ -61,11 +64,34 @@ bool use_tensor_path(const kda_shape *s) {
   return kda::chunk_tc_supported(s->d_k, s->d_v, bf16);
 }
 
+// Per-pair flags after the status block: the tensor-core path marks there the
+// sequence-heads whose decay left its range, which a second kernel then recomputes
+// token by token.  Without a gate there is no decay and no flag.
+size_t flag_bytes(const kda_shape *s) {
+  if (!use_tensor_path(s) || s->gate == KDA_GATE_NONE) return 0;
+  const size_t pairs = (size_t)s->num_seqs * (size_t)s->num_heads;
+  return (pairs * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
 }  // namespace
+
+namespace kda {
+// The workspace a call needs to give the same results as with
+// kda_chunk_fwd_workspace_bytes(): the status block and the recomputation flags
+// (the helpers' ring only speeds a call up).  0 for an invalid shape.
+size_t chunk_fwd_required_workspace(const kda_shape *s) {
+  if (check_shape(s, false) != KDA_OK) return 0;
+  return kStatusBytes + flag_bytes(s);
+}
+}  // namespace kda
 
 extern "C" {
 
-int kda_version(void) { return 1002; }  // 1.1: kda_recurrent_fwd; 1.2: kda_shape.prep
+// 1.1: kda_recurrent_fwd; 1.2: kda_shape.prep; 1.3: device-checked offsets
+// (KDA_ERR_SEQLENS, kda_last_device_status), the exact recomputation of sequence-heads
+// beyond the tensor-core decay range, kda_noalloc_status; 1.4: KDA_PREP_G_SOFTPLUS and
+// kda_shape.gate_scale
+int kda_version(void) { return 1004; }
 
 const char *kda_status_string(int status) {
   switch (status) {
@@ -80,13 +106,14 @@ const char *kda_status_string(int status) {
     case KDA_ERR_GATE_RANGE: return "a chunk's cumulative decay exceeded the tensor-core path's range";
     case KDA_ERR_UNSUPPORTED: return "the requested algorithm does not support this dtype or size";
     case KDA_ERR_NOALLOC_LIMIT: return "the shape needs more scratch than the built-in no-allocation buffer";
+    case KDA_ERR_SEQLENS: return "cu_seqlens offsets decrease or leave [0, total_tokens] (found on the device)";
     default: return "unknown status";
   }
 }
 
 size_t kda_chunk_fwd_workspace_bytes(const kda_shape *s) {
   if (check_shape(s, false) != KDA_OK) return 0;
-  size_t bytes = kda::kStatusBytes;
+  size_t bytes = kda::kStatusBytes + flag_bytes(s);
   if (use_tensor_path(s)) bytes += kda::chunk_tc_scratch_bytes(s->num_seqs, s->num_heads, s->d_k, s->d_v);
   return bytes;
 }
@@ -123,7 +150,11 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
   rc = check_device(&num_sms);
   if (rc != KDA_OK) return rc;
 
-  if (cudaMemsetAsync(workspace, 0, kda::kStatusBytes, stream) != cudaSuccess) return KDA_ERR_LAUNCH;
+  // the flags of the exact recomputation, when the workspace has room for them
+  const size_t fbytes = flag_bytes(s);
+  const bool flags = fbytes > 0 && workspace_bytes >= kda::kStatusBytes + fbytes;
+  const size_t head = kda::kStatusBytes + (flags ? fbytes : 0);
+  if (cudaMemsetAsync(workspace, 0, head, stream) != cudaSuccess) return KDA_ERR_LAUNCH;
   if (s->num_seqs == 0) return KDA_OK;
 
   kda::ChunkArgs a;
@@ -137,21 +168,53 @@ int kda_chunk_fwd(const kda_shape *s, const void *q, const void *k, const void *
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate = s->gate;
   a.prep = s->prep;
+  a.gate_scale = effective_gate_scale(s);
   a.init_state = init_state;
   a.cu_seqlens = cu_seqlens;
   a.out = out;
   a.final_state = final_state;
   a.status = static_cast<uint32_t *>(workspace);
-  a.scratch = static_cast<unsigned char *>(workspace) + kda::kStatusBytes;
-  a.scratch_bytes = workspace_bytes - kda::kStatusBytes;
+  a.pair_flags = flags ? reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(workspace) +
+                                                      kda::kStatusBytes)
+                       : nullptr;
+  a.scratch = static_cast<unsigned char *>(workspace) + head;
+  a.scratch_bytes = workspace_bytes - head;
   a.num_sms = num_sms;
   // Test hook: KDA_TEST_FORCE_WAIT_TIMEOUT=1 makes the tensor-core kernel wait once on a
   // barrier that nothing arrives on, so its bounded-wait error path can be exercised.
   const char *force = getenv("KDA_TEST_FORCE_WAIT_TIMEOUT");
   a.test_flags = (force && force[0] == '1') ? 1 : 0;
-  const cudaError_t err = tensor ? kda::launch_chunk_tc(a, stream) : kda::launch_chunk_simt(a, stream);
+  cudaError_t err = tensor ? kda::launch_chunk_tc(a, stream) : kda::launch_chunk_simt(a, stream);
   if (err == cudaErrorInvalidValue) return KDA_ERR_UNSUPPORTED;
-  return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  if (err != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (a.pair_flags) {
+    // The sequence-heads the tensor-core kernel marked (a chunk's decay beyond its range)
+    // are recomputed token by token with exact decays; the kernel leaves at once when
+    // none was marked (status word 3 counts them).
+    kda::RecurrentArgs r;
+    r.num_seqs = a.num_seqs;
+    r.total_tokens = a.total_tokens;
+    r.num_heads = a.num_heads;
+    r.d_k = a.d_k;
+    r.d_v = a.d_v;
+    r.scale = a.scale;
+    r.bf16 = a.bf16;
+    r.q = q; r.k = k; r.v = v; r.g = g; r.beta = beta;
+    r.gate = a.gate;
+    r.prep = a.prep;
+    r.gate_scale = a.gate_scale;
+    r.init_state = init_state;
+    r.cu_seqlens = cu_seqlens;
+    r.accepted = nullptr;
+    r.out = out;
+    r.final_state = final_state;
+    r.status = a.status;
+    r.only_flags = a.pair_flags;
+    r.only_count = a.status + 3;
+    err = kda::launch_recurrent(r, stream);
+    if (err != cudaSuccess) return KDA_ERR_LAUNCH;
+  }
+  return KDA_OK;
 }
 
 int kda_recurrent_fwd(const kda_shape *s, const void *q, const void *k, const void *v,
@@ -184,11 +247,15 @@ int kda_recurrent_fwd(const kda_shape *s, const void *q, const void *k, const vo
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate = s->gate;
   a.prep = s->prep;
+  a.gate_scale = effective_gate_scale(s);
   a.init_state = init_state;
   a.cu_seqlens = cu_seqlens;
   a.accepted = accepted;
   a.out = out;
   a.final_state = final_state;
+  a.status = nullptr;  // offsets found out of range go to the library's device word
+  a.only_flags = nullptr;
+  a.only_count = nullptr;
   const cudaError_t err = kda::launch_recurrent(a, stream);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
@@ -217,10 +284,17 @@ int kda_decode_step(const kda_shape *s, const void *q, const void *k, const void
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate = s->gate;
   a.prep = s->prep;
+  a.gate_scale = effective_gate_scale(s);
   a.state = state;
   a.out = out;
   const cudaError_t err = kda::launch_decode(a, stream);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+int kda_last_device_status(cudaStream_t stream) {
+  uint32_t word = 0;
+  if (kda::take_device_status(&word, stream) != cudaSuccess) return KDA_ERR_LAUNCH;
+  return word == 0 ? KDA_OK : -(int)word;
 }
 
 int kda_workspace_status(const void *workspace, cudaStream_t stream) {

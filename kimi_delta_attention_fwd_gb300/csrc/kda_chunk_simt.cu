@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(NT)
                           const IO *__restrict__ beta, const float *__restrict__ init_state,
                           const int32_t *__restrict__ cu_seqlens, IO *__restrict__ out,
                           float *__restrict__ final_state, int H, int DV, float scale,
-                          int gate, int prep) {
+                          int gate, int prep, float gs, int T, uint32_t *status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<DK> &sm = *reinterpret_cast<SimtSmem<DK> *>(smem_raw);
 
@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(NT)
   const int n = pair / H, h = pair % H;
   const int col0 = blockIdx.y * BV;
   const int tid = threadIdx.x;
-  const int bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
+  // offsets out of order or out of range: no token read or written, no state stored
+  int bos, eos;
+  const bool seq_ok = seq_range(cu_seqlens, n, T, tid == 0 ? status : nullptr, bos, eos);
   const size_t state_off = (size_t)pair * DK * DV;
 
   for (int idx = tid; idx < DK * BV; idx += NT) {
@@ -108,8 +110,9 @@ __global__ void __launch_bounds__(NT)
           qv = silu_f32(qv);
         }
         // g per key channel (KDA), one per token for every channel (Gated DeltaNet), or 0
-        if (gate == 0) gv = ld_f32(g + o);
-        else if (gate == 1) gv = ld_f32(g + (size_t)(c0 + r) * H + h);
+        // (gate logits through -c softplus with KDA_PREP_G_SOFTPLUS)
+        if (gate == 0) gv = gate_log<true>(ld_f32(g + o), prep, gs);
+        else if (gate == 1) gv = gate_log<true>(ld_f32(g + (size_t)(c0 + r) * H + h), prep, gs);
       }
       sm.K[r][j] = kv;
       sm.Q[r][j] = qv;
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(NT)
     }
   }
   __syncthreads();
-  if (final_state) {
+  if (final_state && seq_ok) {
     for (int idx = tid; idx < DK * BV; idx += NT) {
       const int r = idx / BV, c = idx % BV;
       final_state[state_off + (size_t)r * DV + col0 + c] = sm.S[r][c];
@@ -246,7 +249,8 @@ cudaError_t launch_t(const ChunkArgs &a, cudaStream_t stream) {
   kern<<<grid, NT, smem, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
-      static_cast<IO *>(a.out), a.final_state, a.num_heads, a.d_v, a.scale, a.gate, a.prep);
+      static_cast<IO *>(a.out), a.final_state, a.num_heads, a.d_v, a.scale, a.gate, a.prep,
+      a.gate_scale, a.total_tokens, a.status);
   return cudaGetLastError();
 }
 

@@ -24,8 +24,11 @@
 // be about -V there, and its rounding large against E).
 //
 // exp(G) <= 1 and exp(-G) <= exp(-G_last); every factor stays finite as long
-// as a chunk's total log decay per channel is above -80 (checked; beyond it
-// the call reports KDA_ERR_GATE_RANGE).  The products use bf16 operands with
+// as a chunk's total log decay per channel is above -80.  The state side checks
+// it per chunk; a sequence-head that leaves the range is marked in the
+// workspace's per-pair flags, its outputs and final state are left unwritten,
+// and the launcher's next kernel recomputes it token by token with exact decays
+// (without room for the flags the call reports KDA_ERR_GATE_RANGE instead).  The products use bf16 operands with
 // fp32 accumulation in tensor memory; the state, the cumsum and the solve are fp32.
 //
 // One CTA owns (sequence, head, 64-column d_v tile) and walks its chunks in
@@ -66,8 +69,6 @@ constexpr int kThreads = 448;  // 8 K-side warps, 4 S-side warps, 2 producer war
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinChunkLogDecay = -80.f;
-constexpr uint32_t kStatusTimeout = 7;      // -KDA_ERR_DEVICE_TIMEOUT
-constexpr uint32_t kStatusGateRange = 8;    // -KDA_ERR_GATE_RANGE
 
 // Solve helpers (few sequence-heads).  With at most 38 (sequence, head) pairs and
 // room for the ring, the launch is cooperative (all CTAs resident) and each pair
@@ -136,12 +137,16 @@ struct TcParams {
   const __nv_bfloat16 *beta;
   const __nv_bfloat16 *g_tok;  // [T, H] log alpha per (token, head) when gate == 1
   int gate;                    // 0: g per key channel (TMA), 1: per token (g_tok), 2: none
-  int prep;                    // KDA_PREP_* bits: silu / L2 norm of q and k, sigmoid of beta
+  int prep;                    // KDA_PREP_* bits: silu / L2 norm of q and k, sigmoid of beta,
+                               // softplus of the gate
+  float gate_scale;            // c of log alpha = -c softplus(x)
   const float *init_state;
   const int32_t *cu_seqlens;
   __nv_bfloat16 *out;
   float *final_state;
   uint32_t *status;
+  uint32_t *pair_flags;      // [P]: set for a pair whose decay left the range (or NULL)
+  int T;                     // tokens in all (cu_seqlens must stay within [0, T])
   int H;
   float scale;
   int flags;  // bit 0: test hook, wait once on a barrier nothing arrives on
@@ -303,6 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *glast = reinterpret_cast<float *>(smem + L::kGlast);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+  // set by the state side once this pair's decay has left the range: nothing more is stored
+  volatile int *skip_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -326,15 +333,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *rdata = kSched ? p.ring + (size_t)pair * kRingSlots * kRingSlotBytes : nullptr;
   const int H = p.H;
   const int n = pair / H, h = pair % H;
-  const int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+  // a pair whose offsets are out of order or out of range runs no chunk and writes nothing
+  // (its skip flag is set below); bos and eos stay reloadable from cu_seqlens
+  const int bos = p.cu_seqlens[n];
+  const bool seq_ok = 0 <= bos && bos <= p.cu_seqlens[n + 1] && p.cu_seqlens[n + 1] <= p.T;
+  const int eos = seq_ok ? p.cu_seqlens[n + 1] : bos;
   const int nchunks = (eos - bos + C - 1) / C;
 
   Ctx ctx{sbase + L::kBars, abort_flag, p.status};
 
   if (tid == 0) {
     *abort_flag = 0;
+    *skip_flag = seq_ok ? 0 : 1;
+    if (!seq_ok) atomicCAS(p.status, 0u, kStatusSeqlens);
     for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(ctx.bar(i), 1);
     fence_mbar_init();
+    if (blockIdx.x == 0) p.status[2] = kSched ? kSchedHelpers : kSchedPlain;  // which schedule ran
   }
   if (warp == 12) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -444,6 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Ys = reinterpret_cast<float *>(smem + L::kTP + kw * 16384);          // TP rows 0-63
     const uint32_t mma_bar = ctx.bar(kMmaK0 + kw);
     const bool chan = p.gate == 0;  // g per key channel: G by the cumsum product below
+    // g holds gate logits: each group turns its g tile into -c softplus(g) in place before
+    // the cumsum product, which is then issued at the top of the chunk (not ahead)
+    const bool gsp = kPrep && chan && (p.prep & kPrepGSoftplus);
     // a1: G = [Ltri; Ltri] g on the tensor cores, straight from the TMA'd g tile:
     // the chunk-local inclusive cumsum per channel (rows 64-127 repeat rows 0-63)
     auto issue_cumsum = [&]() {
@@ -489,8 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float g_row = 0.f;
       if (p.gate == 1) {
         const int lane = t & 31;
-        float ga = lane < len ? __bfloat162float(p.g_tok[(size_t)(t0 + lane) * H + h]) : 0.f;
-        float gb = 32 + lane < len ? __bfloat162float(p.g_tok[(size_t)(t0 + 32 + lane) * H + h]) : 0.f;
+        float ga = lane < len ? gate_log<kPrep>(__bfloat162float(p.g_tok[(size_t)(t0 + lane) * H + h]),
+                                                p.prep, p.gate_scale) : 0.f;
+        float gb = 32 + lane < len ? gate_log<kPrep>(__bfloat162float(p.g_tok[(size_t)(t0 + 32 + lane) * H + h]),
+                                                     p.prep, p.gate_scale) : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float xa = __shfl_up_sync(0xffffffffu, ga, o), xb = __shfl_up_sync(0xffffffffu, gb, o);
@@ -498,9 +517,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         g_row = (wq & 1) ? __shfl_sync(0xffffffffu, ga, 31) + gb : ga;  // row r = 32 (wq & 1) + lane
       }
+      if (gsp) {
+        // -c softplus of the chunk's gate logits, in place (bf16), then the cumsum product
+        if (t == 0) ctx.wait(kFullG0 + s, cur);
+        bar_sync(bar_id, 128);
+        const uint32_t grow = st + L::kG + (t >> 6) * 8192;  // row t mod 64, channel half t / 64
+#pragma unroll 2
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t addr = grow + sw128(t & 63, j);
+          float f[8];
+          unpack8(ld_shared_v4(addr), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = neg_softplus(f[e], p.gate_scale);
+          st8(addr, f);
+        }
+        fence_async_smem();
+        bar_sync(bar_id, 128);
+        if (t == 0) issue_cumsum();
+      }
       if (t == 0) {
         if (chan) {
-          if (it == 0) {  // later chunks had their cumsum product issued at the end of the previous one
+          if (it == 0 && !gsp) {  // later chunks had their cumsum product issued at the end of the previous one
             ctx.wait(kFullG0 + s, cur);
             issue_cumsum();
           }
@@ -909,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bar_sync(bar_id, 128);
           if (t == 0) {
             st_release_gpu(rflags + 2 * slot, static_cast<uint32_t>(c + 1));
-            if (chan && c + c_step < nchunks) {  // a1 of the group's next chunk
+            if (chan && !gsp && c + c_step < nchunks) {  // a1 of the group's next chunk
               ctx.wait(kFullG0 + s, cur ^ 1);
               issue_cumsum();
             }
@@ -993,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_sync(bar_id, 128);
       if (t == 0) {
         mbar_arrive(ctx.bar(kReady0 + s));
-        if (chan && c + 2 < nchunks) {  // a1 of chunk c + 2: the group's TMEM columns are free again
+        if (chan && !gsp && c + 2 < nchunks) {  // a1 of chunk c + 2: the group's TMEM columns are free again
           ctx.wait(kFullG0 + s, cur ^ 1);
           issue_cumsum();
         }
@@ -1043,11 +1080,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bar_sync(2, 128);
       tc_fence_after();
-      // gamma = exp(G_last) of this thread's key channel; a chunk whose total log decay
-      // is beyond the range the factors exp(+-G) are formed in is reported
+      // gamma = exp(G_last) of this thread's key channel.  A chunk whose total log decay
+      // is beyond the range the factors exp(+-G) are formed in marks the pair for the
+      // exact recomputation (or is reported without the flags): from here on this CTA
+      // stores nothing for it; the pipeline itself runs on unchanged
       const float gl = glast[(c % kGl) * 128 + t];
       const float gm = fast_exp2(gl * kLog2e);
-      if (!(gl >= kMinChunkLogDecay)) atomicCAS(p.status, 0u, kStatusGateRange);
+      if (!(gl >= kMinChunkLogDecay) && !*skip_flag) {
+        *skip_flag = 1;
+        if (p.pair_flags) {
+          if (atomicExch(p.pair_flags + pair, 1u) == 0u) atomicAdd(p.status + 3, 1u);
+        } else {
+          atomicCAS(p.status, 0u, kStatusGateRange);
+        }
+      }
       // a4/a5: [E; X] = [U; A^qk V] + [-W; Qh] S, the A operand from Aop[s] in TMEM
       if (t == 0) {
         constexpr uint32_t id = idesc_bf16(128, BV, false, true);
@@ -1109,6 +1155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++sph;
       bar_sync(2, 128);
       tc_fence_after();
+      const bool store = !*skip_flag;  // read after the barrier that follows every setter
       if (t >= 64) {  // output rows
         float a[32];
         const int i = t - 64;
@@ -1116,7 +1163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int hh = 0; hh < BV / 32; ++hh) {
           tmem_ld32(tmem + lane_base + kAcc0 + s * BV + 32 * hh, a);
-          if (i < len) {
+          if (i < len && store) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               float v[8];
@@ -1138,7 +1185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
-    if (p.final_state) {
+    bar_sync(2, 128);  // every setter of the skip flag is done
+    if (p.final_state && !*skip_flag) {
 #pragma unroll
       for (int j = 0; j < BV; j += 4)
         *reinterpret_cast<float4 *>(p.final_state + soff + j) =
@@ -1257,11 +1305,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.g_tok = a.gate == 1 ? static_cast<const __nv_bfloat16 *>(a.g) : nullptr;
   prm.gate = a.gate;
   prm.prep = a.prep;
+  prm.gate_scale = a.gate_scale;
   prm.init_state = a.init_state;
   prm.cu_seqlens = a.cu_seqlens;
   prm.out = static_cast<__nv_bfloat16 *>(a.out);
   prm.final_state = a.final_state;
   prm.status = a.status;
+  prm.pair_flags = a.pair_flags;
+  prm.T = a.total_tokens;
   prm.H = a.num_heads;
   prm.scale = a.scale;
   prm.flags = a.test_flags;

@@ -12,10 +12,17 @@
 // d_k * d_v bytes of state traffic against ~7 d_k d_v flops.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
+
+// First error the recurrent kernels recorded on this device (0 = none): offsets out
+// of order or out of range.  Read and cleared by take_device_status().
+__device__ uint32_t g_device_status;
 
 template <typename IO>
 __device__ __forceinline__ float to_f32(IO x);
@@ -65,7 +72,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                       const IO *__restrict__ v, const IO *__restrict__ g,
                       const IO *__restrict__ beta, float *__restrict__ state,
-                      IO *__restrict__ out, float scale, int gate, int prep) {
+                      IO *__restrict__ out, float scale, int gate, int prep, float gs) {
   constexpr int TPR = DV / 4;               // threads covering one state row (float4 each)
   constexpr int RPP = kDecodeThreads / TPR;  // rows covered per pass of the block
   constexpr int RPT = DK / RPP;              // rows held by each thread
@@ -89,13 +96,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 
   const size_t koff = (size_t)pair * DK, voff = (size_t)pair * DV;
   // alpha per key channel (KDA), one alpha for every channel (Gated DeltaNet), or 1 (DeltaNet)
-  const float a_tok = gate == 1 ? __expf(to_f32(g[pair])) : 1.f;
+  const float a_tok = gate == 1 ? __expf(gate_log<kPrep>(to_f32(g[pair]), prep, gs)) : 1.f;
   const bool silu = kPrep && (prep & kPrepSilu);
   for (int i = tid; i < DK; i += kDecodeThreads) {
     const float qi = to_f32(q[koff + i]), ki = to_f32(k[koff + i]);
     s_q[i] = silu ? silu_f32(qi) : qi;
     s_k[i] = silu ? silu_f32(ki) : ki;
-    s_a[i] = gate == 0 ? __expf(to_f32(g[koff + i])) : a_tok;
+    s_a[i] = gate == 0 ? __expf(gate_log<kPrep>(to_f32(g[koff + i]), prep, gs)) : a_tok;
   }
   for (int i = tid; i < DV; i += kDecodeThreads) s_v[i] = to_f32(v[voff + i]);
   if (tid == 0) {
@@ -207,15 +214,21 @@ __device__ __forceinline__ void cp_async_wait_but_last() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
-template <typename IO, int DK, int DV, bool kPrep>
+// kFixup: the exact recomputation of the pairs a tensor-core prefill marked (only_flags,
+// only_count); the plain launches run the instantiation without that code.
+template <typename IO, int DK, int DV, bool kPrep, bool kFixup>
 __global__ void __launch_bounds__(kRecThreads, 2)
     kda_recurrent_kernel(const IO *__restrict__ q, const IO *__restrict__ k,
                          const IO *__restrict__ v, const IO *__restrict__ g,
                          const IO *__restrict__ beta, const float *init_state,
                          const int32_t *__restrict__ cu_seqlens,
                          const int32_t *__restrict__ accepted, IO *__restrict__ out,
-                         float *final_state, int H, float scale, int gate, int prep,
-                         int npairs, bool staged) {
+                         float *final_state, int H, float scale, int gate, int prep, float gs,
+                         int npairs, bool staged, int T, uint32_t *status,
+                         const uint32_t *only_flags, const uint32_t *only_count) {
+  // only_flags: run only the pairs whose flag is set (the exact recomputation of pairs
+  // the tensor-core prefill marked), and nothing at all while *only_count is 0
+  if (kFixup && *only_count == 0u) return;
   constexpr int kWarps = kRecThreads / 32;
   static_assert(kTokBlock <= kWarps, "one warp per token of a block normalises its q and k");
   constexpr int CW = DV / kWarps;  // columns per warp (16 or 8)
@@ -253,8 +266,11 @@ __global__ void __launch_bounds__(kRecThreads, 2)
   IO *s_raw = reinterpret_cast<IO *>(s_next + RPL * kRecThreads);
   auto pair_steps = [&](int p, int &pbos) {
     const int pn = p / H;
+    if (kFixup && only_flags[p] == 0u) return 0;
+    // offsets out of order or out of range: no token (recorded when the pair runs)
     pbos = cu_seqlens[pn];
-    const int plen = cu_seqlens[pn + 1] - pbos;
+    const bool ok = 0 <= pbos && pbos <= cu_seqlens[pn + 1] && cu_seqlens[pn + 1] <= T;
+    const int plen = ok ? cu_seqlens[pn + 1] - pbos : 0;
     const int pacc = accepted ? min(max(accepted[pn], 0), plen) : plen;
     return out ? plen : pacc;
   };
@@ -289,8 +305,14 @@ __global__ void __launch_bounds__(kRecThreads, 2)
   }
 
   for (int pair = blockIdx.x; pair < npairs; pair += gridDim.x) {  // pair = n * H + h
+  if (kFixup && only_flags[pair] == 0u) continue;  // (fixup launches are unstaged)
   const int n = pair / H, h = pair % H;
-  const int bos = cu_seqlens[n], len = cu_seqlens[n + 1] - bos;
+  // offsets out of order or out of range: no token and no state written for the pair (the
+  // test is written so that bos and len stay reloadable from cu_seqlens: no extra registers)
+  const int bos = cu_seqlens[n];
+  const bool seq_ok = 0 <= bos && bos <= cu_seqlens[n + 1] && cu_seqlens[n + 1] <= T;
+  const int len = seq_ok ? cu_seqlens[n + 1] - bos : 0;
+  if (!seq_ok && tid == 0) atomicCAS(status, 0u, kStatusSeqlens);
   const int acc = accepted ? min(max(accepted[n], 0), len) : len;
   const int steps = out ? len : acc;  // outputs need every token, the state only the first acc
 
@@ -321,7 +343,7 @@ __global__ void __launch_bounds__(kRecThreads, 2)
     for (int i = 0; i < RPL; ++i)
       __stcs(reinterpret_cast<float4 *>(final_state + soff + (size_t)(rg + RG * i) * DV), s[i]);
   };
-  if (final_state && acc == 0) store_state();
+  if (final_state && acc == 0 && seq_ok) store_state();
   if (more && steps == 0) {  // nothing reads this pair's staged inputs
     cp_async_wait_but_last();  // they have landed before the next pair's overwrite them
     prefetch_inputs(pair + gridDim.x);
@@ -336,7 +358,7 @@ __global__ void __launch_bounds__(kRecThreads, 2)
     if (from_raw) {
       if (tid < nb) {
         s_beta[tid] = kPrep && (prep & kPrepBetaSigmoid) ? sigmoid_f32(beta_pre) : beta_pre;
-        if (gate == 1) s_alpha_tok[tid] = __expf(gtok_pre);
+        if (gate == 1) s_alpha_tok[tid] = __expf(gate_log<kPrep>(gtok_pre, prep, gs));
       }
       cp_async_wait_but_last();  // [inputs(pair)] done; [state(next)] may be in flight
       __syncthreads();           // every thread's pieces
@@ -349,7 +371,8 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       const int pi = (i % RG) * RPL + i / RG;
       s_q[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(qi) : qi;
       s_k[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(ki) : ki;
-      s_a[j][pi] = gate == 0 ? __expf(to_f32(rr[2 * DK + i])) : (gate == 1 ? s_alpha_tok[j] : 1.f);
+      s_a[j][pi] = gate == 0 ? __expf(gate_log<kPrep>(to_f32(rr[2 * DK + i]), prep, gs))
+                             : (gate == 1 ? s_alpha_tok[j] : 1.f);
     }
     for (int idx = tid; idx < nb * DV; idx += kRecThreads) {
       if (!from_raw) break;
@@ -364,8 +387,8 @@ __global__ void __launch_bounds__(kRecThreads, 2)
       const int pi = (i % RG) * RPL + i / RG;
       s_q[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(qi) : qi;
       s_k[j][pi] = kPrep && (prep & kPrepSilu) ? silu_f32(ki) : ki;
-      s_a[j][pi] = gate == 0 ? __expf(to_f32(g[row * DK + i]))
-                             : (gate == 1 ? __expf(to_f32(g[row])) : 1.f);
+      s_a[j][pi] = gate == 0 ? __expf(gate_log<kPrep>(to_f32(g[row * DK + i]), prep, gs))
+                             : (gate == 1 ? __expf(gate_log<kPrep>(to_f32(g[row]), prep, gs)) : 1.f);
     }
     for (int idx = tid; idx < nb * DV; idx += kRecThreads) {
       if (from_raw) break;
@@ -472,7 +495,15 @@ template <typename IO, int DK, int DV>
 cudaError_t launch_recurrent_t(const RecurrentArgs &a, cudaStream_t stream) {
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   if (pairs == 0 || (!a.out && !a.final_state)) return cudaSuccess;
-  auto kern = a.prep ? kda_recurrent_kernel<IO, DK, DV, true> : kda_recurrent_kernel<IO, DK, DV, false>;
+  auto kern = a.prep ? kda_recurrent_kernel<IO, DK, DV, true, false>
+                     : kda_recurrent_kernel<IO, DK, DV, false, false>;
+  if (a.only_flags) {  // the tensor-core path's recomputation: bf16, d_k = d_v = 128 only
+    if constexpr (std::is_same<IO, __nv_bfloat16>::value && DK == 128 && DV == 128)
+      kern = a.prep ? kda_recurrent_kernel<IO, DK, DV, true, true>
+                    : kda_recurrent_kernel<IO, DK, DV, false, true>;
+    else
+      return cudaErrorInvalidValue;
+  }
   // with two or more tokens per sequence on average: persistent CTAs, two per SM (the
   // launch bound), each staging its next pair's state in DK * DV * 4 bytes of dynamic
   // shared memory while it runs the current one (4 drafts 0.288 -> 0.277 ms, 8 drafts
@@ -485,14 +516,20 @@ cudaError_t launch_recurrent_t(const RecurrentArgs &a, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  const bool staged = (long long)a.total_tokens >= 2LL * a.num_seqs && pairs > 2LL * sms &&
-                      al16(a.q) && al16(a.k) && al16(a.v) && (a.gate != 0 || al16(a.g));
-  const long long grid = staged ? 2LL * sms : pairs;
+  // the exact recomputation of marked pairs runs unstaged, two CTAs per SM at most
+  const bool staged = !a.only_flags && (long long)a.total_tokens >= 2LL * a.num_seqs &&
+                      pairs > 2LL * sms && al16(a.q) && al16(a.k) && al16(a.v) &&
+                      (a.gate != 0 || al16(a.g));
+  const long long grid = staged ? 2LL * sms : (a.only_flags ? std::min(pairs, 2LL * sms) : pairs);
+  uint32_t *status = a.status;
+  if (!status && cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_device_status) != cudaSuccess)
+    return cudaErrorInvalidDevice;
   kern<<<(unsigned)grid, kRecThreads, staged ? smem : 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.init_state, a.cu_seqlens,
       a.accepted, static_cast<IO *>(a.out), a.final_state, a.num_heads, a.scale, a.gate, a.prep,
-      static_cast<int>(pairs), staged);
+      a.gate_scale, static_cast<int>(pairs), staged, a.total_tokens, status, a.only_flags,
+      a.only_count);
   return cudaGetLastError();
 }
 
@@ -513,7 +550,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
   kern<<<pairs, kDecodeThreads, 0, stream>>>(
       static_cast<const IO *>(a.q), static_cast<const IO *>(a.k), static_cast<const IO *>(a.v),
       static_cast<const IO *>(a.g), static_cast<const IO *>(a.beta), a.state,
-      static_cast<IO *>(a.out), a.scale, a.gate, a.prep);
+      static_cast<IO *>(a.out), a.scale, a.gate, a.prep, a.gate_scale);
   return cudaGetLastError();
 }
 
@@ -530,6 +567,20 @@ cudaError_t launch_decode_io(const DecodeArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   return a.bf16 ? launch_decode_io<__nv_bfloat16>(a, stream) : launch_decode_io<float>(a, stream);
+}
+
+cudaError_t take_device_status(uint32_t *word, cudaStream_t stream) {
+  *word = 0;
+  cudaError_t err = cudaMemcpyFromSymbolAsync(word, g_device_status, sizeof(uint32_t), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  if (err == cudaSuccess && *word != 0) {
+    static const uint32_t zero = 0;
+    err = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(uint32_t), 0,
+                                  cudaMemcpyHostToDevice, stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  }
+  return err;
 }
 
 cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream) {

@@ -12,41 +12,74 @@
 //
 // The buffer is a file-scope __device__ array of kScratchBytes.  Every GPU
 // that loads this library holds it until the process exits.  Its device
-// address is looked up once per device, on the first call made while that
-// device is current, so that first call should come before any stream
-// capture.  All calls on a device share the one buffer and it keeps the last
+// address is looked up once per device and context, on the first call made
+// while that device is current, so that first call should come before any
+// stream capture.  kda_noalloc_status() reads the status block in it, as
+// kda_workspace_status() does for a caller workspace.  All calls on a device share the one buffer and it keeps the last
 // call's contents; the status block in it is cleared by every call, as
 // kda_chunk_fwd does with a caller workspace.  Calls whose kernels overlap on
 // the GPU (different streams, or different host threads) race on the buffer:
 // order them on one stream.
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "kda.h"
+
+namespace kda {
+size_t chunk_fwd_required_workspace(const kda_shape *s);  // kda_abi.cu
+}
 
 namespace {
 
 constexpr size_t kScratchBytes = 256 * 1024;
-constexpr size_t kMinWorkspaceBytes = 256;  // the device status block
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char kda_noalloc_scratch[kScratchBytes];
 
-std::atomic<void *> g_scratch_addr[kMaxDevices];
+// The buffer's address per device, with the context it was looked up in: after a
+// cudaDeviceReset (or in another context of the device) the address is looked up
+// again instead of reusing one that no longer belongs to the current context.
+struct Cached {
+  CUcontext ctx;
+  void *addr;
+};
+Cached g_cache[kMaxDevices];
+std::mutex g_cache_lock;
 
-// Device address of the built-in buffer on the current device, or nullptr.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  CUcontext ctx = nullptr;
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
+// Device address of the built-in buffer in the current context, or nullptr.
 void *scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p) return p;
+  if (cudaSetDevice(dev) != cudaSuccess) return nullptr;  // makes the device's context current
+  const CUcontext ctx = current_context();
+  if (!ctx) return nullptr;
+  std::lock_guard<std::mutex> lock(g_cache_lock);
+  if (g_cache[dev].addr && g_cache[dev].ctx == ctx) return g_cache[dev].addr;
   void *addr = nullptr;
   if (cudaGetSymbolAddress(&addr, kda_noalloc_scratch) != cudaSuccess || addr == nullptr) {
     cudaGetLastError();  // do not leave the lookup failure as a sticky "last error"
     return nullptr;
   }
-  g_scratch_addr[dev].store(addr, std::memory_order_release);
+  g_cache[dev] = Cached{ctx, addr};
   return addr;
 }
 
@@ -56,11 +89,24 @@ extern "C" int kda_chunk_fwd_noalloc(const kda_shape *shape, const void *q, cons
                                      const void *v, const void *g, const void *beta,
                                      const float *init_state, const int32_t *cu_seqlens,
                                      void *out, float *final_state, cudaStream_t stream) {
-  if (kda_chunk_fwd_workspace_bytes(shape) == 0) return shape ? KDA_ERR_SHAPE : KDA_ERR_NULL;
-  // every schedule needs the status block; kda_chunk_fwd runs the one that fits the rest
-  if (kMinWorkspaceBytes > kScratchBytes) return KDA_ERR_NOALLOC_LIMIT;
+  if (!shape) return KDA_ERR_NULL;
+  const size_t need = kda::chunk_fwd_required_workspace(shape);
+  if (need == 0) return KDA_ERR_SHAPE;
+  // the status block and one recomputation flag per sequence-head must fit (the
+  // schedule that fits the rest runs): beyond about 65,000 sequence-heads they do not
+  if (need > kScratchBytes) return KDA_ERR_NOALLOC_LIMIT;
   void *scratch = scratch_on_current_device();
   if (!scratch) return KDA_ERR_DEVICE;
   return kda_chunk_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state, scratch,
                        kScratchBytes, stream);
+}
+
+extern "C" int kda_noalloc_status(uint32_t *words, cudaStream_t stream) {
+  void *scratch = scratch_on_current_device();
+  if (!scratch) return KDA_ERR_DEVICE;
+  const int rc = kda_workspace_status(scratch, stream);  // synchronises the stream
+  if (words && rc != KDA_ERR_LAUNCH &&
+      cudaMemcpy(words, scratch, 4 * sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KDA_ERR_LAUNCH;
+  return rc;
 }

@@ -16,9 +16,10 @@ import torch
 from . import build as _build
 
 KDA_OK = 0
+KDA_ERR_GATE_RANGE, KDA_ERR_SEQLENS = -8, -11
 KDA_F32, KDA_BF16 = 0, 1
 KDA_GATE_CHANNEL, KDA_GATE_SCALAR, KDA_GATE_NONE = 0, 1, 2
-KDA_PREP_QK_SILU, KDA_PREP_QK_L2NORM, KDA_PREP_BETA_SIGMOID = 1, 2, 4
+KDA_PREP_QK_SILU, KDA_PREP_QK_L2NORM, KDA_PREP_BETA_SIGMOID, KDA_PREP_G_SOFTPLUS = 1, 2, 4, 8
 _ALGOS = {"auto": 0, "tensor": 1, "simt": 2}
 _DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
 
@@ -34,7 +35,7 @@ class kda_shape(ctypes.Structure):
                 ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("io_dtype", ctypes.c_int32), ("algo", ctypes.c_int32), ("gate", ctypes.c_int32),
-                ("prep", ctypes.c_int32)]
+                ("prep", ctypes.c_int32), ("gate_scale", ctypes.c_float)]
 
 
 _lock = threading.Lock()
@@ -68,6 +69,12 @@ def load_library():
         lib.kda_recurrent_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.kda_workspace_status.restype = ctypes.c_int
         lib.kda_workspace_status.argtypes = [vp, vp]
+        lib.kda_last_device_status.restype = ctypes.c_int
+        lib.kda_last_device_status.argtypes = [vp]
+        lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.kda_chunk_fwd_noalloc.argtypes = [sp] + [vp] * 10
+        lib.kda_noalloc_status.restype = ctypes.c_int
+        lib.kda_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_version.restype = ctypes.c_int
@@ -94,16 +101,18 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _make_shape(num_seqs, total_tokens, H, dk, dv, scale, io, algo="auto", gate=0, prep=0):
+def _make_shape(num_seqs, total_tokens, H, dk, dv, scale, io, algo="auto", gate=0, prep=0,
+                gate_scale=None):
     return kda_shape(int(num_seqs), int(total_tokens), int(H), int(dk), int(dv), 64,
                      float(scale) if scale is not None else 0.0, io, _ALGOS[algo], int(gate),
-                     int(prep))
+                     int(prep), float(gate_scale) if gate_scale is not None else 0.0)
 
 
-def _prep_bits(qk_silu, qk_l2norm, beta_sigmoid):
+def _prep_bits(qk_silu, qk_l2norm, beta_sigmoid, g_softplus=False):
     """KDA_PREP_* bits of the optional input steps (see include/kda.h)."""
     return ((KDA_PREP_QK_SILU if qk_silu else 0) | (KDA_PREP_QK_L2NORM if qk_l2norm else 0)
-            | (KDA_PREP_BETA_SIGMOID if beta_sigmoid else 0))
+            | (KDA_PREP_BETA_SIGMOID if beta_sigmoid else 0)
+            | (KDA_PREP_G_SOFTPLUS if g_softplus else 0))
 
 
 def _gate_of(g, lead, H, dk):
@@ -178,7 +187,8 @@ def kda_chunk_fwd_selected_algo(num_seqs, total_tokens, num_heads, d_k, d_v, io_
 
 def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, final_state=None,
                   output_final_state=True, workspace=None, scale=None, algo="auto", stream=None,
-                  check=False, qk_silu=False, qk_l2norm=False, beta_sigmoid=False):
+                  check=False, qk_silu=False, qk_l2norm=False, beta_sigmoid=False,
+                  g_softplus=False, gate_scale=None):
     """Chunkwise prefill over packed sequences (see include/kda.h).
 
     q, k: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (one dtype: bf16 or fp32, CUDA);
@@ -188,6 +198,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
     final_state may be the init_state tensor itself (in-place update).
     qk_silu, qk_l2norm, beta_sigmoid: the kernels apply silu and then the L2 norm
     to each (token, head) row of q and k, and read beta as logits (KDA_PREP_*).
+    g_softplus: g holds gate logits x and log alpha = -gate_scale * softplus(x)
+    (gate_scale None or <= 0: 1).
     Returns (out, final_state or None).  With check=True the call first reads
     cu_seqlens back and checks it on the host, then synchronises after the launch and
     raises if a kernel recorded a device-side error in the workspace.
@@ -213,21 +225,24 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, out=None, fi
         _check_cu_seqlens(cu_seqlens.cpu(), T)
     if init_state is not None:
         _check_io("init_state", init_state, (N, H, dk, dv), torch.float32, dev)
-    if out is None:
-        out = torch.empty((T, H, dv), dtype=dt, device=dev)
-    _check_io("out", out, (T, H, dv), dt, dev)
-    if final_state is None and output_final_state:
-        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
-    if final_state is not None:
-        _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
     shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], algo, gate,
-                        _prep_bits(qk_silu, qk_l2norm, beta_sigmoid))
+                        _prep_bits(qk_silu, qk_l2norm, beta_sigmoid, g_softplus), gate_scale)
     lib = load_library()
     need = int(lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(shape)))
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-    else:
-        _check_workspace(workspace, dev)
+    # what is allocated here belongs to the stream the kernels run on, so that the
+    # caching allocator does not hand it to other work before they are done with it
+    with torch.cuda.stream(stream):
+        if out is None:
+            out = torch.empty((T, H, dv), dtype=dt, device=dev)
+        if final_state is None and output_final_state:
+            final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        else:
+            _check_workspace(workspace, dev)
+    _check_io("out", out, (T, H, dv), dt, dev)
+    if final_state is not None:
+        _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
     rc = lib.kda_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                            _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
                            _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -249,8 +264,24 @@ def kda_workspace_status(workspace, stream=None) -> int:
     return int(load_library().kda_workspace_status(_ptr(workspace), _stream(stream)))
 
 
+def workspace_status_words(workspace, stream=None):
+    """Synchronises the stream and returns the four status words of a prefill
+    workspace: (first error, detail, tensor-core schedule that ran (1 plain, 2 solve
+    helpers, 0 CUDA-core path), sequence-heads recomputed token by token)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    s.synchronize()
+    w = workspace[:16].cpu().view(torch.int32).tolist()
+    return tuple(int(x) for x in w)
+
+
+def kda_last_device_status(stream=None) -> int:
+    """Synchronises the stream, then returns and clears the first error the
+    kda_recurrent_fwd kernels recorded on the current device (0 or -11)."""
+    return int(load_library().kda_last_device_status(_stream(stream)))
+
+
 def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=None, qk_silu=False,
-                    qk_l2norm=False, beta_sigmoid=False):
+                    qk_l2norm=False, beta_sigmoid=False, g_softplus=False, gate_scale=None):
     """One single-token step for N sequences: q, k [N, H, d_k]; v [N, H, d_v];
     g [N, H, d_k], [N, H] or None (as for kda_chunk_fwd); beta [N, H];
     state fp32 [N, H, d_k, d_v] updated in place.  The input steps as for
@@ -271,10 +302,12 @@ def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=Non
             _check_io(name, t, shp, dt, dev)
     _check_io("state", state, (N, H, dk, dv), torch.float32, dev)
     if out is None:
-        out = torch.empty((N, H, dv), dtype=dt, device=dev)
+        with torch.cuda.stream(stream):  # allocated on the stream the kernel runs on
+            out = torch.empty((N, H, dv), dtype=dt, device=dev)
     _check_io("out", out, (N, H, dv), dt, dev)
     shape = _make_shape(N, N, H, dk, dv, scale, _DTYPES[dt], gate=gate,
-                        prep=_prep_bits(qk_silu, qk_l2norm, beta_sigmoid))
+                        prep=_prep_bits(qk_silu, qk_l2norm, beta_sigmoid, g_softplus),
+                        gate_scale=gate_scale)
     rc = load_library().kda_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                         _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
     if rc != KDA_OK:
@@ -284,7 +317,8 @@ def kda_decode_step(q, k, v, g, beta, state, *, out=None, scale=None, stream=Non
 
 def kda_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, accepted=None, out=None,
                       final_state=None, output=True, output_final_state=True, scale=None,
-                      stream=None, qk_silu=False, qk_l2norm=False, beta_sigmoid=False):
+                      stream=None, qk_silu=False, qk_l2norm=False, beta_sigmoid=False,
+                      g_softplus=False, gate_scale=None):
     """The recurrence token by token over short packed sequences (see include/kda.h):
     the same tensors as kda_chunk_fwd, plus accepted (int32 [N], CUDA, or None): the
     state returned for sequence n is the one after its first accepted[n] tokens.
@@ -312,20 +346,22 @@ def kda_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, *, accepted
         _check_io("accepted", accepted, (N,), torch.int32, dev)
     if init_state is not None:
         _check_io("init_state", init_state, (N, H, dk, dv), torch.float32, dev)
-    if output:
-        if out is None:
-            out = torch.empty((T, H, dv), dtype=dt, device=dev)
-        _check_io("out", out, (T, H, dv), dt, dev)
-    else:
-        out = None
-    if output_final_state:
-        if final_state is None:
-            final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
-        _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
-    else:
-        final_state = None
+    with torch.cuda.stream(stream):  # allocated on the stream the kernel runs on
+        if output:
+            if out is None:
+                out = torch.empty((T, H, dv), dtype=dt, device=dev)
+            _check_io("out", out, (T, H, dv), dt, dev)
+        else:
+            out = None
+        if output_final_state:
+            if final_state is None:
+                final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+            _check_io("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
+        else:
+            final_state = None
     shape = _make_shape(N, T, H, dk, dv, scale, _DTYPES[dt], gate=gate,
-                        prep=_prep_bits(qk_silu, qk_l2norm, beta_sigmoid))
+                        prep=_prep_bits(qk_silu, qk_l2norm, beta_sigmoid, g_softplus),
+                        gate_scale=gate_scale)
     rc = load_library().kda_recurrent_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                           _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
                                           _ptr(accepted), _ptr(out), _ptr(final_state),

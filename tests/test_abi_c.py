@@ -14,8 +14,9 @@ C_SRC = r"""
 #include "kda.h"
 
 int main(void) {
-  kda_shape s = {2, 128, 4, 128, 128, 64, 0.0f, KDA_BF16, KDA_ALGO_AUTO, KDA_GATE_CHANNEL, 0};
-  if (kda_version() < 1002) return 10;
+  kda_shape s = {2, 128, 4, 128, 128, 64, 0.0f, KDA_BF16, KDA_ALGO_AUTO, KDA_GATE_CHANNEL, 0,
+                 0.0f};
+  if (kda_version() < 1004) return 10;
   size_t ws = kda_chunk_fwd_workspace_bytes(&s);
   if (ws < 256) return 11;
   if (kda_chunk_fwd_selected_algo(&s) != KDA_ALGO_TENSOR) return 12;
@@ -25,8 +26,15 @@ int main(void) {
   if (kda_chunk_fwd(&bad, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0) != KDA_ERR_SHAPE) return 14;
   if (kda_chunk_fwd(NULL, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0) != KDA_ERR_NULL) return 15;
   bad = s;
-  bad.prep = 8;
+  bad.prep = 16;
   if (kda_decode_step(&bad, 0, 0, 0, 0, 0, 0, 0, 0) != KDA_ERR_SHAPE) return 16;
+  bad = s;
+  bad.gate_scale = 1.0f / 0.0f;
+  if (kda_chunk_fwd_workspace_bytes(&bad) != 0) return 18;
+  bad = s;
+  bad.prep = KDA_PREP_G_SOFTPLUS;
+  bad.gate_scale = 0.1f;
+  if (kda_chunk_fwd_workspace_bytes(&bad) < 256) return 19;
   if (kda_workspace_status(NULL, 0) != KDA_ERR_NULL) return 17;
   printf("%s\n", kda_status_string(KDA_ERR_GATE_RANGE));
   return 0;

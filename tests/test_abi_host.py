@@ -75,13 +75,16 @@ def test_workspace_size(lib):
 
 
 def test_workspace_holds_the_solve_helper_ring_for_few_sequence_heads(lib):
-    """Tensor-core path with at most 38 sequence-heads: the status block plus a
-    ring of 4 x 16 KiB and 32 bytes per sequence-head; otherwise the status block."""
+    """Tensor-core path: the status block, one recomputation flag word per
+    sequence-head (rounded up to 256 bytes; none without a gate), and with at most 38
+    sequence-heads a ring of 4 x 16 KiB and 32 bytes per sequence-head."""
     ws = lambda **kw: lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(**kw)))
-    assert ws(num_seqs=1, num_heads=1) == 256 + 65568
-    assert ws(num_seqs=19, num_heads=2) == 256 + 38 * 65568
-    assert ws(num_seqs=13, num_heads=3) == 256            # 39 sequence-heads
-    assert ws(num_seqs=1, num_heads=32) == 256 + 32 * 65568
+    assert ws(num_seqs=1, num_heads=1) == 256 + 256 + 65568
+    assert ws(num_seqs=19, num_heads=2) == 256 + 256 + 38 * 65568
+    assert ws(num_seqs=13, num_heads=3) == 256 + 256       # 39 sequence-heads: no ring
+    assert ws(num_seqs=1, num_heads=32) == 256 + 256 + 32 * 65568
+    assert ws(num_seqs=64, num_heads=32) == 256 + 2048 * 4  # flags only
+    assert ws(num_seqs=1, num_heads=1, gate=K.KDA_GATE_NONE) == 256 + 65568  # no decay, no flag
     assert ws(num_seqs=1, num_heads=1, algo=K._ALGOS["simt"]) == 256
     assert ws(num_seqs=1, num_heads=1, io_dtype=K.KDA_F32) == 256  # CUDA-core path
 
@@ -148,14 +151,14 @@ def test_decode_validation(lib):
 
 def test_status_strings(lib):
     seen = set()
-    for code in range(0, -10, -1):
+    for code in range(0, -12, -1):
         s = lib.kda_status_string(code).decode()
         assert s and s != "unknown status"
         seen.add(s)
-    assert len(seen) == 10
+    assert len(seen) == 12
     assert lib.kda_status_string(-99).decode() == "unknown status"
     assert lib.kda_workspace_status(None, None) == -1
-    assert lib.kda_version() >= 1001  # 1.1 added kda_recurrent_fwd
+    assert lib.kda_version() >= 1003  # 1.3 added the device check of the offsets
 
 
 def test_gate_modes_validation(lib):
@@ -184,24 +187,28 @@ def test_gate_modes_validation(lib):
 
 
 def test_prep_bits_validation(lib):
-    """kda_shape.prep takes the three KDA_PREP_* bits in any combination; any other
-    bit is a shape error on every entry point (before the device check, -6 here)."""
-    assert lib.kda_version() >= 1002  # 1.2 added kda_shape.prep
-    assert ctypes.sizeof(K.kda_shape) == 44
+    """kda_shape.prep takes the four KDA_PREP_* bits in any combination; any other
+    bit, or a gate scale that is not finite, is a shape error on every entry point
+    (before the device check, -6 here)."""
+    assert lib.kda_version() >= 1004  # 1.4 added KDA_PREP_G_SOFTPLUS and kda_shape.gate_scale
+    assert ctypes.sizeof(K.kda_shape) == 48
     p = ctypes.c_void_p(FAKE)
-    for bits in range(8):
+    for bits in range(16):
         s = _shape(prep=bits)
         ws = lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(s))
         assert ws >= 256
         assert lib.kda_chunk_fwd(ctypes.byref(s), p, p, p, p, p, None, p, p, p, p, ws, None) == -6
         d = _shape(total_tokens=2, prep=bits)
         assert lib.kda_decode_step(ctypes.byref(d), p, p, p, p, p, p, p, None) == -6
-    for bits in (8, 16, -1):
-        s = _shape(prep=bits)
+    for bad in (dict(prep=16), dict(prep=-1), dict(gate_scale=float("inf")),
+                dict(gate_scale=float("nan"))):
+        s = _shape(**bad)
+        bits = bad.get("prep", 0)
         assert lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(s)) == 0
         assert lib.kda_chunk_fwd(ctypes.byref(s), p, p, p, p, p, None, p, p, p, p, 256, None) == -2
-        d = _shape(total_tokens=2, prep=bits)
+        d = _shape(total_tokens=2, **bad)
         assert lib.kda_decode_step(ctypes.byref(d), p, p, p, p, p, p, p, None) == -2
         assert lib.kda_recurrent_fwd(ctypes.byref(s), p, p, p, p, p, None, p, None, p, None,
                                      None) == -2
     assert K._prep_bits(True, True, True) == 7 and K._prep_bits(False, True, False) == 2
+    assert K._prep_bits(False, False, False, True) == 8

@@ -4,8 +4,9 @@ With at most 38 (sequence, head) pairs and a workspace of
 kda_chunk_fwd_workspace_bytes(), two solve-helper CTAs per pair compute each
 chunk's [T diag(beta); A^qk] ("Kimi Delta Attention (KDA)", the chunkwise
 algorithm's WY / UT-transform step) and hand it to the two d_v-tile CTAs through
-a ring in the workspace.  A 256-byte workspace selects the plain schedule, where
-each d_v tile solves every chunk itself.  Both run the same arithmetic on the
+a ring in the workspace (after the status block and, with a gate, one flag word per
+pair rounded up to 256 bytes).  A 256-byte workspace selects the plain schedule,
+where each d_v tile solves every chunk itself.  Both run the same arithmetic on the
 same operands, so their results must agree bit for bit; the helper schedule is
 also checked against the oracle, and the ring's hand-over counters are read
 back to show that the helpers ran."""
@@ -14,7 +15,7 @@ import pytest
 import torch
 
 from kimi_delta_attention_fwd_gb300 import (kda_chunk_fwd, kda_chunk_fwd_workspace_bytes,
-                                            kda_workspace_status)
+                                            kda_workspace_status, workspace_status_words)
 from kimi_delta_attention_fwd_gb300 import workloads as W
 
 from parity import TOL_BF16, rel_l2_per_head, rel_l2_states, run_oracle_prefill, to_dev
@@ -22,6 +23,7 @@ from parity import TOL_BF16, rel_l2_per_head, rel_l2_states, run_oracle_prefill,
 pytestmark = pytest.mark.gpu
 
 STATUS_BYTES = 256
+FLAG_BYTES = 256  # one flag word per pair (at most 38 here), rounded up to 256 bytes
 SLOTS, SLOT_BYTES = 4, 16384
 MAX_PAIRS = 38
 
@@ -81,13 +83,15 @@ def test_helper_schedule_matches_plain_schedule_and_oracle(lens, H, mode):
     dv = to_dev(x)
     gd = None if g_gpu is None else g_gpu.cuda()
     ws, need = _full_workspace(x, H)
-    assert need == STATUS_BYTES + pairs * SLOTS * (SLOT_BYTES + 8)
+    assert need == STATUS_BYTES + FLAG_BYTES + pairs * SLOTS * (SLOT_BYTES + 8)
     o_h, s_h = _run(dv, gd, ws)
+    assert workspace_status_words(ws)[2] == 2  # the solve-helper schedule ran
     o_p, s_p = _run(dv, gd, torch.empty(STATUS_BYTES, dtype=torch.uint8, device="cuda"))
     torch.cuda.synchronize()
     assert torch.equal(o_h, o_p)
     assert torch.equal(s_h, s_p)
-    words = ws[STATUS_BYTES + pairs * SLOTS * SLOT_BYTES:].cpu().numpy().view(np.uint32)
+    ring = STATUS_BYTES + (FLAG_BYTES if mode != "none" else 0)  # no decay, no flags
+    words = ws[ring + pairs * SLOTS * SLOT_BYTES:][:pairs * SLOTS * 8].cpu().numpy().view(np.uint32)
     np.testing.assert_array_equal(words, _expected_ring_words(lens, H))
     ro, rs = run_oracle_prefill(dict(x, g=g_ref))
     cu = x["cu_seqlens"].numpy()
@@ -134,12 +138,14 @@ def test_helper_schedule_on_concurrent_streams():
 
 def test_more_pairs_than_helpers_use_the_plain_schedule():
     lens = [100] * 13
-    assert kda_chunk_fwd_workspace_bytes(13, 1300, 3, 128, 128) == STATUS_BYTES  # 39 pairs
-    assert kda_chunk_fwd_workspace_bytes(19, 1900, 2, 128, 128) > STATUS_BYTES   # 38 pairs
+    assert kda_chunk_fwd_workspace_bytes(13, 1300, 3, 128, 128) == STATUS_BYTES + FLAG_BYTES  # 39 pairs
+    assert kda_chunk_fwd_workspace_bytes(19, 1900, 2, 128, 128) > STATUS_BYTES + FLAG_BYTES  # 38
     spec = W.custom_prefill(lens, num_heads=3, d=128, gate="mixed", seed=68)
     x = W.prefill_inputs(spec)
     dv = to_dev(x)
-    o, s = _run(dv, dv["g"], torch.empty(STATUS_BYTES, dtype=torch.uint8, device="cuda"))
+    ws = torch.empty(STATUS_BYTES + FLAG_BYTES, dtype=torch.uint8, device="cuda")
+    o, s = _run(dv, dv["g"], ws)
+    assert workspace_status_words(ws)[2] == 1  # plain
     ro, rs = run_oracle_prefill(x)
     assert rel_l2_per_head(o.float().cpu().numpy(), ro, x["cu_seqlens"].numpy()) <= TOL_BF16
     assert rel_l2_states(s.cpu().numpy(), rs) <= TOL_BF16

@@ -164,3 +164,66 @@ def test_input_steps_at_full_size_sampled(name, pairs):
         eo = rel_l2_per_head(out[a:b, h:h + 1].float().cpu().numpy(), ro, [0, b - a])
         es = rel_l2_states(fin[n:n + 1, h:h + 1].cpu().numpy(), rs)
         assert eo <= TOL_BF16 and es <= TOL_BF16, (n, h, eo, es)
+
+
+# ------------------------------------------------------------------ the gate step
+# g holds gate logits x and the kernels take log alpha = -c softplus(x)
+# (KDA_PREP_G_SOFTPLUS, c = gate_scale); the oracle gets oracle.gate_from_logits(x, c)
+# of the same (rounded) logits.
+@pytest.mark.parametrize("recipe", ["std", "mixed"])
+@pytest.mark.parametrize("algo,io,d,tol", [("tensor", "bf16", 128, TOL_BF16),
+                                            ("simt", "bf16", 128, TOL_BF16),
+                                            ("simt", "f32", 64, TOL_F32)])
+def test_prefill_softplus_gate(recipe, algo, io, d, tol):
+    spec = W.custom_prefill(LENS, num_heads=2, d=d, io=io, gate=recipe, seed=63)
+    x = W.prefill_inputs(spec, raw_gate=True)
+    c = W.gate_scale(spec)
+    out, fin = _prefill(x, x["g"], {}, algo=algo, g_softplus=True, gate_scale=c)
+    g_ref = oracle.gate_from_logits(x["g"], c)
+    ro, rs = oracle.kda_fwd(x["q"], x["k"], x["v"], g_ref, x["beta"], x["cu_seqlens"],
+                            x["init_state"])
+    assert rel_l2_per_head(out, ro, x["cu_seqlens"].numpy()) <= tol
+    assert rel_l2_states(fin, rs) <= tol
+
+
+@pytest.mark.parametrize("schedule", ["helper", "plain"])
+def test_tensor_prefill_softplus_gate_all_steps(schedule):
+    """Every input step at once, per-token gate logits too, both schedules."""
+    spec = W.custom_prefill(LENS, num_heads=2, d=128, gate="mixed", seed=64)
+    x = W.prefill_inputs(spec, raw=True, raw_gate=True)
+    ws = None if schedule == "helper" else torch.zeros(512, dtype=torch.uint8, device="cuda")
+    for mode in ("channel", "scalar"):
+        g_gpu, g_logit = _gates(x, mode)
+        out, fin = _prefill(x, g_gpu, dict(ALL, g_softplus=True), algo="tensor", workspace=ws)
+        ro, rs = _oracle_prefill(x, oracle.gate_from_logits(g_logit, 1.0), ALL)
+        assert rel_l2_per_head(out, ro, x["cu_seqlens"].numpy()) <= TOL_BF16
+        assert rel_l2_states(fin, rs) <= TOL_BF16
+
+
+@pytest.mark.parametrize("io,d,tol", [("bf16", 128, TOL_BF16), ("f32", 64, TOL_F32)])
+def test_decode_and_recurrent_softplus_gate(io, d, tol):
+    ds = W.DecodeSpec(5, 2, d, d, 3, io, "std", 65)
+    y = W.decode_inputs(ds, raw_gate=True)
+    c = W.gate_scale(ds)
+    g_ref = oracle.gate_from_logits(y["g"], c)
+    ro, rs = oracle.kda_decode_steps(y["q"], y["k"], y["v"], g_ref, y["beta"], y["state"])
+    st = y["state"].clone().cuda()
+    outs = []
+    for t in range(ds.steps):
+        outs.append(kda_decode_step(y["q"][t].cuda(), y["k"][t].cuda(), y["v"][t].cuda(),
+                                    y["g"][t].cuda(), y["beta"][t].cuda(), st, g_softplus=True,
+                                    gate_scale=c).float().cpu().numpy())
+    np.testing.assert_array_less(
+        np.linalg.norm(np.stack(outs) - ro) / np.linalg.norm(ro), tol)
+    assert rel_l2_states(st.cpu().numpy(), rs) <= tol
+    # the same steps as one recurrent pass per sequence
+    N = ds.num_seqs
+    pack = lambda t: t.transpose(0, 1).reshape(N * ds.steps, *t.shape[2:]).contiguous().cuda()
+    cu = torch.arange(N + 1, dtype=torch.int32, device="cuda") * ds.steps
+    o2, f2 = kda_recurrent_fwd(pack(y["q"]), pack(y["k"]), pack(y["v"]), pack(y["g"]),
+                               pack(y["beta"]), cu, y["state"].cuda(), g_softplus=True,
+                               gate_scale=c)
+    ro_packed = np.swapaxes(ro, 0, 1).reshape(N * ds.steps, 2, d)
+    np.testing.assert_array_less(
+        np.linalg.norm(o2.float().cpu().numpy() - ro_packed) / np.linalg.norm(ro_packed), tol)
+    assert rel_l2_states(f2.cpu().numpy(), rs) <= tol
