@@ -10,37 +10,43 @@
 //   Kb  = diag(beta) K * exp(G)   Qh = Q * exp(G)   Kc = K * exp(-G)   Vb = diag(beta) V
 //   [Kb; Qh] Kc^T              -> rows: A^kk (j < i, beta_i included), A^qk (j <= i)
 //   T   = (I + A^kk)^-1                                (fp32 triangular solve)
-//   [T; A^qk] [Kb | Vb]        -> rows 0-63: W = T Kb, U = T Vb;  rows 64-127: A^qk Vb
-//   [E; X] = [U; A^qk Vb] + [-W; Qh] S                 (state-dependent; E = U - W S)
-//   O / s  = X + A^qk (E - Vb) = Qh S + A^qk E         (state-dependent)
-//   S  <- gamma * S + gamma * (Kc^T (E - Vb) + Kc^T Vb) (state-dependent)
+//   W   = T Kb = (T - I) Kb + Kb                       ([T - I; A^qk] Kb, rows 0-63)
+//   with E = U - W S, U = T Vb and X = Qh S + A^qk Vb, all transposed (d_v rows):
+//   [(E - Vb)^T | X^T] = Vb^T [T - I; A^qk]^T + S^T [-W; Qh]^T
+//   O^T / s            = X^T + (E - Vb)^T A^qk^T       (= (Qh S + A^qk E)^T)
+//   S^T <- (S^T + (E - Vb)^T Kc + Vb^T Kc) Diag(gamma) (= gamma (S + Kc^T E), transposed)
 //
 // The output is the inter-chunk term Qh S plus the masked intra-chunk product
 // A^qk applied to the new values E.  E - Vb is the operand the state side rounds
-// to bf16 for both of its last two products: the A^qk Vb and Kc^T Vb terms it is
-// combined with were formed from Vb itself, so they add back what was
-// subtracted.  E - Vb = (T - I) Vb - W S scales with beta like E does, so its
-// bf16 rounding stays small against E for small write strengths too (E - V would
-// be about -V there, and its rounding large against E).
+// to bf16 for both of its last products: the Vb^T A^qk^T and Vb^T Kc terms it is
+// combined with are formed from Vb itself, so they add back what was subtracted.
+// E - Vb = (T - I) Vb - W S scales with beta like E does, so its bf16 rounding
+// stays small against E for small write strengths too.
+//
+// The state side works on S^T, one d_v row per TMEM lane: S^T in bf16 is the A
+// operand (in tensor memory) of its first product, and each of its products covers
+// the whole d_v = 128 in one M = 128 instruction.  One CTA therefore owns a
+// (sequence, head) and does the state-independent work of each chunk once.
 //
 // exp(G) <= 1 and exp(-G) <= exp(-G_last); every factor stays finite as long
 // as a chunk's total log decay per channel is above -80.  The state side checks
 // it per chunk; a sequence-head that leaves the range is marked in the
 // workspace's per-pair flags, its outputs and final state are left unwritten,
 // and the launcher's next kernel recomputes it token by token with exact decays
-// (without room for the flags the call reports KDA_ERR_GATE_RANGE instead).  The products use bf16 operands with
-// fp32 accumulation in tensor memory; the state, the cumsum and the solve are fp32.
+// (without room for the flags the call reports KDA_ERR_GATE_RANGE instead).  The
+// products use bf16 operands with fp32 accumulation in tensor memory; the state,
+// the cumsum and the solve are fp32.
 //
-// One CTA owns (sequence, head, 64-column d_v tile) and walks its chunks in
-// order.  Warp roles:
+// One CTA walks the chunks of its (sequence, head) in order.  Warp roles:
 //   warps 0-7    K-side: two groups of 4 warps on alternating chunks, everything
-//                that does not depend on S
-//   warps 8-11   S-side: holds S (fp32, one key channel per thread) in registers
-//                and runs the state-dependent products per chunk
-//   warps 12-13  TMA producers, one per stage: the q, g, k and v parts of a stage
-//                are refilled as soon as each is released; warp 12 owns the TMEM
-// With few sequence-heads, two more CTAs per sequence-head run the solve of its
-// chunks for both d_v tiles ("Solve helpers" below).
+//                that does not depend on S; group kw owns stage kw
+//   warps 8-15   state side: S^T (fp32) in registers, thread (d_v row, key-channel
+//                half); the state-dependent products of each chunk
+// The TMA loads that refill a stage are issued by whoever releases each part: a
+// K-side group its g tile (after the solve), the state side its k and q tiles
+// (after its first product has read [-W; Qh]) and its v tile (after its last
+// product).  With few sequence-heads, one or two more CTAs per sequence-head run
+// the solve of its chunks ("Solve helpers" below).
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // KDA_ERR_DEVICE_TIMEOUT in the status word and runs to completion without
 // waiting again (outputs are then undefined, nothing blocks or faults).
@@ -64,25 +70,25 @@ using namespace ptx;
 constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DV = 128;
-constexpr int BV = 64;                      // d_v columns per CTA
-constexpr int kThreads = 448;  // 8 K-side warps, 4 S-side warps, 2 producer warps
+constexpr int kThreads = 512;  // 8 K-side warps, 8 state-side warps
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMinChunkLogDecay = -80.f;
+constexpr float kMinGamma = 1.8e-35f;  // about exp(-80): the state side checks gamma = exp(G_last)
 
-// Solve helpers (few sequence-heads).  With at most 38 (sequence, head) pairs and
+// Solve helpers (few sequence-heads).  With at most 76 (sequence, head) pairs and
 // room for the ring, the launch is cooperative (all CTAs resident) and each pair
-// gets two helper CTAs beside its two d_v tiles: K-side group kw of helper hp
-// solves the chunks c = hp + 2 kw + 4 i (the state-independent [T; A^qk])
-// and hands each to both tiles through a ring in the workspace, slot c % 4
-// holding chunk c's 16 KiB shared-memory image.  Each slot has two words: the
+// gets hpp = 2 (at most 50 pairs) or 1 helper CTAs beside its tile: K-side group kw
+// of helper hp solves the chunks c = hp + hpp kw + 2 hpp i (the state-independent
+// [T - I; A^qk]) and hands each to the tile through a ring in the workspace, slot
+// c % 4 holding chunk c's 16 KiB shared-memory image.  Each slot has two words: the
 // last chunk published + 1 (a release store after the image) and the number of
-// reads so far (a release add by each tile once its copy is in shared memory);
-// a helper overwrites a slot when both tiles have read the chunk four before.
+// reads so far (a release add by the tile once its copy is in shared memory); a
+// helper overwrites a slot when the tile has read the chunk four before.
 // Every wait on these words is bounded.
 constexpr int kRingSlots = 4;
 constexpr uint32_t kRingSlotBytes = 16384;
-constexpr int kHelperMaxPairs = 38;  // 4 CTAs per sequence-head, one per SM, all resident
+constexpr int kHelperMaxPairs = 76;  // (1 + helpers) CTAs per sequence-head, one per SM, all resident
+constexpr int kGl = 3;               // G_last slots: chunk c + 3 reuses chunk c's
 
 // Compact fp32 layout of the 64 x 64 unit-lower-triangular solve (12 KB):
 // the four 16 x 16 diagonal blocks, the sub-diagonal blocks (1,0) and (3,2), and
@@ -95,43 +101,42 @@ __device__ __forceinline__ int sl_idx(int r, int c) { return r * kSlLd + c; }
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 struct L {
-  // stage: [k ch0-63 | q ch0-63] [k ch64-127 | q ch64-127] [g ch0-63] [g ch64-127] [v tile];
-  // the g area later holds the fp32 A^kk / T in the compact solve layout
+  // stage: [k ch0-63 | q ch0-63] [k ch64-127 | q ch64-127] [g ch0-63] [g ch64-127]
+  //        [v ch0-63] [v ch64-127];
+  // the g area later holds the fp32 A^kk / T in the compact solve layout; the k rows
+  // hold Kb, then -W; the q rows Qh ([-W; Qh] is the B operand of the state product)
   static constexpr uint32_t kKQ1 = 16384, kQoff = 8192, kG = 32768, kV = 49152;
-  static constexpr uint32_t kStageBytes = 49152 + C * BV * 2;
+  static constexpr uint32_t kStageBytes = 65536;
   static constexpr uint32_t kKc = 2 * kStageBytes;      // 3 x Kc [ch0-63 | ch64-127], slot = chunk % 3
-  static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [T rows 0-63 | A^qk rows 64-127]
-  static constexpr uint32_t kSb = kTP + 2 * 16384;        // S in bf16 [DK rows][BV]; rows 0-63 then E - Vb
-  static constexpr uint32_t kLtri = kSb + DK * BV * 2;    // bf16 [Ltri; Ltri], 128 x 64
-  static constexpr uint32_t kGlast = kLtri + 16384;       // fp32 G_last [3][128] (2 slots used unfed)
-  static constexpr uint32_t kBars = kGlast + 1536;        // mbarriers
-  static constexpr uint32_t kMisc = kBars + 272;          // tmem slot, abort flag
+  static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [T - I rows 0-63 | A^qk rows 64-127]
+  static constexpr uint32_t kEVt = kTP + 2 * 16384;       // (E - Vb)^T: 128 d_v rows x 64 tokens, bf16
+  static constexpr uint32_t kGlast = kEVt + 16384;        // fp32 G_last [kGl][128]
+  static constexpr uint32_t kBars = kGlast + kGl * 512;   // mbarriers
+  static constexpr uint32_t kMisc = kBars + 256;          // tmem slot, abort / skip flags, issued loads
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
-static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kSb % 1024 == 0 &&
-                  L::kLtri % 1024 == 0,
+static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kEVt % 1024 == 0,
               "operand tiles must be 1024-byte aligned");
 static_assert(L::kAlloc <= 232448, "shared memory budget");
 
-// mbarrier slots (count 1 each; [s] = stage / K-side group, [b] = Kc slot)
+// mbarrier slots (count 1 each; [s] = stage / K-side group, [b] = Kc / G_last slot)
 enum : uint32_t {
-  kFullQ0 = 0, kFullG0 = 2, kFullK0 = 4, kFullV0 = 6,        // part of stage s loaded
-  kEmptyQ0 = 8, kEmptyG0 = 10, kEmptyK0 = 12, kEmptyV0 = 14,  // part of stage s released
-  kReady0 = 16,   // K-side -> S-side: the chunk's state-independent operands are complete
-  kSDone0 = 18,   // S-side -> K-side: Aop[s] and ACC[s] have been read
-  kGmRead0 = 20,  // S-side -> K-side: G_last[b] has been read (up to 3 slots)
-  kKcFree0 = 23,  // S-side -> K-side: Kc[b] (and TP of that chunk) read (3 slots)
-  kMmaK0 = 26, kMmaS = 28, kFinK0 = 29, kFinS = 31, kNever = 32, kNumBars = 33
+  kFullQ0 = 0, kFullG0 = 2, kFullK0 = 4, kFullV0 = 6,  // part of stage s loaded
+  kReady0 = 8,     // K-side -> state side: the chunk's state-independent operands are complete
+  kGmRead0 = 10,   // state side -> K-side: G_last[b] has been read (3 slots)
+  kKcFree0 = 13,   // state side -> K-side: Kc[b] and TP of that chunk read (3 slots)
+  kMmaK0 = 16, kMmaS = 18, kFinK0 = 19, kFinS = 21, kNever = 22, kNumBars = 23
 };
-static_assert(kNumBars * 8 <= 272, "mbarrier area");
+static_assert(kNumBars * 8 <= 256, "mbarrier area");
 
 // TMEM columns
-//   [128 kw, +128)   K-side group kw: G, then D1 (+0), then D2
-//   [256 + 64 s, +64) Aop[s]: the A operand [-W; Qh] of the state product (bf16
-//                    pairs), then D4 = Kc^T E (fp32)
-//   [384 + 64 s, +64) ACC[s]: [U; A^qk V], then [E; X], then [.; O / s]
-constexpr uint32_t kAop0 = 256, kAcc0 = 384;
+//   [128 kw, +128)  K-side group kw: G, then D1 (+0), then D2 (-W before the epilogue)
+//   [256, 320)      S^T in bf16 pairs: the A operand of the state product
+//   [320, 448)      [(E - Vb)^T | X^T], then [. | O^T / s]
+//   [256, 384)      (Kc^T E)^T: over S^T and the first half of the above, once both are read
+//   [448, 480)      [Ltri; Ltri] in bf16 pairs: the A operand of the cumsum product
+constexpr uint32_t kRA = 256, kRD1 = 320, kRD4 = 256, kRLtri = 448;
 
 struct TcParams {
   const __nv_bfloat16 *beta;
@@ -140,6 +145,7 @@ struct TcParams {
   int prep;                    // KDA_PREP_* bits: silu / L2 norm of q and k, sigmoid of beta,
                                // softplus of the gate
   float gate_scale;            // c of log alpha = -c softplus(x)
+  int helpers_per_pair;        // 1 or 2 (solve-helper schedule)
   const float *init_state;
   const int32_t *cu_seqlens;
   __nv_bfloat16 *out;
@@ -291,10 +297,10 @@ __device__ __forceinline__ void row_sumsq32x2(uint32_t tk, uint32_t tq, int rbas
   ssq = out[1];
 }
 
-// kSched = false: every CTA is a d_v tile that solves its own chunks (the plain
-// schedule); true: CTAs 2 P .. 4 P - 1 are solve helpers for the first 2 P.
-// kPrep: the input steps of TcParams::prep are compiled in (a call without them runs
-// the instantiation that has none of their code).
+// kSched = false: every CTA is a (sequence, head) tile that solves its own chunks
+// (the plain schedule); true: CTAs P .. (1 + hpp) P - 1 are solve helpers for the
+// first P.  kPrep: the input steps of TcParams::prep are compiled in (a call without
+// them runs the instantiation that has none of their code).
 template <bool kSched, bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -310,25 +316,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
   // set by the state side once this pair's decay has left the range: nothing more is stored
   volatile int *skip_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
+  // the last chunk loaded into each stage part [stage][q, g, k, v] (-1: none), for the drain
+  volatile int *issued = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  constexpr int kTiles = DV / BV;
-  // roles: a d_v-tile CTA (pair, tile) runs everything, or with helpers takes each
-  // chunk's [T; A^qk] from the ring; a helper (pair, parity hp) runs the chunk
-  // solve of the chunks c = hp mod 2 and publishes it
-  const bool helper = kSched && (int)blockIdx.x >= 2 * p.npairs;
+  // roles: a tile CTA (one per pair) runs everything, or with helpers takes each chunk's
+  // [T - I; A^qk] from the ring; a helper (pair, hp) runs the chunk solve of the chunks
+  // c = hp + hpp kw + 2 hpp i of its K-side group kw and publishes it
+  const int P = p.npairs;
+  const bool helper = kSched && (int)blockIdx.x >= P;
   const bool fed = kSched && !helper;
-  const int hb = (int)blockIdx.x - 2 * p.npairs;
-  const int hp = helper ? (hb & 1) : 0;
-  const int tile = helper ? 0 : (int)blockIdx.x % kTiles;
-  const int pair = helper ? (hb >> 1) : (int)blockIdx.x / kTiles;
-  // the chunks a stage / K-side group takes: c = c_first + i * c_step, phase i & 1
-  const int c_step = helper ? 4 : 2;
-  const int c_shift = helper ? 2 : 1;
-  // G_last slots: with helpers the tiles run ahead of the state side, so a third slot
-  // lets a tile's gate wait for the state side of chunk c - 3 instead of c - 2
-  constexpr int kGl = kSched ? 3 : 2;
+  const int hpp = kSched ? p.helpers_per_pair : 1;
+  const int hb = (int)blockIdx.x - P;
+  const int hp = helper ? hb % hpp : 0;
+  const int pair = helper ? hb / hpp : (int)blockIdx.x;
+  // the chunks a stage / K-side group kw takes: c = c_first(kw) + i * c_step, phase i & 1
+  const int c_step = helper ? 2 * hpp : 2;
+  const int c_shift = helper && hpp == 2 ? 2 : 1;
   uint32_t *rflags = kSched ? p.ring_flags + (size_t)pair * kRingSlots * 2 : nullptr;
   uint8_t *rdata = kSched ? p.ring + (size_t)pair * kRingSlots * kRingSlotBytes : nullptr;
   const int H = p.H;
@@ -342,113 +347,108 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   Ctx ctx{sbase + L::kBars, abort_flag, p.status};
 
+  // TMA loads of the stage parts of chunk c (stage s), each completing on its full barrier
+  auto stage_at = [&](int st_idx) { return sbase + st_idx * L::kStageBytes; };
+  auto load_q = [&](int sidx, int c) {
+    const uint32_t fb = ctx.bar(kFullQ0 + sidx), st = stage_at(sidx);
+    mbar_arrive_expect_tx(fb, 16384);
+    tma_load_3d(st + L::kQoff, &tm_q, fb, 0, h, bos + c * C);
+    tma_load_3d(st + L::kKQ1 + L::kQoff, &tm_q, fb, 64, h, bos + c * C);
+    issued[4 * sidx + 0] = c;
+  };
+  auto load_g = [&](int sidx, int c) {
+    const uint32_t fb = ctx.bar(kFullG0 + sidx), st = stage_at(sidx);
+    if (p.gate == 0) {
+      mbar_arrive_expect_tx(fb, 16384);
+      tma_load_3d(st + L::kG, &tm_g, fb, 0, h, bos + c * C);
+      tma_load_3d(st + L::kG + 8192, &tm_g, fb, 64, h, bos + c * C);
+    } else {
+      mbar_arrive(fb);  // no g tile: the part's phase still completes
+    }
+    issued[4 * sidx + 1] = c;
+  };
+  auto load_k = [&](int sidx, int c) {
+    const uint32_t fb = ctx.bar(kFullK0 + sidx), st = stage_at(sidx);
+    mbar_arrive_expect_tx(fb, 16384);
+    tma_load_3d(st, &tm_k, fb, 0, h, bos + c * C);
+    tma_load_3d(st + L::kKQ1, &tm_k, fb, 64, h, bos + c * C);
+    issued[4 * sidx + 2] = c;
+  };
+  auto load_v = [&](int sidx, int c) {
+    const uint32_t fb = ctx.bar(kFullV0 + sidx), st = stage_at(sidx);
+    mbar_arrive_expect_tx(fb, 16384);
+    tma_load_3d(st + L::kV, &tm_v, fb, 0, h, bos + c * C);
+    tma_load_3d(st + L::kV + 8192, &tm_v, fb, 64, h, bos + c * C);
+    issued[4 * sidx + 3] = c;
+  };
+
   if (tid == 0) {
     *abort_flag = 0;
     *skip_flag = seq_ok ? 0 : 1;
+    for (int i = 0; i < 8; ++i) issued[i] = -1;
     if (!seq_ok) atomicCAS(p.status, 0u, kStatusSeqlens);
     for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(ctx.bar(i), 1);
     fence_mbar_init();
     if (blockIdx.x == 0) p.status[2] = kSched ? kSchedHelpers : kSchedPlain;  // which schedule ran
   }
-  if (warp == 12) {
+  if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  // constant A operand of the cumsum product: [Ltri; Ltri], Ltri[r][u] = (u <= r), bf16
-  for (int idx = tid; idx < 128 * 8; idx += kThreads) {
-    const int r = idx >> 3, ch = idx & 7, r64 = r & 63;
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int lo = 8 * ch + 2 * i;
-      w[i] = (lo <= r64 ? 0x3F80u : 0u) | ((lo + 1 <= r64 ? 0x3F80u : 0u) << 16);
-    }
-    st_shared_v4(sbase + L::kLtri + sw128(r, ch), w[0], w[1], w[2], w[3]);
-  }
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp >= 12) {
-    // ------------------------------------------------------------ producers
-    // warp 12 fills stage 0 (even chunks), warp 13 stage 1 (odd chunks).  The parts
-    // of a stage are released at different points of the chunk (g after the solve,
-    // or after the gate in a tile fed by helpers; q after the state-product operand
-    // has been copied out; k after the W / U product; v after the state side's last
-    // product) and each is refilled for chunk c + 2 in that order, so the g tile the
-    // next cumsum product reads is in flight while the chunk's W / U product runs.
-    // In a helper, stage s holds the chunks hp + 2 s + 4 i and no v; q and k are
-    // released after [Kb; Qh] Kc^T, g after the solve, and are refilled in that order.
-    if ((tid & 31) == 0) {
-      const int s = warp - 12;
-      if (s == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_g);
-        tma_prefetch_desc(&tm_v);
-      }
-      const uint32_t st = sbase + s * L::kStageBytes;
-      int last[4] = {-1, -1, -1, -1};  // last chunk loaded, per part
-      const int c_first = helper ? hp + 2 * s : s;
-      const int nparts = helper ? 3 : 4;  // a helper reads no v
-      for (int c = c_first; c < nchunks && !*abort_flag; c += c_step) {
-        const int it = c >> c_shift;
-        const uint32_t prev = (it - 1) & 1;
-        const int t0 = bos + c * C;
-#pragma unroll 1
-        for (int pi = 0; pi < nparts; ++pi) {
-          // part 0 q, 1 g, 2 k, 3 v; loaded in the order they are released
-          const int part = helper ? (pi == 0 ? 0 : pi == 1 ? 2 : 1) : (pi == 0 ? 1 : pi == 1 ? 0 : pi);
-          if (it >= 1) ctx.wait(kEmptyQ0 + 2 * part + s, prev);
-          if (*abort_flag) break;
-          const uint32_t fb = ctx.bar(kFullQ0 + 2 * part + s);
-          if (part == 0) {
-            mbar_arrive_expect_tx(fb, 16384);
-            tma_load_3d(st + L::kQoff, &tm_q, fb, 0, h, t0);
-            tma_load_3d(st + L::kKQ1 + L::kQoff, &tm_q, fb, 64, h, t0);
-          } else if (part == 1) {
-            if (p.gate == 0) {
-              mbar_arrive_expect_tx(fb, 16384);
-              tma_load_3d(st + L::kG, &tm_g, fb, 0, h, t0);
-              tma_load_3d(st + L::kG + 8192, &tm_g, fb, 64, h, t0);
-            } else {
-              mbar_arrive(fb);  // no g tile: the part's phase still completes
-            }
-          } else if (part == 2) {
-            mbar_arrive_expect_tx(fb, 16384);
-            tma_load_3d(st, &tm_k, fb, 0, h, t0);
-            tma_load_3d(st + L::kKQ1, &tm_k, fb, 64, h, t0);
-          } else {
-            mbar_arrive_expect_tx(fb, C * BV * 2);
-            tma_load_3d(st + L::kV, &tm_v, fb, tile * BV, h, t0);
-          }
-          last[part] = c;
-        }
-      }
-      // never leave a copy in flight: wait (bounded) for the last load of every part
-      for (int part = 0; part < 4; ++part)
-        if (last[part] >= 0)
-          mbar_wait(ctx.bar(kFullQ0 + 2 * part + s), (last[part] >> c_shift) & 1, kWaitCycles);
+  if (warp < 4) {
+    // the cumsum product's constant A operand [Ltri; Ltri] (Ltri[r][u] = (u <= r)) in
+    // tensor memory, bf16 pairs: lane m holds row m mod 64
+    const int r = tid & 63;
+    uint32_t w[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      w[j] = (2 * j <= r ? 0x3F80u : 0u) | ((2 * j + 1 <= r ? 0x3F80u : 0u) << 16);
+    tmem_st32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kRLtri, w);
+  } else if (tid == 128 || tid == 160) {
+    // the first chunk of each stage, loaded by one thread per stage
+    const int sidx = tid == 128 ? 0 : 1;
+    if (sidx == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_g);
+      tma_prefetch_desc(&tm_v);
     }
-  } else if (warp < 8) {
+    const int c0 = helper ? hp + hpp * sidx : sidx;
+    if (c0 < nchunks) {
+      load_g(sidx, c0);
+      load_k(sidx, c0);
+      load_q(sidx, c0);
+      if (!helper) load_v(sidx, c0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // Register split: the state side holds 64 fp32 state values per thread.  The launch
+  // gives every thread 128 registers (512 x 128 = 65,536); the K-side warpgroups hand
+  // 24 each back and the state side takes them: 256 x 104 + 256 x 152 = 65,536.
+  if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     // ------------------------------------------------------------ K-side
     // Two groups of 4 warps; group kw takes the chunks c = kw, kw + 2, ... and
-    // owns stage kw, TP[kw], Aop[kw], ACC[kw] and TMEM columns
-    // [128 kw, 128 kw + 128), so the dependent chain of one chunk overlaps the
-    // other group's chunk.  Kc rotates over three slots (chunk % 3).
-    // A helper's groups take c = hp + 2 kw + 4 i, run the gate, a2 and the solve, and
-    // publish [T; A^qk]; a tile fed by helpers runs the gate and takes [T; A^qk]
-    // from the ring in place of a2 and the solve.
+    // owns stage kw, TP[kw] and TMEM columns [128 kw, 128 kw + 128), so the
+    // dependent chain of one chunk overlaps the other group's chunk.  Kc rotates
+    // over three slots (chunk % 3).
+    // A helper's groups take c = hp + hpp kw + 2 hpp i, run the gate, a2 and the solve,
+    // and publish [T - I; A^qk]; a tile fed by helpers runs the gate and takes
+    // [T - I; A^qk] from the ring in place of a2 and the solve.
     const int kw = warp >> 2;
     const int t = tid & 127;            // thread within the group
     const int wq = warp & 3;            // TMEM lane quarter of this warp
     const int row = 32 * wq + (t & 31); // TMEM lane = row of an M = 128 result (== t)
     const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t bar_id = kw ? 3u : 1u;
-    const uint32_t tm = tmem + 128u * kw;          // G, then D1 (+0), then D2
-    const uint32_t aop = tmem + kAop0 + 64u * kw;  // [-W; Qh] for the state product
+    const uint32_t tm = tmem + 128u * kw;  // G, then D1 (+0), then D2
     const uint32_t st = sbase + kw * L::kStageBytes;
     const uint32_t tp = sbase + L::kTP + kw * 16384;
     // compact fp32 solve layout in the stage's g area (after the cumsum product has read g)
@@ -461,16 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // g holds gate logits: each group turns its g tile into -c softplus(g) in place before
     // the cumsum product, which is then issued at the top of the chunk (not ahead)
     const bool gsp = kPrep && chan && (p.prep & kPrepGSoftplus);
-    // a1: G = [Ltri; Ltri] g on the tensor cores, straight from the TMA'd g tile:
-    // the chunk-local inclusive cumsum per channel (rows 64-127 repeat rows 0-63)
+    // a1: G = [Ltri; Ltri] g on the tensor cores, straight from the TMA'd g tile with
+    // the constant operand in tensor memory: the chunk-local inclusive cumsum per
+    // channel (rows 64-127 repeat rows 0-63)
     auto issue_cumsum = [&]() {
       tc_fence_after();
       constexpr uint32_t id = idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
-        const uint64_t ad = sdesc_sw128(sbase + L::kLtri + k4 * 32, 16, 1024);
         const uint64_t bd = sdesc_sw128(st + L::kG + k4 * 2048, 8192, 1024);
-        mma_bf16(tm, ad, bd, id, k4 > 0);
+        mma_bf16_tmem_a(tm, tmem + kRLtri + 8u * k4, bd, id, k4 > 0);
       }
       mma_commit(mma_bar);
     };
@@ -482,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     uint32_t kph = 0;
-    // chunks of this group: c = kw, kw + 2, ...; in a helper c = hp + 2 kw + 4 i
-    for (int c = helper ? hp + 2 * kw : kw; c < nchunks; c += c_step) {
+    // chunks of this group: c = kw, kw + 2, ...; in a helper c = hp + hpp kw + 2 hpp i
+    for (int c = helper ? hp + hpp * kw : kw; c < nchunks; c += c_step) {
       const int s = kw;
       const int t0 = bos + c * C;
       const int len = min(C, eos - t0);
@@ -499,7 +499,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                              ? fast_rcp(1.f + fast_exp2(-kLog2e * braw)) : braw;
       // one thread polls the mbarriers, the others park on the named barrier
       const int it = c >> c_shift;                // this group's it-th chunk
-      const uint32_t prev = (it - 1) & 1;         // parity of the group's previous release signals
       const uint32_t cur = it & 1;                // parity of this chunk's loads
       // a1 with one log alpha per (token, head): G_r is one inclusive scan over the
       // chunk's rows (rows r and 32 + r of two per-warp scans), the same for every channel
@@ -639,11 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) G[j] = g_row;
         }
-        if (r == len - 1) {  // the chunk's last valid row: G_last for the state side
+        if (r == len - 1) {  // the chunk's last valid row: gamma = exp(G_last) for the state side
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4 *>(glast + (c % kGl) * 128 + 64 * half + 32 * hh + j) =
-                make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
+                make_float4(fast_exp2(G[j] * kLog2e), fast_exp2(G[j + 1] * kLog2e),
+                            fast_exp2(G[j + 2] * kLog2e), fast_exp2(G[j + 3] * kLog2e));
         }
         // bf16 pairs: exp(+-G) (and beta exp(G) for Kb) rounded to bf16, then one bf16
         // product per output pair.  With one G per row (a per-token gate, or none) the
@@ -700,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // above): it is read into registers while TP[s] is still being read by chunk
         // c - 2's output product, then stored there.  The read is counted while the
         // W / U product runs.
-        if (t == 0) mbar_arrive(ctx.bar(kEmptyG0 + s));  // g was read by the cumsum product only
+        if (t == 0 && c + 2 < nchunks && !*abort_flag) load_g(s, c + 2);  // g was read by the cumsum product only
         const uint4 *src = reinterpret_cast<const uint4 *>(rdata + slot * kRingSlotBytes);
         uint4 w[8];
 #pragma unroll
@@ -722,9 +722,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(mma_bar);
           ctx.wait(kMmaK0 + kw, kph & 1);
-          if (helper) {  // Kb and Qh are read by a2 only in a helper
-            mbar_arrive(ctx.bar(kEmptyQ0 + s));
-            mbar_arrive(ctx.bar(kEmptyK0 + s));
+          if (helper) {  // Kb and Qh are read by a2 only in a helper: the next chunk's k and q
+            if (c + c_step < nchunks && !*abort_flag) {
+              load_k(s, c + c_step);
+              load_q(s, c + c_step);
+            }
           } else if (c >= 2) {
             // TP[s] was last read by chunk c - 2's output product, committed with its Kc release
             ctx.wait(kKcFree0 + (c - 2) % 3, ((c - 2) / 3) & 1);
@@ -897,8 +899,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         bar_sync(bar_id, 128);
-        {  // T -> TP rows 0-63 (bf16), 32 columns per thread; rows 32-63, columns 0-31
-           // come from the fragments above
+        {  // T - I -> TP rows 0-63 (bf16), 32 columns per thread; rows 32-63, columns 0-31
+           // come from the fragments above.  T - I is the operand both products need:
+           // W = (T - I) Kb + Kb, and (T - I) Vb = U - Vb on the state side
           const int i = t & 63, hh = t >> 6, I = i >> 4, il = i & 15;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -917,6 +920,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) tv[jj] = 0.f;
             }
+            if (J == I) {  // the unit diagonal
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj)
+                if (jl + jj == il) tv[jj] -= 1.f;
+            }
             st8(tp + sw128(i, 4 * hh + q), tv);  // T is exactly lower triangular
           }
           uint8_t *tpg = smem + L::kTP + kw * 16384;
@@ -931,12 +939,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         if (helper) {
-          // publish: once both d_v tiles have read chunk c - 4 out of the slot, copy
-          // TP (16 KiB, the shared-memory image) there and release chunk c + 1
+          // publish: once the tile has read chunk c - 4 out of the slot, copy TP (16 KiB,
+          // the shared-memory image) there and release chunk c + 1
+          fence_async_smem();  // the solve scratch in the g area is rewritten by the next load
           bar_sync(bar_id, 128);
           if (t == 0) {
-            mbar_arrive(ctx.bar(kEmptyG0 + s));  // the solve scratch is no longer read
-            ctx.wait_global(rflags + 2 * slot + 1, static_cast<uint32_t>(2 * (c >> 2)));
+            if (c + c_step < nchunks && !*abort_flag) load_g(s, c + c_step);
+            ctx.wait_global(rflags + 2 * slot + 1, static_cast<uint32_t>(c >> 2));
           }
           bar_sync(bar_id, 128);
           uint4 *dst = reinterpret_cast<uint4 *>(rdata + slot * kRingSlotBytes);
@@ -955,77 +964,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }  // !fed
 
-      // Vb = diag(beta) V in place, each thread its part (row t mod 64, half t / 64 of
-      // its columns) once the v tile has landed; one barrier covers it and the waits
+      // Vb = diag(beta) V in place once the v tile has landed: thread t scales the
+      // d_v half t / 64 of row t mod 64, whose beta it holds
       ctx.wait(kFullV0 + s, cur);
       {
         const uint32_t fb = pack_bf16x2(brow, brow);
+        const uint32_t vrow = st + L::kV + (t >> 6) * 8192;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t addr = st + L::kV + sw128(rb, 4 * (t >> 6) + q);
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t addr = vrow + sw128(rb, q);
           const uint4 w = ld_shared_v4(addr);
           st_shared_v4(addr, mul_bf16x2(w.x, fb), mul_bf16x2(w.y, fb), mul_bf16x2(w.z, fb),
                        mul_bf16x2(w.w, fb));
         }
       }
-      fence_async_smem();
-      if (t == 0 && c >= 2) ctx.wait(kSDone0 + s, prev);  // chunk c - 2 is done with Aop[s] and ACC[s]
+      fence_async_smem();  // also orders the solve's scratch writes before the g reload
       bar_sync(bar_id, 128);
-      if (t == 0 && !fed) mbar_arrive(ctx.bar(kEmptyG0 + s));  // the g area (solve scratch) may be refilled
+      // the g area (solve scratch) is free: the group's next chunk's g tile
+      if (t == 0 && !fed && c + 2 < nchunks && !*abort_flag) load_g(s, c + 2);
 
-      // [T; A^qk] [Kb | Vb] -> D2 (rows 0-63: W) and ACC[s] (U | A^qk Vb)
+      // [T - I; A^qk] Kb -> D2, rows 0-63: W - Kb = (T - I) Kb
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
-        constexpr uint32_t id_v = idesc_bf16(128, BV, false, true);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
           const uint64_t bk = sdesc_sw128(st + k4 * 2048, L::kKQ1, 1024);
-          const uint64_t bv = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
           mma_bf16(tm, ad, bk, id_k, k4 > 0);
-          mma_bf16(tmem + kAcc0 + s * BV, ad, bv, id_v, k4 > 0);
         }
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
-        mbar_arrive(ctx.bar(kEmptyK0 + s));  // Kb (the k area) is no longer read
       } else if (fed && t == 32) {
         // every thread's ring loads have completed (their values are in TP[s]): count
         // the read (a gpu-scope release, kept off the issuing thread)
         red_release_gpu_add(rflags + 2 * slot + 1, 1u);
-      } else if (row >= 64) {
-        // while that runs, rows 64-127 copy Qh (bf16 pairs, all 128 channels of token
-        // row - 64) into Aop[s]: the lower half of the state product's A operand
-        const int i = row - 64;
-        const uint32_t rx = static_cast<uint32_t>(i & 7);
-#pragma unroll 1
-        for (int hq = 0; hq < 2; ++hq) {
-          const uint32_t base = st + hq * L::kKQ1 + L::kQoff + i * 128;
-          uint32_t pk[32];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 w = ld_shared_v4(base + ((static_cast<uint32_t>(q) ^ rx) << 4));
-            pk[4 * q] = w.x; pk[4 * q + 1] = w.y; pk[4 * q + 2] = w.z; pk[4 * q + 3] = w.w;
-          }
-          tmem_st32(aop + lane_base + 32 * hq, pk);
-        }
-        tc_fence_before();
       }
       ++kph;
       bar_sync(bar_id, 128);
-      if (t == 0) mbar_arrive(ctx.bar(kEmptyQ0 + s));  // the q area has been read by a2 and the copy
       tc_fence_after();
-      if (row < 64) {  // -W (bf16 pairs) -> Aop[s] rows 0-63, from the fp32 W rows of D2
+      if (row < 64) {
+        // -W = -((T - I) Kb + Kb), bf16, over the row's Kb: rows 0-63 of the state
+        // product's B operand [-W; Qh] (its rows 64-127 are Qh in the q area)
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {  // channels 64 hh .. 64 hh + 63
           float a[64];
           tmem_ld64(tm + lane_base + 64 * hh, a);
-          uint32_t pk[32];
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16x2(-a[2 * jj], -a[2 * jj + 1]);
-          tmem_st32(aop + lane_base + 32 * hh, pk);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t addr = st + hh * L::kKQ1 + sw128(row, j);
+            float kbv[8];
+            unpack8(ld_shared_v4(addr), kbv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kbv[e] = -(a[8 * j + e] + kbv[e]);
+            st8(addr, kbv);
+          }
         }
       }
+      fence_async_smem();
       tc_fence_before();
       bar_sync(bar_id, 128);
       if (t == 0) {
@@ -1041,166 +1037,198 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(ctx.bar(kFinK0 + kw), 0, kWaitCycles);
     }
   } else if (!helper) {
-    // ------------------------------------------------------------ S-side
-    const int t = tid - 256;  // key channel of the state row this thread holds
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp - 8)) << 16;
-    const size_t soff = (size_t)pair * DK * DV + (size_t)t * DV + tile * BV;
-    float S[BV];
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;" ::: "memory");
+    // ------------------------------------------------------------ state side
+    // Thread (d_v row v = 32 (warp % 4) + lane, key-channel half hs = (warp - 8) / 4)
+    // holds S[64 hs + j][v], j = 0..63, in fp32: column v of the state, which is row v
+    // of S^T and TMEM lane v of every state-side product.
+    const int st_id = tid - 256;
+    const int qd = warp & 3, hs = (warp - 8) >> 2;
+    const int v = 32 * qd + (tid & 31);
+    const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+    const size_t soff = (size_t)pair * DK * DV + (size_t)(64 * hs) * DV + v;
+    float S[64];
     if (p.init_state) {
 #pragma unroll
-      for (int j = 0; j < BV; j += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(p.init_state + soff + j);
-        S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
-      }
+      for (int j = 0; j < 64; ++j) S[j] = p.init_state[soff + (size_t)j * DV];
     } else {
 #pragma unroll
-      for (int j = 0; j < BV; ++j) S[j] = 0.f;
+      for (int j = 0; j < 64; ++j) S[j] = 0.f;
     }
     uint32_t sph = 0;
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1;
       const int t0 = bos + c * C;
       const int len = min(C, eos - t0);
-      const int kb = c % 3;
+      const int kb = c % 3, gb = c % kGl;
       const uint32_t st = sbase + s * L::kStageBytes;
+      const uint32_t tps = sbase + L::kTP + s * 16384;
+      const uint32_t kcb = sbase + L::kKc + kb * 16384;
+      // S^T in bf16 pairs -> columns [kRA + 32 hs, +32) of lane v: the state product's A operand
 #pragma unroll
-      for (int q = 0; q < BV / 8; ++q) {
-        float v[8];
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) v[jj] = S[8 * q + jj];
-        st8(sbase + L::kSb + sw128(t, q), v);
+        for (int jj = 0; jj < 16; ++jj) pk[jj] = pack_bf16x2(S[32 * hh + 2 * jj], S[32 * hh + 2 * jj + 1]);
+        tmem_st16(tmem + lane_base + kRA + 32 * hs + 16 * hh, pk);
       }
-      fence_async_smem();
       tc_fence_before();
-      bar_sync(2, 128);
-      if (t == 0) {
-        // the previous chunk's outputs and state update have been read out of TMEM
-        if (c >= 1) mbar_arrive(ctx.bar(kSDone0 + (s ^ 1)));
+      bar_sync(2, 256);
+      if (st_id == 0) {
         ctx.wait(kReady0 + s, (c >> 1) & 1);
-      }
-      bar_sync(2, 128);
-      tc_fence_after();
-      // gamma = exp(G_last) of this thread's key channel.  A chunk whose total log decay
-      // is beyond the range the factors exp(+-G) are formed in marks the pair for the
-      // exact recomputation (or is reported without the flags): from here on this CTA
-      // stores nothing for it; the pipeline itself runs on unchanged
-      const float gl = glast[(c % kGl) * 128 + t];
-      const float gm = fast_exp2(gl * kLog2e);
-      if (!(gl >= kMinChunkLogDecay) && !*skip_flag) {
-        *skip_flag = 1;
-        if (p.pair_flags) {
-          if (atomicExch(p.pair_flags + pair, 1u) == 0u) atomicAdd(p.status + 3, 1u);
-        } else {
-          atomicCAS(p.status, 0u, kStatusGateRange);
+        tc_fence_after();
+        // [(E - Vb)^T | X^T] = Vb^T [T - I; A^qk]^T + S^T [-W; Qh]^T, one commit
+        constexpr uint32_t id_init = idesc_bf16(128, 128, true, false);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint64_t av = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);  // Vb^T (MN-major)
+          const uint64_t bt = sdesc_sw128(tps + k4 * 32, 16, 1024);            // [T - I; A^qk] rows
+          mma_bf16(tmem + kRD1, av, bt, id_init, k4 > 0);
         }
-      }
-      // a4/a5: [E; X] = [U; A^qk V] + [-W; Qh] S, the A operand from Aop[s] in TMEM
-      if (t == 0) {
-        constexpr uint32_t id = idesc_bf16(128, BV, false, true);
+        constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8) {
-          const uint64_t bd = sdesc_sw128(sbase + L::kSb + k8 * 2048, 8192, 1024);
-          mma_bf16_tmem_a(tmem + kAcc0 + s * BV, tmem + kAop0 + 64u * s + 8 * k8, bd, id, 1);
+          const uint64_t bw = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);  // [-W; Qh]
+          mma_bf16_tmem_a(tmem + kRD1, tmem + kRA + 8u * k8, bw, id_s, 1);
         }
         mma_commit(ctx.bar(kMmaS));
-      }
-      bar_sync(2, 128);  // while the product runs: every thread has read G_last[c % kGl]
-      if (t == 0) {
-        mbar_arrive(ctx.bar(kGmRead0 + c % kGl));
         ctx.wait(kMmaS, sph & 1);
+        // the stage's k and q tiles ([-W; Qh]) have been read: the group's next chunk's
+        if (c + 2 < nchunks && !*abort_flag) {
+          load_k(s, c + 2);
+          load_q(s, c + 2);
+        }
       }
       ++sph;
-      bar_sync(2, 128);
+      bar_sync(2, 256);
       tc_fence_after();
-      if (t < 64) {  // E - Vb (rows 0-63) -> bf16 over the first half of Sb
-#pragma unroll
-        for (int hh = 0; hh < BV / 32; ++hh) {
-          float a[32];
-          tmem_ld32(tmem + lane_base + kAcc0 + s * BV + 32 * hh, a);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float vv[8], e[8];
-            unpack8(ld_shared_v4(st + L::kV + sw128(t, 4 * hh + q)), vv);
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) e[jj] = a[8 * q + jj] - vv[jj];
-            st8(sbase + L::kSb + sw128(t, 4 * hh + q), e);
+      if (st_id < 128) {
+        // gamma = exp(G_last) of key channel st_id (written before Ready, which thread 0
+        // waited on before the barrier above).  A chunk whose total log decay is beyond
+        // the range the factors exp(+-G) are formed in marks the pair for the exact
+        // recomputation (or is reported without the flags): from here on this CTA stores
+        // nothing for it; the pipeline itself runs on unchanged
+        const float gam = glast[gb * 128 + st_id];
+        if (!(gam >= kMinGamma) && !*skip_flag) {
+          *skip_flag = 1;
+          if (p.pair_flags) {
+            if (atomicExch(p.pair_flags + pair, 1u) == 0u) atomicAdd(p.status + 3, 1u);
+          } else {
+            atomicCAS(p.status, 0u, kStatusGateRange);
           }
         }
       }
+      // (E - Vb)^T of tokens 32 hs .. 32 hs + 31, bf16 -> row v of the smem operand
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float a[16];
+        tmem_ld16(tmem + lane_base + kRD1 + 32 * hs + 16 * hh, a);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float e8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) e8[e] = a[8 * q + e];
+          st8(sbase + L::kEVt + sw128(v, 4 * hs + 2 * hh + q), e8);
+        }
+      }
       fence_async_smem();
       tc_fence_before();
-      bar_sync(2, 128);
-      // a4: D4 = Kc^T (E - Vb) + Kc^T Vb over Aop[s] (read by the product above);
-      // a5: ACC[s] += [T; A^qk] (E - Vb), which turns rows 64-127 into O / s
-      if (t == 0) {
+      bar_sync(2, 256);
+      if (st_id == 0) {
         tc_fence_after();
-        constexpr uint32_t id4 = idesc_bf16(128, BV, true, true);
-        constexpr uint32_t ido = idesc_bf16(128, BV, false, true);
-        const uint32_t kc = sbase + L::kKc + kb * 16384;
-        const uint32_t tps = sbase + L::kTP + s * 16384;
+        // (Kc^T E)^T = (E - Vb)^T Kc + Vb^T Kc over S^T and (E - Vb)^T (both read by now);
+        // O^T / s = X^T + (E - Vb)^T A^qk^T
+        constexpr uint32_t id_e = idesc_bf16(128, 128, false, true);
+        constexpr uint32_t id_v = idesc_bf16(128, 128, true, true);
+        constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(kc + k4 * 2048, 8192, 1024);
-          const uint64_t be = sdesc_sw128(sbase + L::kSb + k4 * 2048, 8192, 1024);
-          const uint64_t bv = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
-          mma_bf16(tmem + kAop0 + 64u * s, ad, be, id4, k4 > 0);
-          mma_bf16(tmem + kAop0 + 64u * s, ad, bv, id4, 1);
-          mma_bf16(tmem + kAcc0 + s * BV, sdesc_sw128(tps + k4 * 32, 16, 1024), be, ido, 1);
+          const uint64_t ae = sdesc_sw128(sbase + L::kEVt + k4 * 32, 16, 1024);
+          const uint64_t bk = sdesc_sw128(kcb + k4 * 2048, 8192, 1024);
+          mma_bf16(tmem + kRD4, ae, bk, id_e, k4 > 0);
+        }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint64_t av = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
+          const uint64_t bk = sdesc_sw128(kcb + k4 * 2048, 8192, 1024);
+          mma_bf16(tmem + kRD4, av, bk, id_v, 1);
+        }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint64_t ae = sdesc_sw128(sbase + L::kEVt + k4 * 32, 16, 1024);
+          const uint64_t bq = sdesc_sw128(tps + 8192 + k4 * 32, 16, 1024);  // A^qk rows
+          mma_bf16(tmem + kRD1 + 64, ae, bq, id_o, 1);
         }
         mma_commit(ctx.bar(kMmaS));
         ctx.wait(kMmaS, sph & 1);
-        mbar_arrive(ctx.bar(kKcFree0 + kb));  // Kc[kb] has been read
-        mbar_arrive(ctx.bar(kEmptyV0 + s));   // the v tile has been read
+        mbar_arrive(ctx.bar(kKcFree0 + kb));  // Kc[kb] and TP[s] have been read
+        if (c + 2 < nchunks && !*abort_flag) load_v(s, c + 2);  // the v tile has been read
       }
       ++sph;
-      bar_sync(2, 128);
+      bar_sync(2, 256);
       tc_fence_after();
       const bool store = !*skip_flag;  // read after the barrier that follows every setter
-      if (t >= 64) {  // output rows
-        float a[32];
-        const int i = t - 64;
-        __nv_bfloat16 *orow = p.out + ((size_t)(t0 + i) * H + h) * DV + tile * BV;
+      {  // S <- gamma (S + Kc^T E), elementwise per key channel
+        const float4 *g4 = reinterpret_cast<const float4 *>(glast + gb * 128 + 64 * hs);
 #pragma unroll
-        for (int hh = 0; hh < BV / 32; ++hh) {
-          tmem_ld32(tmem + lane_base + kAcc0 + s * BV + 32 * hh, a);
-          if (i < len && store) {
+        for (int hh = 0; hh < 4; ++hh) {
+          float a[16];
+          tmem_ld16(tmem + lane_base + kRD4 + 64 * hs + 16 * hh, a);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float v[8];
+          for (int q = 0; q < 4; ++q) {
+            const float4 gm = g4[4 * hh + q];
+            const float gv[4] = {gm.x, gm.y, gm.z, gm.w};
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) v[jj] = p.scale * a[8 * q + jj];
-              *reinterpret_cast<uint4 *>(orow + 32 * hh + 8 * q) = pack8(v);
+            for (int e = 0; e < 4; ++e) {
+              float &sv = S[16 * hh + 4 * q + e];
+              sv = gv[e] * (sv + a[4 * q + e]);
             }
           }
         }
       }
-      {  // the state update, D4 from Aop[s]
-        float a[32];
+      // outputs: row v of O^T / s, tokens 32 hs .. 32 hs + 31
 #pragma unroll
-        for (int hh = 0; hh < BV / 32; ++hh) {
-          tmem_ld32(tmem + lane_base + kAop0 + 64u * s + 32 * hh, a);
+      for (int hh = 0; hh < 2; ++hh) {
+        float a[16];
+        tmem_ld16(tmem + lane_base + kRD1 + 64 + 32 * hs + 16 * hh, a);
+        if (store) {
+          const int i0 = 32 * hs + 16 * hh;  // first token of these columns
+          __nv_bfloat16 *ocol = p.out + ((size_t)(t0 + i0) * H + h) * DV + v;
+          const int nt = min(16, len - i0);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) S[32 * hh + jj] = fmaf(gm, S[32 * hh + jj], gm * a[jj]);
+          for (int i = 0; i < 16; ++i)
+            if (i < nt) ocol[(size_t)i * H * DV] = __float2bfloat16_rn(p.scale * a[i]);
         }
       }
       tc_fence_before();
+      bar_sync(2, 256);  // every thread has read kRD4, kRD1 and G_last[gb]
+      if (st_id == 0) mbar_arrive(ctx.bar(kGmRead0 + gb));
     }
-    bar_sync(2, 128);  // every setter of the skip flag is done
+    bar_sync(2, 256);  // every setter of the skip flag is done
     if (p.final_state && !*skip_flag) {
 #pragma unroll
-      for (int j = 0; j < BV; j += 4)
-        *reinterpret_cast<float4 *>(p.final_state + soff + j) =
-            make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+      for (int j = 0; j < 64; ++j) p.final_state[soff + (size_t)j * DV] = S[j];
     }
-    if (t == 0) {
+    if (st_id == 0) {
       mma_commit(ctx.bar(kFinS));
       mbar_wait(ctx.bar(kFinS), 0, kWaitCycles);
     }
   }
 
+  // no TMA load may still be in flight when the CTA leaves (possible only after a
+  // timeout stopped its consumer): wait (bounded) for the last load of every part
+  __syncthreads();
+  if (tid == 0) {
+    constexpr uint32_t kFull[4] = {kFullQ0, kFullG0, kFullK0, kFullV0};
+    for (int sidx = 0; sidx < 2; ++sidx)
+      for (int part = 0; part < 4; ++part) {
+        const int c = issued[4 * sidx + part];
+        if (c >= 0) mbar_wait(ctx.bar(kFull[part] + sidx), (c >> c_shift) & 1, kWaitCycles);
+      }
+  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 12) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -1253,35 +1281,37 @@ size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int, int) {
 // otherwise the plain one.
 template <bool kPrep>
 static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
-                      CUtensorMap &mg, CUtensorMap &mv, TcParams &prm, long long pairs,
-                      long long blocks) {
+                             CUtensorMap &mg, CUtensorMap &mv, TcParams &prm, long long pairs) {
   cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false, kPrep>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (err != cudaSuccess) return err;
-  // Few sequence-heads leave most SMs idle: with room for the ring, two solve helpers
-  // per sequence-head join the two d_v tiles in one cooperative launch (every CTA
+  // Few sequence-heads leave most SMs idle: with room for the ring, one or two solve
+  // helpers per sequence-head join its tile in one cooperative launch (every CTA
   // resident, as the hand-over through global memory needs).
+  const int hpp = 3 * pairs <= a.num_sms ? 2 : (2 * pairs <= a.num_sms ? 1 : 0);
   int dev = 0, coop = 0;
-  if (pairs <= kHelperMaxPairs && 4 * pairs <= a.num_sms && a.scratch &&
-      a.scratch_bytes >= ring_bytes(pairs) && cudaGetDevice(&dev) == cudaSuccess &&
+  if (hpp > 0 && pairs <= kHelperMaxPairs && a.scratch && a.scratch_bytes >= ring_bytes(pairs) &&
+      cudaGetDevice(&dev) == cudaSuccess &&
       cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
     err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true, kPrep>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (err != cudaSuccess) return err;
     prm.ring = static_cast<uint8_t *>(a.scratch);
     prm.ring_flags = reinterpret_cast<uint32_t *>(prm.ring + pairs * kRingSlots * kRingSlotBytes);
+    prm.helpers_per_pair = hpp;
     err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
     if (err != cudaSuccess) return err;
     void *args[] = {&mq, &mk, &mg, &mv, &prm};
     err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true, kPrep>),
-                                      dim3(static_cast<unsigned>(4 * pairs)), dim3(kThreads), args,
-                                      L::kAlloc, stream);
+                                      dim3(static_cast<unsigned>((1 + hpp) * pairs)), dim3(kThreads),
+                                      args, L::kAlloc, stream);
     if (err != cudaErrorCooperativeLaunchTooLarge) return err;
     (void)cudaGetLastError();  // not all resident (SMs taken): the plain schedule below
     prm.ring = nullptr;
     prm.ring_flags = nullptr;
+    prm.helpers_per_pair = 1;
   }
-  kda_chunk_tc_kernel<false, kPrep><<<(unsigned)blocks, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, prm);
+  kda_chunk_tc_kernel<false, kPrep><<<(unsigned)pairs, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, prm);
   return cudaGetLastError();
 }
 
@@ -1306,6 +1336,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.gate = a.gate;
   prm.prep = a.prep;
   prm.gate_scale = a.gate_scale;
+  prm.helpers_per_pair = 1;
   prm.init_state = a.init_state;
   prm.cu_seqlens = a.cu_seqlens;
   prm.out = static_cast<__nv_bfloat16 *>(a.out);
@@ -1320,10 +1351,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.ring_flags = nullptr;
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   prm.npairs = static_cast<int>(pairs);
-  const long long blocks = pairs * (DV / BV);
-  if (blocks == 0) return cudaSuccess;
-  return a.prep ? launch_tc<true>(a, stream, mq, mk, mg, mv, prm, pairs, blocks)
-                : launch_tc<false>(a, stream, mq, mk, mg, mv, prm, pairs, blocks);
+  if (pairs == 0) return cudaSuccess;
+  return a.prep ? launch_tc<true>(a, stream, mq, mk, mg, mv, prm, pairs)
+                : launch_tc<false>(a, stream, mq, mk, mg, mv, prm, pairs);
 }
 
 }  // namespace kda

@@ -1,12 +1,12 @@
 """The few-sequence-head schedule of the tensor-core prefill.
 
-With at most 38 (sequence, head) pairs and a workspace of
-kda_chunk_fwd_workspace_bytes(), two solve-helper CTAs per pair compute each
-chunk's [T diag(beta); A^qk] ("Kimi Delta Attention (KDA)", the chunkwise
-algorithm's WY / UT-transform step) and hand it to the two d_v-tile CTAs through
+With at most 76 (sequence, head) pairs and a workspace of
+kda_chunk_fwd_workspace_bytes(), one (up to 76 pairs) or two (up to 50) solve-helper
+CTAs per pair compute each chunk's [T - I; A^qk] ("Kimi Delta Attention (KDA)", the
+chunkwise algorithm's WY / UT-transform step) and hand it to the pair's tile CTA through
 a ring in the workspace (after the status block and, with a gate, one flag word per
 pair rounded up to 256 bytes).  A 256-byte workspace selects the plain schedule,
-where each d_v tile solves every chunk itself.  Both run the same arithmetic on the
+where the tile solves every chunk itself.  Both run the same arithmetic on the
 same operands, so their results must agree bit for bit; the helper schedule is
 also checked against the oracle, and the ring's hand-over counters are read
 back to show that the helpers ran."""
@@ -23,9 +23,9 @@ from parity import TOL_BF16, rel_l2_per_head, rel_l2_states, run_oracle_prefill,
 pytestmark = pytest.mark.gpu
 
 STATUS_BYTES = 256
-FLAG_BYTES = 256  # one flag word per pair (at most 38 here), rounded up to 256 bytes
+FLAG_BYTES = 256  # one flag word per pair (at most 64 here), rounded up to 256 bytes
 SLOTS, SLOT_BYTES = 4, 16384
-MAX_PAIRS = 38
+MAX_PAIRS = 64
 
 
 def _run(dv, g, workspace):
@@ -49,7 +49,7 @@ def _expected_ring_words(lens, H):
         for _ in range(H):
             for slot in range(SLOTS):
                 cs = [c for c in range(nch) if c % SLOTS == slot]
-                words += [cs[-1] + 1 if cs else 0, 2 * len(cs)]
+                words += [cs[-1] + 1 if cs else 0, len(cs)]  # one read per chunk
     return np.array(words, dtype=np.uint32)
 
 
@@ -69,6 +69,8 @@ CASES = [
     ([0, 130, 0, 64], 3),
     ([64 * 13 + 7], 4),
     ([5 + 37 * i for i in range(19)], 2),
+    # 60 pairs: one helper per pair (two fit up to 50 pairs on 152 SMs)
+    ([40 + 23 * i for i in range(30)], 2),
 ]
 
 
@@ -137,13 +139,13 @@ def test_helper_schedule_on_concurrent_streams():
 
 
 def test_more_pairs_than_helpers_use_the_plain_schedule():
-    lens = [100] * 13
-    assert kda_chunk_fwd_workspace_bytes(13, 1300, 3, 128, 128) == STATUS_BYTES + FLAG_BYTES  # 39 pairs
-    assert kda_chunk_fwd_workspace_bytes(19, 1900, 2, 128, 128) > STATUS_BYTES + FLAG_BYTES  # 38
-    spec = W.custom_prefill(lens, num_heads=3, d=128, gate="mixed", seed=68)
+    lens = [100] * 11
+    assert kda_chunk_fwd_workspace_bytes(11, 1100, 7, 128, 128) == STATUS_BYTES + 512  # 77 pairs
+    assert kda_chunk_fwd_workspace_bytes(38, 3800, 2, 128, 128) > STATUS_BYTES + 512  # 76
+    spec = W.custom_prefill(lens, num_heads=7, d=128, gate="mixed", seed=68)
     x = W.prefill_inputs(spec)
     dv = to_dev(x)
-    ws = torch.empty(STATUS_BYTES + FLAG_BYTES, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(STATUS_BYTES + 512, dtype=torch.uint8, device="cuda")
     o, s = _run(dv, dv["g"], ws)
     assert workspace_status_words(ws)[2] == 1  # plain
     ro, rs = run_oracle_prefill(x)

@@ -5,8 +5,8 @@ Both schedules (plain, and the solve helpers with their ring in the workspace) a
 deterministic: the same inputs must give the same bits on every call.  A race in
 the hand-over between the K-side groups, the state side and the producers would
 show up as an occasional call that differs, most likely with many short
-sequences (38 sequence-heads, the largest pair count with helpers) and a gate
-without per-channel decay (the shortest K-side chain).  A change withdrawn during
+sequences (38 sequence-heads with two helpers each, 60 with one) and a gate without
+per-channel decay (the shortest K-side chain).  A change withdrawn during
 development failed this check in about one call in twenty."""
 import pytest
 import torch
@@ -17,19 +17,21 @@ from kimi_delta_attention_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-LENS = [5 + 37 * i for i in range(19)]
+LENS = [5 + 37 * i for i in range(19)]       # 38 sequence-heads: two helpers each
+LENS60 = [40 + 23 * i for i in range(30)]    # 60 sequence-heads: one helper each
 H = 2
 REPS = 30
 
 
 @pytest.mark.parametrize("mode", ["none", "scalar", "channel"])
-@pytest.mark.parametrize("schedule", ["plain", "helper"])
+@pytest.mark.parametrize("schedule", ["plain", "helper", "helper1"])
 def test_repeated_calls_are_bitwise_identical(mode, schedule):
-    x = W.prefill_inputs(W.custom_prefill(LENS, num_heads=H, d=128, gate="mixed", seed=90),
+    lens = LENS60 if schedule == "helper1" else LENS
+    x = W.prefill_inputs(W.custom_prefill(lens, num_heads=H, d=128, gate="mixed", seed=90),
                          device="cuda")
     g = None if mode == "none" else (x["g"][..., 0].contiguous() if mode == "scalar" else x["g"])
-    need = kda_chunk_fwd_workspace_bytes(len(LENS), x["q"].shape[0], H, 128, 128)
-    ws = torch.zeros(need if schedule == "helper" else 256, dtype=torch.uint8, device="cuda")
+    need = kda_chunk_fwd_workspace_bytes(len(lens), x["q"].shape[0], H, 128, 128)
+    ws = torch.zeros(need if schedule != "plain" else 256, dtype=torch.uint8, device="cuda")
     args = (x["q"], x["k"], x["v"], g, x["beta"], x["cu_seqlens"], x["init_state"])
     o0, f0 = kda_chunk_fwd(*args, workspace=ws, algo="tensor", check=True)
     o0, f0 = o0.clone(), f0.clone()
