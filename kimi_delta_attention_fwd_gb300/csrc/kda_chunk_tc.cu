@@ -10,9 +10,9 @@
 //   Kb  = diag(beta) K * exp(G)   Qh = Q * exp(G)   Kc = K * exp(-G)   Vb = diag(beta) V
 //   [Kb; Qh] Kc^T              -> rows: A^kk (j < i, beta_i included), A^qk (j <= i)
 //   T   = (I + A^kk)^-1                                (fp32 triangular solve)
-//   W   = T Kb = (T - I) Kb + Kb                       ([T - I; A^qk] Kb, rows 0-63)
+//   W   = T Kb                                         ([T; A^qk] Kb, rows 0-63)
 //   with E = U - W S, U = T Vb and X = Qh S + A^qk Vb, all transposed (d_v rows):
-//   [(E - Vb)^T | X^T] = Vb^T [T - I; A^qk]^T + S^T [-W; Qh]^T
+//   [(E - Vb)^T | X^T] = Vb^T [T; A^qk]^T - Vb^T [I | 0] + S^T [-W; Qh]^T
 //   O^T / s            = X^T + (E - Vb)^T A^qk^T       (= (Qh S + A^qk E)^T)
 //   S^T <- (S^T + (E - Vb)^T Kc + Vb^T Kc) Diag(gamma) (= gamma (S + Kc^T E), transposed)
 //
@@ -21,7 +21,8 @@
 // to bf16 for both of its last products: the Vb^T A^qk^T and Vb^T Kc terms it is
 // combined with are formed from Vb itself, so they add back what was subtracted.
 // E - Vb = (T - I) Vb - W S scales with beta like E does, so its bf16 rounding
-// stays small against E for small write strengths too.
+// stays small against E for small write strengths too.  (E - Vb)^T in bf16 is the A
+// operand of the state side's last products, in tensor memory.
 //
 // The state side works on S^T, one d_v row per TMEM lane: S^T in bf16 is the A
 // operand (in tensor memory) of its first product, and each of its products covers
@@ -44,9 +45,9 @@
 //                half); the state-dependent products of each chunk
 // The TMA loads that refill a stage are issued by whoever releases each part: a
 // K-side group its g tile (after the solve), the state side its k and q tiles
-// (after its first product has read [-W; Qh]) and its v tile (after its last
-// product).  With few sequence-heads, one or two more CTAs per sequence-head run
-// the solve of its chunks ("Solve helpers" below).
+// (after its first product has read [-W; Qh]) and its v tile (after the chunk's
+// outputs, staged there, have been stored by TMA).  With few sequence-heads, one or
+// two more CTAs per sequence-head run the solve of its chunks ("Solve helpers" below).
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // KDA_ERR_DEVICE_TIMEOUT in the status word and runs to completion without
 // waiting again (outputs are then undefined, nothing blocks or faults).
@@ -79,7 +80,7 @@ constexpr float kMinGamma = 1.8e-35f;  // about exp(-80): the state side checks 
 // room for the ring, the launch is cooperative (all CTAs resident) and each pair
 // gets hpp = 2 (at most 50 pairs) or 1 helper CTAs beside its tile: K-side group kw
 // of helper hp solves the chunks c = hp + hpp kw + 2 hpp i (the state-independent
-// [T - I; A^qk]) and hands each to the tile through a ring in the workspace, slot
+// [T; A^qk]) and hands each to the tile through a ring in the workspace, slot
 // c % 4 holding chunk c's 16 KiB shared-memory image.  Each slot has two words: the
 // last chunk published + 1 (a release store after the image) and the number of
 // reads so far (a release add by the tile once its copy is in shared memory); a
@@ -104,19 +105,20 @@ struct L {
   // stage: [k ch0-63 | q ch0-63] [k ch64-127 | q ch64-127] [g ch0-63] [g ch64-127]
   //        [v ch0-63] [v ch64-127];
   // the g area later holds the fp32 A^kk / T in the compact solve layout; the k rows
-  // hold Kb, then -W; the q rows Qh ([-W; Qh] is the B operand of the state product)
+  // hold Kb, then -W; the q rows Qh ([-W; Qh] is the B operand of the state product);
+  // the v area holds Vb, then the chunk's outputs for their TMA store
   static constexpr uint32_t kKQ1 = 16384, kQoff = 8192, kG = 32768, kV = 49152;
   static constexpr uint32_t kStageBytes = 65536;
   static constexpr uint32_t kKc = 2 * kStageBytes;      // 3 x Kc [ch0-63 | ch64-127], slot = chunk % 3
-  static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [T - I rows 0-63 | A^qk rows 64-127]
-  static constexpr uint32_t kEVt = kTP + 2 * 16384;       // (E - Vb)^T: 128 d_v rows x 64 tokens, bf16
-  static constexpr uint32_t kGlast = kEVt + 16384;        // fp32 G_last [kGl][128]
+  static constexpr uint32_t kTP = kKc + 3 * 16384;        // 2 x [T rows 0-63 | A^qk rows 64-127]
+  static constexpr uint32_t kNegI = kTP + 2 * 16384;      // -I, 64 x 64 bf16 (K-major B operand)
+  static constexpr uint32_t kGlast = kNegI + 8192;        // gamma = exp(G_last) [kGl][128]
   static constexpr uint32_t kBars = kGlast + kGl * 512;   // mbarriers
   static constexpr uint32_t kMisc = kBars + 256;          // tmem slot, abort / skip flags, issued loads
   static constexpr uint32_t kTotal = kMisc + 64;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
-static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kEVt % 1024 == 0,
+static_assert(L::kKc % 1024 == 0 && L::kTP % 1024 == 0 && L::kNegI % 1024 == 0,
               "operand tiles must be 1024-byte aligned");
 static_assert(L::kAlloc <= 232448, "shared memory budget");
 
@@ -136,7 +138,8 @@ static_assert(kNumBars * 8 <= 256, "mbarrier area");
 //   [320, 448)      [(E - Vb)^T | X^T], then [. | O^T / s]
 //   [256, 384)      (Kc^T E)^T: over S^T and the first half of the above, once both are read
 //   [448, 480)      [Ltri; Ltri] in bf16 pairs: the A operand of the cumsum product
-constexpr uint32_t kRA = 256, kRD1 = 320, kRD4 = 256, kRLtri = 448;
+//   [480, 512)      (E - Vb)^T in bf16 pairs: the A operand of the state side's last products
+constexpr uint32_t kRA = 256, kRD1 = 320, kRD4 = 256, kRLtri = 448, kREV = 480;
 
 struct TcParams {
   const __nv_bfloat16 *beta;
@@ -306,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_g,
-                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   // roles: a tile CTA (one per pair) runs everything, or with helpers takes each chunk's
-  // [T - I; A^qk] from the ring; a helper (pair, hp) runs the chunk solve of the chunks
+  // [T; A^qk] from the ring; a helper (pair, hp) runs the chunk solve of the chunks
   // c = hp + hpp kw + 2 hpp i of its K-side group kw and publishes it
   const int P = p.npairs;
   const bool helper = kSched && (int)blockIdx.x >= P;
@@ -408,6 +412,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 32; ++j)
       w[j] = (2 * j <= r ? 0x3F80u : 0u) | ((2 * j + 1 <= r ? 0x3F80u : 0u) << 16);
     tmem_st32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kRLtri, w);
+  } else if (warp >= 8 && warp < 10) {
+    // -I (64 x 64, bf16, K-major rows): the state side subtracts Vb^T with it
+    const int r = tid - 256;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = (8 * j + 2 * e == r ? 0xBF80u : 0u) | ((8 * j + 2 * e + 1 == r ? 0xBF80u : 0u) << 16);
+      st_shared_v4(sbase + L::kNegI + sw128(r, j), w[0], w[1], w[2], w[3]);
+    }
+    fence_async_smem();
   } else if (tid == 128 || tid == 160) {
     // the first chunk of each stage, loaded by one thread per stage
     const int sidx = tid == 128 ? 0 : 1;
@@ -440,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dependent chain of one chunk overlaps the other group's chunk.  Kc rotates
     // over three slots (chunk % 3).
     // A helper's groups take c = hp + hpp kw + 2 hpp i, run the gate, a2 and the solve,
-    // and publish [T - I; A^qk]; a tile fed by helpers runs the gate and takes
-    // [T - I; A^qk] from the ring in place of a2 and the solve.
+    // and publish [T; A^qk]; a tile fed by helpers runs the gate and takes [T; A^qk]
+    // from the ring in place of a2 and the solve.
     const int kw = warp >> 2;
     const int t = tid & 127;            // thread within the group
     const int wq = warp & 3;            // TMEM lane quarter of this warp
@@ -899,9 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         bar_sync(bar_id, 128);
-        {  // T - I -> TP rows 0-63 (bf16), 32 columns per thread; rows 32-63, columns 0-31
-           // come from the fragments above.  T - I is the operand both products need:
-           // W = (T - I) Kb + Kb, and (T - I) Vb = U - Vb on the state side
+        {  // T -> TP rows 0-63 (bf16), 32 columns per thread; rows 32-63, columns 0-31
+           // come from the fragments above
           const int i = t & 63, hh = t >> 6, I = i >> 4, il = i & 15;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -920,22 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) tv[jj] = 0.f;
             }
-            uint4 pk = pack8(tv);
-            if (J == I) {
-              // T - I: T's diagonal is exactly 1, so the diagonal element (column i, in the
-              // bf16 pair (i - j0) / 2 of this chunk) is cleared.  (A per-element float
-              // subtraction here measured ~4.4 K cycles slower per chunk.)
-              const int d = il - jl;  // 0..7 when the diagonal is in this chunk
-              const uint32_t keep = (d & 1) ? 0x0000FFFFu : 0xFFFF0000u;
-              if (d >= 0 && d < 8) {
-                const int w = d >> 1;
-                pk.x &= w == 0 ? keep : 0xFFFFFFFFu;
-                pk.y &= w == 1 ? keep : 0xFFFFFFFFu;
-                pk.z &= w == 2 ? keep : 0xFFFFFFFFu;
-                pk.w &= w == 3 ? keep : 0xFFFFFFFFu;
-              }
-            }
-            st_shared_v4(tp + sw128(i, 4 * hh + q), pk.x, pk.y, pk.z, pk.w);  // T is exactly lower triangular
+            st8(tp + sw128(i, 4 * hh + q), tv);  // T is exactly lower triangular
           }
           uint8_t *tpg = smem + L::kTP + kw * 16384;
 #pragma unroll
@@ -993,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the g area (solve scratch) is free: the group's next chunk's g tile
       if (t == 0 && !fed && c + 2 < nchunks && !*abort_flag) load_g(s, c + 2);
 
-      // [T - I; A^qk] Kb -> D2, rows 0-63: W - Kb = (T - I) Kb
+      // [T; A^qk] Kb -> D2, rows 0-63: W = T Kb
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
@@ -1014,20 +1014,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_sync(bar_id, 128);
       tc_fence_after();
       if (row < 64) {
-        // -W = -((T - I) Kb + Kb), bf16, over the row's Kb: rows 0-63 of the state
-        // product's B operand [-W; Qh] (its rows 64-127 are Qh in the q area)
+        // -W in bf16 over the row's Kb: rows 0-63 of the state product's B operand
+        // [-W; Qh] (its rows 64-127 are Qh in the q area)
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {  // channels 64 hh .. 64 hh + 63
-          float a[64];
-          tmem_ld64(tm + lane_base + 64 * hh, a);
+        for (int hq = 0; hq < 4; ++hq) {  // channels 32 hq .. 32 hq + 31
+          float a[32];
+          tmem_ld32(tm + lane_base + 32 * hq, a);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t addr = st + hh * L::kKQ1 + sw128(row, j);
-            float kbv[8];
-            unpack8(ld_shared_v4(addr), kbv);
+          for (int j = 0; j < 4; ++j) {
+            float w8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) kbv[e] = -(a[8 * j + e] + kbv[e]);
-            st8(addr, kbv);
+            for (int e = 0; e < 8; ++e) w8[e] = -a[8 * j + e];
+            st8(st + (hq >> 1) * L::kKQ1 + sw128(row, 4 * (hq & 1) + j), w8);
           }
         }
       }
@@ -1066,6 +1064,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 64; ++j) S[j] = 0.f;
     }
     uint32_t sph = 0;
+    int pend_v = -1;  // chunk whose v tile (stage pend_v & 1) is loaded once the outputs left it
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1;
       const int t0 = bos + c * C;
@@ -1085,15 +1084,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       bar_sync(2, 256);
       if (st_id == 0) {
+        if (pend_v >= 0) {
+          // the previous chunk's outputs have been read out of its v area: the next v tile
+          bulk_wait_read();
+          if (!*abort_flag) load_v(pend_v & 1, pend_v);
+          pend_v = -1;
+        }
         ctx.wait(kReady0 + s, (c >> 1) & 1);
         tc_fence_after();
-        // [(E - Vb)^T | X^T] = Vb^T [T - I; A^qk]^T + S^T [-W; Qh]^T, one commit
+        // [(E - Vb)^T | X^T] = Vb^T [T; A^qk]^T - Vb^T [I | 0] + S^T [-W; Qh]^T, one commit
         constexpr uint32_t id_init = idesc_bf16(128, 128, true, false);
+        constexpr uint32_t id_negi = idesc_bf16(128, 64, true, false);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const uint64_t av = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);  // Vb^T (MN-major)
-          const uint64_t bt = sdesc_sw128(tps + k4 * 32, 16, 1024);            // [T - I; A^qk] rows
+          const uint64_t bt = sdesc_sw128(tps + k4 * 32, 16, 1024);            // [T; A^qk] rows
           mma_bf16(tmem + kRD1, av, bt, id_init, k4 > 0);
+        }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint64_t av = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
+          const uint64_t bi = sdesc_sw128(sbase + L::kNegI + k4 * 32, 16, 1024);  // -I rows
+          mma_bf16(tmem + kRD1, av, bi, id_negi, 1);
         }
         constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
 #pragma unroll
@@ -1128,34 +1140,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // (E - Vb)^T of tokens 32 hs .. 32 hs + 31, bf16 -> row v of the smem operand
+      {  // (E - Vb)^T of tokens 32 hs .. 32 hs + 31, bf16 pairs -> columns [kREV + 16 hs, +16)
+        uint32_t pk[16];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float a[16];
-        tmem_ld16(tmem + lane_base + kRD1 + 32 * hs + 16 * hh, a);
+        for (int hh = 0; hh < 2; ++hh) {
+          float a[16];
+          tmem_ld16(tmem + lane_base + kRD1 + 32 * hs + 16 * hh, a);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float e8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) e8[e] = a[8 * q + e];
-          st8(sbase + L::kEVt + sw128(v, 4 * hs + 2 * hh + q), e8);
+          for (int jj = 0; jj < 8; ++jj) pk[8 * hh + jj] = pack_bf16x2(a[2 * jj], a[2 * jj + 1]);
         }
+        tmem_st16(tmem + lane_base + kREV + 16 * hs, pk);
       }
-      fence_async_smem();
       tc_fence_before();
       bar_sync(2, 256);
       if (st_id == 0) {
         tc_fence_after();
-        // (Kc^T E)^T = (E - Vb)^T Kc + Vb^T Kc over S^T and (E - Vb)^T (both read by now);
-        // O^T / s = X^T + (E - Vb)^T A^qk^T
+        // (Kc^T E)^T = (E - Vb)^T Kc + Vb^T Kc over S^T and the first half of the above
+        // (both read by now); O^T / s = X^T + (E - Vb)^T A^qk^T
         constexpr uint32_t id_e = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id_v = idesc_bf16(128, 128, true, true);
         constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ae = sdesc_sw128(sbase + L::kEVt + k4 * 32, 16, 1024);
           const uint64_t bk = sdesc_sw128(kcb + k4 * 2048, 8192, 1024);
-          mma_bf16(tmem + kRD4, ae, bk, id_e, k4 > 0);
+          mma_bf16_tmem_a(tmem + kRD4, tmem + kREV + 8u * k4, bk, id_e, k4 > 0);
         }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
@@ -1165,14 +1173,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ae = sdesc_sw128(sbase + L::kEVt + k4 * 32, 16, 1024);
           const uint64_t bq = sdesc_sw128(tps + 8192 + k4 * 32, 16, 1024);  // A^qk rows
-          mma_bf16(tmem + kRD1 + 64, ae, bq, id_o, 1);
+          mma_bf16_tmem_a(tmem + kRD1 + 64, tmem + kREV + 8u * k4, bq, id_o, 1);
         }
         mma_commit(ctx.bar(kMmaS));
         ctx.wait(kMmaS, sph & 1);
         mbar_arrive(ctx.bar(kKcFree0 + kb));  // Kc[kb] and TP[s] have been read
-        if (c + 2 < nchunks && !*abort_flag) load_v(s, c + 2);  // the v tile has been read
       }
       ++sph;
       bar_sync(2, 256);
@@ -1196,23 +1202,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // outputs: row v of O^T / s, tokens 32 hs .. 32 hs + 31
+      // outputs: row v of O^T / s, tokens 32 hs .. 32 hs + 31.  A full chunk goes into its
+      // v area (Vb has been read), laid out as the output box, and leaves by TMA; a
+      // sequence's partial last chunk is stored directly (a box would pass its end).
+      const bool full = len == C;
+      const uint32_t ostage = st + L::kV + (v >> 6) * 8192;  // this d_v half's 64-column box
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float a[16];
         tmem_ld16(tmem + lane_base + kRD1 + 64 + 32 * hs + 16 * hh, a);
         if (store) {
           const int i0 = 32 * hs + 16 * hh;  // first token of these columns
-          __nv_bfloat16 *ocol = p.out + ((size_t)(t0 + i0) * H + h) * DV + v;
-          const int nt = min(16, len - i0);
+          if (full) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (i < nt) ocol[(size_t)i * H * DV] = __float2bfloat16_rn(p.scale * a[i]);
+            for (int i = 0; i < 16; ++i)
+              st_shared_u16(ostage + sw128(i0 + i, (v & 63) >> 3) + 2 * (v & 7),
+                            __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * a[i])));
+          } else {
+            __nv_bfloat16 *ocol = p.out + ((size_t)(t0 + i0) * H + h) * DV + v;
+            const int nt = min(16, len - i0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (i < nt) ocol[(size_t)i * H * DV] = __float2bfloat16_rn(p.scale * a[i]);
+          }
         }
       }
+      fence_async_smem();
       tc_fence_before();
-      bar_sync(2, 256);  // every thread has read kRD4, kRD1 and G_last[gb]
-      if (st_id == 0) mbar_arrive(ctx.bar(kGmRead0 + gb));
+      bar_sync(2, 256);  // every thread has read kRD4, kRD1 and G_last[gb], and staged its outputs
+      if (st_id == 0) {
+        mbar_arrive(ctx.bar(kGmRead0 + gb));
+        if (store && full && !*abort_flag) {
+          tma_store_3d(&tm_o, st + L::kV, 0, h, t0);
+          tma_store_3d(&tm_o, st + L::kV + 8192, 64, h, t0);
+        }
+        bulk_commit();
+        // the v area is reloaded (for chunk c + 2) once the store has read it: next chunk
+        if (c + 2 < nchunks) pend_v = c + 2;
+      }
     }
     bar_sync(2, 256);  // every setter of the skip flag is done
     if (p.final_state && !*skip_flag) {
@@ -1220,6 +1247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 64; ++j) p.final_state[soff + (size_t)j * DV] = S[j];
     }
     if (st_id == 0) {
+      bulk_wait();  // the last outputs' stores are complete
       mma_commit(ctx.bar(kFinS));
       mbar_wait(ctx.bar(kFinS), 0, kWaitCycles);
     }
@@ -1291,7 +1319,8 @@ size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int, int) {
 // otherwise the plain one.
 template <bool kPrep>
 static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
-                             CUtensorMap &mg, CUtensorMap &mv, TcParams &prm, long long pairs) {
+                             CUtensorMap &mg, CUtensorMap &mv, CUtensorMap &mo, TcParams &prm,
+                             long long pairs) {
   cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false, kPrep>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (err != cudaSuccess) return err;
@@ -1311,7 +1340,7 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     prm.helpers_per_pair = hpp;
     err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
     if (err != cudaSuccess) return err;
-    void *args[] = {&mq, &mk, &mg, &mv, &prm};
+    void *args[] = {&mq, &mk, &mg, &mv, &mo, &prm};
     err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true, kPrep>),
                                       dim3(static_cast<unsigned>((1 + hpp) * pairs)), dim3(kThreads),
                                       args, L::kAlloc, stream);
@@ -1321,23 +1350,26 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     prm.ring_flags = nullptr;
     prm.helpers_per_pair = 1;
   }
-  kda_chunk_tc_kernel<false, kPrep><<<(unsigned)pairs, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, prm);
+  kda_chunk_tc_kernel<false, kPrep><<<(unsigned)pairs, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, mo,
+                                                                                          prm);
   return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   if (!chunk_tc_supported(a.d_k, a.d_v, a.bf16)) return cudaErrorInvalidValue;
   if (!encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap mq, mk, mg, mv;
+  CUtensorMap mq, mk, mg, mv, mo;
   memset(&mq, 0, sizeof(mq));
   memset(&mk, 0, sizeof(mk));
   memset(&mg, 0, sizeof(mg));
   memset(&mv, 0, sizeof(mv));
+  memset(&mo, 0, sizeof(mo));
   if (a.total_tokens > 0) {
     if (!make_map(&mq, a.q, a.total_tokens, a.num_heads) ||
         !make_map(&mk, a.k, a.total_tokens, a.num_heads) ||
         !make_map(&mg, a.gate == 0 ? a.g : a.q, a.total_tokens, a.num_heads) ||
-        !make_map(&mv, a.v, a.total_tokens, a.num_heads))
+        !make_map(&mv, a.v, a.total_tokens, a.num_heads) ||
+        !make_map(&mo, a.out, a.total_tokens, a.num_heads))
       return cudaErrorInvalidValue;
   }
   TcParams prm;
@@ -1362,8 +1394,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   prm.npairs = static_cast<int>(pairs);
   if (pairs == 0) return cudaSuccess;
-  return a.prep ? launch_tc<true>(a, stream, mq, mk, mg, mv, prm, pairs)
-                : launch_tc<false>(a, stream, mq, mk, mg, mv, prm, pairs);
+  return a.prep ? launch_tc<true>(a, stream, mq, mk, mg, mv, mo, prm, pairs)
+                : launch_tc<false>(a, stream, mq, mk, mg, mv, mo, prm, pairs);
 }
 
 }  // namespace kda
