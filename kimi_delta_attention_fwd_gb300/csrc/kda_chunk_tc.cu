@@ -447,9 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Register split: the state side holds 64 fp32 state values per thread.  The launch
   // gives every thread 128 registers (512 x 128 = 65,536); the K-side warpgroups hand
-  // 24 each back and the state side takes them: 256 x 104 + 256 x 152 = 65,536.
+  // 16 each back and the state side takes them: 256 x 112 + 256 x 144 = 65,536.
   if (warp < 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
     // ------------------------------------------------------------ K-side
     // Two groups of 4 warps; group kw takes the chunks c = kw, kw + 2, ... and
     // owns stage kw, TP[kw] and TMEM columns [128 kw, 128 kw + 128), so the
@@ -483,11 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_cumsum = [&]() {
       tc_fence_after();
       constexpr uint32_t id = idesc_bf16(128, 128, false, true);
+      const uint32_t bg = sdesc_lo(st + L::kG, 8192);
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const uint64_t bd = sdesc_sw128(st + L::kG + k4 * 2048, 8192, 1024);
-        mma_bf16_tmem_a(tm, tmem + kRLtri + 8u * k4, bd, id, k4 > 0);
-      }
+      for (int k4 = 0; k4 < 4; ++k4)
+        mma_ts(tm, tmem + kRLtri + 8u * k4, bg + 128 * k4, sdesc_hi(1024), id, k4 > 0);
       mma_commit(mma_bar);
     };
     if ((p.flags & 1) && tid == 0) {
@@ -506,6 +505,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = helper ? kw : c % 3;  // Kc slot (a helper's own two are read by its a2 only)
       const uint32_t kcb = sbase + L::kKc + kb * 16384;
       const int slot = c & (kRingSlots - 1);  // ring slot of this chunk's [T; A^qk]
+      if (t == 0 && c + c_step < nchunks) {
+        // the group's next chunk into L2: its stage loads, issued when each part is
+        // released, then wait for L2 rather than HBM
+        const int tn = bos + (c + c_step) * C;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          tma_prefetch_3d(&tm_k, 64 * x, h, tn);
+          tma_prefetch_3d(&tm_q, 64 * x, h, tn);
+          if (p.gate == 0) tma_prefetch_3d(&tm_g, 64 * x, h, tn);
+          if (!helper) tma_prefetch_3d(&tm_v, 64 * x, h, tn);
+        }
+      }
       // beta of this thread's row (row t mod 64 of the chunk; 0 past the sequence end),
       // folded into Kb and Vb; loaded early to hide the global latency
       const int rb = t & 63;
@@ -730,12 +741,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) {
           tc_fence_after();
           constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+          const uint32_t akq = sdesc_lo(st, 16), bkc = sdesc_lo(kcb, 16);
 #pragma unroll
-          for (int k8 = 0; k8 < 8; ++k8) {
-            const uint64_t ad = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kcb + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
-            mma_bf16(tm, ad, bd, id, k8 > 0);
-          }
+          for (int k8 = 0; k8 < 8; ++k8)
+            mma_ss(tm, akq + (k8 >> 2) * (L::kKQ1 >> 4) + 2 * (k8 & 3), sdesc_hi(1024),
+                   bkc + (k8 >> 2) * 512 + 2 * (k8 & 3), sdesc_hi(1024), id, k8 > 0);
           mma_commit(mma_bar);
           ctx.wait(kMmaK0 + kw, kph & 1);
           if (helper) {  // Kb and Qh are read by a2 only in a helper: the next chunk's k and q
@@ -997,12 +1007,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
+        const uint32_t atp = sdesc_lo(tp, 16), bkb = sdesc_lo(st, L::kKQ1);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(tp + k4 * 32, 16, 1024);
-          const uint64_t bk = sdesc_sw128(st + k4 * 2048, L::kKQ1, 1024);
-          mma_bf16(tm, ad, bk, id_k, k4 > 0);
-        }
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_ss(tm, atp + 2 * k4, sdesc_hi(1024), bkb + 128 * k4, sdesc_hi(1024), id_k, k4 > 0);
         mma_commit(mma_bar);
         ctx.wait(kMmaK0 + kw, kph & 1);
       } else if (fed && t == 32) {
@@ -1045,7 +1053,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(ctx.bar(kFinK0 + kw), 0, kWaitCycles);
     }
   } else if (!helper) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
     // ------------------------------------------------------------ state side
     // Thread (d_v row v = 32 (warp % 4) + lane, key-channel half hs = (warp - 8) / 4)
     // holds S[64 hs + j][v], j = 0..63, in fp32: column v of the state, which is row v
@@ -1095,24 +1103,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [(E - Vb)^T | X^T] = Vb^T [T; A^qk]^T - Vb^T [I | 0] + S^T [-W; Qh]^T, one commit
         constexpr uint32_t id_init = idesc_bf16(128, 128, true, false);
         constexpr uint32_t id_negi = idesc_bf16(128, 64, true, false);
+        const uint32_t avb = sdesc_lo(st + L::kV, 8192);  // Vb^T (MN-major)
+        const uint32_t btp = sdesc_lo(tps, 16);           // [T; A^qk] rows
+        const uint32_t bni = sdesc_lo(sbase + L::kNegI, 16);  // -I rows
+        const uint32_t bwq = sdesc_lo(st, 16);            // [-W; Qh]
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t av = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);  // Vb^T (MN-major)
-          const uint64_t bt = sdesc_sw128(tps + k4 * 32, 16, 1024);            // [T; A^qk] rows
-          mma_bf16(tmem + kRD1, av, bt, id_init, k4 > 0);
-        }
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_ss(tmem + kRD1, avb + 128 * k4, sdesc_hi(1024), btp + 2 * k4, sdesc_hi(1024), id_init, k4 > 0);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t av = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
-          const uint64_t bi = sdesc_sw128(sbase + L::kNegI + k4 * 32, 16, 1024);  // -I rows
-          mma_bf16(tmem + kRD1, av, bi, id_negi, 1);
-        }
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_ss(tmem + kRD1, avb + 128 * k4, sdesc_hi(1024), bni + 2 * k4, sdesc_hi(1024), id_negi, 1);
         constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
 #pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {
-          const uint64_t bw = sdesc_sw128(st + (k8 >> 2) * L::kKQ1 + (k8 & 3) * 32, 16, 1024);  // [-W; Qh]
-          mma_bf16_tmem_a(tmem + kRD1, tmem + kRA + 8u * k8, bw, id_s, 1);
-        }
+        for (int k8 = 0; k8 < 8; ++k8)
+          mma_ts(tmem + kRD1, tmem + kRA + 8u * k8, bwq + (k8 >> 2) * (L::kKQ1 >> 4) + 2 * (k8 & 3),
+                 sdesc_hi(1024), id_s, 1);
         mma_commit(ctx.bar(kMmaS));
         ctx.wait(kMmaS, sph & 1);
         // the stage's k and q tiles ([-W; Qh]) have been read: the group's next chunk's
@@ -1160,22 +1165,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t id_e = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id_v = idesc_bf16(128, 128, true, true);
         constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);
+        const uint32_t bkc = sdesc_lo(kcb, 8192), avb = sdesc_lo(st + L::kV, 8192);
+        const uint32_t baq = sdesc_lo(tps + 8192, 16);  // A^qk rows
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t bk = sdesc_sw128(kcb + k4 * 2048, 8192, 1024);
-          mma_bf16_tmem_a(tmem + kRD4, tmem + kREV + 8u * k4, bk, id_e, k4 > 0);
-        }
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_ts(tmem + kRD4, tmem + kREV + 8u * k4, bkc + 128 * k4, sdesc_hi(1024), id_e, k4 > 0);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t av = sdesc_sw128(st + L::kV + k4 * 2048, 8192, 1024);
-          const uint64_t bk = sdesc_sw128(kcb + k4 * 2048, 8192, 1024);
-          mma_bf16(tmem + kRD4, av, bk, id_v, 1);
-        }
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_ss(tmem + kRD4, avb + 128 * k4, sdesc_hi(1024), bkc + 128 * k4, sdesc_hi(1024), id_v, 1);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t bq = sdesc_sw128(tps + 8192 + k4 * 32, 16, 1024);  // A^qk rows
-          mma_bf16_tmem_a(tmem + kRD1 + 64, tmem + kREV + 8u * k4, bq, id_o, 1);
-        }
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_ts(tmem + kRD1 + 64, tmem + kREV + 8u * k4, baq + 2 * k4, sdesc_hi(1024), id_o, 1);
         mma_commit(ctx.bar(kMmaS));
         ctx.wait(kMmaS, sph & 1);
         mbar_arrive(ctx.bar(kKcFree0 + kb));  // Kc[kb] and TP[s] have been read
@@ -1202,34 +1202,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // outputs: row v of O^T / s, tokens 32 hs .. 32 hs + 31.  A full chunk goes into its
-      // v area (Vb has been read), laid out as the output box, and leaves by TMA; a
-      // sequence's partial last chunk is stored directly (a box would pass its end).
+      // outputs: row v of O^T / s, tokens 32 hs .. 32 hs + 31, into the chunk's v area (Vb
+      // has been read) laid out as the two 64-channel output boxes (128-byte swizzle: token
+      // row r, 16-byte piece j at r * 128 + ((j ^ (r & 7)) << 4)).  A full chunk leaves by
+      // TMA; a sequence's partial last chunk is copied out row by row (a box would pass its
+      // end).
       const bool full = len == C;
-      const uint32_t ostage = st + L::kV + (v >> 6) * 8192;  // this d_v half's 64-column box
+      const uint32_t obase = st + L::kV + (v >> 6) * 8192 + 2 * (v & 7);
+      const uint32_t opiece = ((v & 63) >> 3) << 4;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float a[16];
         tmem_ld16(tmem + lane_base + kRD1 + 64 + 32 * hs + 16 * hh, a);
         if (store) {
-          const int i0 = 32 * hs + 16 * hh;  // first token of these columns
-          if (full) {
+          const uint32_t ob = obase + (32 * hs + 16 * hh) * 128;  // first token of these columns
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              st_shared_u16(ostage + sw128(i0 + i, (v & 63) >> 3) + 2 * (v & 7),
-                            __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * a[i])));
-          } else {
-            __nv_bfloat16 *ocol = p.out + ((size_t)(t0 + i0) * H + h) * DV + v;
-            const int nt = min(16, len - i0);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (i < nt) ocol[(size_t)i * H * DV] = __float2bfloat16_rn(p.scale * a[i]);
-          }
+          for (int i = 0; i < 16; ++i)
+            st_shared_u16(ob + i * 128 + (opiece ^ ((i & 7) << 4)),
+                          __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * a[i])));
         }
       }
       fence_async_smem();
       tc_fence_before();
       bar_sync(2, 256);  // every thread has read kRD4, kRD1 and G_last[gb], and staged its outputs
+      if (!full && store) {
+#pragma unroll 1
+        for (int idx = st_id; idx < len * 16; idx += 256) {
+          const int r = idx >> 4, box = (idx >> 3) & 1, j = idx & 7;  // token r, channels 64 box + 8 j
+          const uint4 w = ld_shared_v4(st + L::kV + box * 8192 + r * 128 + ((j ^ (r & 7)) << 4));
+          *reinterpret_cast<uint4 *>(p.out + ((size_t)(t0 + r) * H + h) * DV + 64 * box + 8 * j) = w;
+        }
+      }
       if (st_id == 0) {
         mbar_arrive(ctx.bar(kGmRead0 + gb));
         if (store && full && !*abort_flag) {
