@@ -73,6 +73,7 @@ constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr int kThreads = 512;  // 8 K-side warps, 8 state-side warps
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr uint32_t kWaitCycles32 = 2000000000u;  // ~1 s: the bound of the in-loop waits (32-bit clock)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinGamma = 1.8e-35f;  // about exp(-80): the state side checks gamma = exp(G_last)
 
@@ -182,11 +183,17 @@ struct Ctx {
   volatile int *abort;
   uint32_t *status;
   __device__ __forceinline__ uint32_t bar(uint32_t i) const { return bars + 8 * i; }
+  // Bounded wait on mbarrier i (about 1 s of SM clock); a timeout is recorded in the
+  // CTA's abort flag, which ends every later wait at once and is reported in the status
+  // word when the CTA leaves (one site, so each inlined wait stays small).
   __device__ __forceinline__ void wait(uint32_t i, uint32_t parity) const {
-    if (*abort) return;
-    if (!mbar_wait(bar(i), parity, kWaitCycles)) {
-      *abort = 1;
-      atomicCAS(status, 0u, kStatusTimeout);
+    if (*abort || mbar_try_wait(bar(i), parity)) return;
+    const uint32_t t0 = static_cast<uint32_t>(clock());
+    while (!mbar_try_wait(bar(i), parity)) {
+      if (static_cast<uint32_t>(clock()) - t0 > kWaitCycles32) {
+        *abort = 1;
+        return;
+      }
     }
   }
   // Bounded wait until the global word *w (written by another CTA) reaches target;
@@ -657,18 +664,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        float G[32];
+      for (int hh = 0; hh < 4; ++hh) {  // channels 64 half + 16 hh .. + 15
+        float G[16];
         if (chan) {
-          tmem_ld32(tm + lane_base + 64 * half + 32 * hh, G);
+          tmem_ld16(tm + lane_base + 64 * half + 16 * hh, G);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) G[j] = g_row;
+          for (int j = 0; j < 16; ++j) G[j] = g_row;
         }
         if (r == len - 1) {  // the chunk's last valid row: gamma = exp(G_last) for the state side
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4 *>(glast + (c % kGl) * 128 + 64 * half + 32 * hh + j) =
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(glast + (c % kGl) * 128 + 64 * half + 16 * hh + j) =
                 make_float4(fast_exp2(G[j] * kLog2e), fast_exp2(G[j + 1] * kLog2e),
                             fast_exp2(G[j + 2] * kLog2e), fast_exp2(G[j + 3] * kLog2e));
         }
@@ -677,8 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // factors are the row's own, formed once before the loop.
         auto products = [&](auto per_channel, auto normed) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t addr = kq + sw128(r, 4 * hh + q);
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t addr = kq + sw128(r, 2 * hh + q);
             uint4 kw = ld_shared_v4(addr), qw = ld_shared_v4(addr + L::kQoff);
             if (!valid) kw = qw = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t kp[4] = {kw.x, kw.y, kw.z, kw.w}, qp[4] = {qw.x, qw.y, qw.z, qw.w};
@@ -705,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             st_shared_v4(addr, kh[0], kh[1], kh[2], kh[3]);
             st_shared_v4(addr + L::kQoff, qh[0], qh[1], qh[2], qh[3]);
-            st_shared_v4(kcb + half * 8192 + sw128(r, 4 * hh + q), kc[0], kc[1], kc[2], kc[3]);
+            st_shared_v4(kcb + half * 8192 + sw128(r, 2 * hh + q), kc[0], kc[1], kc[2], kc[3]);
           }
         };
         if (!chan) {
@@ -767,19 +774,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 32 x 32 block; the zero blocks above the diagonal are not stored).  T is
         // then computed in place there.
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float a[32];
-          tmem_ld32(tm + lane_base + 32 * hh, a);
+        for (int hh = 0; hh < 4; ++hh) {  // columns 16 hh .. 16 hh + 15
+          float a[16];
+          tmem_ld16(tm + lane_base + 16 * hh, a);
           if (row < 64) {  // A^kk row (strictly lower)
             // Entries on and above the diagonal of a diagonal block are stored unmasked:
             // the substitution below reads only the strictly lower ones and then
             // overwrites each block with its inverse.
             const int I = row >> 4, rl = row & 15;
+            const int J = hh;  // block column
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int j = 32 * hh + 4 * q;  // global column of this float4
+            for (int q = 0; q < 4; ++q) {
+              const int j = 16 * hh + 4 * q;  // global column of this float4
               const float4 v = make_float4(a[4 * q + 0], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
-              const int J = j >> 4;  // block column (compile-time)
               if (J == I) *reinterpret_cast<float4 *>(Sd + sd_idx(I, rl, j & 15)) = v;
               if ((I == 1 && J == 0) || (I == 3 && J == 2))
                 *reinterpret_cast<float4 *>(So + so_idx(I >> 1, rl, j & 15)) = v;
@@ -788,14 +795,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {  // A^qk row (lower, diagonal included) -> bf16 TP rows 64-127
             const int i = row - 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
               float v[8];
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) {
-                const int j = 32 * hh + 8 * q + jj;
+                const int j = 16 * hh + 8 * q + jj;
                 v[jj] = j <= i ? a[8 * q + jj] : 0.f;
               }
-              st8(tp + sw128(row, 4 * hh + q), v);
+              st8(tp + sw128(row, 2 * hh + q), v);
             }
           }
         }
@@ -1025,15 +1032,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -W in bf16 over the row's Kb: rows 0-63 of the state product's B operand
         // [-W; Qh] (its rows 64-127 are Qh in the q area)
 #pragma unroll 1
-        for (int hq = 0; hq < 4; ++hq) {  // channels 32 hq .. 32 hq + 31
-          float a[32];
-          tmem_ld32(tm + lane_base + 32 * hq, a);
+        for (int hq = 0; hq < 8; ++hq) {  // channels 16 hq .. 16 hq + 15
+          float a[16];
+          tmem_ld16(tm + lane_base + 16 * hq, a);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 2; ++j) {
             float w8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) w8[e] = -a[8 * j + e];
-            st8(st + (hq >> 1) * L::kKQ1 + sw128(row, 4 * (hq & 1) + j), w8);
+            st8(st + (hq >> 2) * L::kKQ1 + sw128(row, 2 * (hq & 3) + j), w8);
           }
         }
       }
@@ -1267,6 +1274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c >= 0) mbar_wait(ctx.bar(kFull[part] + sidx), (c >> c_shift) & 1, kWaitCycles);
       }
   }
+  if (tid == 0 && *abort_flag) atomicCAS(p.status, 0u, kStatusTimeout);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
