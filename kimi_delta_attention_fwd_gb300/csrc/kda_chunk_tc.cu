@@ -129,7 +129,9 @@ enum : uint32_t {
   kReady0 = 8,     // K-side -> state side: the chunk's state-independent operands are complete
   kGmRead0 = 10,   // state side -> K-side: G_last[b] has been read (3 slots)
   kKcFree0 = 13,   // state side -> K-side: Kc[b] and TP of that chunk read (3 slots)
-  kMmaK0 = 16, kMmaS = 18, kFinK0 = 19, kFinS = 21, kNever = 22, kNumBars = 23
+  kMmaK0 = 16, kMmaS = 18, kFinK0 = 19, kFinS = 21, kNever = 22,
+  kTPReady0 = 23,  // K-side -> state side: [T; A^qk] (and Vb, with helpers) of the stage are complete
+  kNumBars = 25
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier area");
 
@@ -648,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rq = fast_exp2(-0.5f * fast_log2(fmaxf(ssq, 1e-24f)));
       }
       const float bk = kPrep ? brow * rk : brow;  // Kb's row factor
+      const uint32_t bb = pack_bf16x2(brow, brow);  // beta in bf16 pairs: Kb's factor is beta exp(G)
       // exp(G), beta exp(G) and exp(-G) of the row, when G is one per row
       uint32_t f_row = 0u, fk_row = 0u, fe_row = 0u;
       if (!chan) {
@@ -702,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   fe = pack_bf16x2(fast_exp2(lk - d0), fast_exp2(lk - d1));
                 } else {
                   f = pack_bf16x2(e0, e1);
-                  fk = pack_bf16x2(brow * e0, brow * e1);
+                  fk = mul_bf16x2(f, bb);
                   fe = pack_bf16x2(fast_exp2(-d0), fast_exp2(-d1));
                 }
               }
@@ -991,10 +994,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }  // !fed
 
-      // Vb = diag(beta) V in place once the v tile has landed: thread t scales the
-      // d_v half t / 64 of row t mod 64, whose beta it holds
-      ctx.wait(kFullV0 + s, cur);
-      {
+      // With the solve helpers (where the state side is the longer chain) the K-side forms
+      // Vb = diag(beta) V in place once the v tile has landed: thread t scales the d_v half
+      // t / 64 of row t mod 64, whose beta it holds.  In the plain schedule the state side
+      // does it (only the state side reads Vb).
+      if constexpr (kSched) {
+        ctx.wait(kFullV0 + s, cur);
         const uint32_t fb = pack_bf16x2(brow, brow);
         const uint32_t vrow = st + L::kV + (t >> 6) * 8192;
 #pragma unroll
@@ -1007,8 +1012,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();  // also orders the solve's scratch writes before the g reload
       bar_sync(bar_id, 128);
-      // the g area (solve scratch) is free: the group's next chunk's g tile
-      if (t == 0 && !fed && c + 2 < nchunks && !*abort_flag) load_g(s, c + 2);
+      if (t == 0) {
+        // the state side's first products need [T; A^qk] and Vb only: they can start now
+        mbar_arrive(ctx.bar(kTPReady0 + s));
+        // the g area (solve scratch) is free: the group's next chunk's g tile
+        if (!fed && c + 2 < nchunks && !*abort_flag) load_g(s, c + 2);
+      }
 
       // [T; A^qk] Kb -> D2, rows 0-63: W = T Kb
       if (t == 0) {
@@ -1088,6 +1097,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = sbase + s * L::kStageBytes;
       const uint32_t tps = sbase + L::kTP + s * 16384;
       const uint32_t kcb = sbase + L::kKc + kb * 16384;
+      // plain schedule: this thread's share of Vb = diag(beta) V, row vr and d_v columns
+      // 32 (st_id / 64) .. + 31; its beta is loaded first
+      const int vr = st_id & 63;
+      float vbeta = 0.f;
+      if constexpr (!kSched) {
+        if (vr < len) {
+          vbeta = __bfloat162float(p.beta[(size_t)(t0 + vr) * H + h]);
+          if (kPrep && (p.prep & kPrepBetaSigmoid)) vbeta = fast_rcp(1.f + fast_exp2(-kLog2e * vbeta));
+        }
+      }
       // S^T in bf16 pairs -> columns [kRA + 32 hs, +32) of lane v: the state product's A operand
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -1095,6 +1114,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) pk[jj] = pack_bf16x2(S[32 * hh + 2 * jj], S[32 * hh + 2 * jj + 1]);
         tmem_st16(tmem + lane_base + kRA + 32 * hs + 16 * hh, pk);
+      }
+      if constexpr (!kSched) {
+        ctx.wait(kFullV0 + s, (c >> 1) & 1);
+        const uint32_t fb = pack_bf16x2(vbeta, vbeta);
+        const uint32_t vrow = st + L::kV + (st_id >> 7) * 8192;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t addr = vrow + sw128(vr, 4 * ((st_id >> 6) & 1) + q);
+          const uint4 w = ld_shared_v4(addr);
+          st_shared_v4(addr, mul_bf16x2(w.x, fb), mul_bf16x2(w.y, fb), mul_bf16x2(w.z, fb),
+                       mul_bf16x2(w.w, fb));
+        }
+        fence_async_smem();  // Vb is read by the state products
       }
       tc_fence_before();
       bar_sync(2, 256);
@@ -1105,9 +1137,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!*abort_flag) load_v(pend_v & 1, pend_v);
           pend_v = -1;
         }
-        ctx.wait(kReady0 + s, (c >> 1) & 1);
+        ctx.wait(kTPReady0 + s, (c >> 1) & 1);
         tc_fence_after();
-        // [(E - Vb)^T | X^T] = Vb^T [T; A^qk]^T - Vb^T [I | 0] + S^T [-W; Qh]^T, one commit
+        // [(E - Vb)^T | X^T] = Vb^T [T; A^qk]^T - Vb^T [I | 0] + S^T [-W; Qh]^T, one commit:
+        // the first two terms as soon as [T; A^qk] is there, the state product once -W is
         constexpr uint32_t id_init = idesc_bf16(128, 128, true, false);
         constexpr uint32_t id_negi = idesc_bf16(128, 64, true, false);
         const uint32_t avb = sdesc_lo(st + L::kV, 8192);  // Vb^T (MN-major)
@@ -1120,6 +1153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
           mma_ss(tmem + kRD1, avb + 128 * k4, sdesc_hi(1024), bni + 2 * k4, sdesc_hi(1024), id_negi, 1);
+        ctx.wait(kReady0 + s, (c >> 1) & 1);
+        tc_fence_after();
         constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8)
