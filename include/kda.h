@@ -159,8 +159,10 @@ int kda_chunk_fwd(const kda_shape *shape, const void *q, const void *k, const vo
 /* Bytes of workspace with which kda_chunk_fwd can run every schedule for this
  * shape (always >= 256), or 0 if the shape is invalid: the status block, on the
  * tensor-core path with a gate one flag word per sequence-head (rounded up to 256
- * bytes), and for few sequence-heads a ring through which extra CTAs hand over the
- * chunk solve (4 x 16 KiB + 32 bytes per sequence-head). */
+ * bytes), and either, for few sequence-heads, a ring through which extra CTAs hand
+ * over the chunk solve (4 x 16 KiB + 32 bytes per sequence-head) or, for 2 to 2048
+ * sequences, the launch order (4 bytes per sequence, rounded up to 256) with which
+ * the longest sequences start first when the launch takes more than one wave. */
 size_t kda_chunk_fwd_workspace_bytes(const kda_shape *shape);
 
 /* The prefill kernel a call with this shape runs: KDA_ALGO_TENSOR or

@@ -165,6 +165,8 @@ struct TcParams {
   int npairs;                // P, the number of (sequence, head) pairs
   uint8_t *ring;             // [P][kRingSlots][kRingSlotBytes]
   uint32_t *ring_flags;      // [P][kRingSlots][2]: chunk + 1 published, consumptions (zeroed)
+  const int32_t *order;      // plain schedule: sequences longest first (CTA i takes sequence
+                             // order[i / H], head i % H), or NULL for the given order
 };
 
 // Global-memory hand-over between CTAs of one launch (all resident: cooperative launch).
@@ -343,7 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hpp = kSched ? p.helpers_per_pair : 1;
   const int hb = (int)blockIdx.x - P;
   const int hp = helper ? hb % hpp : 0;
-  const int pair = helper ? hb / hpp : (int)blockIdx.x;
+  const int pair = helper ? hb / hpp
+                          : (kSched || !p.order ? (int)blockIdx.x
+                                                : p.order[blockIdx.x / p.H] * p.H + (int)(blockIdx.x % p.H));
   // the chunks a stage / K-side group kw takes: c = c_first(kw) + i * c_step, phase i & 1
   const int c_step = helper ? 2 * hpp : 2;
   const int c_shift = helper && hpp == 2 ? 2 : 1;
@@ -1348,6 +1352,30 @@ bool make_map(CUtensorMap *m, const void *base, int T, int H) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch order of the plain schedule when it needs more than one wave: the sequences
+// sorted longest first (ties by index), so the longest chains start first and the last
+// wave holds the short ones.  One CTA ranks the (length, index) keys in shared memory
+// (all threads read the same key at a time); offsets out of order count as length 0
+// (the prefill kernel skips and reports them).
+constexpr int kOrderMaxSeqs = 2048;
+__global__ void __launch_bounds__(1024) kda_tc_order_kernel(const int32_t *cu_seqlens, int N, int T,
+                                                            int32_t *order) {
+  extern __shared__ unsigned long long okeys[];
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int a = cu_seqlens[i], b = cu_seqlens[i + 1];
+    const int len = (0 <= a && a <= b && b <= T) ? b - a : 0;
+    okeys[i] = (static_cast<unsigned long long>(0x7FFFFFFF - len) << 32) | static_cast<unsigned>(i);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const unsigned long long ki = okeys[i];
+    int rank = 0;
+    for (int j = 0; j < N; ++j) rank += okeys[j] < ki;
+    order[rank] = i;
+  }
+}
+size_t order_bytes(long long num_seqs) { return (static_cast<size_t>(num_seqs) * 4 + 255) / 256 * 256; }
+
 // Ring of the helper schedule: [P][kRingSlots] slot images, then [P][kRingSlots][2] words.
 size_t ring_bytes(long long pairs) {
   return static_cast<size_t>(pairs) * kRingSlots * (kRingSlotBytes + 2 * sizeof(uint32_t));
@@ -1358,7 +1386,8 @@ size_t ring_bytes(long long pairs) {
 bool chunk_tc_supported(int d_k, int d_v, bool bf16) { return bf16 && d_k == 128 && d_v == 128; }
 size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int, int) {
   const long long pairs = (long long)num_seqs * num_heads;
-  return pairs >= 1 && pairs <= kHelperMaxPairs ? ring_bytes(pairs) : 0;
+  if (pairs >= 1 && pairs <= kHelperMaxPairs) return ring_bytes(pairs);  // solve helpers
+  return num_seqs >= 2 && num_seqs <= kOrderMaxSeqs ? order_bytes(num_seqs) : 0;  // launch order
 }
 
 // The launch of one instantiation: the solve-helper schedule when it fits (cooperative),
@@ -1395,6 +1424,16 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     prm.ring = nullptr;
     prm.ring_flags = nullptr;
     prm.helpers_per_pair = 1;
+  }
+  // More than one wave: start the longest sequences first (when the workspace has room)
+  if (pairs > a.num_sms && a.num_seqs >= 2 && a.num_seqs <= kOrderMaxSeqs && a.scratch &&
+      a.scratch_bytes >= order_bytes(a.num_seqs)) {
+    int32_t *order = static_cast<int32_t *>(a.scratch);
+    kda_tc_order_kernel<<<1, 1024, a.num_seqs * sizeof(unsigned long long), stream>>>(
+        a.cu_seqlens, a.num_seqs, a.total_tokens, order);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    prm.order = order;
   }
   kda_chunk_tc_kernel<false, kPrep><<<(unsigned)pairs, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, mo,
                                                                                           prm);
@@ -1437,6 +1476,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.flags = a.test_flags;
   prm.ring = nullptr;
   prm.ring_flags = nullptr;
+  prm.order = nullptr;
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   prm.npairs = static_cast<int>(pairs);
   if (pairs == 0) return cudaSuccess;

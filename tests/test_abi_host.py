@@ -77,15 +77,18 @@ def test_workspace_size(lib):
 def test_workspace_holds_the_solve_helper_ring_for_few_sequence_heads(lib):
     """Tensor-core path: the status block, one recomputation flag word per
     sequence-head (rounded up to 256 bytes; none without a gate), and with at most 76
-    sequence-heads a ring of 4 x 16 KiB and 32 bytes per sequence-head."""
+    sequence-heads a ring of 4 x 16 KiB and 32 bytes per sequence-head; with more, for 2 to
+    2048 sequences, the launch order (4 bytes per sequence, rounded up to 256)."""
     ws = lambda **kw: lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(**kw)))
     assert ws(num_seqs=1, num_heads=1) == 256 + 256 + 65568
     assert ws(num_seqs=19, num_heads=2) == 256 + 256 + 38 * 65568
     assert ws(num_seqs=13, num_heads=3) == 256 + 256 + 39 * 65568
     assert ws(num_seqs=38, num_heads=2) == 256 + 512 + 76 * 65568   # the most with a ring
-    assert ws(num_seqs=11, num_heads=7) == 256 + 512                 # 77 sequence-heads: no ring
+    assert ws(num_seqs=11, num_heads=7) == 256 + 512 + 256           # 77 sequence-heads: no ring
     assert ws(num_seqs=1, num_heads=32) == 256 + 256 + 32 * 65568
-    assert ws(num_seqs=64, num_heads=32) == 256 + 2048 * 4  # flags only
+    assert ws(num_seqs=64, num_heads=32) == 256 + 2048 * 4 + 256  # flags, launch order
+    assert ws(num_seqs=2048, num_heads=1) == 256 + 2048 * 4 + 2048 * 4  # the most sequences ordered
+    assert ws(num_seqs=2049, num_heads=1) == 256 + 8448  # flags only: too many to order
     assert ws(num_seqs=1, num_heads=1, gate=K.KDA_GATE_NONE) == 256 + 65568  # no decay, no flag
     assert ws(num_seqs=1, num_heads=1, algo=K._ALGOS["simt"]) == 256
     assert ws(num_seqs=1, num_heads=1, io_dtype=K.KDA_F32) == 256  # CUDA-core path

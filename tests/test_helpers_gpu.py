@@ -140,7 +140,7 @@ def test_helper_schedule_on_concurrent_streams():
 
 def test_more_pairs_than_helpers_use_the_plain_schedule():
     lens = [100] * 11
-    assert kda_chunk_fwd_workspace_bytes(11, 1100, 7, 128, 128) == STATUS_BYTES + 512  # 77 pairs
+    assert kda_chunk_fwd_workspace_bytes(11, 1100, 7, 128, 128) == STATUS_BYTES + 512 + 256  # 77: order
     assert kda_chunk_fwd_workspace_bytes(38, 3800, 2, 128, 128) > STATUS_BYTES + 512  # 76
     spec = W.custom_prefill(lens, num_heads=7, d=128, gate="mixed", seed=68)
     x = W.prefill_inputs(spec)
