@@ -269,10 +269,17 @@ def run_prefill(args, ws, rank, dev, workload, e2e=True, steps=None):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    from kimi_delta_attention_fwd_gb300 import kda_workspace_status
+    from kimi_delta_attention_fwd_gb300 import kda_workspace_status, workspace_status_words
     status = kda_workspace_status(work, stream)
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
+    # the tensor-core schedule that ran (status word 2): the segment-parallel scan of one
+    # sequence launches the run tables, the start states, the first pass, the combine, the
+    # second pass and the final-state copy in place of the one prefill kernel
+    schedule = {1: "plain", 2: "solve helpers", 3: "segments"}.get(
+        int(workspace_status_words(work)[2]), "none") if tensor_path else "none"
+    if schedule == "segments":
+        per_call += 5
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
@@ -311,7 +318,7 @@ def run_prefill(args, ws, rank, dev, workload, e2e=True, steps=None):
     config = {"workload": workload, "num_seqs": N, "total_tokens": T, "num_heads": H,
               "d_k": dk, "d_v": dv, "chunk": 64, "io_dtype": spec.io_dtype, "gate": args.gate,
               "prep": "silu + l2norm of q, k; sigmoid of beta" if args.prep else "none",
-              "kernel": kind, "l2": "inputs larger than L2 (%.0f MB read+written per step)" % (alg_bytes / 1e6),
+              "kernel": kind, "schedule": schedule, "l2": "inputs larger than L2 (%.0f MB read+written per step)" % (alg_bytes / 1e6),
               "parallelism": f"replicas x{ws} (independent sequences per GPU)"}
     if not e2e:
         del d, out, fin, work

@@ -90,8 +90,8 @@ extern "C" {
 // 1.1: kda_recurrent_fwd; 1.2: kda_shape.prep; 1.3: device-checked offsets
 // (KDA_ERR_SEQLENS, kda_last_device_status), the exact recomputation of sequence-heads
 // beyond the tensor-core decay range, kda_noalloc_status; 1.4: KDA_PREP_G_SOFTPLUS and
-// kda_shape.gate_scale
-int kda_version(void) { return 1004; }
+// kda_shape.gate_scale; 1.5: the segment-parallel scan of one sequence
+int kda_version(void) { return 1005; }
 
 const char *kda_status_string(int status) {
   switch (status) {
@@ -114,7 +114,8 @@ const char *kda_status_string(int status) {
 size_t kda_chunk_fwd_workspace_bytes(const kda_shape *s) {
   if (check_shape(s, false) != KDA_OK) return 0;
   size_t bytes = kda::kStatusBytes + flag_bytes(s);
-  if (use_tensor_path(s)) bytes += kda::chunk_tc_scratch_bytes(s->num_seqs, s->num_heads, s->d_k, s->d_v);
+  if (use_tensor_path(s))
+    bytes += kda::chunk_tc_scratch_bytes(s->num_seqs, s->total_tokens, s->num_heads, s->d_k, s->d_v);
   return bytes;
 }
 

@@ -47,7 +47,9 @@
 // K-side group its g tile (after the solve), the state side its k and q tiles
 // (after its first product has read [-W; Qh]) and its v tile (after the chunk's
 // outputs, staged there, have been stored by TMA).  With few sequence-heads, one or
-// two more CTAs per sequence-head run the solve of its chunks ("Solve helpers" below).
+// two more CTAs per sequence-head run the solve of its chunks ("Solve helpers" below);
+// one long sequence with few heads is cut into segments that run side by side and are
+// chained through their affine state maps ("Segment-parallel scan" below).
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // KDA_ERR_DEVICE_TIMEOUT in the status word and runs to completion without
 // waiting again (outputs are then undefined, nothing blocks or faults).
@@ -58,6 +60,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "kda_internal.h"
@@ -167,7 +170,15 @@ struct TcParams {
   uint32_t *ring_flags;      // [P][kRingSlots][2]: chunk + 1 published, consumptions (zeroed)
   const int32_t *order;      // plain schedule: sequences longest first (CTA i takes sequence
                              // order[i / H], head i % H), or NULL for the given order
+  int seq_stride;            // 1: sequence n spans cu_seqlens[n] .. cu_seqlens[n + 1]; 4 (plain
+                             // schedule, the segment passes of one sequence): cu_seqlens holds
+                             // runs {first token, end token, kRun* mode, 0} instead, order unused
 };
+
+// Modes of a segment run (the segment-parallel scan of one long sequence): V enters as zero
+// (from the identity as start state the run then gives the segment's transfer matrix); the
+// outputs are not stored; the run is skipped altogether.
+constexpr int kRunZeroV = 1, kRunNoOut = 2, kRunSkip = 4;
 
 // Global-memory hand-over between CTAs of one launch (all resident: cooperative launch).
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
@@ -330,9 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
   // set by the state side once this pair's decay has left the range: nothing more is stored
+  // bit 0: no chunk runs and nothing is written; bit 1: the outputs are not stored
   volatile int *skip_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
   // the last chunk loaded into each stage part [stage][q, g, k, v] (-1: none), for the drain
   volatile int *issued = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
+  // the token coordinate of the V tile of chunk 0: bos, or far below zero when V enters as
+  // zero (the tiles then lie wholly outside the tensor and TMA fills them with zeros)
+  volatile int *v_tok0 = reinterpret_cast<volatile int *>(smem + L::kMisc + 48);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -357,9 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = pair / H, h = pair % H;
   // a pair whose offsets are out of order or out of range runs no chunk and writes nothing
   // (its skip flag is set below); bos and eos stay reloadable from cu_seqlens
-  const int bos = p.cu_seqlens[n];
-  const bool seq_ok = 0 <= bos && bos <= p.cu_seqlens[n + 1] && p.cu_seqlens[n + 1] <= p.T;
-  const int eos = seq_ok ? p.cu_seqlens[n + 1] : bos;
+  const bool seg_run = !kSched && p.seq_stride == 4;
+  const int32_t *bnd = p.cu_seqlens + (seg_run ? 4 * n : n);
+  const int bos = bnd[0];
+  const bool seq_ok = 0 <= bos && bos <= bnd[1] && bnd[1] <= p.T;
+  // a segment run is skipped when its table says so, or when an earlier pass marked its head
+  // for the exact recomputation (whose outputs and final state replace the run's)
+  const bool run_skip = seg_run && ((bnd[2] & kRunSkip) || (p.pair_flags && p.pair_flags[h]));
+  const int eos = seq_ok && !run_skip ? bnd[1] : bos;
   const int nchunks = (eos - bos + C - 1) / C;
 
   Ctx ctx{sbase + L::kBars, abort_flag, p.status};
@@ -394,19 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto load_v = [&](int sidx, int c) {
     const uint32_t fb = ctx.bar(kFullV0 + sidx), st = stage_at(sidx);
     mbar_arrive_expect_tx(fb, 16384);
-    tma_load_3d(st + L::kV, &tm_v, fb, 0, h, bos + c * C);
-    tma_load_3d(st + L::kV + 8192, &tm_v, fb, 64, h, bos + c * C);
+    const int tok = *v_tok0 + c * C;
+    tma_load_3d(st + L::kV, &tm_v, fb, 0, h, tok);
+    tma_load_3d(st + L::kV + 8192, &tm_v, fb, 64, h, tok);
     issued[4 * sidx + 3] = c;
   };
 
   if (tid == 0) {
     *abort_flag = 0;
-    *skip_flag = seq_ok ? 0 : 1;
+    *skip_flag = (seq_ok && !run_skip ? 0 : 1) | (seg_run && (bnd[2] & kRunNoOut) ? 2 : 0);
+    *v_tok0 = seg_run && (bnd[2] & kRunZeroV) ? -(1 << 30) : bos;  // T < 2^30: c C - 2^30 < 0
     for (int i = 0; i < 8; ++i) issued[i] = -1;
     if (!seq_ok) atomicCAS(p.status, 0u, kStatusSeqlens);
     for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(ctx.bar(i), 1);
     fence_mbar_init();
-    if (blockIdx.x == 0) p.status[2] = kSched ? kSchedHelpers : kSchedPlain;  // which schedule ran
+    if (blockIdx.x == 0) p.status[2] = kSched ? kSchedHelpers : (seg_run ? kSchedSegments : kSchedPlain);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -1182,10 +1204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // recomputation (or is reported without the flags): from here on this CTA stores
         // nothing for it; the pipeline itself runs on unchanged
         const float gam = glast[gb * 128 + st_id];
-        if (!(gam >= kMinGamma) && !*skip_flag) {
+        if (!(gam >= kMinGamma) && !(*skip_flag & 1)) {
           *skip_flag = 1;
           if (p.pair_flags) {
-            if (atomicExch(p.pair_flags + pair, 1u) == 0u) atomicAdd(p.status + 3, 1u);
+            // (segment runs belong to the one sequence: its head h is the pair to recompute)
+            if (atomicExch(p.pair_flags + (!kSched && p.seq_stride == 4 ? h : pair), 1u) == 0u) atomicAdd(p.status + 3, 1u);
           } else {
             atomicCAS(p.status, 0u, kStatusGateRange);
           }
@@ -1229,7 +1252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++sph;
       bar_sync(2, 256);
       tc_fence_after();
-      const bool store = !*skip_flag;  // read after the barrier that follows every setter
+      // read after the barrier that follows every setter of the skip flag
+      const bool store = !*skip_flag;
       {  // S <- gamma (S + Kc^T E), elementwise per key channel
         const float4 *g4 = reinterpret_cast<const float4 *>(glast + gb * 128 + 64 * hs);
 #pragma unroll
@@ -1291,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     bar_sync(2, 256);  // every setter of the skip flag is done
-    if (p.final_state && !*skip_flag) {
+    if (p.final_state && !(*skip_flag & 1)) {
 #pragma unroll
       for (int j = 0; j < 64; ++j) p.final_state[soff + (size_t)j * DV] = S[j];
     }
@@ -1376,6 +1400,139 @@ __global__ void __launch_bounds__(1024) kda_tc_order_kernel(const int32_t *cu_se
 }
 size_t order_bytes(long long num_seqs) { return (static_cast<size_t>(num_seqs) * 4 + 255) / 256 * 256; }
 
+// Segment-parallel scan of one long sequence ("Kimi Delta Attention (KDA)", the state
+// recurrence is affine in the start state: S_end = M S_start + B over any stretch of
+// tokens, M the product of the per-token transitions (I - beta k k^T) Diag(alpha)).
+// With few heads the helpers still leave most SMs idle, so the sequence is cut into P
+// segments of whole chunks:
+//   pass 1  segment 0 from the true start (its outputs are final); every middle segment
+//           p = 1 .. P - 2 twice, from zero (its end state B_p) and from the identity with
+//           V taken as zero (its transfer matrix M_p, as d_k = d_v);
+//   combine S_1 = end of segment 0, S_{p+1} = M_p S_p + B_p (fp32, column blocks apart);
+//   pass 2  segments 1 .. P - 1 from S_p, storing their outputs; the last one's end state
+//           is the sequence's final state.
+// The first pass runs H (2P - 3) CTAs in one wave: at least 3 segments of at least 32
+// chunks each, otherwise the other schedules run.
+constexpr int kSegMinChunks = 32;
+int seg_count(long long T, int H, int sms) {
+  if (H < 1 || sms < 1 || T >= (1LL << 30)) return 0;  // (zero V tiles are read below token 0)
+  const long long nch = (T + C - 1) / C;
+  const long long P = std::min<long long>((sms / H + 3) / 2, nch / kSegMinChunks);
+  return P >= 3 ? static_cast<int>(P) : 0;
+}
+size_t seg_table_bytes(int P) { return (static_cast<size_t>(3 * P) * sizeof(int4) + 255) / 256 * 256; }
+size_t seg_bytes(int P, int H) {  // run tables, pass-1 end states, start states, pass-2 end states
+  return seg_table_bytes(P) + static_cast<size_t>(4 * P - 5) * H * DK * DV * sizeof(float);
+}
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 152;  // no device: size for a GB300
+  }
+  return sms;
+}
+
+// The run tables of both passes, from the sequence's offsets as the device holds them
+// (checked like every other kernel does: out of order or range, every run is skipped
+// and KDA_ERR_SEQLENS recorded).  Segment q takes chunks q n / P .. (q + 1) n / P - 1 of
+// the sequence's n chunks (sizes differ by one chunk at most); the last one ends at the
+// sequence's end.
+__global__ void kda_seg_table_kernel(const int32_t *cu_seqlens, int T, int P, int4 *runs1, int4 *runs2,
+                                     uint32_t *status) {
+  const int b = cu_seqlens[0], e = cu_seqlens[1];
+  const bool ok = 0 <= b && b <= e && e <= T;
+  if (!ok && threadIdx.x == 0) atomicCAS(status, 0u, kStatusSeqlens);
+  const int skip = ok ? 0 : kRunSkip;
+  const long long n = ok ? (static_cast<long long>(e) - b + C - 1) / C : 0;
+  for (int q = threadIdx.x; q < P; q += blockDim.x) {
+    const int sb = ok ? static_cast<int>(std::min<long long>(b + q * n / P * C, e)) : b;
+    const int se = ok ? static_cast<int>(std::min<long long>(b + (q + 1) * n / P * C, e)) : b;
+    if (q == 0) {
+      runs1[0] = make_int4(sb, se, skip, 0);
+    } else {
+      runs2[q - 1] = make_int4(sb, se, skip, 0);
+      if (q < P - 1) {
+        runs1[2 * q - 1] = make_int4(sb, se, kRunNoOut | skip, 0);
+        runs1[2 * q] = make_int4(sb, se, kRunZeroV | kRunNoOut | skip, 0);
+      }
+    }
+  }
+}
+
+// The start states of the pass-1 runs, in the buffer their end states then overwrite (each
+// thread of the chunk kernel reads and later writes the same elements): run 0 the given
+// initial state (zero without one), runs 2p - 1 zero, runs 2p the identity.
+__global__ void __launch_bounds__(256) kda_seg_init_kernel(float *F1, const float *init, int H) {
+  const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;  // < (2P-3) H d_k d_v
+  const size_t per_run = static_cast<size_t>(H) * DK * DV;
+  const int run = static_cast<int>(i / per_run);
+  const size_t e = i % per_run;  // element of head e / (d_k d_v)
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (run == 0) {
+    if (init) x = *reinterpret_cast<const float4 *>(init + e);
+  } else if (run % 2 == 0) {
+    const int r = static_cast<int>(e % (DK * DV)) / DV, c = static_cast<int>(e % DV);  // c .. c + 3
+    x = make_float4(r == c ? 1.f : 0.f, r == c + 1 ? 1.f : 0.f, r == c + 2 ? 1.f : 0.f, r == c + 3 ? 1.f : 0.f);
+  }
+  *reinterpret_cast<float4 *>(F1 + i) = x;
+}
+
+// S_1 = the end state of segment 0 (pass-1 run 0); S_{p+1} = M_p S_p + B_p with M_p, B_p
+// the end states of pass-1 runs 2p and 2p - 1.  CTA (h, cb) keeps columns 16 cb .. + 15 of
+// head h's state in shared memory (the columns do not mix) and stages each M_p there;
+// thread t forms column t % 16 of rows t / 16 + 16 k.
+__global__ void __launch_bounds__(256) kda_seg_combine_kernel(const float *F1, float *starts, int P, int H) {
+  extern __shared__ float seg_smem[];
+  float *Msh = seg_smem;             // [128][128] M_p
+  float *Ssh = seg_smem + DK * DK;   // [128][16] the current start state's columns
+  const int h = blockIdx.x / 8, cb = blockIdx.x % 8, t = threadIdx.x;
+  const size_t stride = static_cast<size_t>(H) * DK * DV;
+  const float *S1 = F1 + static_cast<size_t>(h) * DK * DV;  // run 0
+  for (int i = t; i < DK * 16; i += blockDim.x) {
+    const int r = i / 16, cc = i % 16;
+    const float x = S1[static_cast<size_t>(r) * DV + 16 * cb + cc];
+    Ssh[i] = x;
+    starts[static_cast<size_t>(h) * DK * DV + static_cast<size_t>(r) * DV + 16 * cb + cc] = x;
+  }
+  const int cc = t % 16, r0 = t / 16;
+  for (int q = 1; q <= P - 2; ++q) {
+    const float *M = F1 + (2 * q) * stride + static_cast<size_t>(h) * DK * DV;
+    const float *B = F1 + (2 * q - 1) * stride + static_cast<size_t>(h) * DK * DV;
+    __syncthreads();  // the previous step's reads of Msh are done
+    for (int i = t; i < DK * DK / 4; i += blockDim.x)
+      reinterpret_cast<float4 *>(Msh)[i] = reinterpret_cast<const float4 *>(M)[i];
+    __syncthreads();
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = B[static_cast<size_t>(r0 + 16 * k) * DV + 16 * cb + cc];
+    for (int j = 0; j < DK; ++j) {
+      const float sj = Ssh[j * 16 + cc];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = fmaf(Msh[(r0 + 16 * k) * DK + j], sj, acc[k]);
+    }
+    __syncthreads();  // every thread has read the old Ssh
+    float *dst = starts + (q * stride) + static_cast<size_t>(h) * DK * DV;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      Ssh[(r0 + 16 * k) * 16 + cc] = acc[k];
+      dst[static_cast<size_t>(r0 + 16 * k) * DV + 16 * cb + cc] = acc[k];
+    }
+  }
+}
+
+// The sequence's final state from the last segment's end state, for every head whose runs
+// all went through (not skipped, not marked for the exact recomputation, which writes it
+// from the untouched initial state instead).
+__global__ void __launch_bounds__(256) kda_seg_final_kernel(const float *Flast, float *final_state,
+                                                            const int4 *last_run, const uint32_t *pair_flags) {
+  const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;  // < H d_k d_v
+  const int h = static_cast<int>(i / (DK * DV));
+  if ((last_run->z & kRunSkip) || (pair_flags && pair_flags[h])) return;
+  *reinterpret_cast<float4 *>(final_state + i) = *reinterpret_cast<const float4 *>(Flast + i);
+}
+
 // Ring of the helper schedule: [P][kRingSlots] slot images, then [P][kRingSlots][2] words.
 size_t ring_bytes(long long pairs) {
   return static_cast<size_t>(pairs) * kRingSlots * (kRingSlotBytes + 2 * sizeof(uint32_t));
@@ -1384,10 +1541,16 @@ size_t ring_bytes(long long pairs) {
 }  // namespace
 
 bool chunk_tc_supported(int d_k, int d_v, bool bf16) { return bf16 && d_k == 128 && d_v == 128; }
-size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int, int) {
+size_t chunk_tc_scratch_bytes(int num_seqs, int total_tokens, int num_heads, int, int) {
   const long long pairs = (long long)num_seqs * num_heads;
-  if (pairs >= 1 && pairs <= kHelperMaxPairs) return ring_bytes(pairs);  // solve helpers
-  return num_seqs >= 2 && num_seqs <= kOrderMaxSeqs ? order_bytes(num_seqs) : 0;  // launch order
+  size_t bytes = 0;
+  if (pairs >= 1 && pairs <= kHelperMaxPairs) bytes = ring_bytes(pairs);  // solve helpers
+  else if (num_seqs >= 2 && num_seqs <= kOrderMaxSeqs) bytes = order_bytes(num_seqs);  // launch order
+  if (num_seqs == 1) {  // one long sequence: the segment-parallel scan, when it applies
+    const int P = seg_count(total_tokens, num_heads, device_sms());
+    if (P) bytes = std::max(bytes, seg_bytes(P, num_heads));
+  }
+  return bytes;
 }
 
 // The launch of one instantiation: the solve-helper schedule when it fits (cooperative),
@@ -1399,6 +1562,47 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
   cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false, kPrep>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (err != cudaSuccess) return err;
+  // One long sequence with few heads: the segment-parallel scan (two passes and a combine)
+  const int P = a.num_seqs == 1 ? seg_count(a.total_tokens, a.num_heads, a.num_sms) : 0;
+  if (P && a.scratch && a.scratch_bytes >= seg_bytes(P, a.num_heads)) {
+    const int H = a.num_heads;
+    const size_t st = static_cast<size_t>(H) * DK * DV;
+    unsigned char *base = static_cast<unsigned char *>(a.scratch);
+    int4 *runs1 = reinterpret_cast<int4 *>(base);
+    int4 *runs2 = runs1 + (2 * P - 3);
+    float *F1 = reinterpret_cast<float *>(base + seg_table_bytes(P));
+    float *starts = F1 + static_cast<size_t>(2 * P - 3) * st;
+    float *F2 = starts + static_cast<size_t>(P - 1) * st;
+    kda_seg_table_kernel<<<1, 128, 0, stream>>>(a.cu_seqlens, a.total_tokens, P, runs1, runs2, a.status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const size_t n1 = static_cast<size_t>(2 * P - 3) * st;  // floats, a multiple of 1024
+    kda_seg_init_kernel<<<(unsigned)(n1 / 1024), 256, 0, stream>>>(F1, a.init_state, H);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    TcParams p1 = prm;
+    p1.cu_seqlens = reinterpret_cast<const int32_t *>(runs1);
+    p1.seq_stride = 4;
+    p1.init_state = F1;  // in place
+    p1.final_state = F1;
+    kda_chunk_tc_kernel<false, kPrep><<<(unsigned)((2 * P - 3) * H), kThreads, L::kAlloc, stream>>>(
+        mq, mk, mg, mv, mo, p1);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const int comb_smem = (DK * DK + DK * 16) * sizeof(float);
+    err = cudaFuncSetAttribute(kda_seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, comb_smem);
+    if (err != cudaSuccess) return err;
+    kda_seg_combine_kernel<<<H * 8, 256, comb_smem, stream>>>(F1, starts, P, H);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    TcParams p2 = prm;
+    p2.cu_seqlens = reinterpret_cast<const int32_t *>(runs2);
+    p2.seq_stride = 4;
+    p2.init_state = starts;
+    p2.final_state = F2;
+    kda_chunk_tc_kernel<false, kPrep><<<(unsigned)((P - 1) * H), kThreads, L::kAlloc, stream>>>(
+        mq, mk, mg, mv, mo, p2);
+    if ((err = cudaGetLastError()) != cudaSuccess || !a.final_state) return err;
+    kda_seg_final_kernel<<<(unsigned)(st / 1024), 256, 0, stream>>>(F2 + static_cast<size_t>(P - 2) * st,
+                                                                    a.final_state, runs2 + (P - 2), a.pair_flags);
+    return cudaGetLastError();
+  }
   // Few sequence-heads leave most SMs idle: with room for the ring, one or two solve
   // helpers per sequence-head join its tile in one cooperative launch (every CTA
   // resident, as the hand-over through global memory needs).
@@ -1477,6 +1681,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.ring = nullptr;
   prm.ring_flags = nullptr;
   prm.order = nullptr;
+  prm.seq_stride = 1;
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   prm.npairs = static_cast<int>(pairs);
   if (pairs == 0) return cudaSuccess;

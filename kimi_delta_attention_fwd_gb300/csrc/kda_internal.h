@@ -17,7 +17,7 @@ constexpr int kPrepSilu = 1, kPrepL2 = 2, kPrepBetaSigmoid = 4, kPrepGSoftplus =
 // (kSchedPlain or kSchedHelpers), word 3: sequence-heads recomputed token by token
 // because a chunk's decay left the tensor-core range.
 constexpr size_t kStatusBytes = 256;
-constexpr uint32_t kSchedPlain = 1, kSchedHelpers = 2;
+constexpr uint32_t kSchedPlain = 1, kSchedHelpers = 2, kSchedSegments = 3;
 // device-reported codes (minus the KDA_ERR_* value)
 constexpr uint32_t kStatusTimeout = 7, kStatusGateRange = 8, kStatusSeqlens = 11;
 
@@ -112,6 +112,6 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
 bool chunk_tc_supported(int d_k, int d_v, bool bf16);
 // Scratch that lets the tensor-core path run every schedule (0 = none needed).
-size_t chunk_tc_scratch_bytes(int num_seqs, int num_heads, int d_k, int d_v);
+size_t chunk_tc_scratch_bytes(int num_seqs, int total_tokens, int num_heads, int d_k, int d_v);
 
 }  // namespace kda

@@ -94,6 +94,23 @@ def test_workspace_holds_the_solve_helper_ring_for_few_sequence_heads(lib):
     assert ws(num_seqs=1, num_heads=1, io_dtype=K.KDA_F32) == 256  # CUDA-core path
 
 
+def test_workspace_holds_the_segments_of_one_long_sequence(lib):
+    """One sequence of at least 3 x 32 chunks with at most 50 heads: the run tables
+    (16 bytes per run, 3 runs per segment, rounded up to 256) and 4P - 5 fp32 states per
+    head for P = min((SMs / H + 3) / 2, chunks / 32) segments, when P >= 3 and that is
+    more than the ring.  Without a device the size is taken for 152 SMs."""
+    ws = lambda **kw: lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(num_seqs=1, **kw)))
+    st = 128 * 128 * 4
+    assert ws(num_heads=4, total_tokens=65536) == 512 + 1024 + 75 * 4 * st   # P = 20
+    assert ws(num_heads=32, total_tokens=65536) == 512 + 256 + 7 * 32 * st   # P = 3
+    assert ws(num_heads=2, total_tokens=64 * 96) == 512 + 256 + 7 * 2 * st   # P = 3: 96 chunks
+    assert ws(num_heads=2, total_tokens=64 * 95) == 512 + 2 * 65568          # 95 chunks: the ring
+    assert ws(num_heads=1, total_tokens=1 << 20) == 512 + 3840 + 303 * st    # P = 77
+    assert ws(num_heads=51, total_tokens=1 << 20) == 512 + 51 * 65568        # two runs a head: no
+    assert ws(num_heads=4, total_tokens=65536, gate=K.KDA_GATE_NONE) == 256 + 1024 + 75 * 4 * st
+    assert lib.kda_version() >= 1005  # 1.5 added the segments
+
+
 def test_status_block_alone_is_an_accepted_workspace(lib):
     """256 bytes select the plain schedule; fewer are rejected before any device call."""
     s = _shape(num_seqs=1, num_heads=1)

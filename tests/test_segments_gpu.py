@@ -1,0 +1,201 @@
+"""The segment-parallel scan of one long sequence with few heads.
+
+The state recurrence of "Kimi Delta Attention (KDA)" is affine in the start state: over
+any stretch of tokens S_end = M S_start + B, with M the product of the per-token
+transitions (I - beta k k^T) Diag(alpha) and B the end state from a zero start.  With one
+sequence, at most 50 heads and at least 3 x 32 chunks, kda_chunk_fwd_workspace_bytes()
+includes room for cutting the sequence into P segments: a first launch runs segment 0
+from the true start and every middle segment from zero (B) and from the identity with
+V = 0 (M), a small kernel chains S_{p+1} = M_p S_p + B_p, and a second launch runs
+segments 1 .. P - 1 from those states.  The rounding differs from the one-chain
+schedules, so the results are compared with the oracle at the bf16 tolerance (and with
+the one-chain schedule at twice it), and word 2 of the status block (3) shows that the
+segments ran.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_fwd_gb300 import (kda_chunk_fwd, kda_chunk_fwd_workspace_bytes,
+                                            workspace_status_words)
+from kimi_delta_attention_fwd_gb300 import workloads as W
+
+from parity import TOL_BF16, rel_l2_per_head, rel_l2_states, run_oracle_prefill, to_dev
+
+pytestmark = pytest.mark.gpu
+
+STATUS_BYTES, SCHED_SEGMENTS = 256, 3
+
+
+def _segments(T, H, sms):
+    nch = (T + 63) // 64
+    P = min((sms // H + 3) // 2, nch // 32)
+    return P if P >= 3 else 0
+
+
+def _seg_start(T, P, q):
+    """First token of segment q (q = P: the end): chunks q n / P .. of the n chunks."""
+    n = (T + 63) // 64
+    return min(T, q * n // P * 64)
+
+
+def _seg_bytes(P, H):
+    return (3 * P * 16 + 255) // 256 * 256 + (4 * P - 5) * H * 128 * 128 * 4
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _gates(x, mode):
+    """(g for the GPU call, per-channel g for the oracle).  "slow" and "scalar": the
+    recipe's gate over 100, so that a segment's start state still shows at its end (with
+    the recipe's decay it has fallen below the fp32 range after about 1,500 tokens, and
+    the segments would agree with one chain without their combine being right)."""
+    if mode == "slow":
+        g = (x["g"].float() / 100).to(x["g"].dtype).contiguous()
+        return g, g
+    if mode == "channel":
+        return x["g"], x["g"]
+    if mode == "scalar":  # one log alpha per token and head, slow as well
+        g_tok = (x["g"][..., 0].float() / 100).to(x["g"].dtype).contiguous()
+        return g_tok, g_tok.unsqueeze(-1).expand_as(x["g"]).contiguous()
+    return None, torch.zeros_like(x["g"])
+
+
+def _call(d, g, ws, **kw):
+    return kda_chunk_fwd(d["q"], d["k"], d["v"], g, d["beta"], d["cu_seqlens"], d["init_state"],
+                         workspace=ws, algo="tensor", **kw)
+
+
+CASES = [
+    # T, H, gate, init: P = 4 with a ragged last segment; P = 3 ending on a chunk
+    # boundary; P = 9 over four heads; P = 20 (the most a 152-SM part gives 4 heads);
+    # P = 39 over 2 heads; the recipe's decay
+    (10007, 2, "slow", "normal"),
+    (6144, 1, "slow", "normal"),
+    (20000, 4, "scalar", "zeros"),
+    (41000, 4, "none", "normal"),
+    (80000, 2, "slow", "zeros"),
+    (10007, 2, "channel", "normal"),
+]
+
+
+@pytest.mark.parametrize("T,H,mode,init", CASES)
+def test_segments_match_the_oracle(T, H, mode, init):
+    P = _segments(T, H, _sms())
+    assert P >= 3
+    gate = "std" if mode in ("slow", "scalar") else "mixed"
+    x = W.prefill_inputs(W.custom_prefill([T], num_heads=H, d=128, gate=gate, init=init, seed=101 + H))
+    g_gpu, g_ref = _gates(x, mode)
+    d = to_dev(x)
+    need = kda_chunk_fwd_workspace_bytes(1, T, H, 128, 128)
+    assert need == STATUS_BYTES + 256 + _seg_bytes(P, H)  # status, flags, segments
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")
+    out, fin = _call(d, None if g_gpu is None else g_gpu.cuda(), ws, check=True)
+    words = workspace_status_words(ws)
+    assert words[0] == 0 and words[2] == SCHED_SEGMENTS and words[3] == 0, words
+    xo = dict(x)
+    xo["g"] = g_ref
+    ro, rs = run_oracle_prefill(xo)
+    o, s = out.float().cpu().numpy(), fin.cpu().numpy()
+    assert np.isfinite(o).all() and np.isfinite(s).all()
+    assert rel_l2_per_head(o, ro, x["cu_seqlens"].numpy()) <= TOL_BF16
+    assert rel_l2_states(s, rs) <= TOL_BF16
+    # every segment's outputs, not only the norm over the sequence: the worst segment
+    for p in range(P):
+        lo, hi = _seg_start(T, P, p), _seg_start(T, P, p + 1)
+        cu = np.array([0, hi - lo])
+        assert rel_l2_per_head(o[lo:hi], ro[lo:hi], cu) <= TOL_BF16, p
+    if mode in ("slow", "scalar", "none"):
+        # the last segment's start state still matters: from zero its outputs are far off
+        lo = _seg_start(T, P, P - 1)
+        xs = {kk: xo[kk][lo:] for kk in ("q", "k", "v", "g", "beta")}
+        xs.update(cu_seqlens=torch.tensor([0, T - lo], dtype=torch.int32), init_state=None)
+        rz, _ = run_oracle_prefill(xs)
+        assert rel_l2_per_head(rz, ro[lo:], np.array([0, T - lo])) > 10 * TOL_BF16
+    # the one-chain schedule (a workspace without room for the segments) agrees
+    small = torch.zeros(need - _seg_bytes(P, H), dtype=torch.uint8, device="cuda")
+    o1, s1 = _call(d, None if g_gpu is None else g_gpu.cuda(), small, check=True)
+    assert workspace_status_words(small)[2] in (1, 2)
+    assert rel_l2_per_head(o, o1.float().cpu().numpy(), x["cu_seqlens"].numpy()) <= 2 * TOL_BF16
+    assert rel_l2_states(s, s1.cpu().numpy()) <= 2 * TOL_BF16
+
+
+def test_segments_with_input_steps():
+    """The instantiation with the input steps (silu, L2 norm, sigmoid, softplus gate)
+    runs the segments too."""
+    T, H = 9000, 2
+    x = W.prefill_inputs(W.custom_prefill([T], num_heads=H, d=128, gate="mixed", seed=111),
+                         raw=True, raw_gate=True)
+    d = to_dev(x)
+    ws = torch.zeros(kda_chunk_fwd_workspace_bytes(1, T, H, 128, 128), dtype=torch.uint8, device="cuda")
+    out, fin = _call(d, d["g"], ws, check=True, qk_silu=True, qk_l2norm=True, beta_sigmoid=True,
+                     g_softplus=True, gate_scale=1.0)
+    assert workspace_status_words(ws)[2] == SCHED_SEGMENTS
+    q, k, b = oracle.preprocess(x["q"], x["k"], x["beta"], qk_silu=True, qk_l2norm=True,
+                                beta_sigmoid=True)
+    g_ref = oracle.gate_from_logits(x["g"], gate_scale=1.0)
+    ro, rs = oracle.kda_fwd(q, k, x["v"], g_ref, b, x["cu_seqlens"], x["init_state"])
+    assert rel_l2_per_head(out.float().cpu().numpy(), ro, x["cu_seqlens"].numpy()) <= TOL_BF16
+    assert rel_l2_states(fin.cpu().numpy(), rs) <= TOL_BF16
+
+
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_segments_gate_beyond_range(where, in_place):
+    """A head whose decay leaves the tensor-core range in segment 0, a middle segment or
+    the last one is marked, skipped by the second pass and recomputed token by token
+    from the untouched initial state (also when final_state aliases it); the other head
+    keeps the segment results."""
+    T, H = 10007, 2
+    P = _segments(T, H, _sms())
+    lo = {"first": 100, "middle": _seg_start(T, P, 1) + 300, "last": _seg_start(T, P, P - 1) + 50}[where]
+    x = W.prefill_inputs(W.custom_prefill([T], num_heads=H, d=128, seed=112))
+    g = x["g"].float()
+    g[lo:lo + 200, 1] = -2.0
+    x["g"] = g.to(x["g"].dtype).contiguous()
+    d = to_dev(x)
+    ws = torch.zeros(kda_chunk_fwd_workspace_bytes(1, T, H, 128, 128), dtype=torch.uint8, device="cuda")
+    st = d["init_state"].clone()
+    out, fin = _call(d | {"init_state": st}, d["g"], ws, check=True,
+                     **({"final_state": st} if in_place else {}))
+    words = workspace_status_words(ws)
+    assert words[0] == 0 and words[2] == SCHED_SEGMENTS and words[3] == 1, words
+    if in_place:
+        assert fin.data_ptr() == st.data_ptr()
+    ro, rs = run_oracle_prefill(x)
+    assert rel_l2_per_head(out.float().cpu().numpy(), ro, x["cu_seqlens"].numpy()) <= TOL_BF16
+    assert rel_l2_states(fin.cpu().numpy(), rs) <= TOL_BF16
+
+
+@pytest.mark.parametrize("cu", [[0, 10007 + 64], [5, 3], [-64, 10007]])
+def test_segments_skip_bad_offsets(cu):
+    """Offsets the device finds out of order or out of range: every segment run is
+    skipped, nothing is written, and KDA_ERR_SEQLENS is recorded.  The tensors hold 128
+    rows beyond the declared 10,007 (the largest offset here is 10,071), so even a missed
+    check stays inside them."""
+    T, H = 10007, 2
+    x = W.prefill_inputs(W.custom_prefill([T + 128], num_heads=H, d=128, seed=113))
+    d = to_dev(x)
+    rows = {kk: (vv[:T] if kk in ("q", "k", "v", "g", "beta") else vv) for kk, vv in d.items()}
+    ws = torch.zeros(kda_chunk_fwd_workspace_bytes(1, T, H, 128, 128), dtype=torch.uint8, device="cuda")
+    out = torch.full((T + 128, H, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    fin = torch.full_like(d["init_state"], 7.0)
+    kda_chunk_fwd(rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"],
+                  torch.tensor(cu, dtype=torch.int32, device="cuda"), d["init_state"], out=out[:T],
+                  final_state=fin, workspace=ws, algo="tensor")
+    words = workspace_status_words(ws)
+    assert words[0] == 11 and words[2] == SCHED_SEGMENTS, words  # KDA_ERR_SEQLENS
+    assert torch.equal(out, torch.full_like(out, 5.0))
+    assert torch.equal(fin, torch.full_like(fin, 7.0))
+
+
+def test_many_heads_or_short_sequences_keep_one_chain():
+    """51 heads (fewer than three runs per head fit in one wave), a sequence of 95
+    chunks, and two sequences: no room for segments is asked for."""
+    sms = _sms()
+    assert _segments(65536, 51, sms) == 0 and _segments(64 * 95, 2, sms) == 0
+    for N, T, H in ((1, 64 * 95, 2), (2, 20000, 2)):
+        assert kda_chunk_fwd_workspace_bytes(N, T, H, 128, 128) < _seg_bytes(3, H)
