@@ -170,9 +170,10 @@ struct TcParams {
   uint32_t *ring_flags;      // [P][kRingSlots][2]: chunk + 1 published, consumptions (zeroed)
   const int32_t *order;      // plain schedule: sequences longest first (CTA i takes sequence
                              // order[i / H], head i % H), or NULL for the given order
-  int seq_stride;            // 1: sequence n spans cu_seqlens[n] .. cu_seqlens[n + 1]; 4 (plain
-                             // schedule, the segment passes of one sequence): cu_seqlens holds
-                             // runs {first token, end token, kRun* mode, 0} instead, order unused
+  int seq_stride;            // 1: sequence n spans cu_seqlens[n] .. cu_seqlens[n + 1]; 4 (the
+                             // segment passes of one sequence): cu_seqlens holds runs {first
+                             // token, end token, kRun* mode, 0} instead, order unused
+  const uint32_t *head_skip; // runs: heads to skip ([H], fixed for the launch), or NULL
 };
 
 // Modes of a segment run (the segment-parallel scan of one long sequence): V enters as zero
@@ -372,13 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = pair / H, h = pair % H;
   // a pair whose offsets are out of order or out of range runs no chunk and writes nothing
   // (its skip flag is set below); bos and eos stay reloadable from cu_seqlens
-  const bool seg_run = !kSched && p.seq_stride == 4;
+  const bool seg_run = p.seq_stride == 4;
   const int32_t *bnd = p.cu_seqlens + (seg_run ? 4 * n : n);
   const int bos = bnd[0];
   const bool seq_ok = 0 <= bos && bos <= bnd[1] && bnd[1] <= p.T;
   // a segment run is skipped when its table says so, or when an earlier pass marked its head
-  // for the exact recomputation (whose outputs and final state replace the run's)
-  const bool run_skip = seg_run && ((bnd[2] & kRunSkip) || (p.pair_flags && p.pair_flags[h]));
+  // for the exact recomputation (whose outputs and final state replace the run's); the tile
+  // and its solve helpers must agree, so the marks come from a copy taken before the launch
+  const bool run_skip = seg_run && ((bnd[2] & kRunSkip) || (p.head_skip && p.head_skip[h]));
   const int eos = seq_ok && !run_skip ? bnd[1] : bos;
   const int nchunks = (eos - bos + C - 1) / C;
 
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!seq_ok) atomicCAS(p.status, 0u, kStatusSeqlens);
     for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(ctx.bar(i), 1);
     fence_mbar_init();
-    if (blockIdx.x == 0) p.status[2] = kSched ? kSchedHelpers : (seg_run ? kSchedSegments : kSchedPlain);
+    if (blockIdx.x == 0) p.status[2] = seg_run ? kSchedSegments : (kSched ? kSchedHelpers : kSchedPlain);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -1208,7 +1210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *skip_flag = 1;
           if (p.pair_flags) {
             // (segment runs belong to the one sequence: its head h is the pair to recompute)
-            if (atomicExch(p.pair_flags + (!kSched && p.seq_stride == 4 ? h : pair), 1u) == 0u) atomicAdd(p.status + 3, 1u);
+            if (atomicExch(p.pair_flags + (p.seq_stride == 4 ? h : pair), 1u) == 0u) atomicAdd(p.status + 3, 1u);
           } else {
             atomicCAS(p.status, 0u, kStatusGateRange);
           }
@@ -1420,9 +1422,20 @@ int seg_count(long long T, int H, int sms) {
   const long long P = std::min<long long>((sms / H + 3) / 2, nch / kSegMinChunks);
   return P >= 3 ? static_cast<int>(P) : 0;
 }
-size_t seg_table_bytes(int P) { return (static_cast<size_t>(3 * P) * sizeof(int4) + 255) / 256 * 256; }
-size_t seg_bytes(int P, int H) {  // run tables, pass-1 end states, start states, pass-2 end states
-  return seg_table_bytes(P) + static_cast<size_t>(4 * P - 5) * H * DK * DV * sizeof(float);
+// run tables (3P slots) and the heads the second pass skips
+size_t seg_table_bytes(int P, int H) {
+  return (static_cast<size_t>(3 * P) * sizeof(int4) + static_cast<size_t>(H) * 4 + 255) / 256 * 256;
+}
+// The pairs of the larger pass that can take solve helpers (at most kHelperMaxPairs), or 0.
+long long seg_ring_pairs(int P, int H) {
+  const long long r1 = static_cast<long long>(2 * P - 3) * H, r2 = static_cast<long long>(P - 1) * H;
+  return std::max(r1 <= kHelperMaxPairs ? r1 : 0, r2 <= kHelperMaxPairs ? r2 : 0);
+}
+size_t ring_bytes(long long pairs);
+// run tables, pass-1 end states, start states, pass-2 end states, the helpers' ring
+size_t seg_bytes(int P, int H) {
+  return seg_table_bytes(P, H) + static_cast<size_t>(4 * P - 5) * H * DK * DV * sizeof(float) +
+         ring_bytes(seg_ring_pairs(P, H));
 }
 int device_sms() {
   int dev = 0, sms = 0;
@@ -1480,45 +1493,68 @@ __global__ void __launch_bounds__(256) kda_seg_init_kernel(float *F1, const floa
 }
 
 // S_1 = the end state of segment 0 (pass-1 run 0); S_{p+1} = M_p S_p + B_p with M_p, B_p
-// the end states of pass-1 runs 2p and 2p - 1.  CTA (h, cb) keeps columns 16 cb .. + 15 of
-// head h's state in shared memory (the columns do not mix) and stages each M_p there;
-// thread t forms column t % 16 of rows t / 16 + 16 k.
-__global__ void __launch_bounds__(256) kda_seg_combine_kernel(const float *F1, float *starts, int P, int H) {
-  extern __shared__ float seg_smem[];
-  float *Msh = seg_smem;             // [128][128] M_p
-  float *Ssh = seg_smem + DK * DK;   // [128][16] the current start state's columns
-  const int h = blockIdx.x / 8, cb = blockIdx.x % 8, t = threadIdx.x;
-  const size_t stride = static_cast<size_t>(H) * DK * DV;
-  const float *S1 = F1 + static_cast<size_t>(h) * DK * DV;  // run 0
-  for (int i = t; i < DK * 16; i += blockDim.x) {
-    const int r = i / 16, cc = i % 16;
-    const float x = S1[static_cast<size_t>(r) * DV + 16 * cb + cc];
-    Ssh[i] = x;
-    starts[static_cast<size_t>(h) * DK * DV + static_cast<size_t>(r) * DV + 16 * cb + cc] = x;
+// the end states of pass-1 runs 2p and 2p - 1, in fp32.  CTA (h, cb) keeps columns
+// 4 cb .. 4 cb + 3 of head h's state in shared memory (the columns do not mix).  Warp w
+// takes rows 32 (w mod 4) + lane over the key slice j = 32 (w / 4) .. + 31: its part of
+// row r of M_p sits in registers, loaded while the CTA still works on the step before,
+// and the four slices' partial sums meet in shared memory.  The CTAs with cb = 0 also
+// copy the recomputation marks the first pass left, for the second pass to skip those heads.
+constexpr int kCombThreads = 512;
+__global__ void __launch_bounds__(kCombThreads) kda_seg_combine_kernel(const float *F1, float *starts, int P,
+                                                                       int H, const uint32_t *pair_flags,
+                                                                       uint32_t *head_skip) {
+  __shared__ float4 Ssh[DK];       // S_p[j][4 cb .. 4 cb + 3]
+  __shared__ float4 part[4][DK];   // partial sums of the four key slices
+  const int h = blockIdx.x / (DV / 4), cb = blockIdx.x % (DV / 4);
+  const int w = threadIdx.x >> 5, js = w >> 2, r = 32 * (w & 3) + (threadIdx.x & 31);
+  if (cb == 0 && threadIdx.x == 0) head_skip[h] = pair_flags ? pair_flags[h] : 0u;
+  const size_t stride = static_cast<size_t>(H) * DK * DV, hoff = static_cast<size_t>(h) * DK * DV;
+  const size_t roff = hoff + static_cast<size_t>(r) * DV + 4 * cb;  // element (r, 4 cb) of head h
+  if (js == 0) {
+    const float4 s1 = *reinterpret_cast<const float4 *>(F1 + roff);  // run 0: segment 0's end
+    *reinterpret_cast<float4 *>(starts + roff) = s1;
+    Ssh[r] = s1;
   }
-  const int cc = t % 16, r0 = t / 16;
-  for (int q = 1; q <= P - 2; ++q) {
-    const float *M = F1 + (2 * q) * stride + static_cast<size_t>(h) * DK * DV;
-    const float *B = F1 + (2 * q - 1) * stride + static_cast<size_t>(h) * DK * DV;
-    __syncthreads();  // the previous step's reads of Msh are done
-    for (int i = t; i < DK * DK / 4; i += blockDim.x)
-      reinterpret_cast<float4 *>(Msh)[i] = reinterpret_cast<const float4 *>(M)[i];
-    __syncthreads();
-    float acc[8];
+  auto load = [&](int q, float4 (&m)[8], float4 &b) {
+    const float4 *row = reinterpret_cast<const float4 *>(F1 + 2 * q * stride + hoff +
+                                                         static_cast<size_t>(r) * DV + 32 * js);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = B[static_cast<size_t>(r0 + 16 * k) * DV + 16 * cb + cc];
-    for (int j = 0; j < DK; ++j) {
-      const float sj = Ssh[j * 16 + cc];
+    for (int i = 0; i < 8; ++i) m[i] = row[i];
+    b = js == 0 ? *reinterpret_cast<const float4 *>(F1 + (2 * q - 1) * stride + roff)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  // step q with row part mc and offset bc; the next step's loads go to mn, bn first
+  auto step = [&](int q, float4 (&mc)[8], const float4 &bc, float4 (&mn)[8], float4 &bn) {
+    __syncthreads();  // Ssh holds S_q; part is free
+    if (q + 1 <= P - 2) load(q + 1, mn, bn);
+    float4 acc = bc;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] = fmaf(Msh[(r0 + 16 * k) * DK + j], sj, acc[k]);
+    for (int i = 0; i < 8; ++i) {
+      const float mj[4] = {mc[i].x, mc[i].y, mc[i].z, mc[i].w};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float4 sv = Ssh[32 * js + 4 * i + jj];
+        acc.x = fmaf(mj[jj], sv.x, acc.x);
+        acc.y = fmaf(mj[jj], sv.y, acc.y);
+        acc.z = fmaf(mj[jj], sv.z, acc.z);
+        acc.w = fmaf(mj[jj], sv.w, acc.w);
+      }
     }
-    __syncthreads();  // every thread has read the old Ssh
-    float *dst = starts + (q * stride) + static_cast<size_t>(h) * DK * DV;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      Ssh[(r0 + 16 * k) * 16 + cc] = acc[k];
-      dst[static_cast<size_t>(r0 + 16 * k) * DV + 16 * cb + cc] = acc[k];
+    part[js][r] = acc;
+    __syncthreads();  // all partial sums are in; every thread has read S_q
+    if (js == 0) {
+      const float4 a0 = part[0][r], a1 = part[1][r], a2 = part[2][r], a3 = part[3][r];
+      const float4 sn = make_float4(a0.x + a1.x + a2.x + a3.x, a0.y + a1.y + a2.y + a3.y,
+                                    a0.z + a1.z + a2.z + a3.z, a0.w + a1.w + a2.w + a3.w);
+      Ssh[r] = sn;
+      *reinterpret_cast<float4 *>(starts + q * stride + roff) = sn;
     }
+  };
+  float4 mA[8], mB[8], bA, bB;
+  if (P >= 3) load(1, mA, bA);
+  for (int q = 1; q <= P - 2; q += 2) {
+    step(q, mA, bA, mB, bB);
+    if (q + 1 <= P - 2) step(q + 1, mB, bB, mA, bA);
   }
 }
 
@@ -1553,8 +1589,42 @@ size_t chunk_tc_scratch_bytes(int num_seqs, int total_tokens, int num_heads, int
   return bytes;
 }
 
-// The launch of one instantiation: the solve-helper schedule when it fits (cooperative),
-// otherwise the plain one.
+// The solve-helper schedule over `pairs` pairs in one cooperative launch, every CTA resident
+// as the hand-over through global memory needs: cudaSuccess once enqueued, cudaErrorNotReady
+// when it does not apply or does not fit (nothing launched: the plain schedule runs).
+template <bool kPrep>
+static cudaError_t launch_helpers(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
+                                  CUtensorMap &mg, CUtensorMap &mv, CUtensorMap &mo, TcParams prm,
+                                  long long pairs, uint8_t *ring, size_t ring_avail) {
+  // one or two helpers per pair, all CTAs in one wave
+  const int hpp = 3 * pairs <= a.num_sms ? 2 : (2 * pairs <= a.num_sms ? 1 : 0);
+  int dev = 0, coop = 0;
+  if (hpp == 0 || pairs > kHelperMaxPairs || !ring || ring_avail < ring_bytes(pairs)) return cudaErrorNotReady;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) {
+    (void)cudaGetLastError();
+    return cudaErrorNotReady;
+  }
+  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true, kPrep>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (err != cudaSuccess) return err;
+  prm.npairs = static_cast<int>(pairs);  // the tiles; CTAs from here on are helpers
+  prm.ring = ring;
+  prm.ring_flags = reinterpret_cast<uint32_t *>(ring + pairs * kRingSlots * kRingSlotBytes);
+  prm.helpers_per_pair = hpp;
+  err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
+  if (err != cudaSuccess) return err;
+  void *args[] = {&mq, &mk, &mg, &mv, &mo, &prm};
+  err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true, kPrep>),
+                                    dim3(static_cast<unsigned>((1 + hpp) * pairs)), dim3(kThreads), args,
+                                    L::kAlloc, stream);
+  if (err != cudaErrorCooperativeLaunchTooLarge) return err;
+  (void)cudaGetLastError();  // not all resident (SMs taken)
+  return cudaErrorNotReady;
+}
+
+// The launch of one instantiation: the segment-parallel scan for one long sequence with few
+// heads, else the solve-helper schedule when it fits, else the plain one.
 template <bool kPrep>
 static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
                              CUtensorMap &mg, CUtensorMap &mv, CUtensorMap &mo, TcParams &prm,
@@ -1570,9 +1640,20 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     unsigned char *base = static_cast<unsigned char *>(a.scratch);
     int4 *runs1 = reinterpret_cast<int4 *>(base);
     int4 *runs2 = runs1 + (2 * P - 3);
-    float *F1 = reinterpret_cast<float *>(base + seg_table_bytes(P));
+    uint32_t *head_skip = reinterpret_cast<uint32_t *>(runs1 + 3 * P);
+    float *F1 = reinterpret_cast<float *>(base + seg_table_bytes(P, H));
     float *starts = F1 + static_cast<size_t>(2 * P - 3) * st;
     float *F2 = starts + static_cast<size_t>(P - 1) * st;
+    uint8_t *ring = reinterpret_cast<uint8_t *>(F2 + static_cast<size_t>(P - 1) * st);
+    const size_t ring_avail = ring_bytes(seg_ring_pairs(P, H));
+    // a pass through the helper schedule when it fits, else the plain one
+    auto pass = [&](TcParams &pp, long long np) -> cudaError_t {
+      pp.npairs = static_cast<int>(np);  // (run, head) pairs of this pass
+      cudaError_t e = launch_helpers<kPrep>(a, stream, mq, mk, mg, mv, mo, pp, np, ring, ring_avail);
+      if (e != cudaErrorNotReady) return e;
+      kda_chunk_tc_kernel<false, kPrep><<<(unsigned)np, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, mo, pp);
+      return cudaGetLastError();
+    };
     kda_seg_table_kernel<<<1, 128, 0, stream>>>(a.cu_seqlens, a.total_tokens, P, runs1, runs2, a.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t n1 = static_cast<size_t>(2 * P - 3) * st;  // floats, a multiple of 1024
@@ -1583,52 +1664,25 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     p1.seq_stride = 4;
     p1.init_state = F1;  // in place
     p1.final_state = F1;
-    kda_chunk_tc_kernel<false, kPrep><<<(unsigned)((2 * P - 3) * H), kThreads, L::kAlloc, stream>>>(
-        mq, mk, mg, mv, mo, p1);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    const int comb_smem = (DK * DK + DK * 16) * sizeof(float);
-    err = cudaFuncSetAttribute(kda_seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, comb_smem);
-    if (err != cudaSuccess) return err;
-    kda_seg_combine_kernel<<<H * 8, 256, comb_smem, stream>>>(F1, starts, P, H);
+    if ((err = pass(p1, static_cast<long long>(2 * P - 3) * H)) != cudaSuccess) return err;
+    kda_seg_combine_kernel<<<H * (DV / 4), kCombThreads, 0, stream>>>(F1, starts, P, H, a.pair_flags, head_skip);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     TcParams p2 = prm;
     p2.cu_seqlens = reinterpret_cast<const int32_t *>(runs2);
     p2.seq_stride = 4;
+    p2.head_skip = head_skip;
     p2.init_state = starts;
     p2.final_state = F2;
-    kda_chunk_tc_kernel<false, kPrep><<<(unsigned)((P - 1) * H), kThreads, L::kAlloc, stream>>>(
-        mq, mk, mg, mv, mo, p2);
-    if ((err = cudaGetLastError()) != cudaSuccess || !a.final_state) return err;
+    if ((err = pass(p2, static_cast<long long>(P - 1) * H)) != cudaSuccess || !a.final_state) return err;
     kda_seg_final_kernel<<<(unsigned)(st / 1024), 256, 0, stream>>>(F2 + static_cast<size_t>(P - 2) * st,
                                                                     a.final_state, runs2 + (P - 2), a.pair_flags);
     return cudaGetLastError();
   }
   // Few sequence-heads leave most SMs idle: with room for the ring, one or two solve
-  // helpers per sequence-head join its tile in one cooperative launch (every CTA
-  // resident, as the hand-over through global memory needs).
-  const int hpp = 3 * pairs <= a.num_sms ? 2 : (2 * pairs <= a.num_sms ? 1 : 0);
-  int dev = 0, coop = 0;
-  if (hpp > 0 && pairs <= kHelperMaxPairs && a.scratch && a.scratch_bytes >= ring_bytes(pairs) &&
-      cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
-    err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true, kPrep>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (err != cudaSuccess) return err;
-    prm.ring = static_cast<uint8_t *>(a.scratch);
-    prm.ring_flags = reinterpret_cast<uint32_t *>(prm.ring + pairs * kRingSlots * kRingSlotBytes);
-    prm.helpers_per_pair = hpp;
-    err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
-    if (err != cudaSuccess) return err;
-    void *args[] = {&mq, &mk, &mg, &mv, &mo, &prm};
-    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true, kPrep>),
-                                      dim3(static_cast<unsigned>((1 + hpp) * pairs)), dim3(kThreads),
-                                      args, L::kAlloc, stream);
-    if (err != cudaErrorCooperativeLaunchTooLarge) return err;
-    (void)cudaGetLastError();  // not all resident (SMs taken): the plain schedule below
-    prm.ring = nullptr;
-    prm.ring_flags = nullptr;
-    prm.helpers_per_pair = 1;
-  }
+  // helpers per sequence-head join its tile in one cooperative launch.
+  err = launch_helpers<kPrep>(a, stream, mq, mk, mg, mv, mo, prm, pairs, static_cast<uint8_t *>(a.scratch),
+                              a.scratch ? a.scratch_bytes : 0);
+  if (err != cudaErrorNotReady) return err;
   // More than one wave: start the longest sequences first (when the workspace has room)
   if (pairs > a.num_sms && a.num_seqs >= 2 && a.num_seqs <= kOrderMaxSeqs && a.scratch &&
       a.scratch_bytes >= order_bytes(a.num_seqs)) {
@@ -1682,6 +1736,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   prm.ring_flags = nullptr;
   prm.order = nullptr;
   prm.seq_stride = 1;
+  prm.head_skip = nullptr;
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   prm.npairs = static_cast<int>(pairs);
   if (pairs == 0) return cudaSuccess;

@@ -95,19 +95,21 @@ def test_workspace_holds_the_solve_helper_ring_for_few_sequence_heads(lib):
 
 
 def test_workspace_holds_the_segments_of_one_long_sequence(lib):
-    """One sequence of at least 3 x 32 chunks with at most 50 heads: the run tables
-    (16 bytes per run, 3 runs per segment, rounded up to 256) and 4P - 5 fp32 states per
-    head for P = min((SMs / H + 3) / 2, chunks / 32) segments, when P >= 3 and that is
-    more than the ring.  Without a device the size is taken for 152 SMs."""
+    """One sequence of at least 3 x 32 chunks with at most 50 heads: for P = min((SMs / H
+    + 3) / 2, chunks / 32) >= 3 segments, the run tables and the heads to skip (16 bytes per
+    run slot, 3 slots per segment, 4 bytes per head, rounded up to 256), 4P - 5 fp32 states
+    per head, and a solve-helper ring for the larger of the two passes (2P - 3 and P - 1
+    runs per head) that has at most 76 pairs.  Without a device the size is taken for 152
+    SMs."""
     ws = lambda **kw: lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(num_seqs=1, **kw)))
-    st = 128 * 128 * 4
-    assert ws(num_heads=4, total_tokens=65536) == 512 + 1024 + 75 * 4 * st   # P = 20
-    assert ws(num_heads=32, total_tokens=65536) == 512 + 256 + 7 * 32 * st   # P = 3
-    assert ws(num_heads=2, total_tokens=64 * 96) == 512 + 256 + 7 * 2 * st   # P = 3: 96 chunks
-    assert ws(num_heads=2, total_tokens=64 * 95) == 512 + 2 * 65568          # 95 chunks: the ring
-    assert ws(num_heads=1, total_tokens=1 << 20) == 512 + 3840 + 303 * st    # P = 77
-    assert ws(num_heads=51, total_tokens=1 << 20) == 512 + 51 * 65568        # two runs a head: no
-    assert ws(num_heads=4, total_tokens=65536, gate=K.KDA_GATE_NONE) == 256 + 1024 + 75 * 4 * st
+    st, ring = 128 * 128 * 4, 65568
+    assert ws(num_heads=4, total_tokens=65536) == 512 + 1024 + 75 * 4 * st + 76 * ring    # P = 20
+    assert ws(num_heads=32, total_tokens=65536) == 512 + 512 + 7 * 32 * st + 64 * ring   # P = 3
+    assert ws(num_heads=2, total_tokens=64 * 96) == 512 + 256 + 7 * 2 * st + 6 * ring    # 96 chunks
+    assert ws(num_heads=2, total_tokens=64 * 95) == 512 + 2 * ring                       # the ring only
+    assert ws(num_heads=1, total_tokens=1 << 20) == 512 + 3840 + 303 * st + 76 * ring    # P = 77
+    assert ws(num_heads=51, total_tokens=1 << 20) == 512 + 51 * ring                     # no segments
+    assert ws(num_heads=4, total_tokens=65536, gate=K.KDA_GATE_NONE) == 256 + 1024 + 75 * 4 * st + 76 * ring
     assert lib.kda_version() >= 1005  # 1.5 added the segments
 
 

@@ -7,7 +7,9 @@ sequence, at most 50 heads and at least 3 x 32 chunks, kda_chunk_fwd_workspace_b
 includes room for cutting the sequence into P segments: a first launch runs segment 0
 from the true start and every middle segment from zero (B) and from the identity with
 V = 0 (M), a small kernel chains S_{p+1} = M_p S_p + B_p, and a second launch runs
-segments 1 .. P - 1 from those states.  The rounding differs from the one-chain
+segments 1 .. P - 1 from those states; a pass with at most 76 (run, head) pairs runs
+with solve helpers (every case here has one such pass; the P = 20 and P = 39 cases run
+their first pass without).  The rounding differs from the one-chain
 schedules, so the results are compared with the oracle at the bf16 tolerance (and with
 the one-chain schedule at twice it), and word 2 of the status block (3) shows that the
 segments ran.
@@ -41,7 +43,11 @@ def _seg_start(T, P, q):
 
 
 def _seg_bytes(P, H):
-    return (3 * P * 16 + 255) // 256 * 256 + (4 * P - 5) * H * 128 * 128 * 4
+    """Run tables and skip marks, 4P - 5 states per head, the ring of the larger pass that
+    takes solve helpers (at most 76 pairs)."""
+    pairs = [r * H for r in (2 * P - 3, P - 1) if r * H <= 76]
+    return ((3 * P * 16 + 4 * H + 255) // 256 * 256 + (4 * P - 5) * H * 128 * 128 * 4
+            + max(pairs, default=0) * 4 * (16384 + 8))
 
 
 def _sms():
