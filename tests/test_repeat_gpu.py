@@ -1,8 +1,8 @@
 """Bitwise repeatability of the tensor-core prefill and of the persistent recurrent pass
 under repeated calls.
 
-Both schedules (plain, and the solve helpers with their ring in the workspace) are
-deterministic: the same inputs must give the same bits on every call.  A race in
+The schedules (plain, the solve helpers with their ring in the workspace, and the
+segments of one long sequence) are deterministic: the same inputs must give the same bits on every call.  A race in
 the hand-over between the K-side groups, the state side and the producers would
 show up as an occasional call that differs, most likely with many short
 sequences (38 sequence-heads with two helpers each, 60 with one) and a gate without
@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from kimi_delta_attention_fwd_gb300 import (kda_chunk_fwd, kda_chunk_fwd_workspace_bytes,
-                                            kda_recurrent_fwd)
+                                            kda_recurrent_fwd, workspace_status_words)
 from kimi_delta_attention_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -41,6 +41,28 @@ def test_repeated_calls_are_bitwise_identical(mode, schedule):
         differing += not (torch.equal(o, o0) and torch.equal(f, f0))
     torch.cuda.synchronize()
     assert differing == 0, f"{differing} of {REPS} calls differ from the first"
+
+
+@pytest.mark.parametrize("T,Hs,reps", [(10007, 2, REPS), (41000, 4, 10)])
+@pytest.mark.parametrize("mode", ["none", "channel"])
+def test_segment_schedule_is_bitwise_repeatable(T, Hs, reps, mode):
+    """One long sequence cut into segments (P = 4: both passes with two solve helpers per
+    pair; P = 20: a plain first pass, one helper per pair in the second) and chained
+    through the combine: the same bits on every call."""
+    x = W.prefill_inputs(W.custom_prefill([T], num_heads=Hs, d=128, gate="mixed", seed=93),
+                         device="cuda")
+    g = None if mode == "none" else x["g"]
+    ws = torch.zeros(kda_chunk_fwd_workspace_bytes(1, T, Hs, 128, 128), dtype=torch.uint8, device="cuda")
+    args = (x["q"], x["k"], x["v"], g, x["beta"], x["cu_seqlens"], x["init_state"])
+    o0, f0 = kda_chunk_fwd(*args, workspace=ws, algo="tensor", check=True)
+    assert workspace_status_words(ws)[2] == 3  # the segments ran
+    o0, f0 = o0.clone(), f0.clone()
+    differing = 0
+    for _ in range(reps):
+        o, f = kda_chunk_fwd(*args, workspace=ws, algo="tensor")
+        differing += not (torch.equal(o, o0) and torch.equal(f, f0))
+    torch.cuda.synchronize()
+    assert differing == 0, f"{differing} of {reps} calls differ from the first"
 
 
 @pytest.mark.parametrize("gate", ["channel", "scalar", "none"])

@@ -86,6 +86,27 @@ def test_noalloc_runs_the_schedule_that_fits_its_buffer():
         assert torch.equal(out, ref_o) and torch.equal(fin, ref_f)
 
 
+def test_noalloc_long_sequence_keeps_one_chain():
+    """One sequence long enough for the segment-parallel scan: the built-in buffer has no
+    room for the segments, so the call runs one chain (with the helpers' ring, which fits)
+    and gives kda_chunk_fwd's plain results bit for bit."""
+    kbuild.build()
+    lib = K.load_library()
+    T, H = 10007, 2
+    assert K.kda_chunk_fwd_workspace_bytes(1, T, H, 128, 128) > 256 * 1024  # segments: no room
+    x = W.prefill_inputs(W.custom_prefill([T], num_heads=H, d=128, gate="mixed", seed=58))
+    d = to_dev(x)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    ref_o, ref_f = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                 d["init_state"], workspace=ws, check=True)
+    out = torch.full_like(ref_o, float("nan"))
+    fin = torch.full_like(ref_f, float("nan"))
+    assert _noalloc(lib, d, out, fin) == 0
+    rc, words = _noalloc_words(lib)
+    assert rc == 0 and words[0] == 0 and words[2] == 2, words  # solve helpers
+    assert torch.equal(out, ref_o) and torch.equal(fin, ref_f)
+
+
 def test_noalloc_reports_device_status_and_recomputes_beyond_the_decay_range():
     """A sequence-head whose chunk decay passes the tensor-core range (g = -2 per token:
     -128 per chunk) is recomputed token by token through the built-in buffer too: the
