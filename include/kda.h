@@ -138,17 +138,17 @@ typedef struct {
  *                 kda_chunk_fwd_workspace_bytes() bytes every schedule can run;
  *                 a smaller workspace selects the schedule that fits.  The
  *                 one-chain schedules (plain, solve helpers) give bit-identical
- *                 results; the segment-parallel scan of one sequence (below)
- *                 rounds differently and agrees with them within the bf16
- *                 tolerance.  Calls that share one workspace must be ordered on
- *                 one stream.
- * One sequence (N = 1) of at least 96 chunks with few heads (P >= 3 below) runs as P
- * segments of whole chunks: the recurrence is affine in the start state, S_end =
- * M S_start + B over any stretch of tokens, so a first launch runs segment 0 from the
- * true start and each middle segment from zero (B) and from the identity with V = 0
- * (M, as d_k = d_v), a small kernel chains S_{p+1} = M_p S_p + B_p in fp32, and a
- * second launch runs segments 1 .. P - 1 from those states.  P = min((SMs / H + 3) / 2,
- * chunks / 32), so the first launch's H (2P - 3) CTAs fit in one wave.
+ *                 results; the segment-parallel scan (below) rounds differently
+ *                 and agrees with them within the bf16 tolerance.  Calls that
+ *                 share one workspace must be ordered on one stream.
+ * A few long sequences with few heads (P >= 3 below) run as P segments of whole chunks
+ * each: the recurrence is affine in the start state, S_end = M S_start + B over any
+ * stretch of tokens, so a first launch runs every sequence's segment 0 from the true
+ * start and each middle segment from zero (B) and from the identity with V = 0 (M, as
+ * d_k = d_v), a small kernel chains S_{p+1} = M_p S_p + B_p in fp32, and a second launch
+ * runs segments 1 .. P - 1 from those states.  P = min((SMs / (N H) + 3) / 2, chunks of
+ * the average sequence / 32), so the first launch's N H (2P - 3) CTAs fit in one wave;
+ * each sequence is cut by its own length.
  * The tensor-core kernel forms its decay factors relative to each chunk's start, so
  * they stay finite while a chunk's total log decay per key channel is above -80.  A
  * sequence-head with a chunk beyond that (a very fast decay, alpha -> 0) is marked in
@@ -173,10 +173,11 @@ int kda_chunk_fwd(const kda_shape *shape, const void *q, const void *k, const vo
  * over the chunk solve (4 x 16 KiB + 32 bytes per sequence-head) or, for 2 to 2048
  * sequences, the launch order (4 bytes per sequence, rounded up to 256) with which
  * the longest sequences start first when the launch takes more than one wave.  For
- * one sequence that runs as P >= 3 segments it is the larger of the ring and the
- * segments' room: the run tables (48 P bytes rounded up to 256) and 4P - 5 fp32
- * states of d_k x d_v per head.  P depends on the current device's SM count (152
- * assumed without a device). */
+ * sequences that run as P >= 3 segments it is the larger of that and the segments'
+ * room: the run tables and skip marks (48 P N + 4 N H bytes rounded up to 256), 4P - 5
+ * fp32 states of d_k x d_v per sequence-head, and the solve helpers' ring for the larger
+ * pass with at most 76 (run, head) pairs.  P depends on the current device's SM count
+ * (152 assumed without a device). */
 size_t kda_chunk_fwd_workspace_bytes(const kda_shape *shape);
 
 /* The prefill kernel a call with this shape runs: KDA_ALGO_TENSOR or
@@ -265,7 +266,7 @@ int kda_noalloc_status(uint32_t *words, cudaStream_t stream);
  * last kda_chunk_fwd on this workspace wrote: KDA_OK, KDA_ERR_DEVICE_TIMEOUT,
  * KDA_ERR_SEQLENS or KDA_ERR_GATE_RANGE.  A CUDA error while reading returns
  * KDA_ERR_LAUNCH.  Word 2 of the block holds the tensor-core schedule that ran
- * (1 plain, 2 with solve helpers, 3 the segments of one sequence), word 3 the
+ * (1 plain, 2 with solve helpers, 3 the segment-parallel scan), word 3 the
  * sequence-heads recomputed token by token.
  */
 int kda_workspace_status(const void *workspace, cudaStream_t stream);
@@ -284,7 +285,7 @@ const char *kda_status_string(int status);
  * 1002 the kda_shape.prep field, 1003 the device check of cu_seqlens
  * (KDA_ERR_SEQLENS, kda_last_device_status), the exact recomputation beyond the
  * tensor-core decay range and kda_noalloc_status, 1004 KDA_PREP_G_SOFTPLUS and
- * kda_shape.gate_scale, 1005 the segment-parallel scan of one sequence (schedule
+ * kda_shape.gate_scale, 1005 the segment-parallel scan of long sequences (schedule
  * word 3 and its workspace). */
 int kda_version(void);
 

@@ -48,7 +48,7 @@
 // (after its first product has read [-W; Qh]) and its v tile (after the chunk's
 // outputs, staged there, have been stored by TMA).  With few sequence-heads, one or
 // two more CTAs per sequence-head run the solve of its chunks ("Solve helpers" below);
-// one long sequence with few heads is cut into segments that run side by side and are
+// a few long sequences with few heads are cut into segments that run side by side and are
 // chained through their affine state maps ("Segment-parallel scan" below).
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // KDA_ERR_DEVICE_TIMEOUT in the status word and runs to completion without
@@ -171,12 +171,13 @@ struct TcParams {
   const int32_t *order;      // plain schedule: sequences longest first (CTA i takes sequence
                              // order[i / H], head i % H), or NULL for the given order
   int seq_stride;            // 1: sequence n spans cu_seqlens[n] .. cu_seqlens[n + 1]; 4 (the
-                             // segment passes of one sequence): cu_seqlens holds runs {first
-                             // token, end token, kRun* mode, 0} instead, order unused
-  const uint32_t *head_skip; // runs: heads to skip ([H], fixed for the launch), or NULL
+                             // segment passes): cu_seqlens holds runs {first token, end token,
+                             // kRun* mode, sequence} instead, order unused
+  const uint32_t *head_skip; // runs: (sequence, head) pairs to skip ([N][H], fixed for the
+                             // launch), or NULL
 };
 
-// Modes of a segment run (the segment-parallel scan of one long sequence): V enters as zero
+// Modes of a segment run (the segment-parallel scan of long sequences): V enters as zero
 // (from the identity as start state the run then gives the segment's transfer matrix); the
 // outputs are not stored; the run is skipped altogether.
 constexpr int kRunZeroV = 1, kRunNoOut = 2, kRunSkip = 4;
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a segment run is skipped when its table says so, or when an earlier pass marked its head
   // for the exact recomputation (whose outputs and final state replace the run's); the tile
   // and its solve helpers must agree, so the marks come from a copy taken before the launch
-  const bool run_skip = seg_run && ((bnd[2] & kRunSkip) || (p.head_skip && p.head_skip[h]));
+  const bool run_skip = seg_run && ((bnd[2] & kRunSkip) || (p.head_skip && p.head_skip[bnd[3] * H + h]));
   const int eos = seq_ok && !run_skip ? bnd[1] : bos;
   const int nchunks = (eos - bos + C - 1) / C;
 
@@ -1209,8 +1210,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(gam >= kMinGamma) && !(*skip_flag & 1)) {
           *skip_flag = 1;
           if (p.pair_flags) {
-            // (segment runs belong to the one sequence: its head h is the pair to recompute)
-            if (atomicExch(p.pair_flags + (p.seq_stride == 4 ? h : pair), 1u) == 0u) atomicAdd(p.status + 3, 1u);
+            // (a segment run marks its sequence's pair, the sequence taken from its table entry)
+            const int fp = p.seq_stride == 4 ? p.cu_seqlens[4 * (pair / H) + 3] * H + h : pair;
+            if (atomicExch(p.pair_flags + fp, 1u) == 0u) atomicAdd(p.status + 3, 1u);
           } else {
             atomicCAS(p.status, 0u, kStatusGateRange);
           }
@@ -1402,40 +1404,44 @@ __global__ void __launch_bounds__(1024) kda_tc_order_kernel(const int32_t *cu_se
 }
 size_t order_bytes(long long num_seqs) { return (static_cast<size_t>(num_seqs) * 4 + 255) / 256 * 256; }
 
-// Segment-parallel scan of one long sequence ("Kimi Delta Attention (KDA)", the state
+// Segment-parallel scan of a few long sequences ("Kimi Delta Attention (KDA)", the state
 // recurrence is affine in the start state: S_end = M S_start + B over any stretch of
 // tokens, M the product of the per-token transitions (I - beta k k^T) Diag(alpha)).
-// With few heads the helpers still leave most SMs idle, so the sequence is cut into P
-// segments of whole chunks:
+// With few sequence-heads the helpers still leave most SMs idle, so every sequence is cut
+// into P segments of whole chunks:
 //   pass 1  segment 0 from the true start (its outputs are final); every middle segment
 //           p = 1 .. P - 2 twice, from zero (its end state B_p) and from the identity with
 //           V taken as zero (its transfer matrix M_p, as d_k = d_v);
 //   combine S_1 = end of segment 0, S_{p+1} = M_p S_p + B_p (fp32, column blocks apart);
 //   pass 2  segments 1 .. P - 1 from S_p, storing their outputs; the last one's end state
 //           is the sequence's final state.
-// The first pass runs H (2P - 3) CTAs in one wave: at least 3 segments of at least 32
-// chunks each, otherwise the other schedules run.
+// Runs of sequence n: pass 1 n (2P - 3) + k, pass 2 n (P - 1) + q - 1.  The first pass runs
+// N H (2P - 3) CTAs in one wave: at least 3 segments of at least 32 chunks of the average
+// sequence, otherwise the other schedules run.
 constexpr int kSegMinChunks = 32;
-int seg_count(long long T, int H, int sms) {
-  if (H < 1 || sms < 1 || T >= (1LL << 30)) return 0;  // (zero V tiles are read below token 0)
-  const long long nch = (T + C - 1) / C;
-  const long long P = std::min<long long>((sms / H + 3) / 2, nch / kSegMinChunks);
+int seg_count(int N, long long T, int H, int sms) {
+  if (N < 1 || H < 1 || sms < 1 || T >= (1LL << 30)) return 0;  // (zero V tiles are read below token 0)
+  const long long NH = static_cast<long long>(N) * H;
+  if (NH > sms) return 0;
+  const long long nch = (T / N + C - 1) / C;  // chunks of the average sequence
+  const long long P = std::min<long long>((sms / NH + 3) / 2, nch / kSegMinChunks);
   return P >= 3 ? static_cast<int>(P) : 0;
 }
-// run tables (3P slots) and the heads the second pass skips
-size_t seg_table_bytes(int P, int H) {
-  return (static_cast<size_t>(3 * P) * sizeof(int4) + static_cast<size_t>(H) * 4 + 255) / 256 * 256;
+// run tables (3P slots per sequence) and the (sequence, head) pairs the second pass skips
+size_t seg_table_bytes(int P, int N, int H) {
+  return (static_cast<size_t>(3 * P) * N * sizeof(int4) + static_cast<size_t>(N) * H * 4 + 255) / 256 * 256;
 }
 // The pairs of the larger pass that can take solve helpers (at most kHelperMaxPairs), or 0.
-long long seg_ring_pairs(int P, int H) {
-  const long long r1 = static_cast<long long>(2 * P - 3) * H, r2 = static_cast<long long>(P - 1) * H;
+long long seg_ring_pairs(int P, long long NH) {
+  const long long r1 = (2 * P - 3) * NH, r2 = (P - 1) * NH;
   return std::max(r1 <= kHelperMaxPairs ? r1 : 0, r2 <= kHelperMaxPairs ? r2 : 0);
 }
 size_t ring_bytes(long long pairs);
 // run tables, pass-1 end states, start states, pass-2 end states, the helpers' ring
-size_t seg_bytes(int P, int H) {
-  return seg_table_bytes(P, H) + static_cast<size_t>(4 * P - 5) * H * DK * DV * sizeof(float) +
-         ring_bytes(seg_ring_pairs(P, H));
+size_t seg_bytes(int P, int N, int H) {
+  const long long NH = static_cast<long long>(N) * H;
+  return seg_table_bytes(P, N, H) + static_cast<size_t>(4 * P - 5) * NH * DK * DV * sizeof(float) +
+         ring_bytes(seg_ring_pairs(P, NH));
 }
 int device_sms() {
   int dev = 0, sms = 0;
@@ -1447,45 +1453,47 @@ int device_sms() {
   return sms;
 }
 
-// The run tables of both passes, from the sequence's offsets as the device holds them
-// (checked like every other kernel does: out of order or range, every run is skipped
-// and KDA_ERR_SEQLENS recorded).  Segment q takes chunks q n / P .. (q + 1) n / P - 1 of
-// the sequence's n chunks (sizes differ by one chunk at most); the last one ends at the
-// sequence's end.
+// The run tables of both passes, block n for sequence n, from its offsets as the device
+// holds them (checked like every other kernel does: out of order or range, the sequence's
+// runs are skipped and KDA_ERR_SEQLENS recorded).  Segment q takes chunks q m / P ..
+// (q + 1) m / P - 1 of the sequence's m chunks (sizes differ by one chunk at most); the last
+// one ends at the sequence's end.
 __global__ void kda_seg_table_kernel(const int32_t *cu_seqlens, int T, int P, int4 *runs1, int4 *runs2,
                                      uint32_t *status) {
-  const int b = cu_seqlens[0], e = cu_seqlens[1];
+  const int n = blockIdx.x;
+  const int b = cu_seqlens[n], e = cu_seqlens[n + 1];
   const bool ok = 0 <= b && b <= e && e <= T;
   if (!ok && threadIdx.x == 0) atomicCAS(status, 0u, kStatusSeqlens);
   const int skip = ok ? 0 : kRunSkip;
-  const long long n = ok ? (static_cast<long long>(e) - b + C - 1) / C : 0;
+  const long long m = ok ? (static_cast<long long>(e) - b + C - 1) / C : 0;
+  int4 *r1 = runs1 + n * (2 * P - 3), *r2 = runs2 + n * (P - 1);
   for (int q = threadIdx.x; q < P; q += blockDim.x) {
-    const int sb = ok ? static_cast<int>(std::min<long long>(b + q * n / P * C, e)) : b;
-    const int se = ok ? static_cast<int>(std::min<long long>(b + (q + 1) * n / P * C, e)) : b;
+    const int sb = ok ? static_cast<int>(std::min<long long>(b + q * m / P * C, e)) : b;
+    const int se = ok ? static_cast<int>(std::min<long long>(b + (q + 1) * m / P * C, e)) : b;
     if (q == 0) {
-      runs1[0] = make_int4(sb, se, skip, 0);
+      r1[0] = make_int4(sb, se, skip, n);
     } else {
-      runs2[q - 1] = make_int4(sb, se, skip, 0);
+      r2[q - 1] = make_int4(sb, se, skip, n);
       if (q < P - 1) {
-        runs1[2 * q - 1] = make_int4(sb, se, kRunNoOut | skip, 0);
-        runs1[2 * q] = make_int4(sb, se, kRunZeroV | kRunNoOut | skip, 0);
+        r1[2 * q - 1] = make_int4(sb, se, kRunNoOut | skip, n);
+        r1[2 * q] = make_int4(sb, se, kRunZeroV | kRunNoOut | skip, n);
       }
     }
   }
 }
 
 // The start states of the pass-1 runs, in the buffer their end states then overwrite (each
-// thread of the chunk kernel reads and later writes the same elements): run 0 the given
-// initial state (zero without one), runs 2p - 1 zero, runs 2p the identity.
-__global__ void __launch_bounds__(256) kda_seg_init_kernel(float *F1, const float *init, int H) {
-  const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;  // < (2P-3) H d_k d_v
+// thread of the chunk kernel reads and later writes the same elements): each sequence's
+// run 0 its given initial state (zero without one), runs 2p - 1 zero, runs 2p the identity.
+__global__ void __launch_bounds__(256) kda_seg_init_kernel(float *F1, const float *init, int P, int H) {
+  const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;  // < N (2P-3) H d_k d_v
   const size_t per_run = static_cast<size_t>(H) * DK * DV;
-  const int run = static_cast<int>(i / per_run);
+  const int run = static_cast<int>(i / per_run), k = run % (2 * P - 3), n = run / (2 * P - 3);
   const size_t e = i % per_run;  // element of head e / (d_k d_v)
   float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (run == 0) {
-    if (init) x = *reinterpret_cast<const float4 *>(init + e);
-  } else if (run % 2 == 0) {
+  if (k == 0) {
+    if (init) x = *reinterpret_cast<const float4 *>(init + static_cast<size_t>(n) * per_run + e);
+  } else if (k % 2 == 0) {
     const int r = static_cast<int>(e % (DK * DV)) / DV, c = static_cast<int>(e % DV);  // c .. c + 3
     x = make_float4(r == c ? 1.f : 0.f, r == c + 1 ? 1.f : 0.f, r == c + 2 ? 1.f : 0.f, r == c + 3 ? 1.f : 0.f);
   }
@@ -1493,8 +1501,8 @@ __global__ void __launch_bounds__(256) kda_seg_init_kernel(float *F1, const floa
 }
 
 // S_1 = the end state of segment 0 (pass-1 run 0); S_{p+1} = M_p S_p + B_p with M_p, B_p
-// the end states of pass-1 runs 2p and 2p - 1, in fp32.  CTA (h, cb) keeps columns
-// 4 cb .. 4 cb + 3 of head h's state in shared memory (the columns do not mix).  Warp w
+// the end states of pass-1 runs 2p and 2p - 1, in fp32.  CTA (n, h, cb) keeps columns
+// 4 cb .. 4 cb + 3 of sequence n's state of head h in shared memory (the columns do not mix).  Warp w
 // takes rows 32 (w mod 4) + lane over the key slice j = 32 (w / 4) .. + 31: its part of
 // row r of M_p sits in registers, loaded while the CTA still works on the step before,
 // and the four slices' partial sums meet in shared memory.  The CTAs with cb = 0 also
@@ -1505,10 +1513,14 @@ __global__ void __launch_bounds__(kCombThreads) kda_seg_combine_kernel(const flo
                                                                        uint32_t *head_skip) {
   __shared__ float4 Ssh[DK];       // S_p[j][4 cb .. 4 cb + 3]
   __shared__ float4 part[4][DK];   // partial sums of the four key slices
-  const int h = blockIdx.x / (DV / 4), cb = blockIdx.x % (DV / 4);
+  const int nh = blockIdx.x / (DV / 4), cb = blockIdx.x % (DV / 4), n = nh / H, h = nh % H;
   const int w = threadIdx.x >> 5, js = w >> 2, r = 32 * (w & 3) + (threadIdx.x & 31);
-  if (cb == 0 && threadIdx.x == 0) head_skip[h] = pair_flags ? pair_flags[h] : 0u;
-  const size_t stride = static_cast<size_t>(H) * DK * DV, hoff = static_cast<size_t>(h) * DK * DV;
+  if (cb == 0 && threadIdx.x == 0) head_skip[nh] = pair_flags ? pair_flags[nh] : 0u;
+  const size_t stride = static_cast<size_t>(H) * DK * DV;
+  // sequence n's pass-1 runs and start states, head h
+  F1 += static_cast<size_t>(n) * (2 * P - 3) * stride;
+  starts += static_cast<size_t>(n) * (P - 1) * stride;
+  const size_t hoff = static_cast<size_t>(h) * DK * DV;
   const size_t roff = hoff + static_cast<size_t>(r) * DV + 4 * cb;  // element (r, 4 cb) of head h
   if (js == 0) {
     const float4 s1 = *reinterpret_cast<const float4 *>(F1 + roff);  // run 0: segment 0's end
@@ -1558,15 +1570,17 @@ __global__ void __launch_bounds__(kCombThreads) kda_seg_combine_kernel(const flo
   }
 }
 
-// The sequence's final state from the last segment's end state, for every head whose runs
-// all went through (not skipped, not marked for the exact recomputation, which writes it
-// from the untouched initial state instead).
-__global__ void __launch_bounds__(256) kda_seg_final_kernel(const float *Flast, float *final_state,
-                                                            const int4 *last_run, const uint32_t *pair_flags) {
-  const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;  // < H d_k d_v
-  const int h = static_cast<int>(i / (DK * DV));
-  if ((last_run->z & kRunSkip) || (pair_flags && pair_flags[h])) return;
-  *reinterpret_cast<float4 *>(final_state + i) = *reinterpret_cast<const float4 *>(Flast + i);
+// Each sequence's final state from its last segment's end state, for every (sequence, head)
+// whose runs all went through (not skipped, not marked for the exact recomputation, which
+// writes it from the untouched initial state instead).
+__global__ void __launch_bounds__(256) kda_seg_final_kernel(const float *F2, float *final_state, const int4 *runs2,
+                                                            const uint32_t *pair_flags, int P, int H) {
+  const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;  // < N H d_k d_v
+  const int nh = static_cast<int>(i / (DK * DV)), n = nh / H;
+  const int last = n * (P - 1) + P - 2;  // sequence n's last pass-2 run
+  if ((runs2[last].z & kRunSkip) || (pair_flags && pair_flags[nh])) return;
+  const size_t src = (static_cast<size_t>(last) * H + nh % H) * DK * DV + i % (DK * DV);
+  *reinterpret_cast<float4 *>(final_state + i) = *reinterpret_cast<const float4 *>(F2 + src);
 }
 
 // Ring of the helper schedule: [P][kRingSlots] slot images, then [P][kRingSlots][2] words.
@@ -1582,10 +1596,9 @@ size_t chunk_tc_scratch_bytes(int num_seqs, int total_tokens, int num_heads, int
   size_t bytes = 0;
   if (pairs >= 1 && pairs <= kHelperMaxPairs) bytes = ring_bytes(pairs);  // solve helpers
   else if (num_seqs >= 2 && num_seqs <= kOrderMaxSeqs) bytes = order_bytes(num_seqs);  // launch order
-  if (num_seqs == 1) {  // one long sequence: the segment-parallel scan, when it applies
-    const int P = seg_count(total_tokens, num_heads, device_sms());
-    if (P) bytes = std::max(bytes, seg_bytes(P, num_heads));
-  }
+  // a few long sequences: the segment-parallel scan, when it applies
+  const int P = seg_count(num_seqs, total_tokens, num_heads, device_sms());
+  if (P) bytes = std::max(bytes, seg_bytes(P, num_seqs, num_heads));
   return bytes;
 }
 
@@ -1623,7 +1636,7 @@ static cudaError_t launch_helpers(const ChunkArgs &a, cudaStream_t stream, CUten
   return cudaErrorNotReady;
 }
 
-// The launch of one instantiation: the segment-parallel scan for one long sequence with few
+// The launch of one instantiation: the segment-parallel scan for a few long sequences with few
 // heads, else the solve-helper schedule when it fits, else the plain one.
 template <bool kPrep>
 static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
@@ -1632,20 +1645,21 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
   cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false, kPrep>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (err != cudaSuccess) return err;
-  // One long sequence with few heads: the segment-parallel scan (two passes and a combine)
-  const int P = a.num_seqs == 1 ? seg_count(a.total_tokens, a.num_heads, a.num_sms) : 0;
-  if (P && a.scratch && a.scratch_bytes >= seg_bytes(P, a.num_heads)) {
-    const int H = a.num_heads;
-    const size_t st = static_cast<size_t>(H) * DK * DV;
+  // A few long sequences with few heads: the segment-parallel scan (two passes and a combine)
+  const int P = seg_count(a.num_seqs, a.total_tokens, a.num_heads, a.num_sms);
+  if (P && a.scratch && a.scratch_bytes >= seg_bytes(P, a.num_seqs, a.num_heads)) {
+    const int N = a.num_seqs, H = a.num_heads;
+    const long long NH = static_cast<long long>(N) * H;
+    const size_t st = static_cast<size_t>(H) * DK * DV;  // floats of one run's states
     unsigned char *base = static_cast<unsigned char *>(a.scratch);
     int4 *runs1 = reinterpret_cast<int4 *>(base);
-    int4 *runs2 = runs1 + (2 * P - 3);
-    uint32_t *head_skip = reinterpret_cast<uint32_t *>(runs1 + 3 * P);
-    float *F1 = reinterpret_cast<float *>(base + seg_table_bytes(P, H));
-    float *starts = F1 + static_cast<size_t>(2 * P - 3) * st;
-    float *F2 = starts + static_cast<size_t>(P - 1) * st;
-    uint8_t *ring = reinterpret_cast<uint8_t *>(F2 + static_cast<size_t>(P - 1) * st);
-    const size_t ring_avail = ring_bytes(seg_ring_pairs(P, H));
+    int4 *runs2 = runs1 + static_cast<size_t>(N) * (2 * P - 3);
+    uint32_t *head_skip = reinterpret_cast<uint32_t *>(runs1 + static_cast<size_t>(N) * 3 * P);
+    float *F1 = reinterpret_cast<float *>(base + seg_table_bytes(P, N, H));
+    float *starts = F1 + static_cast<size_t>(N) * (2 * P - 3) * st;
+    float *F2 = starts + static_cast<size_t>(N) * (P - 1) * st;
+    uint8_t *ring = reinterpret_cast<uint8_t *>(F2 + static_cast<size_t>(N) * (P - 1) * st);
+    const size_t ring_avail = ring_bytes(seg_ring_pairs(P, NH));
     // a pass through the helper schedule when it fits, else the plain one
     auto pass = [&](TcParams &pp, long long np) -> cudaError_t {
       pp.npairs = static_cast<int>(np);  // (run, head) pairs of this pass
@@ -1654,18 +1668,19 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
       kda_chunk_tc_kernel<false, kPrep><<<(unsigned)np, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, mo, pp);
       return cudaGetLastError();
     };
-    kda_seg_table_kernel<<<1, 128, 0, stream>>>(a.cu_seqlens, a.total_tokens, P, runs1, runs2, a.status);
+    kda_seg_table_kernel<<<N, 128, 0, stream>>>(a.cu_seqlens, a.total_tokens, P, runs1, runs2, a.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    const size_t n1 = static_cast<size_t>(2 * P - 3) * st;  // floats, a multiple of 1024
-    kda_seg_init_kernel<<<(unsigned)(n1 / 1024), 256, 0, stream>>>(F1, a.init_state, H);
+    const size_t n1 = static_cast<size_t>(N) * (2 * P - 3) * st;  // floats, a multiple of 1024
+    kda_seg_init_kernel<<<(unsigned)(n1 / 1024), 256, 0, stream>>>(F1, a.init_state, P, H);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     TcParams p1 = prm;
     p1.cu_seqlens = reinterpret_cast<const int32_t *>(runs1);
     p1.seq_stride = 4;
     p1.init_state = F1;  // in place
     p1.final_state = F1;
-    if ((err = pass(p1, static_cast<long long>(2 * P - 3) * H)) != cudaSuccess) return err;
-    kda_seg_combine_kernel<<<H * (DV / 4), kCombThreads, 0, stream>>>(F1, starts, P, H, a.pair_flags, head_skip);
+    if ((err = pass(p1, (2 * P - 3) * NH)) != cudaSuccess) return err;
+    kda_seg_combine_kernel<<<(unsigned)(NH * (DV / 4)), kCombThreads, 0, stream>>>(F1, starts, P, H,
+                                                                                  a.pair_flags, head_skip);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     TcParams p2 = prm;
     p2.cu_seqlens = reinterpret_cast<const int32_t *>(runs2);
@@ -1673,9 +1688,9 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     p2.head_skip = head_skip;
     p2.init_state = starts;
     p2.final_state = F2;
-    if ((err = pass(p2, static_cast<long long>(P - 1) * H)) != cudaSuccess || !a.final_state) return err;
-    kda_seg_final_kernel<<<(unsigned)(st / 1024), 256, 0, stream>>>(F2 + static_cast<size_t>(P - 2) * st,
-                                                                    a.final_state, runs2 + (P - 2), a.pair_flags);
+    if ((err = pass(p2, (P - 1) * NH)) != cudaSuccess || !a.final_state) return err;
+    kda_seg_final_kernel<<<(unsigned)(NH * DK * DV / 1024), 256, 0, stream>>>(F2, a.final_state, runs2,
+                                                                              a.pair_flags, P, H);
     return cudaGetLastError();
   }
   // Few sequence-heads leave most SMs idle: with room for the ring, one or two solve

@@ -267,7 +267,7 @@ def kda_workspace_status(workspace, stream=None) -> int:
 def workspace_status_words(workspace, stream=None):
     """Synchronises the stream and returns the four status words of a prefill
     workspace: (first error, detail, tensor-core schedule that ran (1 plain, 2 solve
-    helpers, 3 segments of one sequence, 0 CUDA-core path), sequence-heads recomputed
+    helpers, 3 segment-parallel scan, 0 CUDA-core path), sequence-heads recomputed
     token by token)."""
     s = stream if stream is not None else torch.cuda.current_stream()
     s.synchronize()

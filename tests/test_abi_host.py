@@ -95,11 +95,12 @@ def test_workspace_holds_the_solve_helper_ring_for_few_sequence_heads(lib):
 
 
 def test_workspace_holds_the_segments_of_one_long_sequence(lib):
-    """One sequence of at least 3 x 32 chunks with at most 50 heads: for P = min((SMs / H
-    + 3) / 2, chunks / 32) >= 3 segments, the run tables and the heads to skip (16 bytes per
-    run slot, 3 slots per segment, 4 bytes per head, rounded up to 256), 4P - 5 fp32 states
-    per head, and a solve-helper ring for the larger of the two passes (2P - 3 and P - 1
-    runs per head) that has at most 76 pairs.  Without a device the size is taken for 152
+    """Sequences of at least 3 x 32 chunks on average with at most 50 sequence-heads: for
+    P = min((SMs / (N H) + 3) / 2, average chunks / 32) >= 3 segments per sequence, the run
+    tables and the pairs to skip (16 bytes per run slot, 3 slots per segment and sequence,
+    4 bytes per sequence-head, rounded up to 256), 4P - 5 fp32 states per sequence-head, and
+    a solve-helper ring for the larger of the two passes (2P - 3 and P - 1 runs per
+    sequence-head) that has at most 76 pairs.  Without a device the size is taken for 152
     SMs."""
     ws = lambda **kw: lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(num_seqs=1, **kw)))
     st, ring = 128 * 128 * 4, 65568
@@ -110,6 +111,12 @@ def test_workspace_holds_the_segments_of_one_long_sequence(lib):
     assert ws(num_heads=1, total_tokens=1 << 20) == 512 + 3840 + 303 * st + 76 * ring    # P = 77
     assert ws(num_heads=51, total_tokens=1 << 20) == 512 + 51 * ring                     # no segments
     assert ws(num_heads=4, total_tokens=65536, gate=K.KDA_GATE_NONE) == 256 + 1024 + 75 * 4 * st + 76 * ring
+    # several sequences: P from the average length, N H (2P - 3) runs in the first pass
+    ws2 = lambda **kw: lib.kda_chunk_fwd_workspace_bytes(ctypes.byref(_shape(**kw)))
+    assert ws2(num_seqs=2, num_heads=2, total_tokens=20014) == 512 + 512 + 11 * 4 * st + 20 * ring   # P = 4
+    assert ws2(num_seqs=3, num_heads=1, total_tokens=18500) == 512 + 512 + 7 * 3 * st + 9 * ring    # P = 3
+    assert ws2(num_seqs=2, num_heads=26, total_tokens=1 << 20) == 512 + 52 * ring                   # 52 pairs: no
+    assert ws2(num_seqs=64, num_heads=32, total_tokens=1 << 20) == 256 + 8192 + 256                 # varlen: order
     assert lib.kda_version() >= 1005  # 1.5 added the segments
 
 

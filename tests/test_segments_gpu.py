@@ -1,4 +1,4 @@
-"""The segment-parallel scan of one long sequence with few heads.
+"""The segment-parallel scan of a few long sequences with few heads.
 
 The state recurrence of "Kimi Delta Attention (KDA)" is affine in the start state: over
 any stretch of tokens S_end = M S_start + B, with M the product of the per-token
@@ -30,9 +30,13 @@ pytestmark = pytest.mark.gpu
 STATUS_BYTES, SCHED_SEGMENTS = 256, 3
 
 
-def _segments(T, H, sms):
-    nch = (T + 63) // 64
-    P = min((sms // H + 3) // 2, nch // 32)
+def _segments(T, H, sms, N=1):
+    """Segments per sequence: from the average sequence's chunks, while the first pass's
+    N H (2P - 3) runs fit one wave."""
+    if N * H > sms:
+        return 0
+    nch = (T // N + 63) // 64
+    P = min((sms // (N * H) + 3) // 2, nch // 32)
     return P if P >= 3 else 0
 
 
@@ -42,11 +46,11 @@ def _seg_start(T, P, q):
     return min(T, q * n // P * 64)
 
 
-def _seg_bytes(P, H):
-    """Run tables and skip marks, 4P - 5 states per head, the ring of the larger pass that
-    takes solve helpers (at most 76 pairs)."""
-    pairs = [r * H for r in (2 * P - 3, P - 1) if r * H <= 76]
-    return ((3 * P * 16 + 4 * H + 255) // 256 * 256 + (4 * P - 5) * H * 128 * 128 * 4
+def _seg_bytes(P, H, N=1):
+    """Run tables and skip marks, 4P - 5 states per sequence-head, the ring of the larger
+    pass that takes solve helpers (at most 76 pairs)."""
+    pairs = [r * N * H for r in (2 * P - 3, P - 1) if r * N * H <= 76]
+    return ((3 * P * 16 * N + 4 * N * H + 255) // 256 * 256 + (4 * P - 5) * N * H * 128 * 128 * 4
             + max(pairs, default=0) * 4 * (16384 + 8))
 
 
@@ -199,9 +203,75 @@ def test_segments_skip_bad_offsets(cu):
 
 
 def test_many_heads_or_short_sequences_keep_one_chain():
-    """51 heads (fewer than three runs per head fit in one wave), a sequence of 95
-    chunks, and two sequences: no room for segments is asked for."""
+    """51 sequence-heads (fewer than three runs each fit in one wave) and sequences of 95
+    chunks on average: no room for segments is asked for."""
     sms = _sms()
     assert _segments(65536, 51, sms) == 0 and _segments(64 * 95, 2, sms) == 0
-    for N, T, H in ((1, 64 * 95, 2), (2, 20000, 2)):
-        assert kda_chunk_fwd_workspace_bytes(N, T, H, 128, 128) < _seg_bytes(3, H)
+    assert _segments(2 * 65536, 26, sms, N=2) == 0 and _segments(2 * 64 * 95, 2, sms, N=2) == 0
+    for N, T, H in ((1, 64 * 95, 2), (2, 2 * 64 * 95, 2), (2, 2 * 65536, 26)):
+        assert kda_chunk_fwd_workspace_bytes(N, T, H, 128, 128) < _seg_bytes(3, H, N)
+
+
+def _slow(x):
+    x["g"] = (x["g"].float() / 100).to(x["g"].dtype).contiguous()
+    return x
+
+
+@pytest.mark.parametrize("lens,H", [([7000, 12000], 2), ([9000, 0, 9500], 1), ([6500, 6200, 7000, 6400], 2)])
+def test_several_sequences_match_the_oracle(lens, H):
+    """Several long sequences (one empty among them): each cut into the same number of
+    segments from its own length, the runs of all of them in the same two passes."""
+    N, T = len(lens), sum(lens)
+    P = _segments(T, H, _sms(), N)
+    assert P >= 3
+    x = _slow(W.prefill_inputs(W.custom_prefill(lens, num_heads=H, d=128, gate="std", seed=121)))
+    d = to_dev(x)
+    need = kda_chunk_fwd_workspace_bytes(N, T, H, 128, 128)
+    assert need == STATUS_BYTES + (4 * N * H + 255) // 256 * 256 + _seg_bytes(P, H, N)
+    ws = torch.full((need,), 0x5A, dtype=torch.uint8, device="cuda")
+    out, fin = _call(d, d["g"], ws, check=True)
+    words = workspace_status_words(ws)
+    assert words[0] == 0 and words[2] == SCHED_SEGMENTS and words[3] == 0, words
+    ro, rs = run_oracle_prefill(x)
+    o, s = out.float().cpu().numpy(), fin.cpu().numpy()
+    cu = x["cu_seqlens"].numpy()
+    assert rel_l2_per_head(o, ro, cu) <= TOL_BF16
+    nonempty = [n for n, L in enumerate(lens) if L > 0]
+    assert rel_l2_states(s[nonempty], rs[nonempty]) <= TOL_BF16
+    for n, L in enumerate(lens):
+        if L == 0:  # an empty sequence passes its initial state through
+            assert torch.equal(fin[n], d["init_state"][n])
+            continue
+        for p in range(P):  # every segment of every sequence
+            lo, hi = cu[n] + _seg_start(L, P, p), cu[n] + _seg_start(L, P, p + 1)
+            assert rel_l2_per_head(o[lo:hi], ro[lo:hi], np.array([0, hi - lo])) <= TOL_BF16, (n, p)
+
+
+def test_several_sequences_gate_beyond_range_and_bad_offsets():
+    """Two of three sequences' offsets are valid: the third (out of order) is skipped and
+    reported, and one head of the second, whose decay leaves the tensor-core range, is
+    recomputed token by token; everything else keeps the segment results."""
+    lens, H = [8000, 9000, 8000], 2
+    x = _slow(W.prefill_inputs(W.custom_prefill(lens + [128], num_heads=H, d=128, gate="std", seed=122)))
+    g = x["g"].float()
+    g[8000 + 3000:8000 + 3200, 0] = -2.0
+    x["g"] = g.to(x["g"].dtype).contiguous()
+    T = sum(lens)
+    d = to_dev(x)
+    rows = {kk: (vv[:T] if kk in ("q", "k", "v", "g", "beta") else vv) for kk, vv in d.items()}
+    cu = torch.tensor([0, 8000, 17000, 16000], dtype=torch.int32, device="cuda")  # sequence 2 = [17000, 16000)
+    init = d["init_state"][:3].contiguous()
+    ws = torch.zeros(kda_chunk_fwd_workspace_bytes(3, T, H, 128, 128), dtype=torch.uint8, device="cuda")
+    out = torch.full((T + 128, H, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    fin = torch.full_like(init, 7.0)
+    kda_chunk_fwd(rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"], cu, init, out=out[:T],
+                  final_state=fin, workspace=ws, algo="tensor")
+    words = workspace_status_words(ws)
+    assert words[0] == 11 and words[2] == SCHED_SEGMENTS and words[3] == 1, words  # KDA_ERR_SEQLENS
+    assert torch.equal(fin[2], torch.full_like(fin[2], 7.0))  # the skipped sequence
+    assert torch.equal(out[17000:], torch.full_like(out[17000:], 5.0))
+    xs = {kk: x[kk][:17000] for kk in ("q", "k", "v", "g", "beta")}
+    xs.update(cu_seqlens=torch.tensor([0, 8000, 17000], dtype=torch.int32), init_state=x["init_state"][:2])
+    ro, rs = run_oracle_prefill(xs)
+    assert rel_l2_per_head(out[:17000].float().cpu().numpy(), ro, xs["cu_seqlens"].numpy()) <= TOL_BF16
+    assert rel_l2_states(fin[:2].cpu().numpy(), rs) <= TOL_BF16
