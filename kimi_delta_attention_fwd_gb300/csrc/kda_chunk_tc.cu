@@ -327,8 +327,11 @@ __device__ __forceinline__ void row_sumsq32x2(uint32_t tk, uint32_t tq, int rbas
 // kSched = false: every CTA is a (sequence, head) tile that solves its own chunks
 // (the plain schedule); true: CTAs P .. (1 + hpp) P - 1 are solve helpers for the
 // first P.  kPrep: the input steps of TcParams::prep are compiled in (a call without
-// them runs the instantiation that has none of their code).
-template <bool kSched, bool kPrep>
+// them runs the instantiation that has none of their code).  kChan: g is one log alpha per
+// key channel, compiled in (the per-token and no-gate code is left out, which keeps the
+// hot loops smaller for the instruction cache); without it the gate mode is read from
+// TcParams::gate.
+template <bool kSched, bool kPrep, bool kChan>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto load_g = [&](int sidx, int c) {
     const uint32_t fb = ctx.bar(kFullG0 + sidx), st = stage_at(sidx);
-    if (p.gate == 0) {
+    if (kChan || p.gate == 0) {
       mbar_arrive_expect_tx(fb, 16384);
       tma_load_3d(st + L::kG, &tm_g, fb, 0, h, bos + c * C);
       tma_load_3d(st + L::kG + 8192, &tm_g, fb, 64, h, bos + c * C);
@@ -485,9 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Register split: the state side holds 64 fp32 state values per thread.  The launch
   // gives every thread 128 registers (512 x 128 = 65,536); the K-side warpgroups hand
-  // 16 each back and the state side takes them: 256 x 112 + 256 x 144 = 65,536.
+  // 8 each back and the state side takes them: 256 x 120 + 256 x 136 = 65,536.
   if (warp < 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
     // ------------------------------------------------------------ K-side
     // Two groups of 4 warps; group kw takes the chunks c = kw, kw + 2, ... and
     // owns stage kw, TP[kw] and TMEM columns [128 kw, 128 kw + 128), so the
@@ -511,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Sl = So + 2 * 16 * kSdLd;                                            // [32][36]
     float *Ys = reinterpret_cast<float *>(smem + L::kTP + kw * 16384);          // TP rows 0-63
     const uint32_t mma_bar = ctx.bar(kMmaK0 + kw);
-    const bool chan = p.gate == 0;  // g per key channel: G by the cumsum product below
+    // g per key channel (G by the cumsum product below): compiled in, or read from p.gate
+    const bool chan = kChan || p.gate == 0;
     // g holds gate logits: each group turns its g tile into -c softplus(g) in place before
     // the cumsum product, which is then issued at the top of the chunk (not ahead)
     const bool gsp = kPrep && chan && (p.prep & kPrepGSoftplus);
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 2; ++x) {
           tma_prefetch_3d(&tm_k, 64 * x, h, tn);
           tma_prefetch_3d(&tm_q, 64 * x, h, tn);
-          if (p.gate == 0) tma_prefetch_3d(&tm_g, 64 * x, h, tn);
+          if (kChan || p.gate == 0) tma_prefetch_3d(&tm_g, 64 * x, h, tn);
           if (!helper) tma_prefetch_3d(&tm_v, 64 * x, h, tn);
         }
       }
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a1 with one log alpha per (token, head): G_r is one inclusive scan over the
       // chunk's rows (rows r and 32 + r of two per-warp scans), the same for every channel
       float g_row = 0.f;
-      if (p.gate == 1) {
+      if (!kChan && p.gate == 1) {
         const int lane = t & 31;
         float ga = lane < len ? gate_log<kPrep>(__bfloat162float(p.g_tok[(size_t)(t0 + lane) * H + h]),
                                                 p.prep, p.gate_scale) : 0.f;
@@ -1098,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(ctx.bar(kFinK0 + kw), 0, kWaitCycles);
     }
   } else if (!helper) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 136;" ::: "memory");
     // ------------------------------------------------------------ state side
     // Thread (d_v row v = 32 (warp % 4) + lane, key-channel half hs = (warp - 8) / 4)
     // holds S[64 hs + j][v], j = 0..63, in fp32: column v of the state, which is row v
@@ -1605,7 +1609,7 @@ size_t chunk_tc_scratch_bytes(int num_seqs, int total_tokens, int num_heads, int
 // The solve-helper schedule over `pairs` pairs in one cooperative launch, every CTA resident
 // as the hand-over through global memory needs: cudaSuccess once enqueued, cudaErrorNotReady
 // when it does not apply or does not fit (nothing launched: the plain schedule runs).
-template <bool kPrep>
+template <bool kPrep, bool kChan>
 static cudaError_t launch_helpers(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
                                   CUtensorMap &mg, CUtensorMap &mv, CUtensorMap &mo, TcParams prm,
                                   long long pairs, uint8_t *ring, size_t ring_avail) {
@@ -1618,7 +1622,7 @@ static cudaError_t launch_helpers(const ChunkArgs &a, cudaStream_t stream, CUten
     (void)cudaGetLastError();
     return cudaErrorNotReady;
   }
-  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true, kPrep>,
+  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<true, kPrep, kChan>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (err != cudaSuccess) return err;
   prm.npairs = static_cast<int>(pairs);  // the tiles; CTAs from here on are helpers
@@ -1628,7 +1632,7 @@ static cudaError_t launch_helpers(const ChunkArgs &a, cudaStream_t stream, CUten
   err = cudaMemsetAsync(prm.ring_flags, 0, pairs * kRingSlots * 2 * sizeof(uint32_t), stream);
   if (err != cudaSuccess) return err;
   void *args[] = {&mq, &mk, &mg, &mv, &mo, &prm};
-  err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true, kPrep>),
+  err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kda_chunk_tc_kernel<true, kPrep, kChan>),
                                     dim3(static_cast<unsigned>((1 + hpp) * pairs)), dim3(kThreads), args,
                                     L::kAlloc, stream);
   if (err != cudaErrorCooperativeLaunchTooLarge) return err;
@@ -1638,11 +1642,11 @@ static cudaError_t launch_helpers(const ChunkArgs &a, cudaStream_t stream, CUten
 
 // The launch of one instantiation: the segment-parallel scan for a few long sequences with few
 // heads, else the solve-helper schedule when it fits, else the plain one.
-template <bool kPrep>
+template <bool kPrep, bool kChan>
 static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMap &mq, CUtensorMap &mk,
                              CUtensorMap &mg, CUtensorMap &mv, CUtensorMap &mo, TcParams &prm,
                              long long pairs) {
-  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false, kPrep>,
+  cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel<false, kPrep, kChan>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (err != cudaSuccess) return err;
   // A few long sequences with few heads: the segment-parallel scan (two passes and a combine)
@@ -1663,9 +1667,10 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     // a pass through the helper schedule when it fits, else the plain one
     auto pass = [&](TcParams &pp, long long np) -> cudaError_t {
       pp.npairs = static_cast<int>(np);  // (run, head) pairs of this pass
-      cudaError_t e = launch_helpers<kPrep>(a, stream, mq, mk, mg, mv, mo, pp, np, ring, ring_avail);
+      cudaError_t e = launch_helpers<kPrep, kChan>(a, stream, mq, mk, mg, mv, mo, pp, np, ring, ring_avail);
       if (e != cudaErrorNotReady) return e;
-      kda_chunk_tc_kernel<false, kPrep><<<(unsigned)np, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, mo, pp);
+      kda_chunk_tc_kernel<false, kPrep, kChan><<<(unsigned)np, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, mo,
+                                                                                                pp);
       return cudaGetLastError();
     };
     kda_seg_table_kernel<<<N, 128, 0, stream>>>(a.cu_seqlens, a.total_tokens, P, runs1, runs2, a.status);
@@ -1695,8 +1700,8 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
   }
   // Few sequence-heads leave most SMs idle: with room for the ring, one or two solve
   // helpers per sequence-head join its tile in one cooperative launch.
-  err = launch_helpers<kPrep>(a, stream, mq, mk, mg, mv, mo, prm, pairs, static_cast<uint8_t *>(a.scratch),
-                              a.scratch ? a.scratch_bytes : 0);
+  err = launch_helpers<kPrep, kChan>(a, stream, mq, mk, mg, mv, mo, prm, pairs,
+                                     static_cast<uint8_t *>(a.scratch), a.scratch ? a.scratch_bytes : 0);
   if (err != cudaErrorNotReady) return err;
   // More than one wave: start the longest sequences first (when the workspace has room)
   if (pairs > a.num_sms && a.num_seqs >= 2 && a.num_seqs <= kOrderMaxSeqs && a.scratch &&
@@ -1708,8 +1713,8 @@ static cudaError_t launch_tc(const ChunkArgs &a, cudaStream_t stream, CUtensorMa
     if (err != cudaSuccess) return err;
     prm.order = order;
   }
-  kda_chunk_tc_kernel<false, kPrep><<<(unsigned)pairs, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv, mo,
-                                                                                          prm);
+  kda_chunk_tc_kernel<false, kPrep, kChan><<<(unsigned)pairs, kThreads, L::kAlloc, stream>>>(mq, mk, mg, mv,
+                                                                                                 mo, prm);
   return cudaGetLastError();
 }
 
@@ -1755,8 +1760,10 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   prm.npairs = static_cast<int>(pairs);
   if (pairs == 0) return cudaSuccess;
-  return a.prep ? launch_tc<true>(a, stream, mq, mk, mg, mv, mo, prm, pairs)
-                : launch_tc<false>(a, stream, mq, mk, mg, mv, mo, prm, pairs);
+  // the input steps with any gate, or one instantiation per gate family without them
+  if (a.prep) return launch_tc<true, false>(a, stream, mq, mk, mg, mv, mo, prm, pairs);
+  return a.gate == 0 ? launch_tc<false, true>(a, stream, mq, mk, mg, mv, mo, prm, pairs)
+                     : launch_tc<false, false>(a, stream, mq, mk, mg, mv, mo, prm, pairs);
 }
 
 }  // namespace kda
