@@ -538,6 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicCAS(p.status, 0u, kStatusTimeout);
       }
     }
+    // The chunk loop, compiled once per role: a solve helper's and a tile's copies each
+    // leave out the other's code (a helper schedule launch runs both kinds of CTA).
+    auto kloop = [&](auto role) {
+    constexpr bool helper = decltype(role)::value;
+    constexpr bool fed = kSched && !helper;
     uint32_t kph = 0;
     // chunks of this group: c = kw, kw + 2, ...; in a helper c = hp + hpp kw + 2 hpp i
     for (int c = helper ? hp + hpp * kw : kw; c < nchunks; c += c_step) {
@@ -1097,6 +1102,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    };
+    if (kSched && helper)
+      kloop(std::true_type{});
+    else
+      kloop(std::false_type{});
     if (t == 0) {  // all of this group's MMAs retired before TMEM is released
       mma_commit(ctx.bar(kFinK0 + kw));
       mbar_wait(ctx.bar(kFinK0 + kw), 0, kWaitCycles);
@@ -1760,8 +1770,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream) {
   const long long pairs = (long long)a.num_seqs * a.num_heads;
   prm.npairs = static_cast<int>(pairs);
   if (pairs == 0) return cudaSuccess;
-  // the input steps with any gate, or one instantiation per gate family without them
-  if (a.prep) return launch_tc<true, false>(a, stream, mq, mk, mg, mv, mo, prm, pairs);
+  // one instantiation per gate family (one log alpha per key channel, or the others),
+  // with or without the input steps
+  if (a.prep)
+    return a.gate == 0 ? launch_tc<true, true>(a, stream, mq, mk, mg, mv, mo, prm, pairs)
+                       : launch_tc<true, false>(a, stream, mq, mk, mg, mv, mo, prm, pairs);
   return a.gate == 0 ? launch_tc<false, true>(a, stream, mq, mk, mg, mv, mo, prm, pairs)
                      : launch_tc<false, false>(a, stream, mq, mk, mg, mv, mo, prm, pairs);
 }
