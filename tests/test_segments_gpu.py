@@ -275,3 +275,55 @@ def test_several_sequences_gate_beyond_range_and_bad_offsets():
     ro, rs = run_oracle_prefill(xs)
     assert rel_l2_per_head(out[:17000].float().cpu().numpy(), ro, xs["cu_seqlens"].numpy()) <= TOL_BF16
     assert rel_l2_states(fin[:2].cpu().numpy(), rs) <= TOL_BF16
+
+
+def _random_case(seed):
+    import random
+    r = random.Random(seed)
+    n = r.randint(1, 3)
+    short = n > 1 and r.random() < 0.5
+    lens = [r.randint(12300 if short else 6200, 16000) for _ in range(n)]  # 96 chunks on average
+    if short:
+        lens[r.randrange(n)] = r.choice([0, 1, 63, 64, 65, 700])  # a short one among them
+    return dict(lens=lens, H=r.randint(1, 4), gate=r.choice(["channel", "scalar", "none"]),
+                decay=r.choice([1.0, 0.05, 0.01]), init=r.choice(["normal", "zeros"]),
+                beta_scale=r.choice([1.0, 0.3]), state_scale=r.choice([1.0, 50.0]))
+
+
+@pytest.mark.parametrize("seed", range(2000, 2008))
+def test_random_long_sequences(seed):
+    """Seeded random calls that take the segments: one to three sequences (a short or empty
+    one among them at times), one to four heads, every gate form, decays from the recipe's
+    down to a hundredth of it, with and without an initial state (of standard deviation
+    0.02 or 1), write strengths at the recipe's or 0.3 of it."""
+    c = _random_case(seed)
+    lens, H = c["lens"], c["H"]
+    N, T = len(lens), sum(lens)
+    P = _segments(T, H, _sms(), N)
+    if P < 3:
+        pytest.skip(f"average length too short for segments: {lens}")
+    x = W.prefill_inputs(W.custom_prefill(lens, num_heads=H, d=128, gate="std", init=c["init"], seed=seed))
+    x["g"] = (x["g"].float() * c["decay"]).to(x["g"].dtype)
+    x["beta"] = (x["beta"].float() * c["beta_scale"]).to(x["beta"].dtype)
+    if x["init_state"] is not None:
+        x["init_state"] = x["init_state"] * c["state_scale"]
+    if c["gate"] == "channel":
+        g_gpu = g_ref = x["g"]
+    elif c["gate"] == "scalar":
+        g_gpu = x["g"][..., 0].contiguous()
+        g_ref = g_gpu.unsqueeze(-1).expand_as(x["g"]).contiguous()
+    else:
+        g_gpu, g_ref = None, torch.zeros_like(x["g"])
+    d = to_dev(x)
+    ws = torch.zeros(kda_chunk_fwd_workspace_bytes(N, T, H, 128, 128), dtype=torch.uint8, device="cuda")
+    out, fin = _call(d, None if g_gpu is None else g_gpu.cuda(), ws, check=True)
+    assert workspace_status_words(ws)[2] == SCHED_SEGMENTS
+    xo = dict(x)
+    xo["g"] = g_ref
+    ro, rs = run_oracle_prefill(xo)
+    o, s = out.float().cpu().numpy(), fin.cpu().numpy()
+    cu = x["cu_seqlens"].numpy()
+    assert np.isfinite(o).all() and np.isfinite(s).all()
+    assert rel_l2_per_head(o, ro, cu) <= TOL_BF16, c
+    nonempty = [n for n, L in enumerate(lens) if L > 0]
+    assert rel_l2_states(s[nonempty], rs[nonempty]) <= TOL_BF16, c
