@@ -360,8 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [T; A^qk] from the ring; a helper (pair, hp) runs the chunk solve of the chunks
   // c = hp + hpp kw + 2 hpp i of its K-side group kw and publishes it
   const int P = p.npairs;
-  const bool helper = kSched && (int)blockIdx.x >= P;
-  const bool fed = kSched && !helper;
+  const bool helper = kSched && (int)blockIdx.x >= P;  // (a tile "fed" by helpers otherwise)
   const int hpp = kSched ? p.helpers_per_pair : 1;
   const int hb = (int)blockIdx.x - P;
   const int hp = helper ? hb % hpp : 0;
@@ -1516,67 +1515,79 @@ __global__ void __launch_bounds__(256) kda_seg_init_kernel(float *F1, const floa
 
 // S_1 = the end state of segment 0 (pass-1 run 0); S_{p+1} = M_p S_p + B_p with M_p, B_p
 // the end states of pass-1 runs 2p and 2p - 1, in fp32.  CTA (n, h, cb) keeps columns
-// 4 cb .. 4 cb + 3 of sequence n's state of head h in shared memory (the columns do not mix).  Warp w
-// takes rows 32 (w mod 4) + lane over the key slice j = 32 (w / 4) .. + 31: its part of
-// row r of M_p sits in registers, loaded while the CTA still works on the step before,
-// and the four slices' partial sums meet in shared memory.  The CTAs with cb = 0 also
-// copy the recomputation marks the first pass left, for the second pass to skip those heads.
+// 4 cb .. 4 cb + 3 of sequence n's state of head h in shared memory (the columns do not
+// mix).  Warp w forms rows 8 w .. 8 w + 7: lane l multiplies keys 4 l .. 4 l + 3 (its
+// part of each row of M_p, read as one float4 per row, the warp's loads coalesced, and
+// loaded while the CTA still works on the step before), and the lanes' 32 partial sums
+// are reduced by a butterfly that leaves row 8 w + l / 4, column l mod 4 in lane l.  The
+// CTAs with cb = 0 also copy the recomputation marks the first pass left, for the second
+// pass to skip those sequence-heads.
 constexpr int kCombThreads = 512;
 __global__ void __launch_bounds__(kCombThreads) kda_seg_combine_kernel(const float *F1, float *starts, int P,
                                                                        int H, const uint32_t *pair_flags,
                                                                        uint32_t *head_skip) {
-  __shared__ float4 Ssh[DK];       // S_p[j][4 cb .. 4 cb + 3]
-  __shared__ float4 part[4][DK];   // partial sums of the four key slices
+  __shared__ float4 Ssh[DK];  // S_p[j][4 cb .. 4 cb + 3]
   const int nh = blockIdx.x / (DV / 4), cb = blockIdx.x % (DV / 4), n = nh / H, h = nh % H;
-  const int w = threadIdx.x >> 5, js = w >> 2, r = 32 * (w & 3) + (threadIdx.x & 31);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (cb == 0 && threadIdx.x == 0) head_skip[nh] = pair_flags ? pair_flags[nh] : 0u;
   const size_t stride = static_cast<size_t>(H) * DK * DV;
   // sequence n's pass-1 runs and start states, head h
   F1 += static_cast<size_t>(n) * (2 * P - 3) * stride;
   starts += static_cast<size_t>(n) * (P - 1) * stride;
   const size_t hoff = static_cast<size_t>(h) * DK * DV;
-  const size_t roff = hoff + static_cast<size_t>(r) * DV + 4 * cb;  // element (r, 4 cb) of head h
-  if (js == 0) {
-    const float4 s1 = *reinterpret_cast<const float4 *>(F1 + roff);  // run 0: segment 0's end
-    *reinterpret_cast<float4 *>(starts + roff) = s1;
-    Ssh[r] = s1;
+  if (threadIdx.x < DK) {  // run 0: segment 0's end
+    const size_t o = hoff + static_cast<size_t>(threadIdx.x) * DV + 4 * cb;
+    const float4 s1 = *reinterpret_cast<const float4 *>(F1 + o);
+    *reinterpret_cast<float4 *>(starts + o) = s1;
+    Ssh[threadIdx.x] = s1;
   }
-  auto load = [&](int q, float4 (&m)[8], float4 &b) {
-    const float4 *row = reinterpret_cast<const float4 *>(F1 + 2 * q * stride + hoff +
-                                                         static_cast<size_t>(r) * DV + 32 * js);
+  const int orow = 8 * w + (l >> 2), ocol = 4 * cb + (l & 3);  // the element lane l forms
+  const size_t ooff = hoff + static_cast<size_t>(orow) * DV + ocol;
+  // row part of M_q (rows 8 w + rr, keys 4 l .. 4 l + 3) and lane l's element of B_q
+  auto load = [&](int q, float4 (&m)[8], float &b) {
+    const float *M = F1 + 2 * q * stride + hoff + static_cast<size_t>(8 * w) * DV + 4 * l;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = row[i];
-    b = js == 0 ? *reinterpret_cast<const float4 *>(F1 + (2 * q - 1) * stride + roff)
-                : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int rr = 0; rr < 8; ++rr) m[rr] = *reinterpret_cast<const float4 *>(M + rr * DV);
+    b = F1[(2 * q - 1) * stride + ooff];
   };
-  // step q with row part mc and offset bc; the next step's loads go to mn, bn first
-  auto step = [&](int q, float4 (&mc)[8], const float4 &bc, float4 (&mn)[8], float4 &bn) {
-    __syncthreads();  // Ssh holds S_q; part is free
+  auto step = [&](int q, float4 (&mc)[8], float bc, float4 (&mn)[8], float &bn) {
+    __syncthreads();  // Ssh holds S_q
     if (q + 1 <= P - 2) load(q + 1, mn, bn);
-    float4 acc = bc;
+    float4 sv[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float mj[4] = {mc[i].x, mc[i].y, mc[i].z, mc[i].w};
+    for (int jj = 0; jj < 4; ++jj) sv[jj] = Ssh[4 * l + jj];
+    float v[32];  // v[4 rr + c]: this lane's part of row 8 w + rr, column c
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      const float mj[4] = {mc[rr].x, mc[rr].y, mc[rr].z, mc[rr].w};
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        const float4 sv = Ssh[32 * js + 4 * i + jj];
-        acc.x = fmaf(mj[jj], sv.x, acc.x);
-        acc.y = fmaf(mj[jj], sv.y, acc.y);
-        acc.z = fmaf(mj[jj], sv.z, acc.z);
-        acc.w = fmaf(mj[jj], sv.w, acc.w);
+        a0 = fmaf(mj[jj], sv[jj].x, a0);
+        a1 = fmaf(mj[jj], sv[jj].y, a1);
+        a2 = fmaf(mj[jj], sv[jj].z, a2);
+        a3 = fmaf(mj[jj], sv[jj].w, a3);
+      }
+      v[4 * rr] = a0, v[4 * rr + 1] = a1, v[4 * rr + 2] = a2, v[4 * rr + 3] = a3;
+    }
+    // butterfly over the lanes: at offset o each lane keeps the half of its values its
+    // bit o selects and adds the partner's copy of that half; lane l ends with v[l]
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = l & o;
+#pragma unroll
+      for (int i = 0; i < o; ++i) {
+        const float send = up ? v[i] : v[i + o], keep = up ? v[i + o] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
     }
-    part[js][r] = acc;
-    __syncthreads();  // all partial sums are in; every thread has read S_q
-    if (js == 0) {
-      const float4 a0 = part[0][r], a1 = part[1][r], a2 = part[2][r], a3 = part[3][r];
-      const float4 sn = make_float4(a0.x + a1.x + a2.x + a3.x, a0.y + a1.y + a2.y + a3.y,
-                                    a0.z + a1.z + a2.z + a3.z, a0.w + a1.w + a2.w + a3.w);
-      Ssh[r] = sn;
-      *reinterpret_cast<float4 *>(starts + q * stride + roff) = sn;
-    }
+    const float sn = v[0] + bc;
+    __syncthreads();  // every thread has read S_q
+    reinterpret_cast<float *>(Ssh)[4 * orow + (l & 3)] = sn;
+    starts[q * stride + ooff] = sn;
   };
-  float4 mA[8], mB[8], bA, bB;
+  float4 mA[8], mB[8];
+  float bA = 0.f, bB = 0.f;
   if (P >= 3) load(1, mA, bA);
   for (int q = 1; q <= P - 2; q += 2) {
     step(q, mA, bA, mB, bB);
