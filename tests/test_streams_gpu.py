@@ -52,3 +52,21 @@ def test_decode_and_recurrent_on_a_side_stream():
                                d["init_state"], stream=side)
     side.synchronize()
     assert torch.equal(o2, ro) and torch.equal(f2, rf)
+
+
+def test_segment_scan_on_a_side_stream_with_default_workspace():
+    """One long sequence (the segment-parallel scan: seven launches on the call's stream,
+    its tables, states and ring in the default workspace) on a side stream: the same bits
+    as on the current stream."""
+    x = W.prefill_inputs(W.custom_prefill([10007], num_heads=2, d=128, seed=73))
+    d = to_dev(x)
+    ref_o, ref_f = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                 d["init_state"])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    out, fin = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                             d["init_state"], stream=side)
+    junk = [torch.full((1 << 22,), 3.0, device="cuda") for _ in range(8)]
+    side.synchronize()
+    del junk
+    assert torch.equal(out, ref_o) and torch.equal(fin, ref_f)
