@@ -1049,14 +1049,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();  // also orders the solve's scratch writes before the g reload
       bar_sync(bar_id, 128);
-      if (t == 0) {
-        // the state side's first products need [T; A^qk] and Vb only: they can start now
-        mbar_arrive(ctx.bar(kTPReady0 + s));
-        // the g area (solve scratch) is free: the group's next chunk's g tile
-        if (!fed && c + 2 < nchunks && !*abort_flag) load_g(s, c + 2);
-      }
 
-      // [T; A^qk] Kb -> D2, rows 0-63: W = T Kb
+      // [T; A^qk] Kb -> D2, rows 0-63: W = T Kb, issued before the state side's first
+      // products (which need [T; A^qk] and Vb only) so that it goes ahead of them
       if (t == 0) {
         tc_fence_after();
         constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
@@ -1065,6 +1060,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k4 = 0; k4 < 4; ++k4)
           mma_ss(tm, atp + 2 * k4, sdesc_hi(1024), bkb + 128 * k4, sdesc_hi(1024), id_k, k4 > 0);
         mma_commit(mma_bar);
+        mbar_arrive(ctx.bar(kTPReady0 + s));
+        // the g area (solve scratch) is free: the group's next chunk's g tile
+        if (!fed && c + 2 < nchunks && !*abort_flag) load_g(s, c + 2);
         ctx.wait(kMmaK0 + kw, kph & 1);
       } else if (fed && t == 32) {
         // every thread's ring loads have completed (their values are in TP[s]): count
