@@ -141,8 +141,8 @@ typedef struct {
  *                 results; the segment-parallel scan (below) rounds differently
  *                 and agrees with them within the bf16 tolerance.  Calls that
  *                 share one workspace must be ordered on one stream.
- * A few long sequences with few heads (P >= 3 below) run as P segments of whole chunks
- * each: the recurrence is affine in the start state, S_end = M S_start + B over any
+ * On the tensor-core path, a few long sequences with few heads (P >= 3 below, and fewer
+ * than 2^30 tokens in the call) run as P segments of whole chunks each: the recurrence is affine in the start state, S_end = M S_start + B over any
  * stretch of tokens, so a first launch runs every sequence's segment 0 from the true
  * start and each middle segment from zero (B) and from the identity with V = 0 (M, as
  * d_k = d_v), a small kernel chains S_{p+1} = M_p S_p + B_p in fp32, and a second launch
