@@ -117,6 +117,9 @@ def test_workspace_holds_the_segments_of_one_long_sequence(lib):
     assert ws2(num_seqs=3, num_heads=1, total_tokens=18500) == 512 + 512 + 7 * 3 * st + 9 * ring    # P = 3
     assert ws2(num_seqs=2, num_heads=26, total_tokens=1 << 20) == 512 + 52 * ring                   # 52 pairs: no
     assert ws2(num_seqs=64, num_heads=32, total_tokens=1 << 20) == 256 + 8192 + 256                 # varlen: order
+    # 2^30 tokens or more: no segments (their zero V tiles are read below token 0)
+    assert ws2(num_seqs=1, num_heads=1, total_tokens=(1 << 30) - 64) == 512 + 3840 + 303 * st + 76 * ring
+    assert ws2(num_seqs=1, num_heads=1, total_tokens=1 << 30) == 512 + ring
     assert lib.kda_version() >= 1005  # 1.5 added the segments
 
 
